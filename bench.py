@@ -1,0 +1,340 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed MoE FFN of a DeepSeek-V4-Flash-shaped layer on GB300.
+
+Default workload: one decode token through one layer with hidden 4096, 256
+routed experts top-6 + 1 shared, FFN width 2048, 2-bit superblock routed
+experts and Q8_0 shared expert and router (about 2.1 GB of routed weights
+resident in HBM). A step is one ds4moe_forward over one batch of synthetic
+input; inputs are resident in HBM before the timed region; L2 is flushed by a
+512 MiB write between timed steps (outside the timed kernels).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own replica
+(weak scaling, no collective on the data path); value = all tokens / max time.
+--impl reference times the CPU oracle (scalar C on the host cores) on the same
+workload: it is the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-FFN tokens/s (decode, prefill) and achieved HBM GB/s vs GB300 peak"
+
+WORKLOADS = {
+    "ds4-decode-1": (synth.DS4, 1, "single decode token, DeepSeek-V4-Flash-shaped layer (H 4096, E 256 top-6 + 1 "
+                                   "shared, F 2048, Q2S routed, Q8_0 shared/router), learned routing"),
+    "ds4-decode-32-zipf": (synth.DS4_ZIPF, 32, "batched decode of 32 tokens on the same layer, router bias with "
+                                               "Zipf(1.1) expert popularity"),
+    "ds4-hash-prefill-512": (synth.DS4_HASH, 512, "hash-routed layer (vocab 129280), prefill chunk of 512 tokens"),
+    "tiny-4": (synth.TINY, 4, "tiny layer H 256, E 16 top-2 + 1 shared, F 128, all Q8_0, fp32 router, 4 tokens"),
+}
+DEFAULT_WORKLOAD = "ds4-decode-1"
+SEED = 2026
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def step_bytes(spec, T, unique_routed):
+    """Algorithmic bytes of one forward: the weights of the experts touched,
+    the shared expert, the router (+ bias) or the hash rows, x read once and y
+    read + written once."""
+    H, F, E, k = spec.hidden, spec.ffn, spec.n_experts, spec.top_k
+    per_expert = 2 * synth.row_bytes(spec.routed_fmt, H) * F + synth.row_bytes(spec.routed_fmt, F) * H
+    shared = (2 * synth.row_bytes(spec.shared_fmt, H) * F + synth.row_bytes(spec.shared_fmt, F) * H) \
+        if spec.n_shared else 0
+    route = (synth.row_bytes(spec.router_fmt, H) * E + 4 * E) if spec.route == "learned" else T * (4 + 4 * k)
+    return unique_routed * per_expert + shared + route + 3 * T * H * 4
+
+
+def gateup_bytes(spec, T, unique_routed):
+    """Algorithmic bytes of one gate/up launch: gate and up weights of the
+    experts touched plus the shared expert's, the activation codes, scales and
+    group sums read, and the SwiGLU codes and scales written."""
+    H, F, k = spec.hidden, spec.ffn, spec.top_k
+    w = unique_routed * 2 * synth.row_bytes(spec.routed_fmt, H) * F
+    if spec.n_shared:
+        w += 2 * synth.row_bytes(spec.shared_fmt, H) * F
+    act = T * (H + H // 32 * 4 + H // 16 * 2)
+    out = T * (k + spec.n_shared) * (F + F // 32 * 4 + F // 16 * 2)
+    return w + act + out
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [s.strip() for s in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def desc_from_spec(ds4, spec, max_tokens):
+    return ds4.LayerDesc(spec.hidden, spec.n_experts, spec.top_k, spec.ffn, spec.n_shared,
+                         ds4.ROUTE_HASH if spec.route == "hash" else ds4.ROUTE_LEARNED, spec.vocab,
+                         ds4.FMT[spec.router_fmt], ds4.FMT[spec.routed_fmt], ds4.FMT[spec.shared_fmt],
+                         spec.route_scale, max_tokens)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, spec, T, desc):
+    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    w = synth.gen_layer(spec, SEED, 0)
+    ol = oracle.get().layer(spec, w)
+    nx = 8
+    xs = [synth.gen_x(spec, SEED + i, T) for i in range(nx)]
+    tok = synth.gen_token_ids(spec, SEED, T) if spec.route == "hash" else None
+    cores = os.cpu_count() or 1
+    for i in range(args.warmup):
+        ol.forward(xs[i % nx], None, tok, nthreads=cores)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        ol.forward(xs[i % nx], None, tok, nthreads=cores)
+    dt = time.perf_counter() - t0
+    value = args.steps * T / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32+f32",
+        "data": "synthetic", "config": {"workload": args.workload, "description": desc, "n_tok": T},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps of the {args.workload} workload ({T} token(s) each), "
+                                   f"scalar C oracle with {cores} threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(spec, T, w, budget_s=12.0):
+    """The oracle as it stands, on this host's cores, on a bounded sample."""
+    import oracle
+    ol = oracle.get().layer(spec, w)
+    cores = os.cpu_count() or 1
+    tok = synth.gen_token_ids(spec, SEED, T) if spec.route == "hash" else None
+    n, t0 = 0, time.perf_counter()
+    while True:
+        x = synth.gen_x(spec, SEED + 1000 + n, T)
+        ol.forward(x, None, tok, nthreads=cores)
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= 4096:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n * T / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} forward(s) of {T} token(s) of the same workload ({dt:.1f} s of CPU work)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    spec, T, desc = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, spec, T, desc)
+        return
+
+    import torch
+
+    import deepseek_v4_flash_gb300 as ds4
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda")
+
+    # Weights: generated on the host, uploaded, re-laid out by ds4moe_create.
+    w = synth.gen_layer(spec, SEED, 0)
+    wd = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in w.items()}
+    layer = ds4.Layer(desc_from_spec(ds4, spec, T), wd)
+    del wd
+    torch.cuda.empty_cache()
+
+    # Inputs resident in HBM: NX distinct batches, cycled.
+    NX = 64
+    xs = torch.from_numpy(np.stack([synth.gen_x(spec, SEED + 7 * i + rank, T) for i in range(NX)])).to(dev)
+    tok = torch.from_numpy(synth.gen_token_ids(spec, SEED + rank, T)).to(dev) if spec.route == "hash" else None
+    y = torch.zeros(T, spec.hidden, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    # Unique routed experts of each input batch (sets the algorithmic bytes).
+    uniq = []
+    for i in range(NX):
+        ids, _ = layer.route(xs[i], tok)
+        uniq.append(len(np.unique(ids.cpu().numpy()[ids.cpu().numpy() >= 0])))
+    uniq = np.array(uniq)
+
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        flush.fill_(i & 255)
+        layer.forward(xs[i % NX], y, tok)
+    torch.cuda.synchronize()
+
+    layer.profile(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = layer.launch_count()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 255)  # L2 flush; also keeps the queue ahead of the GPU
+        ev[i][0].record(stream)
+        layer.forward(xs[i % NX], y, tok)
+        ev[i][1].record(stream)
+        layer.profile_collect()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    launches = layer.launch_count() - launches0
+    clk = clocks.stop()
+    step_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    stage_ms, ncalls = layer.profile_read()
+    layer.profile(False)
+    total_s = float(step_ms.sum()) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = world * args.steps * T / total_s
+
+    hbm_peak, bf16_peak, peak_kind = peaks()
+    u_steps = uniq[np.arange(args.steps) % NX]
+    bytes_step = np.array([step_bytes(spec, T, u) for u in u_steps], dtype=np.float64)
+    gu_bytes = np.array([gateup_bytes(spec, T, u) for u in u_steps], dtype=np.float64)
+    step_gbs = float(bytes_step.sum() / total_s / 1e9) if world == 1 else float(bytes_step.sum() * world / total_s / 1e9)
+    gu_ms = stage_ms["gateup"] / max(ncalls, 1)
+    gu_gbs = float(gu_bytes.mean() / (gu_ms / 1e3) / 1e9)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32+f32", "data": "synthetic",
+        "config": {"workload": args.workload, "description": desc, "n_tok": T,
+                   "l2": "flushed: 512 MiB write between timed steps",
+                   "inputs": f"{NX} seeded batches resident in HBM, cycled"},
+        "hbm_gbs": step_gbs, "hbm_frac": step_gbs / hbm_peak,
+        "bytes_per_step": float(bytes_step.mean()),
+        "unique_experts_per_step": float(u_steps.mean()),
+        "roofline": {"kernel": "gate/up GEMV (k_gateup)", "bound": "hbm", "achieved": gu_gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": gu_gbs / hbm_peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": float(gu_bytes.mean()), "launch_ms": gu_ms,
+                     "traffic": None},
+        "stages_ms": {k: v / max(ncalls, 1) for k, v in stage_ms.items()},
+        "gpu_launches": int(launches),
+        "wall_s": t_wall,
+    }
+    if clk:
+        line["clocks"] = clk
+
+    # End to end through the public API on host buffers (pinned).
+    if rank == 0 and args.e2e_steps > 0:
+        xh = [xs[i % NX].cpu().pin_memory() for i in range(min(args.e2e_steps, NX))]
+        yh = torch.zeros(T, spec.hidden).pin_memory()
+        th = tok.cpu().pin_memory() if tok is not None else None
+        for i in range(3):
+            layer.forward_host(xh[i % len(xh)], yh, th)
+        tot = 0.0
+        for i in range(args.e2e_steps):
+            flush.fill_(i & 255)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            layer.forward_host(xh[i % len(xh)], yh, th)
+            tot += time.perf_counter() - t0
+        line["e2e"] = {"value": args.e2e_steps * T / tot, "unit": "tokens/s",
+                       "h2d_bytes_per_step": 2 * T * spec.hidden * 4 + (T * 4 if tok is not None else 0),
+                       "d2h_bytes_per_step": T * spec.hidden * 4, "steps": args.e2e_steps}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec, T, w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,403 @@
+// api.cu -- host side of the libds4moe C ABI: argument validation, device
+// memory ownership, the create-time re-layout of the weights, and the
+// per-call launch sequence
+//   quantise x -> route (router GEMV + top-k, or hash) -> bucket by expert
+//   -> gate/up (+ SwiGLU + requant) -> down -> fixed-order combine into y.
+// Nothing here does arithmetic on the data; all of it runs in the kernels.
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace ds4;
+
+namespace {
+
+bool is_dev_ptr(const void *p) {
+  if (!p) return false;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+bool fmt_ok(int f) { return f == DS4MOE_Q8_0 || f == DS4MOE_Q2S; }
+
+// K must be a whole number of K-steps of the format.
+bool k_ok(int fmt, int K) { return K > 0 && K % kstep(fmt) == 0; }
+
+ds4moe_status validate_desc(const ds4moe_layer_desc *d) {
+  if (!d || d->abi_version != DS4MOE_ABI_VERSION) return DS4MOE_ERR_INVALID_ARG;
+  if (d->hidden <= 0 || d->hidden % 256 != 0 || d->hidden > (1 << 16)) return DS4MOE_ERR_INVALID_ARG;
+  if (d->ffn <= 0 || d->ffn % 64 != 0 || d->ffn > (1 << 16)) return DS4MOE_ERR_INVALID_ARG;
+  if (d->n_experts < 1 || d->n_experts > 1024) return DS4MOE_ERR_INVALID_ARG;
+  if (d->top_k < 1 || d->top_k > 16 || d->top_k > d->n_experts) return DS4MOE_ERR_INVALID_ARG;
+  if (d->n_shared != 0 && d->n_shared != 1) return DS4MOE_ERR_INVALID_ARG;
+  if (d->max_tokens < 1 || d->max_tokens > (1 << 20)) return DS4MOE_ERR_INVALID_ARG;
+  if (!fmt_ok(d->routed_fmt)) return DS4MOE_ERR_INVALID_ARG;
+  if (d->n_shared && !fmt_ok(d->shared_fmt)) return DS4MOE_ERR_INVALID_ARG;
+  if (!k_ok(d->routed_fmt, d->hidden) || !k_ok(d->routed_fmt, d->ffn)) return DS4MOE_ERR_INVALID_ARG;
+  if (d->n_shared && (!k_ok(d->shared_fmt, d->hidden) || !k_ok(d->shared_fmt, d->ffn)))
+    return DS4MOE_ERR_INVALID_ARG;
+  if (d->route == DS4MOE_ROUTE_LEARNED) {
+    if (d->router_fmt != DS4MOE_F32 && d->router_fmt != DS4MOE_Q8_0) return DS4MOE_ERR_INVALID_ARG;
+  } else if (d->route == DS4MOE_ROUTE_HASH) {
+    if (d->vocab < 1) return DS4MOE_ERR_INVALID_ARG;
+  } else {
+    return DS4MOE_ERR_INVALID_ARG;
+  }
+  if (!(d->route_scale == d->route_scale)) return DS4MOE_ERR_INVALID_ARG;  // NaN
+  // int32 index arithmetic bounds: T*NS*max(H,F) elements per scratch array
+  const long long T = d->max_tokens, NS = d->top_k + d->n_shared;
+  const long long big = d->hidden > d->ffn ? d->hidden : d->ffn;
+  if (T * NS * big >= (1ll << 40)) return DS4MOE_ERR_INVALID_ARG;
+  return DS4MOE_OK;
+}
+
+void free_all(ds4moe_layer *h) {
+  for (int i = 0; i < h->n_allocs; i++) cudaFree(h->allocs[i]);
+  h->n_allocs = 0;
+}
+
+template <typename T>
+ds4moe_status alloc(ds4moe_layer *h, T **p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) return DS4MOE_OK;
+  if (h->n_allocs >= (int)(sizeof(h->allocs) / sizeof(h->allocs[0]))) return DS4MOE_ERR_OOM;
+  void *q = nullptr;
+  if (cudaMalloc(&q, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_OOM;
+  }
+  h->allocs[h->n_allocs++] = q;
+  h->bytes += bytes;
+  *p = (T *)q;
+  return DS4MOE_OK;
+}
+
+ds4moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DS4MOE_OK;
+  cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? DS4MOE_ERR_OOM : DS4MOE_ERR_CUDA;
+}
+
+// Re-lay out a [n_mat][rows][K] tensor into the RG32 layout.
+cudaError_t repack(int fmt, const void *src, uint8_t *dst, int n_mat, int rows, int rows_pad, int K, int pair,
+                   int which, cudaStream_t s) {
+  if (fmt == DS4MOE_Q2S) return repack_q2s((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
+  return repack_q8((const uint8_t *)src, dst, n_mat, rows, rows_pad, K, pair, which, s);
+}
+
+size_t rg32_bytes(int fmt, long long n_mat, long long rows_pad, long long K) {
+  return (size_t)(n_mat * (rows_pad / 32) * (K / kstep(fmt)) * tile_bytes(fmt));
+}
+
+ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
+  const ds4moe_layer_desc &d = h->d;
+  const int E = d.n_experts, H = d.hidden, F = d.ffn, k = d.top_k;
+  const long long T = d.max_tokens, NS = h->NS;
+  ds4moe_status st;
+  cudaStream_t s = 0;
+
+  // ---- weights
+  if (d.route == DS4MOE_ROUTE_LEARNED) {
+    if (!is_dev_ptr(w->router_w) || !is_dev_ptr(w->router_bias)) return DS4MOE_ERR_INVALID_ARG;
+    if (d.router_fmt == DS4MOE_Q8_0) {
+      const size_t nb = rg32_bytes(DS4MOE_Q8_0, 1, h->E_pad, H);
+      if ((st = alloc(h, &h->router, nb)) != DS4MOE_OK) return st;
+      if ((st = cuda_status(cudaMemsetAsync(h->router, 0, nb, s))) != DS4MOE_OK) return st;
+      if ((st = cuda_status(repack(DS4MOE_Q8_0, w->router_w, h->router, 1, E, h->E_pad, H, 0, 0, s))) != DS4MOE_OK)
+        return st;
+    } else {
+      const size_t nb = (size_t)E * H * 4;
+      if ((st = alloc(h, &h->router, nb)) != DS4MOE_OK) return st;
+      if ((st = cuda_status(cudaMemcpyAsync(h->router, w->router_w, nb, cudaMemcpyDeviceToDevice, s))) != DS4MOE_OK)
+        return st;
+    }
+    if ((st = alloc(h, &h->bias, (size_t)E * 4)) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemcpyAsync(h->bias, w->router_bias, (size_t)E * 4, cudaMemcpyDeviceToDevice, s))) !=
+        DS4MOE_OK)
+      return st;
+  } else {
+    if (!is_dev_ptr(w->hash_table)) return DS4MOE_ERR_INVALID_ARG;
+    const size_t nb = (size_t)d.vocab * k * 4;
+    if ((st = alloc(h, &h->hash, nb)) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemcpyAsync(h->hash, w->hash_table, nb, cudaMemcpyDeviceToDevice, s))) != DS4MOE_OK)
+      return st;
+  }
+  if (!is_dev_ptr(w->gate) || !is_dev_ptr(w->up) || !is_dev_ptr(w->down)) return DS4MOE_ERR_INVALID_ARG;
+  const int rf = d.routed_fmt;
+  if ((st = alloc(h, &h->gu, 2 * rg32_bytes(rf, E, F, H))) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->dn, rg32_bytes(rf, E, H, F))) != DS4MOE_OK) return st;
+  if ((st = cuda_status(repack(rf, w->gate, h->gu, E, F, F, H, 1, 0, s))) != DS4MOE_OK) return st;
+  if ((st = cuda_status(repack(rf, w->up, h->gu, E, F, F, H, 1, 1, s))) != DS4MOE_OK) return st;
+  if ((st = cuda_status(repack(rf, w->down, h->dn, E, H, H, F, 0, 0, s))) != DS4MOE_OK) return st;
+  if (d.n_shared) {
+    if (!is_dev_ptr(w->sh_gate) || !is_dev_ptr(w->sh_up) || !is_dev_ptr(w->sh_down)) return DS4MOE_ERR_INVALID_ARG;
+    const int sf = d.shared_fmt;
+    if ((st = alloc(h, &h->sgu, 2 * rg32_bytes(sf, 1, F, H))) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->sdn, rg32_bytes(sf, 1, H, F))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(repack(sf, w->sh_gate, h->sgu, 1, F, F, H, 1, 0, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(repack(sf, w->sh_up, h->sgu, 1, F, F, H, 1, 1, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(repack(sf, w->sh_down, h->sdn, 1, H, H, F, 0, 0, s))) != DS4MOE_OK) return st;
+  }
+
+  // ---- scratch
+  if ((st = alloc(h, &h->xq, (size_t)T * H)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->dx, (size_t)T * (H / 32) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->gs, (size_t)T * (H / 16) * 2)) != DS4MOE_OK) return st;
+  if (d.route == DS4MOE_ROUTE_LEARNED)
+    if ((st = alloc(h, &h->rpart, (size_t)T * ROUTER_SEGS * h->E_pad * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->ids, (size_t)T * k * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->wts, (size_t)T * k * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->bucket, bucket_ints(E, (int)T, (int)NS) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->hq, (size_t)(T * NS) * F)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->dh, (size_t)(T * NS) * (F / 32) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->gsh, (size_t)(T * NS) * (F / 16) * 2)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->apart, (size_t)(T * NS) * H * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->err, 64)) != DS4MOE_OK) return st;
+  if ((st = cuda_status(cudaMemsetAsync(h->err, 0, 64, s))) != DS4MOE_OK) return st;
+
+  if (d.route == DS4MOE_ROUTE_HASH) {
+    // every table entry must name a routed expert
+    if ((st = cuda_status(cudaMemsetAsync(h->bucket, 0, 4, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(check_hash_table(h->hash, (int64_t)d.vocab * k, E, h->bucket, s))) != DS4MOE_OK) return st;
+    int32_t bad = 0;
+    if ((st = cuda_status(cudaMemcpyAsync(&bad, h->bucket, 4, cudaMemcpyDeviceToHost, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaStreamSynchronize(s))) != DS4MOE_OK) return st;
+    if (bad) return DS4MOE_ERR_INVALID_ARG;
+  }
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t ds4moe_abi_version(void) { return DS4MOE_ABI_VERSION; }
+
+const char *ds4moe_status_string(ds4moe_status s) {
+  switch (s) {
+    case DS4MOE_OK: return "DS4MOE_OK";
+    case DS4MOE_ERR_INVALID_ARG: return "DS4MOE_ERR_INVALID_ARG";
+    case DS4MOE_ERR_UNSUPPORTED: return "DS4MOE_ERR_UNSUPPORTED";
+    case DS4MOE_ERR_OOM: return "DS4MOE_ERR_OOM";
+    case DS4MOE_ERR_CUDA: return "DS4MOE_ERR_CUDA";
+    case DS4MOE_ERR_DEVICE: return "DS4MOE_ERR_DEVICE";
+  }
+  return "DS4MOE_ERR_UNKNOWN";
+}
+
+ds4moe_status ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w, ds4moe_layer **out) {
+  if (!out) return DS4MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  ds4moe_status st = validate_desc(desc);
+  if (st != DS4MOE_OK) return st;
+  if (!w) return DS4MOE_ERR_INVALID_ARG;
+  ds4moe_layer *h = new (std::nothrow) ds4moe_layer;
+  if (!h) return DS4MOE_ERR_OOM;
+  memset(h, 0, sizeof(*h));
+  h->d = *desc;
+  if (cudaGetDevice(&h->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return DS4MOE_ERR_CUDA;
+  }
+  h->E_pad = (desc->n_experts + 31) / 32 * 32;
+  h->NS = desc->top_k + desc->n_shared;
+  {
+    const long long routed = (long long)desc->max_tokens * desc->top_k;
+    h->A_max = (int)(routed < desc->n_experts ? routed : desc->n_experts) + desc->n_shared;
+  }
+  st = build(h, w);
+  if (st != DS4MOE_OK) {
+    cudaDeviceSynchronize();
+    cudaGetLastError();
+    free_all(h);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return DS4MOE_OK;
+}
+
+void ds4moe_destroy(ds4moe_layer *h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  if (h->ev_made)
+    for (int i = 0; i < 8; i++) cudaEventDestroy(h->ev[i]);
+  free_all(h);
+  delete h;
+}
+
+uint64_t ds4moe_device_bytes(const ds4moe_layer *h) { return h ? h->bytes : 0; }
+
+static ds4moe_status check_call(ds4moe_layer *h, int32_t n_tok) {
+  if (!h) return DS4MOE_ERR_INVALID_ARG;
+  if (n_tok < 0 || n_tok > h->d.max_tokens) return DS4MOE_ERR_INVALID_ARG;
+  return DS4MOE_OK;
+}
+
+ds4moe_status ds4moe_route(ds4moe_layer *h, const float *x, const int32_t *token_ids, int32_t n_tok,
+                           int32_t *ids_out, float *w_out, void *stream) {
+  ds4moe_status st = check_call(h, n_tok);
+  if (st != DS4MOE_OK) return st;
+  if (n_tok == 0) return DS4MOE_OK;
+  if (!is_dev_ptr(ids_out) || !is_dev_ptr(w_out)) return DS4MOE_ERR_INVALID_ARG;
+  const bool hash = h->d.route == DS4MOE_ROUTE_HASH;
+  if (hash ? !is_dev_ptr(token_ids) : !is_dev_ptr(x)) return DS4MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!hash && h->d.router_fmt == DS4MOE_Q8_0) {
+    st = cuda_status(launch_quantize(x, n_tok, h->d.hidden, h->xq, h->dx, h->gs, h->err, s));
+    if (st != DS4MOE_OK) return st;
+  }
+  h->launches += hash ? 1 : (h->d.router_fmt == DS4MOE_Q8_0 ? 3 : 2);
+  return cuda_status(launch_route(h, x, token_ids, n_tok, ids_out, w_out, s));
+}
+
+ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids, float *y,
+                             void *stream) {
+  ds4moe_status st = check_call(h, n_tok);
+  if (st != DS4MOE_OK) return st;
+  if (n_tok == 0) return DS4MOE_OK;
+  if (!is_dev_ptr(x) || !is_dev_ptr(y) || x == y) return DS4MOE_ERR_INVALID_ARG;
+  if (h->d.route == DS4MOE_ROUTE_HASH && !is_dev_ptr(token_ids)) return DS4MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int H = h->d.hidden;
+  const bool prof = h->prof_on != 0;
+  auto mark = [&](int i) {
+    if (prof) cudaEventRecord(h->ev[i], s);
+  };
+  mark(0);
+  cudaError_t e = launch_quantize(x, n_tok, H, h->xq, h->dx, h->gs, h->err, s);
+  mark(1);
+  if (e == cudaSuccess) e = launch_route(h, x, token_ids, n_tok, h->ids, h->wts, s);
+  mark(2);
+  if (e == cudaSuccess) e = launch_bucket(h, n_tok, s);
+  mark(3);
+  if (e == cudaSuccess) e = launch_gateup(h, n_tok, s);
+  mark(4);
+  if (e == cudaSuccess) e = launch_down(h, n_tok, s);
+  mark(5);
+  if (e == cudaSuccess) e = launch_combine(h, n_tok, y, s);
+  mark(6);
+  h->launches += (h->d.route == DS4MOE_ROUTE_HASH) ? 6 : 7;
+  return cuda_status(e);
+}
+
+ds4moe_status ds4moe_profile_enable(ds4moe_layer *h, int32_t on) {
+  if (!h) return DS4MOE_ERR_INVALID_ARG;
+  if (on && !h->ev_made) {
+    for (int i = 0; i < 8; i++) {
+      cudaError_t e = cudaEventCreate(&h->ev[i]);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    h->ev_made = 1;
+  }
+  h->prof_on = on ? 1 : 0;
+  if (!on) {
+    for (int i = 0; i < 8; i++) h->prof_ms[i] = 0.0;
+    h->prof_calls = 0;
+  }
+  return DS4MOE_OK;
+}
+
+ds4moe_status ds4moe_profile_collect(ds4moe_layer *h) {
+  if (!h || !h->prof_on) return DS4MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaEventSynchronize(h->ev[DS4MOE_N_STAGES]);
+  if (e != cudaSuccess) return cuda_status(e);
+  for (int i = 0; i < DS4MOE_N_STAGES; i++) {
+    float ms = 0.0f;
+    e = cudaEventElapsedTime(&ms, h->ev[i], h->ev[i + 1]);
+    if (e != cudaSuccess) return cuda_status(e);
+    h->prof_ms[i] += ms;
+  }
+  h->prof_calls++;
+  return DS4MOE_OK;
+}
+
+ds4moe_status ds4moe_profile_read(const ds4moe_layer *h, double *ms_out, int32_t n, int64_t *calls) {
+  if (!h || n < 0 || (n > 0 && !ms_out)) return DS4MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n && i < DS4MOE_N_STAGES; i++) ms_out[i] = h->prof_ms[i];
+  if (calls) *calls = h->prof_calls;
+  return DS4MOE_OK;
+}
+
+uint64_t ds4moe_launch_count(const ds4moe_layer *h) { return h ? h->launches : 0; }
+
+ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t n_tok, const int32_t *token_ids_host,
+                                  float *y_host, void *stream) {
+  ds4moe_status st = check_call(h, n_tok);
+  if (st != DS4MOE_OK) return st;
+  if (n_tok == 0) return DS4MOE_OK;
+  if (!x_host || !y_host) return DS4MOE_ERR_INVALID_ARG;
+  const bool hash = h->d.route == DS4MOE_ROUTE_HASH;
+  if (hash && !token_ids_host) return DS4MOE_ERR_INVALID_ARG;
+  const size_t xb = (size_t)h->d.max_tokens * h->d.hidden * 4;
+  if (!h->x_dev) {
+    if ((st = alloc(h, &h->x_dev, xb)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->y_dev, xb)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->tok_dev, (size_t)h->d.max_tokens * 4)) != DS4MOE_OK) return st;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t nb = (size_t)n_tok * h->d.hidden * 4;
+  cudaError_t e = cudaMemcpyAsync(h->x_dev, x_host, nb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->y_dev, y_host, nb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && hash)
+    e = cudaMemcpyAsync(h->tok_dev, token_ids_host, (size_t)n_tok * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  st = ds4moe_forward(h, h->x_dev, n_tok, hash ? h->tok_dev : nullptr, h->y_dev, stream);
+  if (st != DS4MOE_OK) return st;
+  e = cudaMemcpyAsync(y_host, h->y_dev, nb, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return cuda_status(e);
+}
+
+ds4moe_status ds4moe_rmsnorm(const float *x, float *out, int32_t n_tok, int32_t hidden, float eps, void *stream) {
+  if (n_tok < 0 || hidden <= 0 || hidden % 32 != 0 || !(eps == eps)) return DS4MOE_ERR_INVALID_ARG;
+  if (n_tok == 0) return DS4MOE_OK;
+  if (!is_dev_ptr(x) || !is_dev_ptr(out)) return DS4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_rmsnorm(x, out, n_tok, hidden, eps, (cudaStream_t)stream));
+}
+
+ds4moe_status ds4moe_get_device_error(ds4moe_layer *h, void *stream, uint32_t *flags_out) {
+  if (!h) return DS4MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t f = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&f, h->err, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (flags_out) *flags_out = f;
+  return f ? DS4MOE_ERR_DEVICE : DS4MOE_OK;
+}
+
+// Read-only views of the handle's scratch, for inspecting the intermediate
+// results of the last call (integer codes, ids, weights).
+ds4moe_status ds4moe_debug_scratch(ds4moe_layer *h, int32_t which, const void **ptr_out, uint64_t *bytes_out) {
+  if (!h || !ptr_out || !bytes_out) return DS4MOE_ERR_INVALID_ARG;
+  const long long T = h->d.max_tokens, NS = h->NS, H = h->d.hidden, F = h->d.ffn, k = h->d.top_k;
+  const void *p = nullptr;
+  uint64_t n = 0;
+  switch (which) {
+    case 0: p = h->xq, n = T * H; break;
+    case 1: p = h->dx, n = T * (H / 32) * 4; break;
+    case 2: p = h->gs, n = T * (H / 16) * 2; break;
+    case 3: p = h->ids, n = T * k * 4; break;
+    case 4: p = h->wts, n = T * k * 4; break;
+    case 5: p = h->hq, n = T * NS * F; break;
+    case 6: p = h->dh, n = T * NS * (F / 32) * 4; break;
+    case 7: p = h->apart, n = T * NS * H * 4; break;
+    default: return DS4MOE_ERR_INVALID_ARG;
+  }
+  *ptr_out = p;
+  *bytes_out = n;
+  return DS4MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,197 @@
+// common.cuh -- shared device helpers for libds4moe (sm_103a).
+//
+// 1. The canonical arithmetic spec (CAS) as device functions. Every binary32
+//    operation on the numeric path goes through __fadd_rn / __fmul_rn /
+//    __fmaf_rn / __fdiv_rn / __fsqrt_rn, which the compiler never contracts
+//    or reorders, so results are bit-identical to a scalar CPU evaluation of
+//    the same spec.
+// 2. The library's internal weight layouts ("RG32": 32 rows interleaved so a
+//    warp, one row per lane, reads 512 contiguous bytes per 16-byte load).
+// 3. PTX wrappers for mbarriers and 1-D bulk async copies (cp.async.bulk)
+//    with bounded waits.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds4moe.h"
+
+namespace ds4 {
+
+// ---------------------------------------------------------------------------
+// Internal layouts.
+//
+// Q2S RG32 tile = 32 rows x one superblock (256 K):
+//   [0,512)     sm:   lane l -> 16 bytes (scale/min nibbles of its row)
+//   [512,640)   d,dmin: lane l -> 4 bytes (fp16 d, fp16 dmin)
+//   [640,2688)  qs:   4 chunks c x 32 lanes x 16 bytes; chunk c, word w holds
+//               group g = 4c+w with its 2-bit fields transposed so that
+//               ((W >> 2s) & 0x03030303) yields the bytes q[16g+4s .. 16g+4s+3]
+//               in element order (one dp4a against 4 consecutive int8 x).
+// Q8 RG32 tile = 32 rows x two Q8_0 blocks (64 K):
+//   [0,128)     d: lane l -> 4 bytes (fp16 d of block 0, block 1)
+//   [128,2176)  q: 4 pieces m x 32 lanes x 16 bytes; piece m = block m/2,
+//               elements 16*(m%2) .. 16*(m%2)+15.
+// A matrix [R][K] becomes [R/32][K/KSTEP][tile]; gate and up of the same
+// expert are interleaved per K-step: [R/32][K/KSTEP][2][tile].
+constexpr int Q2S_TILE = 2688, Q2S_DD = 512, Q2S_QS = 640, Q2S_KSTEP = 256;
+constexpr int Q8_TILE = 2176, Q8_Q = 128, Q8_KSTEP = 64;
+constexpr int MAX_STAGE = 2 * Q2S_TILE;  // largest ring stage (gate+up Q2S)
+
+__host__ __device__ constexpr int tile_bytes(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_TILE : Q8_TILE; }
+__host__ __device__ constexpr int kstep(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_KSTEP : Q8_KSTEP; }
+
+// Router rows are summed in 8 segments (CAS step 4, S = 8).
+constexpr int ROUTER_SEGS = 8;
+
+// ---------------------------------------------------------------------------
+// CAS device math.
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
+  return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xFFFFu)));
+}
+
+// cas_exp: Cody & Waite reduction with ln2 split into a 16-bit head and a
+// binary32 tail, then a degree-7 Taylor polynomial in fma Horner form, then
+// scaling by 2^n built from exponent bits. Constants: log2(e), the head/tail
+// of ln2, and 1/k! for k = 2..7, each rounded to binary32.
+__device__ __forceinline__ float cas_exp(float z) {
+  if (z != z) return z;
+  z = z < -87.0f ? -87.0f : z;
+  z = z > 88.0f ? 88.0f : z;
+  const float n = rintf(__fmul_rn(z, 0x1.715476p+0f));
+  float r = __fmaf_rn(-n, 0x1.62e4p-1f, z);
+  r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
+  float p = 0x1.a01a02p-13f;
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);
+  p = __fmaf_rn(p, r, 0x1p-1f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const float s = __int_as_float(((int)n + 127) << 23);
+  return __fmul_rn(p, s);
+}
+
+__device__ __forceinline__ float cas_sigmoid(float z) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, cas_exp(-z)));
+}
+
+__device__ __forceinline__ float cas_silu(float g) {
+  return __fdiv_rn(g, __fadd_rn(1.0f, cas_exp(-g)));
+}
+
+// int8 code of v for scale d (CAS step 1): round half away, clamp +-127.
+__device__ __forceinline__ int cas_code(float v, float d) {
+  if (d == 0.0f) return 0;
+  float r = roundf(__fdiv_rn(v, d));
+  r = r > 127.0f ? 127.0f : r;
+  r = r < -127.0f ? -127.0f : r;
+  return (r == r) ? (int)r : 0;
+}
+
+// Q2S block term (CAS step 3): dx * fma(d, A, -(dmin * B)).
+__device__ __forceinline__ float q2s_term(float dx, float d, float dmin, int A, int B) {
+  const float m = __fmul_rn(dmin, __int2float_rn(B));
+  return __fmul_rn(dx, __fmaf_rn(d, __int2float_rn(A), -m));
+}
+
+// Q8_0 block term (CAS step 3): (d * dx) * I.
+__device__ __forceinline__ float q8_term(float d, float dx, int I) {
+  return __fmul_rn(__fmul_rn(d, dx), __int2float_rn(I));
+}
+
+// ---------------------------------------------------------------------------
+// Warp helpers.
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ int half_warp_sum(int v) {
+#pragma unroll
+  for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ int dot16(uint4 w, uint4 x, int acc) {
+  acc = __dp4a((int)w.x, (int)x.x, acc);
+  acc = __dp4a((int)w.y, (int)x.y, acc);
+  acc = __dp4a((int)w.z, (int)x.z, acc);
+  acc = __dp4a((int)w.w, (int)x.w, acc);
+  return acc;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk async copy (global -> shared), non-multicast.
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~2^31 SM cycles (about a second) and returns
+// false; callers then raise DS4MOE_DEVERR_TIMEOUT and leave.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > (1ll << 31)) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void raise_flag(uint32_t *err, uint32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+}  // namespace ds4

@@ -1,0 +1,94 @@
+// internal.h -- the layer handle and the kernel launchers shared by the
+// translation units of libds4moe.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds4moe.h"
+
+struct ds4moe_layer {
+  ds4moe_layer_desc d;
+  int device;
+  int E_pad;   // router rows padded to a multiple of 32
+  int NS;      // expert slots per token: top_k + n_shared
+  int A_max;   // most active experts in one call: min(E, max_tokens*k) + n_shared
+
+  // Weights in the library's layout (see common.cuh).
+  uint8_t *router;       // Q8 RG32 [E_pad/32][H/64][tile], or F32 [E][H]
+  float *bias;           // [E]
+  int32_t *hash;         // [vocab][k]
+  uint8_t *gu;           // routed gate+up [E][F/32][H/KSTEP][2][tile]
+  uint8_t *dn;           // routed down    [E][H/32][F/KSTEP][tile]
+  uint8_t *sgu, *sdn;    // shared, same layouts with E = 1
+
+  // Scratch for max_tokens tokens.
+  int8_t *xq;            // [T][H]
+  float *dx;             // [T][H/32]
+  int16_t *gs;           // [T][H/16]
+  float *rpart;          // [T][8][E_pad] router segment sums
+  int32_t *ids;          // [T][k]
+  float *wts;            // [T][k]
+  int32_t *bucket;       // cnt[E+1] | off[E+2] | active[E+2] | n_active[1] | list[T*NS]
+  int8_t *hq;            // [T*NS][F]
+  float *dh;             // [T*NS][F/32]
+  int16_t *gsh;          // [T*NS][F/16]
+  float *apart;          // [T*NS][H]
+  uint32_t *err;         // device error flags
+
+  // Staging for ds4moe_forward_host.
+  float *x_dev, *y_dev;
+  int32_t *tok_dev;
+
+  // Profiling (ds4moe_profile_*) and launch counting.
+  int prof_on;
+  cudaEvent_t ev[8];
+  int ev_made;
+  double prof_ms[8];
+  int64_t prof_calls;
+  uint64_t launches;
+
+  uint64_t bytes;        // total device bytes owned
+  void *allocs[32];
+  int n_allocs;
+};
+
+namespace ds4 {
+
+struct Bucket {
+  int32_t *cnt, *off, *active, *n_active, *list;
+};
+
+inline Bucket bucket_view(const ds4moe_layer *h) {
+  const int E = h->d.n_experts;
+  Bucket b;
+  b.cnt = h->bucket;
+  b.off = b.cnt + (E + 1);
+  b.active = b.off + (E + 2);
+  b.n_active = b.active + (E + 2);
+  b.list = b.n_active + 1;
+  return b;
+}
+
+inline size_t bucket_ints(int E, int T, int NS) { return (size_t)(E + 1) + (E + 2) + (E + 2) + 1 + (size_t)T * NS; }
+
+// repack.cu
+cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
+                       cudaStream_t s);
+cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int rows_pad, int K, int pair,
+                      int which, cudaStream_t s);
+cudaError_t check_hash_table(const int32_t *table, int64_t n, int E, int32_t *bad_count, cudaStream_t s);
+
+// route.cu
+cudaError_t launch_quantize(const float *x, int T, int H, int8_t *xq, float *dx, int16_t *gs, uint32_t *err,
+                            cudaStream_t s);
+cudaError_t launch_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
+                         float *w, cudaStream_t s);
+cudaError_t launch_bucket(const ds4moe_layer *h, int T, cudaStream_t s);
+cudaError_t launch_combine(const ds4moe_layer *h, int T, float *y, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float *x, float *out, int T, int H, float eps, cudaStream_t s);
+
+// gemv.cu
+cudaError_t launch_gateup(const ds4moe_layer *h, int T, cudaStream_t s);
+cudaError_t launch_down(const ds4moe_layer *h, int T, cudaStream_t s);
+
+}  // namespace ds4

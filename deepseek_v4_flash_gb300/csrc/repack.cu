@@ -1,0 +1,90 @@
+// repack.cu -- create-time conversion of the canonical weight bytes into the
+// library's RG32 layouts (see common.cuh). Runs once per layer handle.
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds4 {
+
+// One thread per canonical Q2S superblock (84 bytes) -> its lane's slices of
+// an RG32 tile. The 2-bit fields of each 16-weight group are transposed:
+// canonical element 4*s+j (byte s of the group, bits 2j) moves to byte j,
+// bits 2s of the group word, so (W >> 2s) & 0x03030303 gives 4 consecutive
+// elements in byte order.
+__global__ void k_repack_q2s(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
+                             int KS, int npair, int which) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t total = (int64_t)n_mat * rows * KS;
+  if (i >= total) return;
+  const int s = (int)(i % KS);
+  const int64_t mr = i / KS;
+  const int r = (int)(mr % rows), m = (int)(mr / rows);
+  const uint8_t *sb = src + i * 84;
+  const int rg = r >> 5, lane = r & 31;
+  uint8_t *tile = dst + ((((int64_t)m * (rows >> 5) + rg) * KS + s) * npair + which) * Q2S_TILE;
+  for (int j = 0; j < 16; j++) tile[16 * lane + j] = sb[j];
+  for (int j = 0; j < 4; j++) tile[Q2S_DD + 4 * lane + j] = sb[80 + j];
+  for (int g = 0; g < 16; g++) {
+    uint32_t W = 0;
+    for (int sbyte = 0; sbyte < 4; sbyte++) {
+      const uint32_t b = sb[16 + 4 * g + sbyte];
+      for (int j = 0; j < 4; j++) W |= ((b >> (2 * j)) & 3u) << (8 * j + 2 * sbyte);
+    }
+    uint8_t *o = tile + Q2S_QS + 512 * (g >> 2) + 16 * lane + 4 * (g & 3);
+    o[0] = (uint8_t)W, o[1] = (uint8_t)(W >> 8), o[2] = (uint8_t)(W >> 16), o[3] = (uint8_t)(W >> 24);
+  }
+}
+
+// One thread per pair of canonical Q8_0 blocks (2 x 34 bytes).
+__global__ void k_repack_q8(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
+                            int rows_pad, int KS, int npair, int which) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t total = (int64_t)n_mat * rows * KS;
+  if (i >= total) return;
+  const int c = (int)(i % KS);
+  const int64_t mr = i / KS;
+  const int r = (int)(mr % rows), m = (int)(mr / rows);
+  const uint8_t *b0 = src + ((int64_t)m * rows + r) * ((int64_t)KS * 68) + (int64_t)c * 68;
+  const uint8_t *b1 = b0 + 34;
+  const int rg = r >> 5, lane = r & 31;
+  uint8_t *tile = dst + ((((int64_t)m * (rows_pad >> 5) + rg) * KS + c) * npair + which) * Q8_TILE;
+  tile[4 * lane + 0] = b0[0], tile[4 * lane + 1] = b0[1];
+  tile[4 * lane + 2] = b1[0], tile[4 * lane + 3] = b1[1];
+  for (int p = 0; p < 4; p++) {
+    const uint8_t *q = (p < 2 ? b0 : b1) + 2 + 16 * (p & 1);
+    uint8_t *o = tile + Q8_Q + 512 * p + 16 * lane;
+    for (int j = 0; j < 16; j++) o[j] = q[j];
+  }
+}
+
+__global__ void k_check_table(const int32_t *__restrict__ t, int64_t n, int E, int32_t *bad) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n && (t[i] < 0 || t[i] >= E)) atomicAdd(bad, 1);
+}
+
+static unsigned blocks_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
+
+cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
+                       cudaStream_t s) {
+  const int KS = K / Q2S_KSTEP;
+  const int64_t n = (int64_t)n_mat * rows * KS;
+  if (n == 0) return cudaSuccess;
+  k_repack_q2s<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair ? 2 : 1, which);
+  return cudaGetLastError();
+}
+
+cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int rows_pad, int K, int pair,
+                      int which, cudaStream_t s) {
+  const int KS = K / Q8_KSTEP;
+  const int64_t n = (int64_t)n_mat * rows * KS;
+  if (n == 0) return cudaSuccess;
+  k_repack_q8<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, rows_pad, KS, pair ? 2 : 1, which);
+  return cudaGetLastError();
+}
+
+cudaError_t check_hash_table(const int32_t *table, int64_t n, int E, int32_t *bad_count, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  k_check_table<<<blocks_for(n, 256), 256, 0, s>>>(table, n, E, bad_count);
+  return cudaGetLastError();
+}
+
+}  // namespace ds4

@@ -1,0 +1,204 @@
+/*
+ * ds4moe.h -- C ABI of libds4moe: the routed mixture-of-experts FFN of one
+ * DeepSeek-V4-Flash-shaped layer on one GB300 GPU (sm_103a).
+ *
+ * What the layer computes (by page title and section):
+ *   - "DeepSeek V4 Flash -- DFlash Integration", Model Architecture: hidden
+ *     4096; 256 routed experts, top-6, plus 1 shared; expert FFN 2048; the
+ *     first 3 layers route by a token-ID -> expert table, the others by
+ *     "top-k over learned router + optional bias"; Execution Modes
+ *     (--ds4-expert-top-k): the kept experts' weights are renormalised.
+ *   - "Baekpica/ds4 dfm Edition" README, two-bank batching notes: the router
+ *     returns selected expert IDs and normalized weights; the expert path is
+ *     gate/up, weighted SwiGLU, expert down, plus the shared expert.
+ *   - DwarfStar README, Model Weights: routed experts 2-bit, shared experts
+ *     and router kept at higher precision (Q8_0, "SExpQ8").
+ *   - ds4-rocm fork README, __launch_bounds__ list: activations are
+ *     pre-quantised to int8 for the Q8_0 matmuls ("_preq" kernels).
+ *
+ * Every float operation follows one fixed binary32 order (the canonical
+ * arithmetic spec): the library's results are bit-identical to a scalar
+ * CPU evaluation of the same spec, for every token count and every code path.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are CUDA device pointers unless the name says host.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Argument and shape errors are detected on the host before anything is
+ *     enqueued; the call then returns an error status and changes nothing.
+ *   - ds4moe_route / ds4moe_forward enqueue work only: no allocation, no
+ *     host synchronisation, so they may be captured in a CUDA graph.
+ *   - Data errors found on the device (a hash token id outside [0, vocab),
+ *     a non-finite activation) never trap: the device sets a flag that
+ *     ds4moe_get_device_error reports; an out-of-range token contributes
+ *     nothing to y.
+ *   - One handle must not be used on two streams at once; distinct handles
+ *     are independent.
+ */
+#ifndef DS4MOE_H
+#define DS4MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS4MOE_ABI_VERSION 1
+
+typedef enum {
+  DS4MOE_OK = 0,
+  DS4MOE_ERR_INVALID_ARG = 1, /* bad pointer, shape, format or token count */
+  DS4MOE_ERR_UNSUPPORTED = 2, /* valid request this build does not handle  */
+  DS4MOE_ERR_OOM = 3,         /* device allocation failed                  */
+  DS4MOE_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed      */
+  DS4MOE_ERR_DEVICE = 5       /* the device error flag was set             */
+} ds4moe_status;
+
+/* Weight formats (canonical byte layouts; all little endian).
+ *   DS4MOE_F32  : row-major binary32 (router only).
+ *   DS4MOE_Q8_0 : blocks of 32 weights, 34 bytes: fp16 d, int8 q[32];
+ *                 w_i = d * q_i.
+ *   DS4MOE_Q2S  : superblocks of 256 weights, 84 bytes:
+ *                 uint8 sm[16] | uint8 qs[64] | fp16 d | fp16 dmin;
+ *                 group g = i/16, sc = sm[g] & 15, mn = sm[g] >> 4,
+ *                 q_i = (qs[i/4] >> 2*(i%4)) & 3,
+ *                 w_i = d*sc*q_i - dmin*mn   (2.625 bits per weight).
+ * A matrix [R][K] is R rows of K/32 (Q8_0) or K/256 (Q2S) blocks, rows
+ * contiguous; expert tensors stack their E matrices contiguously. */
+typedef enum { DS4MOE_F32 = 0, DS4MOE_Q8_0 = 1, DS4MOE_Q2S = 2 } ds4moe_fmt;
+
+typedef enum { DS4MOE_ROUTE_LEARNED = 0, DS4MOE_ROUTE_HASH = 1 } ds4moe_route_kind;
+
+/* Device error flag bits (ds4moe_get_device_error). */
+#define DS4MOE_DEVERR_TOKEN_ID 1u   /* hash token id outside [0, vocab)     */
+#define DS4MOE_DEVERR_NONFINITE 2u  /* non-finite activation quantised      */
+#define DS4MOE_DEVERR_TIMEOUT 4u    /* a bounded on-chip wait gave up       */
+#define DS4MOE_DEVERR_INTERNAL 8u   /* an internal consistency check failed */
+
+typedef struct {
+  uint32_t abi_version; /* = DS4MOE_ABI_VERSION */
+  int32_t hidden;       /* H: multiple of 256 (4096 for DeepSeek-V4-Flash)          */
+  int32_t n_experts;    /* E routed experts, 1..1024 (256)                          */
+  int32_t top_k;        /* k, 1..min(E, 16) (6)                                     */
+  int32_t ffn;          /* F: multiple of 64; of 256 when routed/shared use Q2S (2048) */
+  int32_t n_shared;     /* 0 or 1 shared expert, always added with weight 1         */
+  int32_t route;        /* ds4moe_route_kind                                        */
+  int32_t vocab;        /* hash routing: table rows (129280); ignored otherwise     */
+  int32_t router_fmt;   /* DS4MOE_F32 or DS4MOE_Q8_0 (learned routing)              */
+  int32_t routed_fmt;   /* DS4MOE_Q8_0 or DS4MOE_Q2S                                */
+  int32_t shared_fmt;   /* DS4MOE_Q8_0 or DS4MOE_Q2S                                */
+  float route_scale;    /* multiplies the renormalised routed weights (1.0)         */
+  int32_t max_tokens;   /* largest n_tok of any later call, 1..1048576              */
+} ds4moe_layer_desc;
+
+/* Canonical weight buffers, DEVICE memory, read only during ds4moe_create
+ * (the library keeps its own re-laid-out copy; the caller may free these
+ * when create returns). Unused pointers may be NULL. */
+typedef struct {
+  const void *router_w;       /* [E][H] router_fmt                (learned)   */
+  const float *router_bias;   /* [E] selection bias               (learned)   */
+  const int32_t *hash_table;  /* [vocab][k] expert ids in [0, E)  (hash)      */
+  const void *gate, *up;      /* [E][F][H] routed_fmt                         */
+  const void *down;           /* [E][H][F] routed_fmt                         */
+  const void *sh_gate, *sh_up;/* [F][H] shared_fmt                (n_shared)  */
+  const void *sh_down;        /* [H][F] shared_fmt                (n_shared)  */
+} ds4moe_weights;
+
+typedef struct ds4moe_layer ds4moe_layer; /* opaque handle */
+
+/* Validate `desc`, allocate the handle's device memory on the current device
+ * (weights in the library's layout plus scratch for desc->max_tokens tokens),
+ * re-lay out the weights, and synchronise. On success *out owns all of it;
+ * on error *out is NULL and nothing stays allocated.
+ * Errors: INVALID_ARG (desc, missing or non-device pointer), OOM, CUDA. */
+ds4moe_status ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w,
+                            ds4moe_layer **out);
+
+/* Release everything the handle owns (synchronises the device). NULL is a no-op. */
+void ds4moe_destroy(ds4moe_layer *h);
+
+/* Routing only (steps: int8 quantisation of x, router GEMV, sigmoid,
+ * bias-for-selection top-k, renormalisation; or the hash-table lookup).
+ *   x        [n_tok][H] fp32 (learned routing; may be NULL for hash)
+ *   token_ids[n_tok] int32 (hash routing; may be NULL for learned)
+ *   ids_out  [n_tok][k] int32: expert ids in descending key order
+ *            (hash: table order); -1 for an out-of-range token id
+ *   w_out    [n_tok][k] fp32: renormalised weights * route_scale (0 for -1)
+ * n_tok in 0..max_tokens. Enqueued on `stream`. */
+ds4moe_status ds4moe_route(ds4moe_layer *h, const float *x, const int32_t *token_ids, int32_t n_tok,
+                           int32_t *ids_out, float *w_out, void *stream);
+
+/* The whole layer: y[t] += MoE(x[t]) for t < n_tok, i.e.
+ *   y[t] += sum_j w_j * down_j(hq_j) + shared(x[t])
+ * with hq_j the int8-requantised silu(gate_j x) * (up_j x).
+ *   x         [n_tok][H] fp32, read only
+ *   token_ids [n_tok] int32, required for hash routing, else may be NULL
+ *   y         [n_tok][H] fp32, read and written (must not alias x)
+ * n_tok in 0..max_tokens. Enqueued on `stream`; no host synchronisation. */
+ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids,
+                             float *y, void *stream);
+
+/* ds4moe_forward on HOST buffers: copies x, token_ids and y to the device,
+ * runs the layer, copies y back and synchronises `stream`. Pinned host
+ * memory gives the fastest copies. Same arguments otherwise. */
+ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t n_tok,
+                                  const int32_t *token_ids_host, float *y_host, void *stream);
+
+/* RMSNorm with unit gain between stacked layers:
+ *   out[t] = x[t] / sqrt(mean(x[t]^2) + eps)   (x, out [n_tok][hidden] fp32;
+ * out may equal x). hidden must be a multiple of 32. (DFlash Integration page,
+ * Forward Pass, step 5: RMSNorm before the output projection.) */
+ds4moe_status ds4moe_rmsnorm(const float *x, float *out, int32_t n_tok, int32_t hidden, float eps,
+                             void *stream);
+
+/* Synchronise `stream`, read and clear the handle's device error flag.
+ * *flags_out (may be NULL) receives the DS4MOE_DEVERR_* bits.
+ * Returns DS4MOE_ERR_DEVICE when any bit was set, else DS4MOE_OK. */
+ds4moe_status ds4moe_get_device_error(ds4moe_layer *h, void *stream, uint32_t *flags_out);
+
+/* Read-only device view of the handle's scratch after the last route/forward
+ * call, for inspecting intermediate results. `which`:
+ *   0 xq  int8  [max_tokens][H]        activation codes (CAS step 1)
+ *   1 dx  fp32  [max_tokens][H/32]     activation scales
+ *   2 gs  int16 [max_tokens][H/16]     16-group sums of xq
+ *   3 ids int32 [max_tokens][k]        routed expert ids (forward only)
+ *   4 w   fp32  [max_tokens][k]        renormalised weights (forward only)
+ *   5 hq  int8  [max_tokens*NS][F]     SwiGLU codes, row t*NS+slot (slot k = shared)
+ *   6 dh  fp32  [max_tokens*NS][F/32]  SwiGLU scales
+ *   7 a   fp32  [max_tokens*NS][H]     per-slot down-projection outputs
+ * with NS = k + n_shared. Only rows of tokens of the last call are defined.
+ * Errors: INVALID_ARG for an unknown `which`. */
+ds4moe_status ds4moe_debug_scratch(ds4moe_layer *h, int32_t which, const void **ptr_out, uint64_t *bytes_out);
+
+/* Per-stage timing with CUDA events recorded on the call's stream.
+ * ds4moe_profile_enable(h, 1) makes every later ds4moe_forward record an
+ * event before each stage and after the last one; ds4moe_profile_collect
+ * waits for the last forward's events and adds the stage durations to the
+ * handle's totals; ds4moe_profile_read copies the totals (milliseconds,
+ * summed over collected calls) for the stages
+ *   0 quantise x, 1 route (router GEMV + top-k, or hash), 2 bucket,
+ *   3 gate/up, 4 down, 5 combine
+ * into ms_out[0..n) and the number of collected calls into *calls.
+ * ds4moe_profile_enable(h, 0) stops recording and zeroes the totals.
+ * Profiling adds event records to the stream; it is off by default. */
+#define DS4MOE_N_STAGES 6
+ds4moe_status ds4moe_profile_enable(ds4moe_layer *h, int32_t on);
+ds4moe_status ds4moe_profile_collect(ds4moe_layer *h);
+ds4moe_status ds4moe_profile_read(const ds4moe_layer *h, double *ms_out, int32_t n, int64_t *calls);
+
+/* Number of kernels this handle has launched since create. */
+uint64_t ds4moe_launch_count(const ds4moe_layer *h);
+
+/* Bytes of device memory the handle owns (weights + scratch). */
+uint64_t ds4moe_device_bytes(const ds4moe_layer *h);
+
+/* Human-readable status name (static storage). */
+const char *ds4moe_status_string(ds4moe_status s);
+
+/* = DS4MOE_ABI_VERSION of the loaded library. */
+uint32_t ds4moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DS4MOE_H */

@@ -1,0 +1,230 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.
+
+Bar: expert ids and every integer code bit-exact; floats within the routed-MoE
+tolerance (relative L2 <= 1e-4 and max-abs <= 2e-3 * max|ref|) -- and, because
+both sides follow the same binary32 operation order, bit-exact as well."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import make_layer, margin_inputs, within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ora():
+    return oracle.get()
+
+
+_layers = {}
+
+
+def _layer_pair(ora, spec, seed, max_tokens):
+    key = (spec.name, seed, max_tokens)
+    if key not in _layers:
+        _layers.clear()
+        import torch
+        torch.cuda.empty_cache()
+        w = synth.gen_layer(spec, seed, 0)
+        _layers[key] = (w, ora.layer(spec, w), make_layer(spec, w, max_tokens))
+    return _layers[key]
+
+
+def run_case(ora, spec, seed, T, max_tokens=None, y_init=True):
+    import torch
+    w, ol, layer = _layer_pair(ora, spec, seed, max_tokens or T)
+    x = margin_inputs(ol, spec, seed, T)
+    tok = synth.gen_token_ids(spec, seed, T) if spec.route == "hash" else None
+    y0 = (np.random.default_rng(seed + T).standard_normal(x.shape) * 10).astype(np.float32) if y_init \
+        else np.zeros_like(x)
+    ref, ids_ref, w_ref, bad = ol.forward(x, y0, tok)
+    assert bad == 0
+    xd, yd = torch.from_numpy(x).cuda(), torch.from_numpy(y0).cuda()
+    td = torch.from_numpy(tok).cuda() if tok is not None else None
+    layer.forward(xd, yd, td)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    got = yd.cpu().numpy()
+    k = spec.top_k
+    ids = layer.scratch("ids")[:T * k].view(T, k).cpu().numpy()
+    wts = layer.scratch("w")[:T * k].view(T, k).cpu().numpy()
+    assert np.array_equal(ids, ids_ref), "expert ids differ"
+    assert np.array_equal(wts.view(np.uint32), w_ref.view(np.uint32)), "gate weights differ"
+    assert within_tolerance(got, ref)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), \
+        f"not bit-exact: {np.count_nonzero(got != ref)} of {got.size} differ"
+    return x, tok, got, layer
+
+
+def test_tiny_layer_4_tokens(ora):
+    run_case(ora, synth.TINY, 2026, 4)
+
+
+@pytest.mark.parametrize("T", list(range(1, 17)) + [31, 32, 33, 63, 64, 65])
+def test_micro_widths(ora, T):
+    run_case(ora, synth.MICRO, 7, T, max_tokens=65)
+
+
+@pytest.mark.parametrize("T", [1, 7, 64, 130])
+def test_micro_hash(ora, T):
+    run_case(ora, synth.MICRO_HASH, 9, T, max_tokens=130)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_ds4_decode_1_token(ora, seed):
+    run_case(ora, synth.DS4, seed, 1)
+
+
+def test_ds4_batched_decode_32_zipf(ora):
+    run_case(ora, synth.DS4_ZIPF, 11, 32)
+
+
+def test_ds4_hash_prefill_512(ora):
+    run_case(ora, synth.DS4_HASH, 13, 512)
+
+
+def test_intermediate_codes_bit_exact(ora):
+    """Activation codes, scales and group sums, and the SwiGLU codes of one
+    expert slot, against the oracle's own quantiser and expert evaluation."""
+    spec, T = synth.MICRO, 5
+    x, tok, got, layer = run_case(ora, spec, 17, T, max_tokens=65)
+    H, F, k = spec.hidden, spec.ffn, spec.top_k
+    _, ol, _ = _layer_pair(ora, spec, 17, 65)
+    xq = layer.scratch("xq")[:T * H].view(T, H).cpu().numpy()
+    dx = layer.scratch("dx")[:T * H // 32].view(T, H // 32).cpu().numpy()
+    gs = layer.scratch("gs")[:T * H // 16].view(T, H // 16).cpu().numpy()
+    ids = layer.scratch("ids")[:T * k].view(T, k).cpu().numpy()
+    hq = layer.scratch("hq").view(-1, F)
+    dh = layer.scratch("dh").view(-1, F // 32)
+    NS = k + spec.n_shared
+    for t in range(T):
+        q, d, g = ora.quantize(x[t])
+        assert np.array_equal(xq[t], q) and np.array_equal(dx[t].view(np.uint32), d.view(np.uint32))
+        assert np.array_equal(gs[t], g)
+        for j, e in list(enumerate(ids[t])) + [(k, spec.n_experts)]:
+            o = ol.expert(int(e), x[t])
+            assert np.array_equal(hq[t * NS + j].cpu().numpy(), o["hq"])
+            assert np.array_equal(dh[t * NS + j].cpu().numpy().view(np.uint32), o["dh"].view(np.uint32))
+
+
+def test_route_entry_point(ora):
+    import torch
+    spec, T = synth.DS4, 8
+    w, ol, layer = _layer_pair(ora, spec, 21, 8)
+    x = margin_inputs(ol, spec, 21, T)
+    ids_ref, w_ref, _, _, _ = ol.route(x)
+    ids, wt = layer.route(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.array_equal(wt.cpu().numpy().view(np.uint32), w_ref.view(np.uint32))
+
+
+def test_linearity_and_determinism(ora):
+    """forward(x, y0) == y0 + forward(x, 0) element by element (binary32), and
+    two runs give the same bits."""
+    import torch
+    spec, T = synth.MICRO, 9
+    w, ol, layer = _layer_pair(ora, spec, 23, 65)
+    x = torch.from_numpy(margin_inputs(ol, spec, 23, T)).cuda()
+    y0 = torch.randn(T, spec.hidden, device="cuda") * 50
+    y1 = y0.clone()
+    layer.forward(x, y1)
+    z = torch.zeros_like(y0)
+    layer.forward(x, z)
+    z2 = torch.zeros_like(y0)
+    layer.forward(x, z2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y0 + z)
+    assert torch.equal(z, z2)
+
+
+def test_batch_invariance(ora):
+    """A token's output does not depend on the other tokens of the call."""
+    import torch
+    spec, T = synth.MICRO, 12
+    w, ol, layer = _layer_pair(ora, spec, 29, 65)
+    x = torch.from_numpy(margin_inputs(ol, spec, 29, T)).cuda()
+    yb = torch.zeros(T, spec.hidden, device="cuda")
+    layer.forward(x, yb)
+    for t in range(T):
+        y1 = torch.zeros(1, spec.hidden, device="cuda")
+        layer.forward(x[t:t + 1].contiguous(), y1)
+        torch.cuda.synchronize()
+        assert torch.equal(y1[0], yb[t])
+
+
+def test_forward_host_matches_device(ora):
+    import torch
+    spec, T = synth.MICRO_HASH, 10
+    w, ol, layer = _layer_pair(ora, spec, 31, 130)
+    x = synth.gen_x(spec, 31, T)
+    tok = synth.gen_token_ids(spec, 31, T)
+    ref, *_ = ol.forward(x, None, tok)
+    xh = torch.from_numpy(x).pin_memory()
+    yh = torch.zeros(T, spec.hidden).pin_memory()
+    th = torch.from_numpy(tok).pin_memory()
+    layer.forward_host(xh, yh, th)
+    assert np.array_equal(yh.numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_bad_token_id_sets_flag_and_skips_token(ora):
+    import torch
+    spec, T = synth.MICRO_HASH, 6
+    w, ol, layer = _layer_pair(ora, spec, 33, 130)
+    x = synth.gen_x(spec, 33, T)
+    tok = synth.gen_token_ids(spec, 33, T)
+    tok[2] = spec.vocab + 5
+    tok[4] = -3
+    ref, ids_ref, _, bad = ol.forward(x, None, tok)
+    assert bad == 2
+    yd = torch.zeros(T, spec.hidden, device="cuda")
+    layer.forward(torch.from_numpy(x).cuda(), yd, torch.from_numpy(tok).cuda())
+    flags = layer.device_error()
+    assert flags & 1
+    got = yd.cpu().numpy()
+    assert np.all(got[2] == 0) and np.all(got[4] == 0)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    assert layer.device_error() == 0  # cleared
+
+
+def test_nonfinite_input_sets_flag(ora):
+    import torch
+    spec = synth.MICRO
+    w, ol, layer = _layer_pair(ora, spec, 35, 65)
+    x = torch.randn(3, spec.hidden, device="cuda")
+    x[1, 7] = float("inf")
+    y = torch.zeros_like(x)
+    layer.forward(x, y)
+    assert layer.device_error() & 2
+
+
+def test_rmsnorm_bit_exact(ora):
+    import torch
+    import deepseek_v4_flash_gb300 as ds4
+    rng = np.random.default_rng(37)
+    x = (rng.standard_normal((33, 4096)) * rng.uniform(0.01, 100, (33, 1))).astype(np.float32)
+    ref = ora.rmsnorm(x, 1e-6)
+    xd = torch.from_numpy(x).cuda()
+    out = torch.empty_like(xd)
+    ds4.rmsnorm(xd, out, 1e-6)
+    ds4.rmsnorm(xd, xd, 1e-6)  # in place
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert torch.equal(out, xd)
+
+
+def test_empty_and_too_many_tokens(ora):
+    import torch
+    import deepseek_v4_flash_gb300 as ds4
+    spec = synth.MICRO
+    w, ol, layer = _layer_pair(ora, spec, 39, 65)
+    x = torch.zeros(66, spec.hidden, device="cuda")
+    y = torch.zeros_like(x)
+    layer.forward(x, y, n_tok=0)
+    with pytest.raises(ds4.Ds4MoeError):
+        layer.forward(x, y, n_tok=66)
+    with pytest.raises(ds4.Ds4MoeError):
+        layer.forward(x, x, n_tok=3)  # y must not alias x
