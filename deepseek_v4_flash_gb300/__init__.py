@@ -128,7 +128,7 @@ class _CudaArray:
     """A device buffer described by __cuda_array_interface__ (for torch.as_tensor)."""
 
     def __init__(self, ptr, shape, typestr):
-        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, True),
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
                                          "version": 3, "strides": None}
 
 
@@ -221,7 +221,7 @@ class Layer:
                 "hq": (5, "|i1"), "dh": (6, "<f4"), "a": (7, "<f4")}
 
     def scratch(self, name: str):
-        """Read-only torch view of an intermediate buffer (ds4moe_debug_scratch), flat."""
+        """Torch view (treat as read-only) of an intermediate buffer (ds4moe_debug_scratch), flat."""
         import torch
         which, typestr = self._SCRATCH[name]
         p, n = ctypes.c_void_p(), ctypes.c_uint64()

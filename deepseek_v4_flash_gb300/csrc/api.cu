@@ -145,6 +145,16 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
     if ((st = cuda_status(repack(sf, w->sh_gate, h->sgu, 1, F, F, H, 1, 0, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(repack(sf, w->sh_up, h->sgu, 1, F, F, H, 1, 1, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(repack(sf, w->sh_down, h->sdn, 1, H, H, F, 0, 0, s))) != DS4MOE_OK) return st;
+    if (sf == DS4MOE_Q8_0) {  // 8-row x 4-lane layout for the decode path
+      if ((st = alloc(h, &h->sgu8, 2 * (size_t)F * (H / 32) * 34)) != DS4MOE_OK) return st;
+      if ((st = alloc(h, &h->sdn8, (size_t)H * (F / 32) * 34)) != DS4MOE_OK) return st;
+      if ((st = cuda_status(repack_q8x4((const uint8_t *)w->sh_gate, h->sgu8, 1, F, H, 1, 0, s))) != DS4MOE_OK)
+        return st;
+      if ((st = cuda_status(repack_q8x4((const uint8_t *)w->sh_up, h->sgu8, 1, F, H, 1, 1, s))) != DS4MOE_OK)
+        return st;
+      if ((st = cuda_status(repack_q8x4((const uint8_t *)w->sh_down, h->sdn8, 1, H, F, 0, 0, s))) != DS4MOE_OK)
+        return st;
+    }
   }
 
   // ---- scratch
@@ -162,6 +172,20 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   if ((st = alloc(h, &h->apart, (size_t)(T * NS) * H * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->err, 64)) != DS4MOE_OK) return st;
   if ((st = cuda_status(cudaMemsetAsync(h->err, 0, 64, s))) != DS4MOE_OK) return st;
+  {  // decode path: tickets and queues start at zero and reset themselves
+    const long long Td = T < DEC_MAX_T ? T : DEC_MAX_T;
+    const size_t n_hb = (size_t)(Td * NS) * F * 4, n_ht = (size_t)(Td * NS) * (F / 32) * 4;
+    const size_t n_ct = (size_t)Td * (H / 32) * 4, n_tick = 64 * 4, n_q = 16 * 4;
+    if ((st = alloc(h, &h->hbuf, n_hb)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->hticket, n_ht)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->cticket, n_ct)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->tick, n_tick)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->queue, n_q)) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->hticket, 0, n_ht, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->cticket, 0, n_ct, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->tick, 0, n_tick, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->queue, 0, n_q, s))) != DS4MOE_OK) return st;
+  }
 
   if (d.route == DS4MOE_ROUTE_HASH) {
     // every table entry must name a routed expert
@@ -209,10 +233,20 @@ ds4moe_status ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights 
     return DS4MOE_ERR_CUDA;
   }
   h->E_pad = (desc->n_experts + 31) / 32 * 32;
+  if (cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return DS4MOE_ERR_CUDA;
+  }
   h->NS = desc->top_k + desc->n_shared;
   {
     const long long routed = (long long)desc->max_tokens * desc->top_k;
     h->A_max = (int)(routed < desc->n_experts ? routed : desc->n_experts) + desc->n_shared;
+  }
+  h->dec_ok = route_dec_smem(h) <= DEC_SMEM_LIMIT;
+  if (h->dec_ok && decode_set_attributes() != cudaSuccess) {
+    cudaGetLastError();
+    h->dec_ok = 0;
   }
   st = build(h, w);
   if (st != DS4MOE_OK) {
@@ -273,6 +307,21 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
   auto mark = [&](int i) {
     if (prof) cudaEventRecord(h->ev[i], s);
   };
+  if (h->dec_ok && n_tok <= DEC_MAX_T) {
+    // decode path: fused routing, then the two persistent expert kernels
+    mark(0);
+    mark(1);
+    cudaError_t e = launch_dec_route(h, x, token_ids, n_tok, s);
+    mark(2);
+    mark(3);
+    if (e == cudaSuccess) e = launch_dec_expert(h, n_tok, y, 0, s);
+    mark(4);
+    if (e == cudaSuccess) e = launch_dec_expert(h, n_tok, y, 1, s);
+    mark(5);
+    mark(6);
+    h->launches += 3;
+    return cuda_status(e);
+  }
   mark(0);
   cudaError_t e = launch_quantize(x, n_tok, H, h->xq, h->dx, h->gs, h->err, s);
   mark(1);

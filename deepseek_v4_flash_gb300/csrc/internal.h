@@ -12,6 +12,8 @@ struct ds4moe_layer {
   int E_pad;   // router rows padded to a multiple of 32
   int NS;      // expert slots per token: top_k + n_shared
   int A_max;   // most active experts in one call: min(E, max_tokens*k) + n_shared
+  int n_sm;    // streaming multiprocessors of the device
+  int dec_ok;  // the decode path fits this layer (shared memory)
 
   // Weights in the library's layout (see common.cuh).
   uint8_t *router;       // Q8 RG32 [E_pad/32][H/64][tile], or F32 [E][H]
@@ -20,6 +22,7 @@ struct ds4moe_layer {
   uint8_t *gu;           // routed gate+up [E][F/32][H/KSTEP][2][tile]
   uint8_t *dn;           // routed down    [E][H/32][F/KSTEP][tile]
   uint8_t *sgu, *sdn;    // shared, same layouts with E = 1
+  uint8_t *sgu8, *sdn8;  // shared Q8 in the RG8x4 layout (decode path)
 
   // Scratch for max_tokens tokens.
   int8_t *xq;            // [T][H]
@@ -34,6 +37,11 @@ struct ds4moe_layer {
   int16_t *gsh;          // [T*NS][F/16]
   float *apart;          // [T*NS][H]
   uint32_t *err;         // device error flags
+  float *hbuf;           // [T*NS][F] h before requant (decode, 8-row items)
+  int32_t *hticket;      // [T*NS][F/32] requant tickets (self-resetting)
+  int32_t *cticket;      // [T][H/32] combine tickets (self-resetting)
+  int32_t *tick;         // routing tickets (self-resetting)
+  int32_t *queue;        // work queues of the persistent kernels (self-resetting)
 
   // Staging for ds4moe_forward_host.
   float *x_dev, *y_dev;
@@ -76,6 +84,8 @@ cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, in
                        cudaStream_t s);
 cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int rows_pad, int K, int pair,
                       int which, cudaStream_t s);
+cudaError_t repack_q8x4(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
+                        cudaStream_t s);
 cudaError_t check_hash_table(const int32_t *table, int64_t n, int E, int32_t *bad_count, cudaStream_t s);
 
 // route.cu
@@ -86,6 +96,14 @@ cudaError_t launch_route(const ds4moe_layer *h, const float *x, const int32_t *t
 cudaError_t launch_bucket(const ds4moe_layer *h, int T, cudaStream_t s);
 cudaError_t launch_combine(const ds4moe_layer *h, int T, float *y, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float *x, float *out, int T, int H, float eps, cudaStream_t s);
+
+// decode.cu
+constexpr int DEC_MAX_T = 64;  // largest n_tok served by the decode path
+size_t route_dec_smem(const ds4moe_layer *h);
+cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, cudaStream_t s);
+cudaError_t launch_dec_expert(const ds4moe_layer *h, int T, float *y, int down, cudaStream_t s);
+cudaError_t decode_set_attributes();
+constexpr size_t DEC_SMEM_LIMIT = 227 * 1024;
 
 // gemv.cu
 cudaError_t launch_gateup(const ds4moe_layer *h, int T, cudaStream_t s);
