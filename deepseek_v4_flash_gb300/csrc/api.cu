@@ -42,7 +42,9 @@ ds4moe_status validate_desc(const ds4moe_layer_desc *d) {
   if (!fmt_ok(d->routed_fmt)) return DS4MOE_ERR_INVALID_ARG;
   if (d->n_shared && !fmt_ok(d->shared_fmt)) return DS4MOE_ERR_INVALID_ARG;
   if (!k_ok(d->routed_fmt, d->hidden) || !k_ok(d->routed_fmt, d->ffn)) return DS4MOE_ERR_INVALID_ARG;
-  if (d->n_shared && (!k_ok(d->shared_fmt, d->hidden) || !k_ok(d->shared_fmt, d->ffn)))
+  // the shared expert's rows are summed in SHARED_SEGS segments of whole K-steps
+  if (d->n_shared && (!k_ok(d->shared_fmt, d->hidden / SHARED_SEGS) || !k_ok(d->shared_fmt, d->ffn / SHARED_SEGS) ||
+                      d->hidden % SHARED_SEGS || d->ffn % SHARED_SEGS))
     return DS4MOE_ERR_INVALID_ARG;
   if (d->route == DS4MOE_ROUTE_LEARNED) {
     if (d->router_fmt != DS4MOE_F32 && d->router_fmt != DS4MOE_Q8_0) return DS4MOE_ERR_INVALID_ARG;
@@ -86,11 +88,11 @@ ds4moe_status cuda_status(cudaError_t e) {
   return e == cudaErrorMemoryAllocation ? DS4MOE_ERR_OOM : DS4MOE_ERR_CUDA;
 }
 
-// Re-lay out a [n_mat][rows][K] tensor into the RG32 layout.
-cudaError_t repack(int fmt, const void *src, uint8_t *dst, int n_mat, int rows, int rows_pad, int K, int pair,
-                   int which, cudaStream_t s) {
+// Re-lay out a [n_mat][rows][K] expert tensor into the RG32 layout.
+cudaError_t repack(int fmt, const void *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
+                   cudaStream_t s) {
   if (fmt == DS4MOE_Q2S) return repack_q2s((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
-  return repack_q8((const uint8_t *)src, dst, n_mat, rows, rows_pad, K, pair, which, s);
+  return repack_q8((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
 }
 
 size_t rg32_bytes(int fmt, long long n_mat, long long rows_pad, long long K) {
@@ -108,10 +110,10 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   if (d.route == DS4MOE_ROUTE_LEARNED) {
     if (!is_dev_ptr(w->router_w) || !is_dev_ptr(w->router_bias)) return DS4MOE_ERR_INVALID_ARG;
     if (d.router_fmt == DS4MOE_Q8_0) {
-      const size_t nb = rg32_bytes(DS4MOE_Q8_0, 1, h->E_pad, H);
+      const size_t nb = (size_t)(h->E_pad / 32) * (H / RQ8_KSTEP) * RQ8_TILE;
       if ((st = alloc(h, &h->router, nb)) != DS4MOE_OK) return st;
       if ((st = cuda_status(cudaMemsetAsync(h->router, 0, nb, s))) != DS4MOE_OK) return st;
-      if ((st = cuda_status(repack(DS4MOE_Q8_0, w->router_w, h->router, 1, E, h->E_pad, H, 0, 0, s))) != DS4MOE_OK)
+      if ((st = cuda_status(repack_rq8((const uint8_t *)w->router_w, h->router, E, h->E_pad, H, s))) != DS4MOE_OK)
         return st;
     } else {
       const size_t nb = (size_t)E * H * 4;
@@ -134,27 +136,17 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   const int rf = d.routed_fmt;
   if ((st = alloc(h, &h->gu, 2 * rg32_bytes(rf, E, F, H))) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->dn, rg32_bytes(rf, E, H, F))) != DS4MOE_OK) return st;
-  if ((st = cuda_status(repack(rf, w->gate, h->gu, E, F, F, H, 1, 0, s))) != DS4MOE_OK) return st;
-  if ((st = cuda_status(repack(rf, w->up, h->gu, E, F, F, H, 1, 1, s))) != DS4MOE_OK) return st;
-  if ((st = cuda_status(repack(rf, w->down, h->dn, E, H, H, F, 0, 0, s))) != DS4MOE_OK) return st;
+  if ((st = cuda_status(repack(rf, w->gate, h->gu, E, F, H, 1, 0, s))) != DS4MOE_OK) return st;
+  if ((st = cuda_status(repack(rf, w->up, h->gu, E, F, H, 1, 1, s))) != DS4MOE_OK) return st;
+  if ((st = cuda_status(repack(rf, w->down, h->dn, E, H, F, 0, 0, s))) != DS4MOE_OK) return st;
   if (d.n_shared) {
     if (!is_dev_ptr(w->sh_gate) || !is_dev_ptr(w->sh_up) || !is_dev_ptr(w->sh_down)) return DS4MOE_ERR_INVALID_ARG;
     const int sf = d.shared_fmt;
     if ((st = alloc(h, &h->sgu, 2 * rg32_bytes(sf, 1, F, H))) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->sdn, rg32_bytes(sf, 1, H, F))) != DS4MOE_OK) return st;
-    if ((st = cuda_status(repack(sf, w->sh_gate, h->sgu, 1, F, F, H, 1, 0, s))) != DS4MOE_OK) return st;
-    if ((st = cuda_status(repack(sf, w->sh_up, h->sgu, 1, F, F, H, 1, 1, s))) != DS4MOE_OK) return st;
-    if ((st = cuda_status(repack(sf, w->sh_down, h->sdn, 1, H, H, F, 0, 0, s))) != DS4MOE_OK) return st;
-    if (sf == DS4MOE_Q8_0) {  // 8-row x 4-lane layout for the decode path
-      if ((st = alloc(h, &h->sgu8, 2 * (size_t)F * (H / 32) * 34)) != DS4MOE_OK) return st;
-      if ((st = alloc(h, &h->sdn8, (size_t)H * (F / 32) * 34)) != DS4MOE_OK) return st;
-      if ((st = cuda_status(repack_q8x4((const uint8_t *)w->sh_gate, h->sgu8, 1, F, H, 1, 0, s))) != DS4MOE_OK)
-        return st;
-      if ((st = cuda_status(repack_q8x4((const uint8_t *)w->sh_up, h->sgu8, 1, F, H, 1, 1, s))) != DS4MOE_OK)
-        return st;
-      if ((st = cuda_status(repack_q8x4((const uint8_t *)w->sh_down, h->sdn8, 1, H, F, 0, 0, s))) != DS4MOE_OK)
-        return st;
-    }
+    if ((st = cuda_status(repack(sf, w->sh_gate, h->sgu, 1, F, H, 1, 0, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(repack(sf, w->sh_up, h->sgu, 1, F, H, 1, 1, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(repack(sf, w->sh_down, h->sdn, 1, H, F, 0, 0, s))) != DS4MOE_OK) return st;
   }
 
   // ---- scratch
@@ -174,14 +166,18 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   if ((st = cuda_status(cudaMemsetAsync(h->err, 0, 64, s))) != DS4MOE_OK) return st;
   {  // decode path: tickets and queues start at zero and reset themselves
     const long long Td = T < DEC_MAX_T ? T : DEC_MAX_T;
-    const size_t n_hb = (size_t)(Td * NS) * F * 4, n_ht = (size_t)(Td * NS) * (F / 32) * 4;
+    const size_t n_sp = (size_t)Td * SHARED_SEGS * 2 * F * 4, n_spd = (size_t)Td * SHARED_SEGS * H * 4;
+    const size_t n_st = (size_t)Td * (F / 32) * 4, n_std = (size_t)Td * (H / 32) * 4;
     const size_t n_ct = (size_t)Td * (H / 32) * 4, n_tick = 64 * 4, n_q = 16 * 4;
-    if ((st = alloc(h, &h->hbuf, n_hb)) != DS4MOE_OK) return st;
-    if ((st = alloc(h, &h->hticket, n_ht)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->spart, n_sp)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->spart_dn, n_spd)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->sticket, n_st)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->sticket_dn, n_std)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->cticket, n_ct)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->tick, n_tick)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->queue, n_q)) != DS4MOE_OK) return st;
-    if ((st = cuda_status(cudaMemsetAsync(h->hticket, 0, n_ht, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->sticket, 0, n_st, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->sticket_dn, 0, n_std, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->cticket, 0, n_ct, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->tick, 0, n_tick, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->queue, 0, n_q, s))) != DS4MOE_OK) return st;
@@ -314,9 +310,9 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
     cudaError_t e = launch_dec_route(h, x, token_ids, n_tok, s);
     mark(2);
     mark(3);
-    if (e == cudaSuccess) e = launch_dec_expert(h, n_tok, y, 0, s);
+    if (e == cudaSuccess) e = launch_dec_expert(h, token_ids, n_tok, y, 0, s);
     mark(4);
-    if (e == cudaSuccess) e = launch_dec_expert(h, n_tok, y, 1, s);
+    if (e == cudaSuccess) e = launch_dec_expert(h, token_ids, n_tok, y, 1, s);
     mark(5);
     mark(6);
     h->launches += 3;

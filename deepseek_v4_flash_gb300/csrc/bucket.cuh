@@ -40,7 +40,8 @@ __device__ __forceinline__ int block_exscan(int v, int *sh, int *total) {
 // Shared-memory need of bucket_block, in ints.
 __host__ __device__ constexpr int bucket_smem_ints(int E) { return 2 * (E + 2) + 32; }
 
-// ids: [T][k] routed expert ids (-1 = none). Writes cnt[0..E] (cnt[E] = T if
+// ids: [T][k] routed expert ids (-1 = none), written before the call (shared
+// or global memory). Writes cnt[0..E] (cnt[E] = T if
 // a shared expert exists), off[0..E+1], active[], *n_active and list[].
 // Must be called by every thread of the block.
 __device__ void bucket_block(const int32_t *ids, int T, int E, int k, int NS, int n_shared, int32_t *sm,
@@ -52,7 +53,7 @@ __device__ void bucket_block(const int32_t *ids, int T, int E, int k, int NS, in
   __syncthreads();
   const int n = T * k;
   for (int i = tid; i < n; i += nth) {
-    const int e = __ldcg(ids + i);
+    const int e = ids[i];
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
     else if (e >= E) raise_flag(err, DS4MOE_DEVERR_INTERNAL);
   }
@@ -83,7 +84,7 @@ __device__ void bucket_block(const int32_t *ids, int T, int E, int k, int NS, in
   }
   __syncthreads();
   for (int i = tid; i < n; i += nth) {
-    const int e = __ldcg(ids + i);
+    const int e = ids[i];
     if (e >= 0 && e < E) {
       const int p = atomicAdd(&cur[e], 1);
       list[p] = (i / k) * NS + (i % k);

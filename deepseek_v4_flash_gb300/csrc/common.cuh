@@ -14,7 +14,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ds4moe.h"
+#include "ds4moe.h"
 
 namespace ds4 {
 
@@ -28,21 +28,27 @@ namespace ds4 {
 //               group g = 4c+w with its 2-bit fields transposed so that
 //               ((W >> 2s) & 0x03030303) yields the bytes q[16g+4s .. 16g+4s+3]
 //               in element order (one dp4a against 4 consecutive int8 x).
-// Q8 RG32 tile = 32 rows x two Q8_0 blocks (64 K):
+// Q8 RG32 tile = 32 rows x one Q8_0 block (32 K), 1088 bytes:
+//   [0,64)      d: lane l -> fp16 at 2l
+//   [64,1088)   q: 2 halves h x 32 lanes x 16 bytes (elements 16h .. 16h+15)
+// Router Q8 rows use a 2-block variant (RQ8): 32 rows x 64 K, 2176 bytes:
 //   [0,128)     d: lane l -> 4 bytes (fp16 d of block 0, block 1)
 //   [128,2176)  q: 4 pieces m x 32 lanes x 16 bytes; piece m = block m/2,
 //               elements 16*(m%2) .. 16*(m%2)+15.
 // A matrix [R][K] becomes [R/32][K/KSTEP][tile]; gate and up of the same
 // expert are interleaved per K-step: [R/32][K/KSTEP][2][tile].
 constexpr int Q2S_TILE = 2688, Q2S_DD = 512, Q2S_QS = 640, Q2S_KSTEP = 256;
-constexpr int Q8_TILE = 2176, Q8_Q = 128, Q8_KSTEP = 64;
+constexpr int Q8_TILE = 1088, Q8_Q = 64, Q8_KSTEP = 32;
+constexpr int RQ8_TILE = 2176, RQ8_Q = 128, RQ8_KSTEP = 64;
 constexpr int MAX_STAGE = 2 * Q2S_TILE;  // largest ring stage (gate+up Q2S)
 
 __host__ __device__ constexpr int tile_bytes(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_TILE : Q8_TILE; }
 __host__ __device__ constexpr int kstep(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_KSTEP : Q8_KSTEP; }
 
-// Router rows are summed in 8 segments (CAS step 4, S = 8).
+// Row-sum segments (CAS step 4): router rows 8, shared expert rows 4,
+// routed expert rows 1.
 constexpr int ROUTER_SEGS = 8;
+constexpr int SHARED_SEGS = 4;
 
 // ---------------------------------------------------------------------------
 // CAS device math.

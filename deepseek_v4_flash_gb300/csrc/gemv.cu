@@ -105,21 +105,33 @@ __device__ __forceinline__ bool stream_item(const Ring<NST, STRIDE> &ring, uint3
 constexpr int NST_GU = 4, STRIDE_GU = MAX_STAGE;
 constexpr int NST_DN = 8, STRIDE_DN = MAX_STAGE / 2;
 
+// Row sums in `segs` equal K segments (CAS step 4): the segment chain runs in
+// acc[]; at each segment end it is added into tot[] and restarts at zero.
+template <int TT>
+__device__ __forceinline__ void fold_segment(int s, int seg_steps, float *acc, float *tot) {
+  if ((s + 1) % seg_steps == 0) {
+#pragma unroll
+    for (int i = 0; i < TT; i++) tot[i] = __fadd_rn(tot[i], acc[i]), acc[i] = 0.0f;
+  }
+}
+
 template <int FMT, int TT>
-__device__ void gateup_item(const GemvArgs &a, const uint8_t *src, int rg, int n_e, const int32_t *lst,
+__device__ void gateup_item(const GemvArgs &a, const uint8_t *src, int rg, int n_e, const int32_t *lst, int segs,
                             Ring<NST_GU, STRIDE_GU> &ring, uint32_t &g, int lane) {
   const int H = a.H, F = a.F, NS = a.NS;
-  const int KS = H / kstep(FMT), TB = tile_bytes(FMT);
+  const int KS = H / kstep(FMT), TB = tile_bytes(FMT), seg_steps = KS / segs;
   for (int t0 = 0; t0 < n_e; t0 += TT) {
     int tok[TT];
 #pragma unroll
     for (int i = 0; i < TT; i++) tok[i] = lst[min(t0 + i, n_e - 1)] / NS;
-    float acg[TT], acu[TT];
+    float acg[TT], acu[TT], tg[TT], tu[TT];
 #pragma unroll
-    for (int i = 0; i < TT; i++) acg[i] = 0.0f, acu[i] = 0.0f;
+    for (int i = 0; i < TT; i++) acg[i] = 0.0f, acu[i] = 0.0f, tg[i] = 0.0f, tu[i] = 0.0f;
     const bool ok = stream_item(ring, g, src, KS, 2 * TB, lane, [&](uint32_t st, int s) {
       tile_step<FMT, TT>(st, lane, s, H, tok, a, acg);
       tile_step<FMT, TT>(st + TB, lane, s, H, tok, a, acu);
+      fold_segment<TT>(s, seg_steps, acg, tg);
+      fold_segment<TT>(s, seg_steps, acu, tu);
     });
     if (!ok) {
       if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
@@ -131,7 +143,7 @@ __device__ void gateup_item(const GemvArgs &a, const uint8_t *src, int rg, int n
     for (int i = 0; i < TT; i++) {
       if (t0 + i >= n_e) break;
       const int sr = lst[t0 + i];
-      const float h = __fmul_rn(cas_silu(acg[i]), acu[i]);
+      const float h = __fmul_rn(cas_silu(tg[i]), tu[i]);
       const float amax = warp_max(fabsf(h));
       const float d = __fdiv_rn(amax, 127.0f);
       const int q = cas_code(h, d);
@@ -144,19 +156,21 @@ __device__ void gateup_item(const GemvArgs &a, const uint8_t *src, int rg, int n
 }
 
 template <int FMT, int TT>
-__device__ void down_item(const GemvArgs &a, const uint8_t *src, int rg, int n_e, const int32_t *lst,
+__device__ void down_item(const GemvArgs &a, const uint8_t *src, int rg, int n_e, const int32_t *lst, int segs,
                           Ring<NST_DN, STRIDE_DN> &ring, uint32_t &g, int lane) {
   const int H = a.H, F = a.F;
-  const int KS = F / kstep(FMT), TB = tile_bytes(FMT);
+  const int KS = F / kstep(FMT), TB = tile_bytes(FMT), seg_steps = KS / segs;
   for (int t0 = 0; t0 < n_e; t0 += TT) {
     int sr[TT];
 #pragma unroll
     for (int i = 0; i < TT; i++) sr[i] = lst[min(t0 + i, n_e - 1)];
-    float acc[TT];
+    float acc[TT], tot[TT];
 #pragma unroll
-    for (int i = 0; i < TT; i++) acc[i] = 0.0f;
-    const bool ok = stream_item(ring, g, src, KS, TB, lane,
-                                [&](uint32_t st, int s) { tile_step<FMT, TT>(st, lane, s, F, sr, a, acc); });
+    for (int i = 0; i < TT; i++) acc[i] = 0.0f, tot[i] = 0.0f;
+    const bool ok = stream_item(ring, g, src, KS, TB, lane, [&](uint32_t st, int s) {
+      tile_step<FMT, TT>(st, lane, s, F, sr, a, acc);
+      fold_segment<TT>(s, seg_steps, acc, tot);
+    });
     if (!ok) {
       if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
       return;
@@ -164,7 +178,7 @@ __device__ void down_item(const GemvArgs &a, const uint8_t *src, int rg, int n_e
 #pragma unroll
     for (int i = 0; i < TT; i++) {
       if (t0 + i >= n_e) break;
-      a.apart[(size_t)sr[i] * H + 32 * rg + lane] = acc[i];
+      a.apart[(size_t)sr[i] * H + 32 * rg + lane] = tot[i];
     }
   }
 }
@@ -184,10 +198,10 @@ __global__ void __launch_bounds__(32) k_gateup(GemvArgs a) {
   const int RG = a.F >> 5;
   if (e == a.E) {
     const size_t item = (size_t)(a.H / kstep(SFMT)) * 2 * tile_bytes(SFMT);
-    gateup_item<SFMT, TT>(a, a.w_sh + rg * item, rg, n_e, lst, ring, g, lane);
+    gateup_item<SFMT, TT>(a, a.w_sh + rg * item, rg, n_e, lst, SHARED_SEGS, ring, g, lane);
   } else {
     const size_t item = (size_t)(a.H / kstep(RFMT)) * 2 * tile_bytes(RFMT);
-    gateup_item<RFMT, TT>(a, a.w + ((size_t)e * RG + rg) * item, rg, n_e, lst, ring, g, lane);
+    gateup_item<RFMT, TT>(a, a.w + ((size_t)e * RG + rg) * item, rg, n_e, lst, 1, ring, g, lane);
   }
 }
 
@@ -206,10 +220,10 @@ __global__ void __launch_bounds__(32) k_down(GemvArgs a) {
   const int RG = a.H >> 5;
   if (e == a.E) {
     const size_t item = (size_t)(a.F / kstep(SFMT)) * tile_bytes(SFMT);
-    down_item<SFMT, TT>(a, a.w_sh + rg * item, rg, n_e, lst, ring, g, lane);
+    down_item<SFMT, TT>(a, a.w_sh + rg * item, rg, n_e, lst, SHARED_SEGS, ring, g, lane);
   } else {
     const size_t item = (size_t)(a.F / kstep(RFMT)) * tile_bytes(RFMT);
-    down_item<RFMT, TT>(a, a.w + ((size_t)e * RG + rg) * item, rg, n_e, lst, ring, g, lane);
+    down_item<RFMT, TT>(a, a.w + ((size_t)e * RG + rg) * item, rg, n_e, lst, 1, ring, g, lane);
   }
 }
 

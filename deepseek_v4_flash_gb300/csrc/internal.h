@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ds4moe.h"
+#include "ds4moe.h"
 
 struct ds4moe_layer {
   ds4moe_layer_desc d;
@@ -22,7 +22,6 @@ struct ds4moe_layer {
   uint8_t *gu;           // routed gate+up [E][F/32][H/KSTEP][2][tile]
   uint8_t *dn;           // routed down    [E][H/32][F/KSTEP][tile]
   uint8_t *sgu, *sdn;    // shared, same layouts with E = 1
-  uint8_t *sgu8, *sdn8;  // shared Q8 in the RG8x4 layout (decode path)
 
   // Scratch for max_tokens tokens.
   int8_t *xq;            // [T][H]
@@ -37,9 +36,11 @@ struct ds4moe_layer {
   int16_t *gsh;          // [T*NS][F/16]
   float *apart;          // [T*NS][H]
   uint32_t *err;         // device error flags
-  float *hbuf;           // [T*NS][F] h before requant (decode, 8-row items)
-  int32_t *hticket;      // [T*NS][F/32] requant tickets (self-resetting)
-  int32_t *cticket;      // [T][H/32] combine tickets (self-resetting)
+  float *spart;          // [Td][4][2F] shared-expert segment sums: gate/up then down [Td][4][H]
+  float *spart_dn;
+  int32_t *sticket;      // [Td][F/32] shared gate/up merge tickets (self-resetting)
+  int32_t *sticket_dn;   // [Td][H/32] shared down merge tickets (self-resetting)
+  int32_t *cticket;      // [Td][H/32] combine tickets (self-resetting)
   int32_t *tick;         // routing tickets (self-resetting)
   int32_t *queue;        // work queues of the persistent kernels (self-resetting)
 
@@ -82,10 +83,9 @@ inline size_t bucket_ints(int E, int T, int NS) { return (size_t)(E + 1) + (E + 
 // repack.cu
 cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
                        cudaStream_t s);
-cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int rows_pad, int K, int pair,
-                      int which, cudaStream_t s);
-cudaError_t repack_q8x4(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
-                        cudaStream_t s);
+cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
+                      cudaStream_t s);
+cudaError_t repack_rq8(const uint8_t *src, uint8_t *dst, int rows, int rows_pad, int K, cudaStream_t s);
 cudaError_t check_hash_table(const int32_t *table, int64_t n, int E, int32_t *bad_count, cudaStream_t s);
 
 // route.cu
@@ -101,7 +101,7 @@ cudaError_t launch_rmsnorm(const float *x, float *out, int T, int H, float eps, 
 constexpr int DEC_MAX_T = 64;  // largest n_tok served by the decode path
 size_t route_dec_smem(const ds4moe_layer *h);
 cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, cudaStream_t s);
-cudaError_t launch_dec_expert(const ds4moe_layer *h, int T, float *y, int down, cudaStream_t s);
+cudaError_t launch_dec_expert(const ds4moe_layer *h, const int32_t *tok, int T, float *y, int down, cudaStream_t s);
 cudaError_t decode_set_attributes();
 constexpr size_t DEC_SMEM_LIMIT = 227 * 1024;
 

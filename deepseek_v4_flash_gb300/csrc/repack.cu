@@ -34,48 +34,42 @@ __global__ void k_repack_q2s(const uint8_t *__restrict__ src, uint8_t *__restric
   }
 }
 
-// One thread per pair of canonical Q8_0 blocks (2 x 34 bytes).
+// Expert Q8_0 -> RG32: one thread per canonical block (34 bytes).
 __global__ void k_repack_q8(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
-                            int rows_pad, int KS, int npair, int which) {
+                            int KS, int npair, int which) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = (int64_t)n_mat * rows * KS;
   if (i >= total) return;
   const int c = (int)(i % KS);
   const int64_t mr = i / KS;
   const int r = (int)(mr % rows), m = (int)(mr / rows);
-  const uint8_t *b0 = src + ((int64_t)m * rows + r) * ((int64_t)KS * 68) + (int64_t)c * 68;
+  const uint8_t *b = src + i * 34;
+  const int rg = r >> 5, lane = r & 31;
+  uint8_t *tile = dst + ((((int64_t)m * (rows >> 5) + rg) * KS + c) * npair + which) * Q8_TILE;
+  tile[2 * lane + 0] = b[0], tile[2 * lane + 1] = b[1];
+  for (int h = 0; h < 2; h++)
+    for (int j = 0; j < 16; j++) tile[Q8_Q + 512 * h + 16 * lane + j] = b[2 + 16 * h + j];
+}
+
+// Router Q8_0 -> RQ8: one thread per pair of canonical blocks (2 x 34 bytes);
+// rows beyond `rows` (up to rows_pad) stay zero.
+__global__ void k_repack_rq8(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int rows, int rows_pad,
+                             int KS) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t total = (int64_t)rows * KS;
+  if (i >= total) return;
+  const int c = (int)(i % KS);
+  const int r = (int)(i / KS);
+  const uint8_t *b0 = src + (int64_t)r * ((int64_t)KS * 68) + (int64_t)c * 68;
   const uint8_t *b1 = b0 + 34;
   const int rg = r >> 5, lane = r & 31;
-  uint8_t *tile = dst + ((((int64_t)m * (rows_pad >> 5) + rg) * KS + c) * npair + which) * Q8_TILE;
+  uint8_t *tile = dst + ((int64_t)rg * KS + c) * RQ8_TILE;
+  (void)rows_pad;
   tile[4 * lane + 0] = b0[0], tile[4 * lane + 1] = b0[1];
   tile[4 * lane + 2] = b1[0], tile[4 * lane + 3] = b1[1];
   for (int p = 0; p < 4; p++) {
     const uint8_t *q = (p < 2 ? b0 : b1) + 2 + 16 * (p & 1);
-    uint8_t *o = tile + Q8_Q + 512 * p + 16 * lane;
-    for (int j = 0; j < 16; j++) o[j] = q[j];
-  }
-}
-
-// One thread per pair of canonical Q8_0 blocks -> the RG8x4 layout
-// [n_mat][rows/8][K/64][npair][544]: fp16 d of (row r, block bb) at 4r + 2bb,
-// then lane 4r + c holds row r, block c>>1, elements 16*(c&1) .. +15.
-__global__ void k_repack_q8x4(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
-                              int KS, int npair, int which) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t total = (int64_t)n_mat * rows * KS;
-  if (i >= total) return;
-  const int c = (int)(i % KS);
-  const int64_t mr = i / KS;
-  const int r = (int)(mr % rows), m = (int)(mr / rows);
-  const uint8_t *b0 = src + ((int64_t)m * rows + r) * ((int64_t)KS * 68) + (int64_t)c * 68;
-  const uint8_t *b1 = b0 + 34;
-  const int rg = r >> 3, rr = r & 7;
-  uint8_t *tile = dst + ((((int64_t)m * (rows >> 3) + rg) * KS + c) * npair + which) * 544;
-  tile[4 * rr + 0] = b0[0], tile[4 * rr + 1] = b0[1];
-  tile[4 * rr + 2] = b1[0], tile[4 * rr + 3] = b1[1];
-  for (int cc = 0; cc < 4; cc++) {
-    const uint8_t *q = ((cc >> 1) ? b1 : b0) + 2 + 16 * (cc & 1);
-    uint8_t *o = tile + 32 + 16 * (4 * rr + cc);
+    uint8_t *o = tile + RQ8_Q + 512 * p + 16 * lane;
     for (int j = 0; j < 16; j++) o[j] = q[j];
   }
 }
@@ -96,21 +90,20 @@ cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, in
   return cudaGetLastError();
 }
 
-cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int rows_pad, int K, int pair,
-                      int which, cudaStream_t s) {
+cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
+                      cudaStream_t s) {
   const int KS = K / Q8_KSTEP;
   const int64_t n = (int64_t)n_mat * rows * KS;
   if (n == 0) return cudaSuccess;
-  k_repack_q8<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, rows_pad, KS, pair ? 2 : 1, which);
+  k_repack_q8<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair ? 2 : 1, which);
   return cudaGetLastError();
 }
 
-cudaError_t repack_q8x4(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
-                        cudaStream_t s) {
-  const int KS = K / 64;
-  const int64_t n = (int64_t)n_mat * rows * KS;
+cudaError_t repack_rq8(const uint8_t *src, uint8_t *dst, int rows, int rows_pad, int K, cudaStream_t s) {
+  const int KS = K / RQ8_KSTEP;
+  const int64_t n = (int64_t)rows * KS;
   if (n == 0) return cudaSuccess;
-  k_repack_q8x4<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair ? 2 : 1, which);
+  k_repack_rq8<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, rows, rows_pad, KS);
   return cudaGetLastError();
 }
 

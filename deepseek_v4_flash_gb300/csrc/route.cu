@@ -48,17 +48,17 @@ __global__ void __launch_bounds__(32) k_router_q8(const uint8_t *__restrict__ W,
                                                   const int8_t *__restrict__ xq, const float *__restrict__ dx,
                                                   int T, float *__restrict__ rpart) {
   const int rg = blockIdx.x, seg = blockIdx.y, t0 = blockIdx.z * RT, lane = threadIdx.x;
-  const int nb = H >> 5, per = nb / ROUTER_SEGS, KS = H / Q8_KSTEP;
+  const int nb = H >> 5, per = nb / ROUTER_SEGS, KS = H / RQ8_KSTEP;
   const int nt = min(RT, T - t0);
   float acc[RT];
 #pragma unroll
   for (int i = 0; i < RT; i++) acc[i] = 0.0f;
   for (int b = seg * per; b < (seg + 1) * per; b++) {
-    const uint8_t *tile = W + ((size_t)rg * KS + (b >> 1)) * Q8_TILE;
+    const uint8_t *tile = W + ((size_t)rg * KS + (b >> 1)) * RQ8_TILE;
     const uint32_t dd = *(const uint32_t *)(tile + 4 * lane);
     const float d = half_bits_to_float((b & 1) ? (dd >> 16) : dd);
-    const uint4 w0 = *(const uint4 *)(tile + Q8_Q + 512 * (2 * (b & 1)) + 16 * lane);
-    const uint4 w1 = *(const uint4 *)(tile + Q8_Q + 512 * (2 * (b & 1) + 1) + 16 * lane);
+    const uint4 w0 = *(const uint4 *)(tile + RQ8_Q + 512 * (2 * (b & 1)) + 16 * lane);
+    const uint4 w1 = *(const uint4 *)(tile + RQ8_Q + 512 * (2 * (b & 1) + 1) + 16 * lane);
 #pragma unroll
     for (int i = 0; i < RT; i++) {
       if (i < nt) {
