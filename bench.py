@@ -224,47 +224,70 @@ def main():
         torch.cuda.set_device(0)
     dev = torch.device("cuda")
 
-    # Weights: generated on the host, uploaded, re-laid out by ds4moe_create.
-    w = synth.gen_layer(spec, SEED, 0)
-    wd = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in w.items()}
-    layer = ds4.Layer(desc_from_spec(ds4, spec, T), wd)
-    del wd
-    torch.cuda.empty_cache()
+    # NL layer copies with their own weights: a step uses layer i % NL, so the
+    # weights a step reads were last touched NL steps earlier and the sum of
+    # the per-step working sets exceeds L2 several times over (no flush needed,
+    # and the kernels' code stays resident as it would across a layer stack).
+    # A layer small enough to sit in L2 uses one copy and an L2 flush instead.
+    per_step = step_bytes(spec, T, min(spec.n_experts, T * spec.top_k))
+    NL = 1 if per_step < (32 << 20) else max(2, min(8, int(np.ceil(4 * (128 << 20) / per_step))))
+    use_flush = NL == 1
+    layers, w = [], None
+    for l in range(NL):
+        wl = synth.gen_layer(spec, SEED + 1000 * l, 0)
+        if l == 0:
+            w = wl
+        wd = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in wl.items()}
+        layers.append(ds4.Layer(desc_from_spec(ds4, spec, T), wd))
+        del wd, wl
+        torch.cuda.empty_cache()
+    layer = layers[0]
 
     # Inputs resident in HBM: NX distinct batches, cycled.
     NX = 64
     xs = torch.from_numpy(np.stack([synth.gen_x(spec, SEED + 7 * i + rank, T) for i in range(NX)])).to(dev)
     tok = torch.from_numpy(synth.gen_token_ids(spec, SEED + rank, T)).to(dev) if spec.route == "hash" else None
-    y = torch.zeros(T, spec.hidden, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    ys = [torch.zeros(T, spec.hidden, device=dev) for _ in range(NL)]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if use_flush else None
 
-    # Unique routed experts of each input batch (sets the algorithmic bytes).
-    uniq = []
-    for i in range(NX):
-        ids, _ = layer.route(xs[i], tok)
-        uniq.append(len(np.unique(ids.cpu().numpy()[ids.cpu().numpy() >= 0])))
-    uniq = np.array(uniq)
+    # Unique routed experts of each (layer, input batch) (sets the algorithmic bytes).
+    uniq = np.zeros((NL, NX), np.int64)
+    for l in range(NL):
+        for i in range(NX):
+            ids, _ = layers[l].route(xs[i], tok)
+            v = ids.cpu().numpy()
+            uniq[l, i] = len(np.unique(v[v >= 0]))
 
-    # One forward captured as a CUDA graph on fixed input/output buffers; a
-    # timed step is (outside the events) an L2 flush and the copy of the
-    # step's input batch into the input buffer, then (inside) one replay.
+    # One forward per layer captured as a CUDA graph on fixed input/output
+    # buffers; a timed step is (outside the events) the copy of the step's
+    # input batch into the layer's input buffer (plus the L2 flush when used),
+    # then (inside) one replay.
     stream = torch.cuda.current_stream()
-    x_buf = xs[0].clone()
-    side = torch.cuda.Stream()
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        layer.forward(x_buf, y, tok)
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    n0 = layer.launch_count()
-    with torch.cuda.graph(graph):
-        layer.forward(x_buf, y, tok)
-    launches_per_step = layer.launch_count() - n0
-    for i in range(args.warmup):
-        flush.fill_(i & 255)
-        x_buf.copy_(xs[i % NX])
-        graph.replay()
+    x_bufs = [xs[0].clone() for _ in range(NL)]
+    graphs = []
+    n0 = sum(L.launch_count() for L in layers)
+    for l in range(NL):
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            layers[l].forward(x_bufs[l], ys[l], tok)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layers[l].forward(x_bufs[l], ys[l], tok)
+        graphs.append(g)
+    launches_per_step = (sum(L.launch_count() for L in layers) - n0) // (2 * NL)
+
+    def prep(i):
+        l = i % NL
+        if use_flush:
+            flush.fill_(i & 255)
+        x_bufs[l].copy_(xs[(i // NL) % NX])
+        return l
+
+    for i in range(max(args.warmup, NL)):
+        graphs[prep(i)].replay()
     torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -275,10 +298,9 @@ def main():
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i & 255)
-        x_buf.copy_(xs[i % NX])
+        l = prep(i)
         ev[i][0].record(stream)
-        graph.replay()
+        graphs[l].replay()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -295,24 +317,29 @@ def main():
     value = world * args.steps * T / total_s
 
     # Stage times: events recorded by the library around each kernel of a
-    # forward (no graph). A 2 GiB write before each forward keeps the host's
-    # launches ahead of the GPU, so the events bracket the kernels alone.
-    del graph
-    big = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
-    layer.profile(True)
+    # forward (no graph), same layer rotation.
+    del graphs
+    for L in layers:
+        L.profile(True)
     n_prof = min(args.steps, 400)
     for i in range(n_prof):
-        big.fill_(i & 255)
-        layer.forward(xs[i % NX], y, tok)
-        layer.profile_collect()
-    stage_ms, ncalls = layer.profile_read()
-    layer.profile(False)
-    del big
+        l = prep(i)
+        layers[l].forward(x_bufs[l], ys[l], tok)
+        layers[l].profile_collect()
+    stage_ms, ncalls = {}, 0
+    for L in layers:
+        sm, nc = L.profile_read()
+        ncalls += nc
+        for k2, v2 in sm.items():
+            stage_ms[k2] = stage_ms.get(k2, 0.0) + v2
+        L.profile(False)
 
     hbm_peak, bf16_peak, peak_kind = peaks()
-    u_steps = uniq[np.arange(args.steps) % NX]
+    steps_i = np.arange(args.steps)
+    u_steps = uniq[steps_i % NL, (steps_i // NL) % NX]
     bytes_step = np.array([step_bytes(spec, T, u) for u in u_steps], dtype=np.float64)
-    gu_bytes = np.array([gateup_bytes(spec, T, u) for u in uniq[np.arange(n_prof) % NX]], dtype=np.float64)
+    prof_i = np.arange(n_prof)
+    gu_bytes = np.array([gateup_bytes(spec, T, u) for u in uniq[prof_i % NL, (prof_i // NL) % NX]], dtype=np.float64)
     step_gbs = float(bytes_step.sum() / total_s / 1e9) if world == 1 else float(bytes_step.sum() * world / total_s / 1e9)
     gu_ms = stage_ms["gateup"] / max(ncalls, 1)
     gu_gbs = float(gu_bytes.mean() / (gu_ms / 1e3) / 1e9)
@@ -322,8 +349,10 @@ def main():
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32+f32", "data": "synthetic",
         "config": {"workload": args.workload, "description": desc, "n_tok": T,
-                   "l2": "flushed: 512 MiB write between timed steps",
-                   "inputs": f"{NX} seeded batches resident in HBM, cycled"},
+                   "l2": ("flushed: 512 MiB write between timed steps" if use_flush else
+                          f"not flushed: {NL} layer copies rotated, per-step working sets sum to "
+                          f"{NL * per_step / 2**20:.0f} MiB > L2"),
+                   "inputs": f"{NX} seeded batches resident in HBM, cycled; {NL} layer copies"},
         "hbm_gbs": step_gbs, "hbm_frac": step_gbs / hbm_peak,
         "bytes_per_step": float(bytes_step.mean()),
         "unique_experts_per_step": float(u_steps.mean()),
@@ -348,10 +377,11 @@ def main():
             layer.forward_host(xh[i % len(xh)], yh, th)
         tot = 0.0
         for i in range(args.e2e_steps):
-            flush.fill_(i & 255)
+            if use_flush:
+                flush.fill_(i & 255)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            layer.forward_host(xh[i % len(xh)], yh, th)
+            layers[i % NL].forward_host(xh[i % len(xh)], yh, th)
             tot += time.perf_counter() - t0
         line["e2e"] = {"value": args.e2e_steps * T / tot, "unit": "tokens/s",
                        "h2d_bytes_per_step": 2 * T * spec.hidden * 4 + (T * 4 if tok is not None else 0),

@@ -88,21 +88,21 @@ ds4moe_status cuda_status(cudaError_t e) {
   return e == cudaErrorMemoryAllocation ? DS4MOE_ERR_OOM : DS4MOE_ERR_CUDA;
 }
 
-// Re-lay out a [n_mat][rows][K] expert tensor into the RG32 layout.
+// Re-lay out a [n_mat][rows][K] expert tensor into the RG16 layout.
 cudaError_t repack(int fmt, const void *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
                    cudaStream_t s) {
   if (fmt == DS4MOE_Q2S) return repack_q2s((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
   return repack_q8((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
 }
 
-size_t rg32_bytes(int fmt, long long n_mat, long long rows_pad, long long K) {
-  return (size_t)(n_mat * (rows_pad / 32) * (K / kstep(fmt)) * tile_bytes(fmt));
+size_t rg16_bytes(int fmt, long long n_mat, long long rows, long long K) {
+  return (size_t)(n_mat * (rows / TILE_ROWS) * (K / kstep(fmt)) * tile_bytes(fmt));
 }
 
 ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   const ds4moe_layer_desc &d = h->d;
   const int E = d.n_experts, H = d.hidden, F = d.ffn, k = d.top_k;
-  const long long T = d.max_tokens, NS = h->NS;
+  const long long NS = h->NS;
   ds4moe_status st;
   cudaStream_t s = 0;
 
@@ -134,52 +134,54 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   }
   if (!is_dev_ptr(w->gate) || !is_dev_ptr(w->up) || !is_dev_ptr(w->down)) return DS4MOE_ERR_INVALID_ARG;
   const int rf = d.routed_fmt;
-  if ((st = alloc(h, &h->gu, 2 * rg32_bytes(rf, E, F, H))) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->dn, rg32_bytes(rf, E, H, F))) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->gu, 2 * rg16_bytes(rf, E, F, H))) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->dn, rg16_bytes(rf, E, H, F))) != DS4MOE_OK) return st;
   if ((st = cuda_status(repack(rf, w->gate, h->gu, E, F, H, 1, 0, s))) != DS4MOE_OK) return st;
   if ((st = cuda_status(repack(rf, w->up, h->gu, E, F, H, 1, 1, s))) != DS4MOE_OK) return st;
   if ((st = cuda_status(repack(rf, w->down, h->dn, E, H, F, 0, 0, s))) != DS4MOE_OK) return st;
   if (d.n_shared) {
     if (!is_dev_ptr(w->sh_gate) || !is_dev_ptr(w->sh_up) || !is_dev_ptr(w->sh_down)) return DS4MOE_ERR_INVALID_ARG;
     const int sf = d.shared_fmt;
-    if ((st = alloc(h, &h->sgu, 2 * rg32_bytes(sf, 1, F, H))) != DS4MOE_OK) return st;
-    if ((st = alloc(h, &h->sdn, rg32_bytes(sf, 1, H, F))) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->sgu, 2 * rg16_bytes(sf, 1, F, H))) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->sdn, rg16_bytes(sf, 1, H, F))) != DS4MOE_OK) return st;
     if ((st = cuda_status(repack(sf, w->sh_gate, h->sgu, 1, F, H, 1, 0, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(repack(sf, w->sh_up, h->sgu, 1, F, H, 1, 1, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(repack(sf, w->sh_down, h->sdn, 1, H, F, 0, 0, s))) != DS4MOE_OK) return st;
   }
 
-  // ---- scratch
-  if ((st = alloc(h, &h->xq, (size_t)T * H)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->dx, (size_t)T * (H / 32) * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->gs, (size_t)T * (H / 16) * 2)) != DS4MOE_OK) return st;
+  // ---- scratch, sized for one chunk of at most DEC_MAX_T tokens
+  const long long Tc = h->Tc;
+  if ((st = alloc(h, &h->xq, (size_t)Tc * H)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->dx, (size_t)Tc * (H / 32) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->gs, (size_t)Tc * (H / 16) * 2)) != DS4MOE_OK) return st;
   if (d.route == DS4MOE_ROUTE_LEARNED)
-    if ((st = alloc(h, &h->rpart, (size_t)T * ROUTER_SEGS * h->E_pad * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->ids, (size_t)T * k * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->wts, (size_t)T * k * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->bucket, bucket_ints(E, (int)T, (int)NS) * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->hq, (size_t)(T * NS) * F)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->dh, (size_t)(T * NS) * (F / 32) * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->gsh, (size_t)(T * NS) * (F / 16) * 2)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->apart, (size_t)(T * NS) * H * 4)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->rpart, (size_t)Tc * ROUTER_SEGS * h->E_pad * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->ids, (size_t)Tc * k * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->wts, (size_t)Tc * k * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->bucket, bucket_ints(E, (int)Tc, (int)NS) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->hq, (size_t)(Tc * NS) * F)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->dh, (size_t)(Tc * NS) * (F / 32) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->gsh, (size_t)(Tc * NS) * (F / 16) * 2)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->apart, (size_t)(Tc * NS) * H * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->hbuf, (size_t)(Tc * NS) * F * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->err, 64)) != DS4MOE_OK) return st;
   if ((st = cuda_status(cudaMemsetAsync(h->err, 0, 64, s))) != DS4MOE_OK) return st;
-  {  // decode path: tickets and queues start at zero and reset themselves
-    const long long Td = T < DEC_MAX_T ? T : DEC_MAX_T;
-    const size_t n_sp = (size_t)Td * SHARED_SEGS * 2 * F * 4, n_spd = (size_t)Td * SHARED_SEGS * H * 4;
-    const size_t n_st = (size_t)Td * (F / 32) * 4, n_std = (size_t)Td * (H / 32) * 4;
-    const size_t n_ct = (size_t)Td * (H / 32) * 4, n_tick = 64 * 4, n_q = 16 * 4;
+  {  // tickets and queues start at zero and reset themselves
+    const size_t n_sp = (size_t)Tc * SHARED_SEGS * 2 * F * 4, n_spd = (size_t)Tc * SHARED_SEGS * H * 4;
+    const size_t n_ht = (size_t)(Tc * NS) * (F / 32) * 4;
+    const size_t n_st = (size_t)Tc * (F / TILE_ROWS) * 4, n_std = (size_t)Tc * (H / TILE_ROWS) * 4;
+    const size_t n_ct = (size_t)Tc * (H / 32) * 4, n_q = 16 * 4;
     if ((st = alloc(h, &h->spart, n_sp)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->spart_dn, n_spd)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->hticket, n_ht)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->sticket, n_st)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->sticket_dn, n_std)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->cticket, n_ct)) != DS4MOE_OK) return st;
-    if ((st = alloc(h, &h->tick, n_tick)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->queue, n_q)) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->hticket, 0, n_ht, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->sticket, 0, n_st, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->sticket_dn, 0, n_std, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->cticket, 0, n_ct, s))) != DS4MOE_OK) return st;
-    if ((st = cuda_status(cudaMemsetAsync(h->tick, 0, n_tick, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->queue, 0, n_q, s))) != DS4MOE_OK) return st;
   }
 
@@ -229,6 +231,7 @@ ds4moe_status ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights 
     return DS4MOE_ERR_CUDA;
   }
   h->E_pad = (desc->n_experts + 31) / 32 * 32;
+  h->Tc = desc->max_tokens < DEC_MAX_T ? desc->max_tokens : DEC_MAX_T;
   if (cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -239,10 +242,14 @@ ds4moe_status ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights 
     const long long routed = (long long)desc->max_tokens * desc->top_k;
     h->A_max = (int)(routed < desc->n_experts ? routed : desc->n_experts) + desc->n_shared;
   }
-  h->dec_ok = route_dec_smem(h) <= DEC_SMEM_LIMIT;
-  if (h->dec_ok && decode_set_attributes() != cudaSuccess) {
+  if (route_dec_smem(h) > DEC_SMEM_LIMIT) {  // shapes whose kernels do not fit an SM
+    delete h;
+    return DS4MOE_ERR_UNSUPPORTED;
+  }
+  if (decode_set_attributes() != cudaSuccess) {
     cudaGetLastError();
-    h->dec_ok = 0;
+    delete h;
+    return DS4MOE_ERR_CUDA;
   }
   st = build(h, w);
   if (st != DS4MOE_OK) {
@@ -282,12 +289,17 @@ ds4moe_status ds4moe_route(ds4moe_layer *h, const float *x, const int32_t *token
   const bool hash = h->d.route == DS4MOE_ROUTE_HASH;
   if (hash ? !is_dev_ptr(token_ids) : !is_dev_ptr(x)) return DS4MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (!hash && h->d.router_fmt == DS4MOE_Q8_0) {
-    st = cuda_status(launch_quantize(x, n_tok, h->d.hidden, h->xq, h->dx, h->gs, h->err, s));
-    if (st != DS4MOE_OK) return st;
+  const int H = h->d.hidden, k = h->d.top_k;
+  cudaError_t e = cudaSuccess;
+  for (int c0 = 0; c0 < n_tok && e == cudaSuccess; c0 += h->Tc) {
+    const int nc = n_tok - c0 < h->Tc ? n_tok - c0 : h->Tc;
+    if (!hash) e = launch_dec_route(h, x + (size_t)c0 * H, nullptr, nc, s);
+    if (e == cudaSuccess)
+      e = launch_route_tokens(h, hash ? token_ids + c0 : nullptr, nc, ids_out + (size_t)c0 * k,
+                              w_out + (size_t)c0 * k, s);
+    h->launches += hash ? 1 : 2;
   }
-  h->launches += hash ? 1 : (h->d.router_fmt == DS4MOE_Q8_0 ? 3 : 2);
-  return cuda_status(launch_route(h, x, token_ids, n_tok, ids_out, w_out, s));
+  return cuda_status(e);
 }
 
 ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids, float *y,
@@ -303,35 +315,25 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
   auto mark = [&](int i) {
     if (prof) cudaEventRecord(h->ev[i], s);
   };
-  if (h->dec_ok && n_tok <= DEC_MAX_T) {
-    // decode path: fused routing, then the two persistent expert kernels
+  // Tokens are independent: run chunks of at most Tc tokens.
+  cudaError_t e = cudaSuccess;
+  for (int c0 = 0; c0 < n_tok && e == cudaSuccess; c0 += h->Tc) {
+    const int nc = n_tok - c0 < h->Tc ? n_tok - c0 : h->Tc;
+    const float *xc = x + (size_t)c0 * H;
+    const int32_t *tc = token_ids ? token_ids + c0 : nullptr;
+    float *yc = y + (size_t)c0 * H;
     mark(0);
     mark(1);
-    cudaError_t e = launch_dec_route(h, x, token_ids, n_tok, s);
+    e = launch_dec_route(h, xc, tc, nc, s);
     mark(2);
     mark(3);
-    if (e == cudaSuccess) e = launch_dec_expert(h, token_ids, n_tok, y, 0, s);
+    if (e == cudaSuccess) e = launch_dec_expert(h, tc, nc, yc, 0, s);
     mark(4);
-    if (e == cudaSuccess) e = launch_dec_expert(h, token_ids, n_tok, y, 1, s);
+    if (e == cudaSuccess) e = launch_dec_expert(h, tc, nc, yc, 1, s);
     mark(5);
     mark(6);
     h->launches += 3;
-    return cuda_status(e);
   }
-  mark(0);
-  cudaError_t e = launch_quantize(x, n_tok, H, h->xq, h->dx, h->gs, h->err, s);
-  mark(1);
-  if (e == cudaSuccess) e = launch_route(h, x, token_ids, n_tok, h->ids, h->wts, s);
-  mark(2);
-  if (e == cudaSuccess) e = launch_bucket(h, n_tok, s);
-  mark(3);
-  if (e == cudaSuccess) e = launch_gateup(h, n_tok, s);
-  mark(4);
-  if (e == cudaSuccess) e = launch_down(h, n_tok, s);
-  mark(5);
-  if (e == cudaSuccess) e = launch_combine(h, n_tok, y, s);
-  mark(6);
-  h->launches += (h->d.route == DS4MOE_ROUTE_HASH) ? 6 : 7;
   return cuda_status(e);
 }
 
@@ -426,7 +428,7 @@ ds4moe_status ds4moe_get_device_error(ds4moe_layer *h, void *stream, uint32_t *f
 // results of the last call (integer codes, ids, weights).
 ds4moe_status ds4moe_debug_scratch(ds4moe_layer *h, int32_t which, const void **ptr_out, uint64_t *bytes_out) {
   if (!h || !ptr_out || !bytes_out) return DS4MOE_ERR_INVALID_ARG;
-  const long long T = h->d.max_tokens, NS = h->NS, H = h->d.hidden, F = h->d.ffn, k = h->d.top_k;
+  const long long T = h->Tc, NS = h->NS, H = h->d.hidden, F = h->d.ffn, k = h->d.top_k;
   const void *p = nullptr;
   uint64_t n = 0;
   switch (which) {

@@ -5,8 +5,8 @@
 //    __fmaf_rn / __fdiv_rn / __fsqrt_rn, which the compiler never contracts
 //    or reorders, so results are bit-identical to a scalar CPU evaluation of
 //    the same spec.
-// 2. The library's internal weight layouts ("RG32": 32 rows interleaved so a
-//    warp, one row per lane, reads 512 contiguous bytes per 16-byte load).
+// 2. The library's internal weight layouts (16 rows per tile, two lanes per
+//    row).
 // 3. PTX wrappers for mbarriers and 1-D bulk async copies (cp.async.bulk)
 //    with bounded waits.
 #pragma once
@@ -19,28 +19,33 @@
 namespace ds4 {
 
 // ---------------------------------------------------------------------------
-// Internal layouts.
+// Internal layouts ("RG16": 16 rows per tile, two lanes per row; lane
+// l = 2r + h serves row r with half h of the work, so a warp reads 512
+// contiguous bytes per 16-byte load and the two lanes of a row add their
+// exact integer partial dots with one shuffle).
 //
-// Q2S RG32 tile = 32 rows x one superblock (256 K):
-//   [0,512)     sm:   lane l -> 16 bytes (scale/min nibbles of its row)
-//   [512,640)   d,dmin: lane l -> 4 bytes (fp16 d, fp16 dmin)
-//   [640,2688)  qs:   4 chunks c x 32 lanes x 16 bytes; chunk c, word w holds
-//               group g = 4c+w with its 2-bit fields transposed so that
-//               ((W >> 2s) & 0x03030303) yields the bytes q[16g+4s .. 16g+4s+3]
+// Q2S RG16 tile = 16 rows x one superblock (256 K), 1344 bytes:
+//   [0,256)     sm8: lane l -> 8 bytes: the scale/min nibbles of the groups
+//               of parity h (groups h, h+2, ..., h+14), i.e. of blocks 0..7
+//   [256,320)   dd:  row r -> 4 bytes at 4r (fp16 d, fp16 dmin)
+//   [320,1344)  qs:  2 chunks j x 32 lanes x 16 bytes: lane l, chunk j holds
+//               the group words of blocks 4j..4j+3 (group 2b+h of block b),
+//               each word's 2-bit fields transposed so that
+//               ((W >> 2s) & 0x03030303) yields q[4s .. 4s+3] of the group
 //               in element order (one dp4a against 4 consecutive int8 x).
-// Q8 RG32 tile = 32 rows x one Q8_0 block (32 K), 1088 bytes:
-//   [0,64)      d: lane l -> fp16 at 2l
-//   [64,1088)   q: 2 halves h x 32 lanes x 16 bytes (elements 16h .. 16h+15)
-// Router Q8 rows use a 2-block variant (RQ8): 32 rows x 64 K, 2176 bytes:
-//   [0,128)     d: lane l -> 4 bytes (fp16 d of block 0, block 1)
-//   [128,2176)  q: 4 pieces m x 32 lanes x 16 bytes; piece m = block m/2,
-//               elements 16*(m%2) .. 16*(m%2)+15.
-// A matrix [R][K] becomes [R/32][K/KSTEP][tile]; gate and up of the same
-// expert are interleaved per K-step: [R/32][K/KSTEP][2][tile].
-constexpr int Q2S_TILE = 2688, Q2S_DD = 512, Q2S_QS = 640, Q2S_KSTEP = 256;
-constexpr int Q8_TILE = 1088, Q8_Q = 64, Q8_KSTEP = 32;
+// Q8 RG16 tile = 16 rows x one Q8_0 block (32 K), 544 bytes:
+//   [0,32)      d: row r -> fp16 at 2r
+//   [32,544)    q: lane l -> 16 bytes: row r, elements 16h .. 16h+15
+// Router Q8 rows use a 32-row, 2-block layout (RQ8): 32 rows x 64 K, 2176
+// bytes: [0,128) d: lane l -> 4 bytes (fp16 d of block 0, block 1);
+// [128,2176) q: 4 pieces m x 32 lanes x 16 bytes; piece m = block m/2,
+// elements 16*(m%2) .. 16*(m%2)+15.
+// A matrix [R][K] becomes [R/16][K/KSTEP][tile]; gate and up of the same
+// expert are interleaved per K-step: [R/16][K/KSTEP][2][tile].
+constexpr int TILE_ROWS = 16;
+constexpr int Q2S_TILE = 1344, Q2S_SM = 0, Q2S_DD = 256, Q2S_QS = 320, Q2S_KSTEP = 256;
+constexpr int Q8_TILE = 544, Q8_Q = 32, Q8_KSTEP = 32;
 constexpr int RQ8_TILE = 2176, RQ8_Q = 128, RQ8_KSTEP = 64;
-constexpr int MAX_STAGE = 2 * Q2S_TILE;  // largest ring stage (gate+up Q2S)
 
 __host__ __device__ constexpr int tile_bytes(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_TILE : Q8_TILE; }
 __host__ __device__ constexpr int kstep(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_KSTEP : Q8_KSTEP; }
@@ -191,6 +196,12 @@ __device__ __forceinline__ void raise_flag(uint32_t *err, uint32_t bits) {
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
 

@@ -154,11 +154,13 @@ __global__ void __launch_bounds__(RD_WARPS * 32) k_router_dec(RouteDecArgs a) {
 // K2 / K3: persistent expert GEMV streamers.
 //
 // Work items, largest first:
-//   shared expert: (32-row group rg, K quarter q) for q = 0..3 -- the shared
+//   shared expert: (16-row group rg, K quarter q) for q = 0..3 -- the shared
 //     expert's rows are summed in 4 segments (CAS step 4, S = 4), so each
 //     quarter is an independent chain; the last quarter to finish adds the
 //     four segment sums in order;
-//   routed experts: (active expert, 32-row group), the whole K range.
+//   routed experts: (active expert, 16-row group), the whole K range.
+// A gate/up item's SwiGLU values go to hbuf; the second 16-row item of each
+// 32-row block requantises the block (CAS step 1 on h).
 
 constexpr int DEC_WARPS = 8;     // streamers per CTA
 constexpr int DEC_NST = 4;       // ring stages per streamer
@@ -171,8 +173,8 @@ struct DecArgs {
   int K;                         // reduction length: H (gate/up) or F (down)
   int rows;                      // output rows of the matrices: F (gate/up) or H (down)
   int act_smem;                  // activations staged in shared memory
-  const uint8_t *w_r;            // routed weights, RG32
-  const uint8_t *w_s;            // shared weights, RG32
+  const uint8_t *w_r;            // routed weights, RG16
+  const uint8_t *w_s;            // shared weights, RG16
   const int8_t *aq;              // activation codes: xq [T][H] or hq [T*NS][F]
   const float *ad;
   const int16_t *ag;
@@ -190,7 +192,9 @@ struct DecArgs {
   float *dh;
   int16_t *gsh;
   float *spart;                  // shared segment sums: [T][4][rows][mats]
-  int32_t *sticket;              // [T][rows/32] shared merge tickets
+  int32_t *sticket;              // [T][rows/16] shared merge tickets
+  float *hbuf;                   // [T*NS][F] SwiGLU values before requant
+  int32_t *hticket;              // [T*NS][F/32] requant tickets
   float *apart;                  // [T*NS][H]
   int32_t *cticket;              // [T][H/32] combine tickets
   float *y;
@@ -210,7 +214,9 @@ struct ItemDesc {
   int n_tok, list_off;
 };
 
-__device__ __forceinline__ int shared_items(const DecArgs &a) { return a.n_shared ? SHARED_SEGS * (a.rows / 32) : 0; }
+__device__ __forceinline__ int shared_items(const DecArgs &a) {
+  return a.n_shared ? SHARED_SEGS * (a.rows / TILE_ROWS) : 0;
+}
 
 // K-steps per stage: as many as fit a ring slot, dividing the K-step count.
 __device__ __forceinline__ int stage_ksteps(int kbytes, int nks) {
@@ -224,7 +230,7 @@ __device__ __forceinline__ int stage_ksteps(int kbytes, int nks) {
 // their weights can stream before it exists.
 __device__ ItemDesc item_desc(const DecArgs &a, const Bk *bk, int i) {
   ItemDesc d;
-  const int nsh = shared_items(a), RG = a.rows / 32, mats = a.down ? 1 : 2;
+  const int nsh = shared_items(a), RG = a.rows / TILE_ROWS, mats = a.down ? 1 : 2;
   if (i < nsh) {
     d.fmt = a.sf, d.e = a.E, d.rg = i / SHARED_SEGS, d.quarter = i % SHARED_SEGS;
   } else {
@@ -319,42 +325,53 @@ __device__ __forceinline__ int valid_routed_slots(const DecArgs &a, int t) {
   return n;
 }
 
-// Increment a ticket; true (on every lane) for the caller that completes it.
+// Count one arrival on a ticket; true (on every lane) for the caller that
+// completes it. The release/acquire atomic orders this warp's earlier global
+// writes before the completer's later reads; the completer resets the ticket.
 __device__ __forceinline__ bool ticket_last(int32_t *tk, int expect, int lane) {
-  __threadfence();
   __syncwarp();
   int last = 0;
-  if (lane == 0) last = atomicAdd(tk, 1) == expect - 1;
+  if (lane == 0) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(tk) : "memory");
+    last = old == expect - 1;
+    if (last) *tk = 0;
+  }
   last = __shfl_sync(0xffffffffu, last, 0);
-  if (last) __threadfence();
+  __syncwarp();  // order lane 0's acquire before the other lanes' reads
   return last != 0;
 }
 
-// Down output of 32 rows of slot row sr is complete: count it towards the
-// combine of token t, rows 32*rg.., and run the combine if it was the last.
-__device__ __forceinline__ void down_done(const DecArgs &a, int sr, int rg, int lane) {
-  const int t = sr / a.NS;
-  int32_t *tk = a.cticket + (size_t)t * (a.H >> 5) + rg;
+// 16 rows (rg16) of the down output of slot row sr are in apart: count them
+// towards the combine of token t, rows 32*(rg16/2)..; run it if complete.
+__device__ __forceinline__ void down_done(const DecArgs &a, int sr, int rg16, int lane) {
+  const int t = sr / a.NS, rg = rg16 >> 1;
   int expect = 0;
-  if (lane == 0) expect = valid_routed_slots(a, t) + a.n_shared;
+  if (lane == 0) expect = 2 * (valid_routed_slots(a, t) + a.n_shared);
   expect = __shfl_sync(0xffffffffu, expect, 0);
-  if (ticket_last(tk, expect, lane)) {
-    combine_rows(a, t, rg, lane);
-    if (lane == 0) *tk = 0;
-  }
+  if (ticket_last(a.cticket + (size_t)t * (a.H >> 5) + rg, expect, lane)) combine_rows(a, t, rg, lane);
+}
+
+// SwiGLU value h of row 16*rg16 + lane/2 of slot row sr (both lanes of a row
+// hold it): stage it; the second 16-row half of the 32-row block requantises.
+__device__ __forceinline__ void gateup_done(const DecArgs &a, float h, int sr, int rg16, int lane) {
+  if ((lane & 1) == 0) a.hbuf[(size_t)sr * a.F + 16 * rg16 + (lane >> 1)] = h;
+  const int blk = rg16 >> 1;
+  if (ticket_last(a.hticket + (size_t)sr * (a.F >> 5) + blk, 2, lane))
+    requant_store(a, __ldcg(a.hbuf + (size_t)sr * a.F + 32 * blk + lane), sr, blk, lane);
 }
 
 template <int TT>
 __device__ void item_epilogue(const DecArgs &a, const ItemDesc &d, int lane, const int *srow, int nt,
                               const float *acc0, const float *acc1) {
+  const int r = TILE_ROWS * d.rg + (lane >> 1);
   for (int i = 0; i < nt; i++) {
     const int sr = srow[i];
-    const int r = 32 * d.rg + lane;
     if (d.quarter < 0) {  // routed: the whole chain is in this warp
       if (!a.down) {
-        requant_store(a, __fmul_rn(cas_silu(acc0[i]), acc1[i]), sr, d.rg, lane);
+        gateup_done(a, __fmul_rn(cas_silu(acc0[i]), acc1[i]), sr, d.rg, lane);
       } else {
-        a.apart[(size_t)sr * a.H + r] = acc0[i];
+        if ((lane & 1) == 0) a.apart[(size_t)sr * a.H + r] = acc0[i];
         down_done(a, sr, d.rg, lane);
       }
       continue;
@@ -362,21 +379,21 @@ __device__ void item_epilogue(const DecArgs &a, const ItemDesc &d, int lane, con
     // shared: publish this quarter's segment sums; the last quarter merges
     const int t = sr / a.NS, mats = a.down ? 1 : 2;
     float *sp = a.spart + ((size_t)t * SHARED_SEGS) * a.rows * mats;
-    sp[((size_t)d.quarter * a.rows + r) * mats] = acc0[i];
-    if (!a.down) sp[((size_t)d.quarter * a.rows + r) * mats + 1] = acc1[i];
-    int32_t *tk = a.sticket + (size_t)t * (a.rows >> 5) + d.rg;
-    if (!ticket_last(tk, SHARED_SEGS, lane)) continue;
+    if ((lane & 1) == 0) {
+      sp[((size_t)d.quarter * a.rows + r) * mats] = acc0[i];
+      if (!a.down) sp[((size_t)d.quarter * a.rows + r) * mats + 1] = acc1[i];
+    }
+    if (!ticket_last(a.sticket + (size_t)t * (a.rows / TILE_ROWS) + d.rg, SHARED_SEGS, lane)) continue;
     float g = 0.0f, u = 0.0f;
 #pragma unroll
     for (int q = 0; q < SHARED_SEGS; q++) {
       g = __fadd_rn(g, __ldcg(sp + ((size_t)q * a.rows + r) * mats));
       if (!a.down) u = __fadd_rn(u, __ldcg(sp + ((size_t)q * a.rows + r) * mats + 1));
     }
-    if (lane == 0) *tk = 0;
     if (!a.down) {
-      requant_store(a, __fmul_rn(cas_silu(g), u), sr, d.rg, lane);
+      gateup_done(a, __fmul_rn(cas_silu(g), u), sr, d.rg, lane);
     } else {
-      a.apart[(size_t)sr * a.H + r] = g;
+      if ((lane & 1) == 0) a.apart[(size_t)sr * a.H + r] = g;
       down_done(a, sr, d.rg, lane);
     }
   }
@@ -450,6 +467,16 @@ __device__ void route_token_warp(const DecArgs &a, int t, int lane, float *sv, i
     ids[t * a.k + lane] = sel_mine;
     wts[t * a.k + lane] = sel_mine >= 0 ? __fmul_rn(__fdiv_rn(sv[sel_mine], sum), a.scale) : 0.0f;
   }
+}
+
+// Routing only (ds4moe_route): one warp per token writes its expert ids and
+// weights. Token tile of 8 tokens per CTA; scratch: 8 x 2*E_pad floats.
+__global__ void __launch_bounds__(256) k_route_tokens(DecArgs a, int32_t *ids, float *wts) {
+  extern __shared__ __align__(16) float rsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= a.T) return;
+  route_token_warp(a, t, lane, rsm + warp * 2 * a.E_pad, ids, wts);
 }
 
 // Shared memory after the rings: [bucket ints][scratch]. bucket: cnt[E+1]
@@ -538,7 +565,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_expert_dec(DecArgs a) {
     __syncthreads();
   }
 
-  const int n_items = nsh + (bk.n_active - a.n_shared) * (a.rows / 32);
+  const int n_items = nsh + (bk.n_active - a.n_shared) * (a.rows / TILE_ROWS);
   if (p_item >= n_items) {
     p_done = true;
   } else {
@@ -693,11 +720,11 @@ cudaError_t launch_dec_expert(const ds4moe_layer *h, const int32_t *tok, int T, 
   if (!down) {
     a.K = d.hidden, a.rows = d.ffn, a.w_r = h->gu, a.w_s = h->sgu;
     a.aq = h->xq, a.ad = h->dx, a.ag = h->gs, a.queue = h->queue;
-    a.spart = h->spart, a.sticket = h->sticket;
+    a.spart = h->spart, a.sticket = h->sticket, a.hbuf = h->hbuf, a.hticket = h->hticket;
   } else {
     a.K = d.ffn, a.rows = d.hidden, a.w_r = h->dn, a.w_s = h->sdn;
     a.aq = h->hq, a.ad = h->dh, a.ag = h->gsh, a.queue = h->queue + 2;
-    a.spart = h->spart_dn, a.sticket = h->sticket_dn;
+    a.spart = h->spart_dn, a.sticket = h->sticket_dn, a.hbuf = h->hbuf, a.hticket = h->hticket;
   }
   const bool act = expert_dec_smem(h, T, down != 0, true) <= DEC_SMEM_LIMIT;
   a.act_smem = act;
@@ -705,6 +732,17 @@ cudaError_t launch_dec_expert(const ds4moe_layer *h, const int32_t *tok, int T, 
   void *args[] = {&a};
   const void *fn = act ? expert_fn<true>(T) : expert_fn<false>(T);
   return launch_pdl(fn, dim3(h->n_sm), dim3(DEC_WARPS * 32), smem, s, args, true);
+}
+
+cudaError_t launch_route_tokens(const ds4moe_layer *h, const int32_t *tok, int T, int32_t *ids, float *w,
+                                cudaStream_t s) {
+  const ds4moe_layer_desc &d = h->d;
+  DecArgs a = {};
+  a.E = d.n_experts, a.E_pad = h->E_pad, a.k = d.top_k, a.T = T;
+  a.route = d.route, a.scale = d.route_scale, a.vocab = d.vocab;
+  a.rpart = h->rpart, a.bias = h->bias, a.hash = h->hash, a.tok = tok, a.err = h->err;
+  k_route_tokens<<<(T + 7) / 8, 256, 8 * 2 * h->E_pad * sizeof(float), s>>>(a, ids, w);
+  return cudaGetLastError();
 }
 
 cudaError_t decode_set_attributes() {

@@ -13,7 +13,7 @@ struct ds4moe_layer {
   int NS;      // expert slots per token: top_k + n_shared
   int A_max;   // most active experts in one call: min(E, max_tokens*k) + n_shared
   int n_sm;    // streaming multiprocessors of the device
-  int dec_ok;  // the decode path fits this layer (shared memory)
+  int Tc;      // tokens per chunk: min(max_tokens, DEC_MAX_T); scratch is sized for one chunk
 
   // Weights in the library's layout (see common.cuh).
   uint8_t *router;       // Q8 RG32 [E_pad/32][H/64][tile], or F32 [E][H]
@@ -36,12 +36,13 @@ struct ds4moe_layer {
   int16_t *gsh;          // [T*NS][F/16]
   float *apart;          // [T*NS][H]
   uint32_t *err;         // device error flags
-  float *spart;          // [Td][4][2F] shared-expert segment sums: gate/up then down [Td][4][H]
-  float *spart_dn;
-  int32_t *sticket;      // [Td][F/32] shared gate/up merge tickets (self-resetting)
-  int32_t *sticket_dn;   // [Td][H/32] shared down merge tickets (self-resetting)
-  int32_t *cticket;      // [Td][H/32] combine tickets (self-resetting)
-  int32_t *tick;         // routing tickets (self-resetting)
+  float *hbuf;           // [Tc*NS][F] SwiGLU values before requant
+  int32_t *hticket;      // [Tc*NS][F/32] requant tickets (self-resetting)
+  float *spart;          // [Tc][4][2F] shared-expert gate/up segment sums
+  float *spart_dn;       // [Tc][4][H] shared-expert down segment sums
+  int32_t *sticket;      // [Tc][F/16] shared gate/up merge tickets (self-resetting)
+  int32_t *sticket_dn;   // [Tc][H/16] shared down merge tickets (self-resetting)
+  int32_t *cticket;      // [Tc][H/32] combine tickets (self-resetting)
   int32_t *queue;        // work queues of the persistent kernels (self-resetting)
 
   // Staging for ds4moe_forward_host.
@@ -88,13 +89,7 @@ cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int
 cudaError_t repack_rq8(const uint8_t *src, uint8_t *dst, int rows, int rows_pad, int K, cudaStream_t s);
 cudaError_t check_hash_table(const int32_t *table, int64_t n, int E, int32_t *bad_count, cudaStream_t s);
 
-// route.cu
-cudaError_t launch_quantize(const float *x, int T, int H, int8_t *xq, float *dx, int16_t *gs, uint32_t *err,
-                            cudaStream_t s);
-cudaError_t launch_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
-                         float *w, cudaStream_t s);
-cudaError_t launch_bucket(const ds4moe_layer *h, int T, cudaStream_t s);
-cudaError_t launch_combine(const ds4moe_layer *h, int T, float *y, cudaStream_t s);
+// rmsnorm.cu
 cudaError_t launch_rmsnorm(const float *x, float *out, int T, int H, float eps, cudaStream_t s);
 
 // decode.cu
@@ -102,11 +97,9 @@ constexpr int DEC_MAX_T = 64;  // largest n_tok served by the decode path
 size_t route_dec_smem(const ds4moe_layer *h);
 cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, cudaStream_t s);
 cudaError_t launch_dec_expert(const ds4moe_layer *h, const int32_t *tok, int T, float *y, int down, cudaStream_t s);
+cudaError_t launch_route_tokens(const ds4moe_layer *h, const int32_t *tok, int T, int32_t *ids, float *w,
+                                cudaStream_t s);
 cudaError_t decode_set_attributes();
 constexpr size_t DEC_SMEM_LIMIT = 227 * 1024;
-
-// gemv.cu
-cudaError_t launch_gateup(const ds4moe_layer *h, int T, cudaStream_t s);
-cudaError_t launch_down(const ds4moe_layer *h, int T, cudaStream_t s);
 
 }  // namespace ds4

@@ -1,15 +1,16 @@
 // repack.cu -- create-time conversion of the canonical weight bytes into the
-// library's RG32 layouts (see common.cuh). Runs once per layer handle.
+// library's layouts (RG16 for expert matrices, RQ8 for the router; see
+// common.cuh). Runs once per layer handle.
 #include "common.cuh"
 #include "internal.h"
 
 namespace ds4 {
 
-// One thread per canonical Q2S superblock (84 bytes) -> its lane's slices of
-// an RG32 tile. The 2-bit fields of each 16-weight group are transposed:
-// canonical element 4*s+j (byte s of the group, bits 2j) moves to byte j,
-// bits 2s of the group word, so (W >> 2s) & 0x03030303 gives 4 consecutive
-// elements in byte order.
+// One thread per canonical Q2S superblock (84 bytes) -> its two lanes'
+// slices of an RG16 tile. The 2-bit fields of each 16-weight group are
+// transposed: canonical element 4*s+j of the group (byte s of the group,
+// bits 2j) moves to byte j, bits 2s of the group word, so (W >> 2s) &
+// 0x03030303 gives 4 consecutive elements in byte order.
 __global__ void k_repack_q2s(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
                              int KS, int npair, int which) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -19,22 +20,26 @@ __global__ void k_repack_q2s(const uint8_t *__restrict__ src, uint8_t *__restric
   const int64_t mr = i / KS;
   const int r = (int)(mr % rows), m = (int)(mr / rows);
   const uint8_t *sb = src + i * 84;
-  const int rg = r >> 5, lane = r & 31;
-  uint8_t *tile = dst + ((((int64_t)m * (rows >> 5) + rg) * KS + s) * npair + which) * Q2S_TILE;
-  for (int j = 0; j < 16; j++) tile[16 * lane + j] = sb[j];
-  for (int j = 0; j < 4; j++) tile[Q2S_DD + 4 * lane + j] = sb[80 + j];
-  for (int g = 0; g < 16; g++) {
-    uint32_t W = 0;
-    for (int sbyte = 0; sbyte < 4; sbyte++) {
-      const uint32_t b = sb[16 + 4 * g + sbyte];
-      for (int j = 0; j < 4; j++) W |= ((b >> (2 * j)) & 3u) << (8 * j + 2 * sbyte);
+  const int rg = r >> 4, rr = r & 15;
+  uint8_t *tile = dst + ((((int64_t)m * (rows >> 4) + rg) * KS + s) * npair + which) * Q2S_TILE;
+  for (int j = 0; j < 4; j++) tile[Q2S_DD + 4 * rr + j] = sb[80 + j];
+  for (int h = 0; h < 2; h++) {
+    const int lane = 2 * rr + h;
+    for (int b = 0; b < 8; b++) {
+      const int g = 2 * b + h;
+      tile[Q2S_SM + 8 * lane + b] = sb[g];
+      uint32_t W = 0;
+      for (int sbyte = 0; sbyte < 4; sbyte++) {
+        const uint32_t v = sb[16 + 4 * g + sbyte];
+        for (int j = 0; j < 4; j++) W |= ((v >> (2 * j)) & 3u) << (8 * j + 2 * sbyte);
+      }
+      uint8_t *o = tile + Q2S_QS + 512 * (b >> 2) + 16 * lane + 4 * (b & 3);
+      o[0] = (uint8_t)W, o[1] = (uint8_t)(W >> 8), o[2] = (uint8_t)(W >> 16), o[3] = (uint8_t)(W >> 24);
     }
-    uint8_t *o = tile + Q2S_QS + 512 * (g >> 2) + 16 * lane + 4 * (g & 3);
-    o[0] = (uint8_t)W, o[1] = (uint8_t)(W >> 8), o[2] = (uint8_t)(W >> 16), o[3] = (uint8_t)(W >> 24);
   }
 }
 
-// Expert Q8_0 -> RG32: one thread per canonical block (34 bytes).
+// Expert Q8_0 -> RG16: one thread per canonical block (34 bytes).
 __global__ void k_repack_q8(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
                             int KS, int npair, int which) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -44,11 +49,11 @@ __global__ void k_repack_q8(const uint8_t *__restrict__ src, uint8_t *__restrict
   const int64_t mr = i / KS;
   const int r = (int)(mr % rows), m = (int)(mr / rows);
   const uint8_t *b = src + i * 34;
-  const int rg = r >> 5, lane = r & 31;
-  uint8_t *tile = dst + ((((int64_t)m * (rows >> 5) + rg) * KS + c) * npair + which) * Q8_TILE;
-  tile[2 * lane + 0] = b[0], tile[2 * lane + 1] = b[1];
+  const int rg = r >> 4, rr = r & 15;
+  uint8_t *tile = dst + ((((int64_t)m * (rows >> 4) + rg) * KS + c) * npair + which) * Q8_TILE;
+  tile[2 * rr + 0] = b[0], tile[2 * rr + 1] = b[1];
   for (int h = 0; h < 2; h++)
-    for (int j = 0; j < 16; j++) tile[Q8_Q + 512 * h + 16 * lane + j] = b[2 + 16 * h + j];
+    for (int j = 0; j < 16; j++) tile[Q8_Q + 16 * (2 * rr + h) + j] = b[2 + 16 * h + j];
 }
 
 // Router Q8_0 -> RQ8: one thread per pair of canonical blocks (2 x 34 bytes);

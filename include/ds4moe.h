@@ -88,7 +88,9 @@ typedef struct {
   int32_t routed_fmt;   /* DS4MOE_Q8_0 or DS4MOE_Q2S                                */
   int32_t shared_fmt;   /* DS4MOE_Q8_0 or DS4MOE_Q2S                                */
   float route_scale;    /* multiplies the renormalised routed weights (1.0)         */
-  int32_t max_tokens;   /* largest n_tok of any later call, 1..1048576              */
+  int32_t max_tokens;   /* largest n_tok of any later call, 1..1048576; calls run in */
+                        /* chunks of at most 64 tokens, so scratch is sized for    */
+                        /* min(max_tokens, 64) tokens                               */
 } ds4moe_layer_desc;
 
 /* Canonical weight buffers, DEVICE memory, read only during ds4moe_create
@@ -107,10 +109,12 @@ typedef struct {
 typedef struct ds4moe_layer ds4moe_layer; /* opaque handle */
 
 /* Validate `desc`, allocate the handle's device memory on the current device
- * (weights in the library's layout plus scratch for desc->max_tokens tokens),
+ * (weights in the library's layout plus scratch for one chunk of tokens),
  * re-lay out the weights, and synchronise. On success *out owns all of it;
  * on error *out is NULL and nothing stays allocated.
- * Errors: INVALID_ARG (desc, missing or non-device pointer), OOM, CUDA. */
+ * Errors: INVALID_ARG (desc, missing or non-device pointer), UNSUPPORTED
+ * (a shape whose kernels do not fit one SM, e.g. more than ~700 experts),
+ * OOM, CUDA. */
 ds4moe_status ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights *w,
                             ds4moe_layer **out);
 
@@ -156,17 +160,19 @@ ds4moe_status ds4moe_rmsnorm(const float *x, float *out, int32_t n_tok, int32_t 
  * Returns DS4MOE_ERR_DEVICE when any bit was set, else DS4MOE_OK. */
 ds4moe_status ds4moe_get_device_error(ds4moe_layer *h, void *stream, uint32_t *flags_out);
 
-/* Read-only device view of the handle's scratch after the last route/forward
- * call, for inspecting intermediate results. `which`:
- *   0 xq  int8  [max_tokens][H]        activation codes (CAS step 1)
- *   1 dx  fp32  [max_tokens][H/32]     activation scales
- *   2 gs  int16 [max_tokens][H/16]     16-group sums of xq
- *   3 ids int32 [max_tokens][k]        routed expert ids (forward only)
- *   4 w   fp32  [max_tokens][k]        renormalised weights (forward only)
- *   5 hq  int8  [max_tokens*NS][F]     SwiGLU codes, row t*NS+slot (slot k = shared)
- *   6 dh  fp32  [max_tokens*NS][F/32]  SwiGLU scales
- *   7 a   fp32  [max_tokens*NS][H]     per-slot down-projection outputs
- * with NS = k + n_shared. Only rows of tokens of the last call are defined.
+/* Read-only device view of the handle's scratch after the last forward call,
+ * for inspecting intermediate results. With C = min(max_tokens, 64) and
+ * NS = k + n_shared, `which`:
+ *   0 xq  int8  [C][H]        activation codes (CAS step 1)
+ *   1 dx  fp32  [C][H/32]     activation scales
+ *   2 gs  int16 [C][H/16]     16-group sums of xq
+ *   3 ids int32 [C][k]        routed expert ids
+ *   4 w   fp32  [C][k]        renormalised weights
+ *   5 hq  int8  [C*NS][F]     SwiGLU codes, row t*NS+slot (slot k = shared)
+ *   6 dh  fp32  [C*NS][F/32]  SwiGLU scales
+ *   7 a   fp32  [C*NS][H]     per-slot down-projection outputs
+ * Rows refer to the tokens of the last chunk of that call (a call runs in
+ * chunks of at most 64 tokens); other rows are undefined.
  * Errors: INVALID_ARG for an unknown `which`. */
 ds4moe_status ds4moe_debug_scratch(ds4moe_layer *h, int32_t which, const void **ptr_out, uint64_t *bytes_out);
 

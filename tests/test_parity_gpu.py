@@ -49,10 +49,16 @@ def run_case(ora, spec, seed, T, max_tokens=None, y_init=True):
     assert layer.device_error() == 0
     got = yd.cpu().numpy()
     k = spec.top_k
-    ids = layer.scratch("ids")[:T * k].view(T, k).cpu().numpy()
-    wts = layer.scratch("w")[:T * k].view(T, k).cpu().numpy()
-    assert np.array_equal(ids, ids_ref), "expert ids differ"
-    assert np.array_equal(wts.view(np.uint32), w_ref.view(np.uint32)), "gate weights differ"
+    # routing of every token through ds4moe_route, and the forward's own
+    # routing (scratch of its last chunk of <= 64 tokens)
+    ids, wts = layer.route(xd, td)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ids_ref), "expert ids differ"
+    assert np.array_equal(wts.cpu().numpy().view(np.uint32), w_ref.view(np.uint32)), "gate weights differ"
+    if T <= 64:
+        fids = layer.scratch("ids")[:T * k].view(T, k).cpu().numpy()
+        fw = layer.scratch("w")[:T * k].view(T, k).cpu().numpy()
+        assert np.array_equal(fids, ids_ref) and np.array_equal(fw.view(np.uint32), w_ref.view(np.uint32))
     assert within_tolerance(got, ref)
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), \
         f"not bit-exact: {np.count_nonzero(got != ref)} of {got.size} differ"
