@@ -8,7 +8,8 @@ if the compiled library cannot be loaded, importing the binding fails.
 Entry points mirror the C ABI in include/ds4moe.h:
 ``Layer(desc, weights)`` = ds4moe_create, ``Layer.route`` = ds4moe_route,
 ``Layer.forward`` = ds4moe_forward, ``Layer.forward_host`` =
-ds4moe_forward_host, ``rmsnorm`` = ds4moe_rmsnorm.
+ds4moe_forward_host, ``rmsnorm`` = ds4moe_rmsnorm, ``route_noalloc`` =
+ds4moe_route_noalloc.
 """
 from __future__ import annotations
 
@@ -64,6 +65,8 @@ def lib():
             "ds4moe_create": (i32, [ctypes.POINTER(_Desc), ctypes.POINTER(_Weights), ctypes.POINTER(vp)]),
             "ds4moe_destroy": (None, [vp]),
             "ds4moe_route": (i32, [vp, vp, vp, i32, vp, vp, vp]),
+            "ds4moe_route_noalloc": (i32, [ctypes.POINTER(_Desc), ctypes.POINTER(_Weights), vp, vp, i32, vp, vp,
+                                           vp, vp]),
             "ds4moe_forward": (i32, [vp, vp, i32, vp, vp, vp]),
             "ds4moe_forward_host": (i32, [vp, vp, i32, vp, vp, vp]),
             "ds4moe_rmsnorm": (i32, [vp, vp, i32, i32, ctypes.c_float, vp]),
@@ -234,6 +237,29 @@ def rmsnorm(x, out, eps: float = 1e-6, stream=None):
     """out = x / sqrt(mean(x^2) + eps) row-wise (ds4moe_rmsnorm); out may be x."""
     _check(lib().ds4moe_rmsnorm(_ptr(x), _ptr(out), x.shape[0], x.shape[1], eps, _stream(stream)),
            "ds4moe_rmsnorm")
+
+
+NOALLOC_SCRATCH_BYTES = 512 * 1024
+
+
+def route_noalloc(desc: LayerDesc, weights: dict, x=None, token_ids=None, ids_out=None, w_out=None,
+                  err_flags=None, stream=None, n_tok=None):
+    """Routing from the canonical router buffers in `weights` (router_w,
+    router_bias or hash_table; CUDA tensors) with no handle and no device
+    allocation by the library (ds4moe_route_noalloc). ids_out / w_out are
+    allocated here by torch when not given. Returns (ids_out, w_out)."""
+    import torch
+    n = n_tok if n_tok is not None else (x.shape[0] if x is not None else token_ids.shape[0])
+    dev = (x if x is not None else token_ids).device
+    if ids_out is None:
+        ids_out = torch.empty((n, desc.top_k), dtype=torch.int32, device=dev)
+    if w_out is None:
+        w_out = torch.empty((n, desc.top_k), dtype=torch.float32, device=dev)
+    w = _Weights(*[_ptr(weights.get(name)) for name, _ in _Weights._fields_])
+    _check(lib().ds4moe_route_noalloc(ctypes.byref(desc.c()), ctypes.byref(w), _ptr(x), _ptr(token_ids), n,
+                                      _ptr(ids_out), _ptr(w_out), _ptr(err_flags), _stream(stream)),
+           "ds4moe_route_noalloc")
+    return ids_out, w_out
 
 
 def status_string(status: int) -> str:

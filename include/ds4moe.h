@@ -132,6 +132,44 @@ void ds4moe_destroy(ds4moe_layer *h);
 ds4moe_status ds4moe_route(ds4moe_layer *h, const float *x, const int32_t *token_ids, int32_t n_tok,
                            int32_t *ids_out, float *w_out, void *stream);
 
+/* Routing without a handle and without any device allocation.
+ * No counterpart in the pages: they describe no allocation-free entry point.
+ * It exists for callers that cannot call cudaMalloc: plug-ins and embedders
+ * whose host application owns all device memory (for example a serving engine
+ * that reserves the GPU's memory up front and accounts for every byte, so an
+ * allocation behind its back fails or breaks its budget), and code paths that
+ * cannot afford cudaMalloc's implicit device-wide synchronisation.
+ *
+ * Computes exactly what ds4moe_route computes (same ids, same weight bits)
+ * from the caller's canonical buffers, read on every call:
+ *   desc: hidden, n_experts, top_k, route, vocab, router_fmt and route_scale
+ *         are used (same rules as ds4moe_create); the other fields are ignored.
+ *   w:    router_w + router_bias (learned) or hash_table (hash), device memory;
+ *         other members are ignored.
+ *   x, token_ids, ids_out, w_out: as for ds4moe_route.
+ *   err_flags: device uint32, may be NULL; DS4MOE_DEVERR_* bits are OR-ed in
+ *         (a hash-table entry outside [0, n_experts) gives id -1, weight 0
+ *         and DS4MOE_DEVERR_INTERNAL).
+ * Scratch: one fixed device array of DS4MOE_NOALLOC_SCRATCH_BYTES (512 KiB)
+ * per device, built into the library. Learned routing needs
+ * n_tok * 32 * E_pad bytes of it (E_pad = n_experts rounded up to 32): at most
+ * 64 tokens per call for 256 experts. A larger n_tok returns
+ * DS4MOE_ERR_UNSUPPORTED and enqueues nothing. Hash routing uses no scratch.
+ * Nothing in the array has to start at zero; a call reads only what it wrote.
+ * Every call on a device shares the one array, so calls whose work can
+ * overlap on the GPU (issued on different streams without an order between
+ * them, or from several host threads) race and give wrong results: issue
+ * them on one stream, or order them.
+ * The first call on each device, with that device current, looks up the
+ * array's address (cudaGetSymbolAddress) and sets a kernel attribute; make
+ * that first call before any stream capture.
+ * Errors: INVALID_ARG (desc, pointers, n_tok < 0), UNSUPPORTED (scratch too
+ * small for n_tok), CUDA. */
+#define DS4MOE_NOALLOC_SCRATCH_BYTES (512u * 1024u)
+ds4moe_status ds4moe_route_noalloc(const ds4moe_layer_desc *desc, const ds4moe_weights *w, const float *x,
+                                   const int32_t *token_ids, int32_t n_tok, int32_t *ids_out, float *w_out,
+                                   uint32_t *err_flags, void *stream);
+
 /* The whole layer: y[t] += MoE(x[t]) for t < n_tok, i.e.
  *   y[t] += sum_j w_j * down_j(hq_j) + shared(x[t])
  * with hq_j the int8-requantised silu(gate_j x) * (up_j x).

@@ -87,3 +87,20 @@ def test_cuda_sources_compile_for_sm103a():
     import deepseek_v4_flash_gb300 as ds4
     with open(ds4.LIB_PATH, "rb") as f:
         assert f.read(4) == b"\x7fELF"
+
+
+def test_route_noalloc_checks_on_the_host(L):
+    """ds4moe_route_noalloc rejects bad descriptors, n_tok < 0 and more
+    tokens than its fixed scratch holds before any CUDA call."""
+    import deepseek_v4_flash_gb300 as ds4
+    w = ds4._Weights()
+    f = L.ds4moe_route_noalloc
+    assert f(None, ctypes.byref(w), None, None, 1, None, None, None, None) == 1
+    assert f(ctypes.byref(_desc(hidden=255).c()), ctypes.byref(w), None, None, 1, None, None, None, None) == 1
+    assert f(ctypes.byref(_desc(top_k=17).c()), ctypes.byref(w), None, None, 1, None, None, None, None) == 1
+    assert f(ctypes.byref(_desc().c()), ctypes.byref(w), None, None, -1, None, None, None, None) == 1
+    assert f(ctypes.byref(_desc().c()), ctypes.byref(w), None, None, 0, None, None, None, None) == 0
+    big = _desc(hidden=4096, n_experts=256, top_k=6, router_fmt=1).c()
+    # 65 tokens * 8 segments * 256 experts * 4 bytes > 512 KiB
+    assert f(ctypes.byref(big), ctypes.byref(w), None, None, 65, None, None, None, None) == 2
+    assert f(ctypes.byref(big), ctypes.byref(w), None, None, 64, None, None, None, None) == 1  # null pointers
