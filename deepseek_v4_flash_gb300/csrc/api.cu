@@ -9,6 +9,7 @@
 
 #include <new>
 
+#include "bucket.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -154,11 +155,9 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   if ((st = alloc(h, &h->xq, (size_t)Tc * H)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->dx, (size_t)Tc * (H / 32) * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->gs, (size_t)Tc * (H / 16) * 2)) != DS4MOE_OK) return st;
-  if (d.route == DS4MOE_ROUTE_LEARNED)
-    if ((st = alloc(h, &h->rpart, (size_t)Tc * ROUTER_SEGS * h->E_pad * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->ids, (size_t)Tc * k * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->wts, (size_t)Tc * k * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->bucket, bucket_ints(E, (int)Tc, (int)NS) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->bucket, (size_t)bucket_table_ints(h->A_max, (int)Tc, (int)NS) * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->hq, (size_t)(Tc * NS) * F)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->dh, (size_t)(Tc * NS) * (F / 32) * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->gsh, (size_t)(Tc * NS) * (F / 16) * 2)) != DS4MOE_OK) return st;
@@ -178,6 +177,8 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
     if ((st = alloc(h, &h->sticket_dn, n_std)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->cticket, n_ct)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->queue, n_q)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->rticket, 16)) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->rticket, 0, 16, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->hticket, 0, n_ht, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->sticket, 0, n_st, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->sticket_dn, 0, n_std, s))) != DS4MOE_OK) return st;
@@ -293,11 +294,9 @@ ds4moe_status ds4moe_route(ds4moe_layer *h, const float *x, const int32_t *token
   cudaError_t e = cudaSuccess;
   for (int c0 = 0; c0 < n_tok && e == cudaSuccess; c0 += h->Tc) {
     const int nc = n_tok - c0 < h->Tc ? n_tok - c0 : h->Tc;
-    if (!hash) e = launch_dec_route(h, x + (size_t)c0 * H, nullptr, nc, s);
-    if (e == cudaSuccess)
-      e = launch_route_tokens(h, hash ? token_ids + c0 : nullptr, nc, ids_out + (size_t)c0 * k,
-                              w_out + (size_t)c0 * k, s);
-    h->launches += hash ? 1 : 2;
+    e = launch_dec_route(h, hash ? nullptr : x + (size_t)c0 * H, hash ? token_ids + c0 : nullptr, nc,
+                         ids_out + (size_t)c0 * k, w_out + (size_t)c0 * k, false, s);
+    h->launches += 1;
   }
   return cuda_status(e);
 }
@@ -324,7 +323,7 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
     float *yc = y + (size_t)c0 * H;
     mark(0);
     mark(1);
-    e = launch_dec_route(h, xc, tc, nc, s);
+    e = launch_dec_route(h, xc, tc, nc, h->ids, h->wts, true, s);
     mark(2);
     mark(3);
     if (e == cudaSuccess) e = launch_dec_expert(h, tc, nc, yc, 0, s);

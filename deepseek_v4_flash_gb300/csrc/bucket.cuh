@@ -1,97 +1,81 @@
-// bucket.cuh -- per-expert bucketing of the routed (token, slot) pairs, done
-// by one thread block: counts, offsets, the (token, slot) list of every
-// expert, and the active-expert list (shared expert first, then the routed
-// experts with at least one token in ascending id). The order of pairs
-// within an expert's list does not affect any result: every (token, slot) is
-// computed on its own.
+// bucket.cuh -- per-expert bucketing of the routed (token, slot) pairs of one
+// call, done by one thread block, into a compact table:
+//
+//   int32 header[4]    n_active, n_pairs (routed pairs with a valid id), 0, 0
+//   int4  act[A_cap]   {expert, pair count, offset into list, 0}: the shared
+//                      expert first (expert = E, all tokens), then the routed
+//                      experts with at least one pair in ascending id
+//   int32 list[T*NS]   slot rows t*NS + j, grouped by expert in act order;
+//                      within an expert in (token, slot) order
+//
+// Every position is a rank count (how many pairs sort before this one), so
+// the table is the same on every run. The order of pairs within an expert
+// does not affect any result: every (token, slot) is computed on its own.
 #pragma once
 #include "common.cuh"
 
 namespace ds4 {
 
-// Block-wide exclusive scan of v (one value per thread, blockDim.x <= 1024).
-// Returns the exclusive prefix; *total receives the sum. Uses sh[32].
-__device__ __forceinline__ int block_exscan(int v, int *sh, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sh[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? sh[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    sh[lane] = w;  // inclusive prefix over warps
-  }
-  __syncthreads();
-  const int before = (warp ? sh[warp - 1] : 0) + x - v;
-  *total = sh[nw - 1];
-  __syncthreads();
-  return before;
-}
+constexpr int BKT_HDR = 4;  // header ints before the act table
 
-// Shared-memory need of bucket_block, in ints.
-__host__ __device__ constexpr int bucket_smem_ints(int E) { return 2 * (E + 2) + 32; }
+__host__ __device__ constexpr int bucket_table_ints(int A_cap, int T, int NS) { return BKT_HDR + 4 * A_cap + T * NS; }
 
-// ids: [T][k] routed expert ids (-1 = none), written before the call (shared
-// or global memory). Writes cnt[0..E] (cnt[E] = T if
-// a shared expert exists), off[0..E+1], active[], *n_active and list[].
-// Must be called by every thread of the block.
-__device__ void bucket_block(const int32_t *ids, int T, int E, int k, int NS, int n_shared, int32_t *sm,
-                             int32_t *cnt_g, int32_t *off_g, int32_t *act_g, int32_t *nact_g, int32_t *list,
-                             uint32_t *err) {
-  int32_t *cnt = sm, *cur = sm + (E + 2), *scan = sm + 2 * (E + 2);
-  const int tid = threadIdx.x, nth = blockDim.x;
-  for (int e = tid; e < E + 2; e += nth) cnt[e] = 0, cur[e] = 0;
+// Shared-memory ints bucket_rank needs for n = T*k pairs.
+__host__ __device__ constexpr int bucket_rank_smem_ints(int n) { return 3 * n + 4; }
+
+// ids: [T][k] routed expert ids in shared memory (-1 = none; >= E raises
+// DS4MOE_DEVERR_INTERNAL and is dropped). sm: bucket_rank_smem_ints(T*k)
+// ints. out: the table above in global memory, A_cap >= its rows. All
+// threads of the block call it.
+__device__ inline void bucket_rank(const int32_t *ids, int T, int E, int k, int NS, int n_shared, int32_t *sm,
+                                   int32_t *out, int A_cap, uint32_t *err) {
+  const int n = T * k, tid = threadIdx.x, nth = blockDim.x;
+  int32_t *rank = sm, *first = sm + n, *count = sm + 2 * n, *tot = sm + 3 * n;  // tot: pairs, experts
+  if (tid < 2) tot[tid] = 0;
   __syncthreads();
-  const int n = T * k;
+  int4 *act = (int4 *)(out + BKT_HDR);
+  int32_t *list = out + BKT_HDR + 4 * A_cap;
   for (int i = tid; i < n; i += nth) {
     const int e = ids[i];
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else if (e >= E) raise_flag(err, DS4MOE_DEVERR_INTERNAL);
+    const bool ok = e >= 0 && e < E;
+    if (e >= E) raise_flag(err, DS4MOE_DEVERR_INTERNAL);
+    int r = 0, c = 0, f = 1;
+    if (ok) {
+      for (int j = 0; j < n; j++) {
+        const int ej = ids[j];
+        if (ej < 0 || ej >= E) continue;
+        r += (ej < e || (ej == e && j < i)) ? 1 : 0;
+        c += ej == e ? 1 : 0;
+        f &= (ej == e && j < i) ? 0 : 1;
+      }
+      list[r] = (i / k) * NS + (i % k);
+      atomicAdd(&tot[0], 1);
+      if (f) atomicAdd(&tot[1], 1);
+    }
+    rank[i] = r;
+    first[i] = ok && f;
+    count[i] = c;
   }
-  if (tid == 0) cnt[E] = n_shared ? T : 0;
   __syncthreads();
-  // Each thread owns a contiguous run of experts [e0, e1) of E+1 entries.
-  const int per = (E + 1 + nth - 1) / nth;
-  const int e0 = min(tid * per, E + 1), e1 = min(e0 + per, E + 1);
-  int c_sum = 0, a_sum = 0;
-  for (int e = e0; e < e1; e++) {
-    c_sum += cnt[e];
-    if (e < E && cnt[e] > 0) a_sum++;
+  const int n_pairs = tot[0], n_exp = tot[1];
+  for (int i = tid; i < n; i += nth) {
+    if (!first[i]) continue;
+    const int e = ids[i];
+    int d = 0;  // distinct experts below e
+    for (int j = 0; j < n; j++) d += (first[j] && ids[j] < e) ? 1 : 0;
+    act[n_shared + d] = make_int4(e, count[i], rank[i], 0);
   }
-  int c_tot, a_tot;
-  int c_pre = block_exscan(c_sum, scan, &c_tot);
-  int a_pre = block_exscan(a_sum, scan, &a_tot);
-  for (int e = e0; e < e1; e++) {
-    cur[e] = c_pre;  // temporarily: offset of e
-    off_g[e] = c_pre;
-    cnt_g[e] = cnt[e];
-    if (e < E && cnt[e] > 0) act_g[n_shared + a_pre++] = e;
-    c_pre += cnt[e];
+  if (n_shared) {
+    for (int t = tid; t < T; t += nth) list[n_pairs + t] = t * NS + k;
+    if (tid == 0) act[0] = make_int4(E, T, n_pairs, 0);
   }
   if (tid == 0) {
-    off_g[E + 1] = c_tot;
-    if (n_shared) act_g[0] = E;
-    *nact_g = a_tot + n_shared;
+    out[0] = n_exp + n_shared;
+    out[1] = n_pairs;
+    out[2] = 0;
+    out[3] = 0;
   }
   __syncthreads();
-  for (int i = tid; i < n; i += nth) {
-    const int e = ids[i];
-    if (e >= 0 && e < E) {
-      const int p = atomicAdd(&cur[e], 1);
-      list[p] = (i / k) * NS + (i % k);
-    }
-  }
-  if (n_shared)
-    for (int t = tid; t < T; t += nth) list[cur[E] + t] = t * NS + k;
 }
 
 }  // namespace ds4

@@ -1,14 +1,13 @@
 // decode.cu -- the decode-batch path (n_tok <= DEC_MAX_T): three kernels
 // chained with programmatic dependent launch (PDL):
 //
-//   K1 k_router_dec : int8 quantisation of x and the router GEMV segment sums
-//                     (hash routing: quantisation only).
-//   K2 k_expert_dec (gate/up): every CTA first finishes the routing on its
-//                     own -- logits, sigmoid, bias top-k, renormalisation (or
-//                     the hash lookup) and the per-expert bucketing, all
-//                     deterministic, so every CTA gets the same result and
-//                     CTA 0 publishes it -- then gate/up with in-register
-//                     SwiGLU and the int8 requant of h.
+//   K1 k_router_dec : int8 quantisation of x, the router GEMV segment sums,
+//                     then (last block of each token) the token's routing --
+//                     logits, sigmoid, bias top-k and renormalisation, or the
+//                     hash lookup -- and (block of the last routed token) the
+//                     per-expert bucketing of the call.
+//   K2 k_expert_dec (gate/up): gate/up with in-register SwiGLU and the int8
+//                     requant of h.
 //   K3 k_expert_dec (down): down of every item; the last writer of each
 //                     (token, 32 output rows) adds the fixed-order combine
 //                     into y.
@@ -19,7 +18,7 @@
 // async copies into a shared-memory ring, and crosses item boundaries without
 // draining the ring. Items of the shared expert are claimed and their weights
 // requested before griddepcontrol.wait, so they stream while the previous
-// kernel finishes and while the routing runs. Activations are staged in
+// kernel (the router, or gate/up) finishes. Activations are staged in
 // shared memory when they fit. Queues and tickets reset themselves, so no
 // per-call memset is needed and the whole forward can be captured in a CUDA
 // graph.
@@ -31,6 +30,7 @@
 #include "bucket.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "route.cuh"
 #include "tiles.cuh"
 
 namespace ds4 {
@@ -41,113 +41,215 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 
 // ===========================================================================
-// K1: quantisation + router segment sums.
+// K1: quantisation, router segment sums, routing and bucketing.
+//
+// grid (ROUTER_SEGS, T), clusters of ROUTER_SEGS blocks: the cluster of
+// token t has one block per K segment. Block seg quantises the token's
+// 32-blocks of its segment (and publishes them), then sums every router row
+// over the segment (warp w: row groups w, w + RC_WARPS, ...; lane = row) into
+// its shared memory. After a cluster barrier, block 0 of the cluster adds the
+// eight segment sums of each row in segment order, reading the other blocks'
+// shared memory, and routes the token with all its threads (route.cuh; hash
+// routing: the table lookup). When bucketing is asked for, the block that
+// routed the call's last token (a self-resetting ticket; none for one token)
+// buckets the call (bucket.cuh).
 
-constexpr int RD_RT = 8;     // tokens per token tile
-constexpr int RD_WARPS = 4;  // warps per CTA: one router row group each
+constexpr int RC_WARPS = 8;   // warps per block
+constexpr int RC_HDR = 128;   // shared memory header: ticket flag, mbarriers
+constexpr int RC_MAX_E = 1024;
 
 struct RouteDecArgs {
   const float *x;
-  int T, H, E, E_pad, learned, q8;
-  const uint8_t *W;  // router (RQ8 or F32 [E][H])
+  int T, H, E, E_pad, k, NS, n_shared, learned, q8, vocab, A_cap;
+  float scale;
+  const uint8_t *W;     // router (RQ8 or F32 [E][H])
+  const float *bias;
+  const int32_t *hash, *tok;
   int8_t *xq;
   float *dx;
   int16_t *gs;
-  float *rpart;      // [T][8][E_pad]
+  int32_t *ids;         // [T][k] routing outputs
+  float *w;
+  int32_t *rticket;     // the call's ticket (self-resetting)
+  int32_t *bucket;      // bucket table (null: no bucketing)
   uint32_t *err;
 };
 
-// Quantise block b (32 values) of token t: lane = element.
-__device__ __forceinline__ void quant_block(const float *x, int H, int t, int b, int lane, int8_t *xq_s,
-                                            float *dx_s, int8_t *xq_g, float *dx_g, int16_t *gs_g, uint32_t *err) {
-  const float v = __ldg(x + (size_t)t * H + 32 * b + lane);
+// Layout after the header: lgp [E_pad] f32 (this segment's row sums), dx_s
+// [per] f32, xq_s [per*32] int8, then the 128-aligned work area (router
+// tiles; afterwards the routing and bucketing scratch).
+__host__ __device__ constexpr int rc_dx_off(int E_pad) { return RC_HDR + 4 * E_pad; }
+__host__ __device__ constexpr int rc_xq_off(int E_pad, int per) { return rc_dx_off(E_pad) + ((4 * per + 15) & ~15); }
+__host__ __device__ constexpr int rc_work_off(int E_pad, int per) {
+  return (rc_xq_off(E_pad, per) + 32 * per + 127) & ~127;
+}
+
+// CAS step 1 for one value per lane of block b of token t, already loaded.
+__device__ __forceinline__ void quant_value(float v, int H, int t, int b, int lane, int8_t *xq_s, float *dx_s,
+                                            int8_t *xq_g, float *dx_g, int16_t *gs_g, uint32_t *err) {
   if (__any_sync(0xffffffffu, !isfinite(v)) && lane == 0) raise_flag(err, DS4MOE_DEVERR_NONFINITE);
   const float amax = warp_max(fabsf(v));
   const float d = __fdiv_rn(amax, 127.0f);
   const int q = cas_code(v, d);
-  if (xq_s) xq_s[lane] = (int8_t)q;
-  if (dx_s && lane == 0) *dx_s = d;
-  if (xq_g) {
-    const int s = half_warp_sum(q);
-    xq_g[(size_t)t * H + 32 * b + lane] = (int8_t)q;
-    if (lane == 0) dx_g[(size_t)t * (H >> 5) + b] = d;
-    if ((lane & 15) == 0) gs_g[(size_t)t * (H >> 4) + 2 * b + (lane >> 4)] = (int16_t)s;
-  }
+  const int s = half_warp_sum(q);
+  xq_s[lane] = (int8_t)q;
+  if (lane == 0) *dx_s = d;
+  xq_g[(size_t)t * H + 32 * b + lane] = (int8_t)q;
+  if (lane == 0) dx_g[(size_t)t * (H >> 5) + b] = d;
+  if ((lane & 15) == 0) gs_g[(size_t)t * (H >> 4) + 2 * b + (lane >> 4)] = (int16_t)s;
 }
 
-// grid (ceil(E_pad/32 / RD_WARPS), ROUTER_SEGS, n_tiles); warp w: router row
-// group blockIdx.x*RD_WARPS + w, K segment blockIdx.y, tokens of tile z.
-__global__ void __launch_bounds__(RD_WARPS * 32) k_router_dec(RouteDecArgs a) {
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// A float in the shared memory of block `rank` of this cluster.
+__device__ __forceinline__ float ld_cluster_f32(const float *p, int rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+// One arrival on a block-level ticket (thread 0); true in every thread of
+// the block that completes it. The acquire-release atomic orders the block's
+// earlier global writes (gathered by the barrier) before the completer's
+// later reads; the completer resets the ticket.
+__device__ __forceinline__ bool block_ticket_last(int32_t *tk, int expect, int *s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(tk) : "memory");
+    const int last = old == expect - 1;
+    if (last) *tk = 0;
+    *s_flag = last;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+__global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS * 32, 1)
+    k_router_dec(RouteDecArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = blockIdx.y, t0 = blockIdx.z * RD_RT, nt = min(RD_RT, a.T - t0);
+  const int seg = blockIdx.x, t = blockIdx.y;
   const int nb = a.H >> 5, per = nb / ROUTER_SEGS, b0 = seg * per;
-  pdl_launch_dependents();
   const int c0 = b0 >> 1, c1 = (b0 + per + 1) >> 1;  // RQ8 2-block chunks covering the segment
   const int seg_bytes = a.q8 ? (c1 - c0) * RQ8_TILE : 0;
-  int8_t *xq_s = (int8_t *)(smem + RD_WARPS * seg_bytes);
-  float *dx_s = (float *)(xq_s + RD_RT * per * 32);
-  uint64_t *bars = (uint64_t *)(dx_s + RD_RT * per + 2);
-  const int rg = blockIdx.x * RD_WARPS + warp;
-  const bool row_ok = a.learned && rg < (a.E_pad >> 5);
+  const int nrg = a.learned ? (a.E_pad >> 5) : 0;
+  int *s_flag = (int *)smem;
+  uint64_t *bars = (uint64_t *)(smem + 64);
+  float *lgp = (float *)(smem + RC_HDR);
+  float *dx_s = (float *)(smem + rc_dx_off(a.E_pad));
+  int8_t *xq_s = (int8_t *)(smem + rc_xq_off(a.E_pad, per));
+  uint8_t *work = smem + rc_work_off(a.E_pad, per);
+  pdl_launch_dependents();
   const uint32_t bar = smem_u32(&bars[warp]);
+  const uint32_t wbuf = smem_u32(work + warp * seg_bytes);
+  const size_t rg_stride = (size_t)(a.H / RQ8_KSTEP) * RQ8_TILE;
   if (a.q8 && lane == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    if (row_ok) {
+    if (warp < nrg) {
       mbar_arrive_expect_tx(bar, seg_bytes);
-      bulk_g2s(smem_u32(smem + warp * seg_bytes), a.W + ((size_t)rg * (a.H / RQ8_KSTEP) + c0) * RQ8_TILE,
-               seg_bytes, bar);
+      bulk_g2s(wbuf, a.W + (size_t)warp * rg_stride + (size_t)c0 * RQ8_TILE, seg_bytes, bar);
     }
   }
-  // quantise the segment's blocks of the tile's tokens; CTAs with
-  // blockIdx.x == 0 publish the codes for the expert kernels
-  const bool publish = blockIdx.x == 0;
-  for (int p = warp; p < nt * per; p += RD_WARPS) {
-    const int i = p / per, b = b0 + p % per;
-    quant_block(a.x, a.H, t0 + i, b, lane, xq_s + i * per * 32 + (b - b0) * 32, dx_s + i * per + (b - b0),
-                publish ? a.xq : nullptr, a.dx, a.gs, a.err);
+  // the routing block's bias values, requested early
+  float bias_r[RC_MAX_E / (RC_WARPS * 32)];
+#pragma unroll
+  for (int i = 0; i < RC_MAX_E / (RC_WARPS * 32); i++) {
+    const int e = threadIdx.x + i * RC_WARPS * 32;
+    bias_r[i] = (seg == 0 && a.learned && e < a.E) ? __ldg(a.bias + e) : 0.0f;
   }
-  __syncthreads();
-  if (!row_ok) return;
-  float acc[RD_RT];
+  // quantise the segment's blocks (warp w: blocks b0 + w + RC_WARPS*j), all
+  // loads first
+  if (a.x) {
+    constexpr int QB = 4;
+    for (int bb = warp; bb < per; bb += RC_WARPS * QB) {
+      float v[QB];
 #pragma unroll
-  for (int i = 0; i < RD_RT; i++) acc[i] = 0.0f;
-  const int r = 32 * rg + lane;
-  if (a.q8) {
-    if (!mbar_wait_bounded(bar, 0)) {
-      if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
-      return;
-    }
-    const uint32_t wt = smem_u32(smem + warp * seg_bytes);
-    for (int b = b0; b < b0 + per; b++) {
-      const uint32_t tile = wt + ((b >> 1) - c0) * RQ8_TILE;
-      const uint32_t dd = ld_shared_u32(tile + 4 * lane);
-      const float d = half_bits_to_float((b & 1) ? dd >> 16 : dd);
-      const uint4 w0 = ld_shared_v4(tile + RQ8_Q + 512 * (2 * (b & 1)) + 16 * lane);
-      const uint4 w1 = ld_shared_v4(tile + RQ8_Q + 512 * (2 * (b & 1) + 1) + 16 * lane);
+      for (int j = 0; j < QB; j++) {
+        const int b = bb + j * RC_WARPS;
+        v[j] = b < per ? __ldg(a.x + (size_t)t * a.H + 32 * (b0 + b) + lane) : 0.0f;
+      }
 #pragma unroll
-      for (int i = 0; i < RD_RT; i++) {
-        if (i < nt) {
-          const uint4 *xv = (const uint4 *)(xq_s + i * per * 32 + (b - b0) * 32);
-          const int I = dot16(w1, xv[1], dot16(w0, xv[0], 0));
-          acc[i] = __fadd_rn(acc[i], q8_term(d, dx_s[i * per + (b - b0)], I));
-        }
+      for (int j = 0; j < QB; j++) {
+        const int b = bb + j * RC_WARPS;
+        if (b < per)
+          quant_value(v[j], a.H, t, b0 + b, lane, xq_s + 32 * b, dx_s + b, a.xq, a.dx, a.gs, a.err);
       }
     }
-  } else if (r < a.E) {  // fp32 router rows: fma chains over the segment (x unquantised)
-    const int e0 = seg * (a.H / ROUTER_SEGS), e1 = e0 + a.H / ROUTER_SEGS;
-    const float *wr = (const float *)a.W + (size_t)r * a.H;
-    for (int i = 0; i < nt; i++) {
-      const float *xv = a.x + (size_t)(t0 + i) * a.H;
-      float s = 0.0f;
-      for (int j = e0; j < e1; j++) s = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), s);
-      acc[i] = s;
+  }
+  __syncthreads();
+  // segment sums of router rows 32*rg + lane
+  for (int rg = warp, round = 0; rg < nrg; rg += RC_WARPS, round++) {
+    float acc = 0.0f;
+    const int r = 32 * rg + lane;
+    if (a.q8) {
+      if (round > 0 && lane == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, seg_bytes);
+        bulk_g2s(wbuf, a.W + (size_t)rg * rg_stride + (size_t)c0 * RQ8_TILE, seg_bytes, bar);
+      }
+      __syncwarp();
+      if (!mbar_wait_bounded(bar, round & 1)) {
+        if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
+        break;
+      }
+      for (int b = b0; b < b0 + per; b++) {
+        const uint32_t tile = wbuf + ((b >> 1) - c0) * RQ8_TILE;
+        const uint32_t dd = ld_shared_u32(tile + 4 * lane);
+        const float d = half_bits_to_float((b & 1) ? dd >> 16 : dd);
+        const uint4 w0 = ld_shared_v4(tile + RQ8_Q + 512 * (2 * (b & 1)) + 16 * lane);
+        const uint4 w1 = ld_shared_v4(tile + RQ8_Q + 512 * (2 * (b & 1) + 1) + 16 * lane);
+        const uint4 *xv = (const uint4 *)(xq_s + (b - b0) * 32);
+        const int I = dot16(w1, xv[1], dot16(w0, xv[0], 0));
+        acc = __fadd_rn(acc, q8_term(d, dx_s[b - b0], I));
+      }
+    } else if (r < a.E) {  // fp32 router rows: fma chain over the segment (x unquantised)
+      const int j0 = seg * (a.H / ROUTER_SEGS), j1 = j0 + a.H / ROUTER_SEGS;
+      const float *wr = (const float *)a.W + (size_t)r * a.H;
+      const float *xv = a.x + (size_t)t * a.H;
+      for (int j = j0; j < j1; j++) acc = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), acc);
+    }
+    lgp[r] = acc;
+    __syncwarp();  // every lane is done with the tiles before the next copy
+  }
+  cluster_sync_all();
+  // ---- routing of token t by block 0 of its cluster
+  if (seg == 0) {
+    if (a.learned) {
+      const RouteScratch rs = route_scratch(work, a.E_pad, a.k);
+#pragma unroll
+      for (int i = 0; i < RC_MAX_E / (RC_WARPS * 32); i++) {
+        const int e = threadIdx.x + i * RC_WARPS * 32;
+        if (e < a.E_pad) {
+          float lg = 0.0f;
+          if (e < a.E)
+            for (int g = 0; g < ROUTER_SEGS; g++) lg = __fadd_rn(lg, ld_cluster_f32(lgp + e, g));
+          route_score(rs, e, a.E, lg, bias_r[i]);
+        }
+      }
+      route_select(rs, a.E_pad, a.k, a.scale, a.ids + (size_t)t * a.k, a.w + (size_t)t * a.k);
+    } else if (threadIdx.x < a.k) {
+      const int v = __ldg(a.tok + t);
+      const bool okv = v >= 0 && v < a.vocab;
+      if (!okv && threadIdx.x == 0) raise_flag(a.err, DS4MOE_DEVERR_TOKEN_ID);
+      a.ids[(size_t)t * a.k + threadIdx.x] = okv ? __ldg(a.hash + (size_t)v * a.k + threadIdx.x) : -1;
+      a.w[(size_t)t * a.k + threadIdx.x] = okv ? __fmul_rn(__fdiv_rn(1.0f, (float)a.k), a.scale) : 0.0f;
     }
   }
-#pragma unroll
-  for (int i = 0; i < RD_RT; i++)
-    if (i < nt) a.rpart[((size_t)(t0 + i) * ROUTER_SEGS + seg) * a.E_pad + r] = acc[i];
+  cluster_sync_all();  // the other blocks' segment sums stay until block 0 has read them
+  if (seg != 0 || !a.bucket) return;
+  // ---- bucketing of the call by the block that routed its last token
+  if (a.T > 1 && !block_ticket_last(a.rticket, a.T, s_flag)) return;
+  __syncthreads();
+  int32_t *ids_s = (int32_t *)work;
+  for (int i = threadIdx.x; i < a.T * a.k; i += blockDim.x) ids_s[i] = __ldcg(a.ids + i);
+  __syncthreads();
+  bucket_rank(ids_s, a.T, a.E, a.k, a.NS, a.n_shared, ids_s + ((a.T * a.k + 3) & ~3), a.bucket, a.A_cap, a.err);
 }
 
 // ===========================================================================
@@ -178,16 +280,11 @@ struct DecArgs {
   const int8_t *aq;              // activation codes: xq [T][H] or hq [T*NS][F]
   const float *ad;
   const int16_t *ag;
-  // routing (gate/up kernel)
-  int route;
-  float scale;
-  int vocab;
-  const float *rpart, *bias;
-  const int32_t *hash, *tok;
-  // routing results: written by the gate/up kernel (CTA 0), read by down
+  // routing results (router kernel)
   int32_t *ids;
   float *w;
-  int32_t *cnt, *off, *active, *n_active, *list;
+  const int32_t *bucket;         // bucket table (bucket.cuh)
+  int A_cap;
   int8_t *hq;
   float *dh;
   int16_t *gsh;
@@ -204,7 +301,8 @@ struct DecArgs {
 
 // Routing view used by the streamers (shared memory).
 struct Bk {
-  const int32_t *cnt, *off, *active, *list;
+  const int4 *act;  // {expert, pairs, list offset, 0}
+  const int32_t *list;
   int n_active;
 };
 
@@ -235,7 +333,7 @@ __device__ ItemDesc item_desc(const DecArgs &a, const Bk *bk, int i) {
     d.fmt = a.sf, d.e = a.E, d.rg = i / SHARED_SEGS, d.quarter = i % SHARED_SEGS;
   } else {
     const int j = i - nsh;
-    d.fmt = a.rf, d.e = bk ? bk->active[a.n_shared + j / RG] : -1, d.rg = j % RG, d.quarter = -1;
+    d.fmt = a.rf, d.e = bk ? bk->act[a.n_shared + j / RG].x : -1, d.rg = j % RG, d.quarter = -1;
   }
   const int kb = mats * tile_bytes(d.fmt);
   const int nks_all = a.K / kstep(d.fmt);
@@ -251,7 +349,10 @@ __device__ ItemDesc item_desc(const DecArgs &a, const Bk *bk, int i) {
   else
     d.src = nullptr;
   d.n_tok = 0, d.list_off = 0;
-  if (bk && d.e >= 0) d.n_tok = bk->cnt[d.e], d.list_off = bk->off[d.e];
+  if (bk && d.e >= 0) {
+    const int4 en = bk->act[i < nsh ? 0 : a.n_shared + (i - nsh) / RG];
+    d.n_tok = en.y, d.list_off = en.z;
+  }
   return d;
 }
 
@@ -399,91 +500,9 @@ __device__ void item_epilogue(const DecArgs &a, const ItemDesc &d, int lane, con
   }
 }
 
-// Top-k routing of token t by one warp (CAS step 6): lane owns experts
-// lane + 32j. sv: per-warp scratch of 2*E_pad floats.
-__device__ void route_token_warp(const DecArgs &a, int t, int lane, float *sv, int32_t *ids, float *wts) {
-  if (a.route == DS4MOE_ROUTE_HASH) {
-    const int v = __ldg(a.tok + t);
-    const bool ok = v >= 0 && v < a.vocab;
-    if (!ok && lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TOKEN_ID);
-    const float wk = __fmul_rn(__fdiv_rn(1.0f, (float)a.k), a.scale);
-    if (lane < a.k) {
-      ids[t * a.k + lane] = ok ? __ldg(a.hash + (size_t)v * a.k + lane) : -1;
-      wts[t * a.k + lane] = ok ? wk : 0.0f;
-    }
-    return;
-  }
-  const int nj = (a.E + 31) >> 5;
-  for (int j0 = 0; j0 < nj; j0 += 8) {
-    float part[8][ROUTER_SEGS];  // issue every segment-sum load first, then add in order
-#pragma unroll
-    for (int jj = 0; jj < 8; jj++) {
-      const int e = lane + 32 * (j0 + jj);
-#pragma unroll
-      for (int g = 0; g < ROUTER_SEGS; g++)
-        part[jj][g] = e < a.E ? __ldg(a.rpart + ((size_t)t * ROUTER_SEGS + g) * a.E_pad + e) : 0.0f;
-    }
-#pragma unroll
-    for (int jj = 0; jj < 8; jj++) {
-      const int e = lane + 32 * (j0 + jj);
-      if (e < a.E) {
-        float lg = 0.0f;
-#pragma unroll
-        for (int g = 0; g < ROUTER_SEGS; g++) lg = __fadd_rn(lg, part[jj][g]);
-        const float s = cas_sigmoid(lg);
-        sv[e] = s;
-        sv[a.E_pad + e] = __fadd_rn(s, __ldg(a.bias + e));
-      }
-    }
-  }
-  __syncwarp();
-  uint32_t taken = 0;  // bit j: expert lane + 32j taken (E <= 1024)
-  int sel_mine = -1;   // lane j < k keeps the j-th selection
-  for (int j = 0; j < a.k; j++) {
-    float bk = 0.0f;
-    int bi = -1;
-    for (int jj = 0; jj < nj; jj++) {
-      const int e = lane + 32 * jj;
-      if (e >= a.E || ((taken >> jj) & 1u)) continue;
-      const float ke = sv[a.E_pad + e];
-      if (bi < 0 || ke > bk) bk = ke, bi = e;  // ascending e: ties keep the lower index
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi >= 0 && (bi < 0 || ok > bk || (ok == bk && oi < bi))) bk = ok, bi = oi;
-    }
-    if (lane == j) sel_mine = bi;
-    if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-  }
-  // renormalise: sum in selection order, then each weight
-  float sum = 0.0f;
-  for (int j = 0; j < a.k; j++) {
-    const int e = __shfl_sync(0xffffffffu, sel_mine, j);
-    sum = __fadd_rn(sum, e >= 0 ? sv[e] : 0.0f);
-  }
-  if (lane < a.k) {
-    ids[t * a.k + lane] = sel_mine;
-    wts[t * a.k + lane] = sel_mine >= 0 ? __fmul_rn(__fdiv_rn(sv[sel_mine], sum), a.scale) : 0.0f;
-  }
-}
-
-// Routing only (ds4moe_route): one warp per token writes its expert ids and
-// weights. Token tile of 8 tokens per CTA; scratch: 8 x 2*E_pad floats.
-__global__ void __launch_bounds__(256) k_route_tokens(DecArgs a, int32_t *ids, float *wts) {
-  extern __shared__ __align__(16) float rsm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= a.T) return;
-  route_token_warp(a, t, lane, rsm + warp * 2 * a.E_pad, ids, wts);
-}
-
-// Shared memory after the rings: [bucket ints][scratch]. bucket: cnt[E+1]
-// off[E+2] active[E+2] n_active[1] list[T*NS]; scratch holds the routing
-// work (ids, weights, per-warp score arrays, bucketing scratch) and then the
-// staged activations.
-__host__ __device__ inline int dec_bucket_ints(int E, int T, int NS) { return 3 * E + 6 + T * NS; }
+// Shared memory after the rings: [bucket ints][staged activations]. bucket:
+// cnt[E+1] off[E+2] active[E+2] n_active[1] list[T*NS].
+__host__ __device__ inline int dec_bucket_ints(int A_cap, int T, int NS) { return bucket_table_ints(A_cap, T, NS); }
 
 template <int TT, bool AS>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_expert_dec(DecArgs a) {
@@ -494,10 +513,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_expert_dec(DecArgs a) {
   const uint32_t bar = buf + DEC_NST * DEC_STRIDE;
   int4 *meta = (int4 *)(base + DEC_NST * DEC_STRIDE + DEC_NST * 8);  // per slot: item, pass, stage
   int32_t *bks = (int32_t *)(smem + DEC_RING);
-  const int E = a.E;
-  int32_t *s_cnt = bks, *s_off = bks + (E + 1), *s_act = s_off + (E + 2), *s_nact = s_act + (E + 2);
-  int32_t *s_list = s_nact + 1;
-  uint8_t *scratch = (uint8_t *)(bks + ((dec_bucket_ints(E, a.T, a.NS) + 31) & ~31));
+  const int nbk = dec_bucket_ints(a.A_cap, a.T, a.NS);
+  uint8_t *scratch = (uint8_t *)(bks + ((nbk + 31) & ~31));
   pdl_launch_dependents();
   if (lane == 0) {
     for (int i = 0; i < DEC_NST; i++) mbar_init(bar + 8 * i, 1);
@@ -529,26 +546,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) k_expert_dec(DecArgs a) {
   }
   pdl_wait();
 
-  // ---- routing result into shared memory
-  if (!a.down) {
-    int32_t *r_ids = (int32_t *)scratch;
-    float *r_w = (float *)(r_ids + a.T * a.k);
-    float *sv = r_w + a.T * a.k + warp * 2 * a.E_pad;
-    int32_t *bscr = (int32_t *)(r_w + a.T * a.k + DEC_WARPS * 2 * a.E_pad);
-    for (int t = warp; t < a.T; t += DEC_WARPS) route_token_warp(a, t, lane, sv, r_ids, r_w);
-    __syncthreads();
-    bucket_block(r_ids, a.T, E, a.k, a.NS, a.n_shared, bscr, s_cnt, s_off, s_act, s_nact, s_list, a.err);
-    __syncthreads();
-    if (blockIdx.x == 0) {  // publish for the down kernel and for inspection
-      for (int i = threadIdx.x; i < a.T * a.k; i += blockDim.x) a.ids[i] = r_ids[i], a.w[i] = r_w[i];
-      for (int i = threadIdx.x; i < dec_bucket_ints(E, a.T, a.NS); i += blockDim.x) a.cnt[i] = bks[i];
-    }
-  } else {
-    for (int i = threadIdx.x; i < dec_bucket_ints(E, a.T, a.NS); i += blockDim.x) bks[i] = __ldg(a.cnt + i);
-  }
+  // ---- the routing result (bucketed by the router kernel) into shared memory
+  for (int i = threadIdx.x; i < nbk; i += blockDim.x) bks[i] = __ldcg(a.bucket + i);
   __syncthreads();
   Bk bk;
-  bk.cnt = s_cnt, bk.off = s_off, bk.active = s_act, bk.list = s_list, bk.n_active = *s_nact;
+  bk.act = (const int4 *)(bks + BKT_HDR), bk.list = bks + BKT_HDR + 4 * a.A_cap, bk.n_active = bks[0];
 
   // ---- activations into shared memory (when they fit)
   const int8_t *aq = a.aq;
@@ -647,27 +649,28 @@ static cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem
 }
 
 static size_t router_dec_smem(const ds4moe_layer *h) {
-  const int H = h->d.hidden, nb = H / 32, per = nb / ROUTER_SEGS;
-  const bool q8 = h->d.route == DS4MOE_ROUTE_LEARNED && h->d.router_fmt == DS4MOE_Q8_0;
-  const size_t seg_bytes = q8 ? (size_t)((per + 1) / 2 + 1) * RQ8_TILE : 0;
-  return RD_WARPS * seg_bytes + RD_RT * per * 32 + 4 * (RD_RT * per + 2) + 8 * RD_WARPS + 64;
+  const ds4moe_layer_desc &d = h->d;
+  const int H = d.hidden, nb = H / 32, per = nb / ROUTER_SEGS;
+  const bool q8 = d.route == DS4MOE_ROUTE_LEARNED && d.router_fmt == DS4MOE_Q8_0;
+  size_t work = q8 ? (size_t)RC_WARPS * ((per + 1) / 2 + 1) * RQ8_TILE : 0;
+  const size_t route = route_block_smem(h->E_pad, d.top_k);
+  const int n = h->Tc * d.top_k;
+  const size_t bucket = (size_t)(((n + 3) & ~3) + bucket_rank_smem_ints(n)) * 4;
+  if (route > work) work = route;
+  if (bucket > work) work = bucket;
+  return rc_work_off(h->E_pad, per) + work;
 }
 
 // Shared memory of the streamer kernel for n_tok tokens; act: with staged
 // activations.
 static size_t expert_dec_smem(const ds4moe_layer *h, int T, bool down, bool act) {
   const ds4moe_layer_desc &d = h->d;
-  const size_t bucket = (size_t)((dec_bucket_ints(d.n_experts, T, h->NS) + 31) & ~31) * 4;
+  const size_t bucket = (size_t)((dec_bucket_ints(h->A_max, T, h->NS) + 31) & ~31) * 4;
   size_t scratch = 0;
-  if (!down) {
-    scratch = (size_t)T * d.top_k * 8 + (size_t)DEC_WARPS * 2 * h->E_pad * 4 +
-              (size_t)bucket_smem_ints(d.n_experts) * 4 + 64;
-  }
   if (act) {
     const size_t rows = down ? (size_t)T * h->NS : (size_t)T;
     const size_t K = down ? d.ffn : d.hidden;
-    const size_t need = rows * K + rows * (K / 32) * 4 + rows * (K / 16) * 2;
-    if (need > scratch) scratch = need;
+    scratch = rows * K + rows * (K / 32) * 4 + rows * (K / 16) * 2;
   }
   return DEC_RING + bucket + scratch;
 }
@@ -681,19 +684,21 @@ size_t route_dec_smem(const ds4moe_layer *h) {
   return m;
 }
 
-cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, cudaStream_t s) {
-  (void)tok;
+cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
+                             float *w, bool bucket, cudaStream_t s) {
   const ds4moe_layer_desc &d = h->d;
-  RouteDecArgs r;
-  r.x = x, r.T = T, r.H = d.hidden, r.E = d.n_experts, r.E_pad = h->E_pad;
+  RouteDecArgs r = {};
+  r.x = x, r.T = T, r.H = d.hidden, r.E = d.n_experts, r.E_pad = h->E_pad, r.k = d.top_k, r.NS = h->NS;
+  r.n_shared = d.n_shared, r.vocab = d.vocab, r.scale = d.route_scale, r.A_cap = h->A_max;
   r.learned = d.route == DS4MOE_ROUTE_LEARNED;
   r.q8 = r.learned && d.router_fmt == DS4MOE_Q8_0;
-  r.W = h->router, r.xq = h->xq, r.dx = h->dx, r.gs = h->gs, r.rpart = h->rpart, r.err = h->err;
-  const int n_tiles = (T + RD_RT - 1) / RD_RT;
-  const int gx = r.learned ? (h->E_pad / 32 + RD_WARPS - 1) / RD_WARPS : 1;
+  r.W = h->router, r.bias = h->bias, r.hash = h->hash, r.tok = tok;
+  r.xq = h->xq, r.dx = h->dx, r.gs = h->gs, r.err = h->err;
+  r.ids = ids, r.w = w, r.rticket = h->rticket;
+  r.bucket = bucket ? h->bucket : nullptr;
   void *args[] = {&r};
-  return launch_pdl((const void *)k_router_dec, dim3(gx, ROUTER_SEGS, n_tiles), dim3(RD_WARPS * 32),
-                    router_dec_smem(h), s, args, false);
+  return launch_pdl((const void *)k_router_dec, dim3(ROUTER_SEGS, T), dim3(RC_WARPS * 32), router_dec_smem(h), s,
+                    args, false);
 }
 
 template <bool AS>
@@ -706,14 +711,12 @@ static const void *expert_fn(int T) {
 cudaError_t launch_dec_expert(const ds4moe_layer *h, const int32_t *tok, int T, float *y, int down,
                               cudaStream_t s) {
   const ds4moe_layer_desc &d = h->d;
-  Bucket b = bucket_view(h);
   DecArgs a;
   a.H = d.hidden, a.F = d.ffn, a.E = d.n_experts, a.E_pad = h->E_pad, a.k = d.top_k, a.NS = h->NS;
   a.n_shared = d.n_shared, a.T = T;
   a.rf = d.routed_fmt, a.sf = d.n_shared ? d.shared_fmt : d.routed_fmt;
-  a.route = d.route, a.scale = d.route_scale, a.vocab = d.vocab;
-  a.rpart = h->rpart, a.bias = h->bias, a.hash = h->hash, a.tok = tok;
-  a.cnt = b.cnt, a.off = b.off, a.active = b.active, a.n_active = b.n_active, a.list = b.list;
+  (void)tok;
+  a.bucket = h->bucket, a.A_cap = h->A_max;
   a.ids = h->ids, a.w = h->wts, a.hq = h->hq, a.dh = h->dh, a.gsh = h->gsh;
   a.apart = h->apart, a.cticket = h->cticket, a.y = y, a.err = h->err;
   a.down = down;
@@ -732,17 +735,6 @@ cudaError_t launch_dec_expert(const ds4moe_layer *h, const int32_t *tok, int T, 
   void *args[] = {&a};
   const void *fn = act ? expert_fn<true>(T) : expert_fn<false>(T);
   return launch_pdl(fn, dim3(h->n_sm), dim3(DEC_WARPS * 32), smem, s, args, true);
-}
-
-cudaError_t launch_route_tokens(const ds4moe_layer *h, const int32_t *tok, int T, int32_t *ids, float *w,
-                                cudaStream_t s) {
-  const ds4moe_layer_desc &d = h->d;
-  DecArgs a = {};
-  a.E = d.n_experts, a.E_pad = h->E_pad, a.k = d.top_k, a.T = T;
-  a.route = d.route, a.scale = d.route_scale, a.vocab = d.vocab;
-  a.rpart = h->rpart, a.bias = h->bias, a.hash = h->hash, a.tok = tok, a.err = h->err;
-  k_route_tokens<<<(T + 7) / 8, 256, 8 * 2 * h->E_pad * sizeof(float), s>>>(a, ids, w);
-  return cudaGetLastError();
 }
 
 cudaError_t decode_set_attributes() {

@@ -27,10 +27,9 @@ struct ds4moe_layer {
   int8_t *xq;            // [T][H]
   float *dx;             // [T][H/32]
   int16_t *gs;           // [T][H/16]
-  float *rpart;          // [T][8][E_pad] router segment sums
   int32_t *ids;          // [T][k]
   float *wts;            // [T][k]
-  int32_t *bucket;       // cnt[E+1] | off[E+2] | active[E+2] | n_active[1] | list[T*NS]
+  int32_t *bucket;       // per-expert table of the chunk (bucket.cuh): header, act[A_max], list[Tc*NS]
   int8_t *hq;            // [T*NS][F]
   float *dh;             // [T*NS][F/32]
   int16_t *gsh;          // [T*NS][F/16]
@@ -44,6 +43,7 @@ struct ds4moe_layer {
   int32_t *sticket_dn;   // [Tc][H/16] shared down merge tickets (self-resetting)
   int32_t *cticket;      // [Tc][H/32] combine tickets (self-resetting)
   int32_t *queue;        // work queues of the persistent kernels (self-resetting)
+  int32_t *rticket;      // router-kernel ticket of the call (self-resetting)
 
   // Staging for ds4moe_forward_host.
   float *x_dev, *y_dev;
@@ -64,23 +64,6 @@ struct ds4moe_layer {
 
 namespace ds4 {
 
-struct Bucket {
-  int32_t *cnt, *off, *active, *n_active, *list;
-};
-
-inline Bucket bucket_view(const ds4moe_layer *h) {
-  const int E = h->d.n_experts;
-  Bucket b;
-  b.cnt = h->bucket;
-  b.off = b.cnt + (E + 1);
-  b.active = b.off + (E + 2);
-  b.n_active = b.active + (E + 2);
-  b.list = b.n_active + 1;
-  return b;
-}
-
-inline size_t bucket_ints(int E, int T, int NS) { return (size_t)(E + 1) + (E + 2) + (E + 2) + 1 + (size_t)T * NS; }
-
 // repack.cu
 cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
                        cudaStream_t s);
@@ -95,10 +78,9 @@ cudaError_t launch_rmsnorm(const float *x, float *out, int T, int H, float eps, 
 // decode.cu
 constexpr int DEC_MAX_T = 64;  // largest n_tok served by the decode path
 size_t route_dec_smem(const ds4moe_layer *h);
-cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, cudaStream_t s);
+cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
+                             float *w, bool bucket, cudaStream_t s);
 cudaError_t launch_dec_expert(const ds4moe_layer *h, const int32_t *tok, int T, float *y, int down, cudaStream_t s);
-cudaError_t launch_route_tokens(const ds4moe_layer *h, const int32_t *tok, int T, int32_t *ids, float *w,
-                                cudaStream_t s);
 cudaError_t decode_set_attributes();
 constexpr size_t DEC_SMEM_LIMIT = 227 * 1024;
 
