@@ -170,8 +170,9 @@ void ora_q2s_dot(const uint8_t *sb, int j, const int8_t *xq, const int16_t *gs, 
 /*   Q2S : p_b = dx_b * fmaf(d_s, (float)A_b, -(dmin_s * (float)B_b))       */
 /*   Row sum over nb blocks in S equal contiguous segments: each segment is  */
 /*   acc = 0; acc = acc + p_b for increasing b; the segment sums are then    */
-/*   added the same way in increasing segment order. S = 1 for the routed     */
-/*   experts' matrices, S = 4 for the shared expert's, S = 8 for router rows. */
+/*   added the same way in increasing segment order. Router rows: S = 8.     */
+/*   Expert rows (routed and shared, gate/up/down): S = min(8, units), a     */
+/*   unit being a superblock (Q2S) or a block (Q8_0) -- expert_segs().        */
 /*   F32 rows (router only): each segment is acc = fmaf(w_i, x_i, acc) over  */
 /*   its elements in increasing i.                                            */
 
@@ -342,25 +343,31 @@ int ora_route_token(const ora_layer *L, const float *x, int32_t tok, int32_t *id
 
 /* ------------------------------------------------------------------------ */
 /* One expert (e < E routed, e == E shared) for one token.                   */
-/* g_j, u_j: gate/up rows j against (xq, dx, gs); S = 1 routed, 4 shared.    */
+/* g_j, u_j: gate/up rows j against (xq, dx, gs);                           */
 /* h_j = silu(g_j) * u_j; (hq, dh, gsh) = CAS quantisation of h;              */
-/* a_r: down row r against (hq, dh, gsh); S = 1 routed, 4 shared.            */
+/* a_r: down row r against (hq, dh, gsh); every row in expert_segs segments. */
 /* Any of g, u, h may be NULL.                                               */
 
 typedef struct {
   const uint8_t *gate, *up, *down;
-  int fmt, S; /* S: row-sum segments (CAS step 4) */
+  int fmt;
 } expert_w;
+
+/* Row-sum segments of an expert row of K columns (CAS step 4). */
+static int expert_segs(int fmt, int K) {
+  int units = fmt == FMT_Q2S ? K / 256 : K / 32;
+  return units < 8 ? units : 8;
+}
 
 static expert_w expert_of(const ora_layer *L, int e) {
   expert_w x;
   int H = L->hidden, F = L->ffn;
   if (e == L->n_experts) {
-    x.gate = L->sh_gate, x.up = L->sh_up, x.down = L->sh_down, x.fmt = L->shared_fmt, x.S = 4;
+    x.gate = L->sh_gate, x.up = L->sh_up, x.down = L->sh_down, x.fmt = L->shared_fmt;
   } else {
     size_t gu = (size_t)F * row_bytes(L->routed_fmt, H), dn = (size_t)H * row_bytes(L->routed_fmt, F);
     x.gate = L->gate + (size_t)e * gu, x.up = L->up + (size_t)e * gu, x.down = L->down + (size_t)e * dn;
-    x.fmt = L->routed_fmt, x.S = 1;
+    x.fmt = L->routed_fmt;
   }
   return x;
 }
@@ -371,8 +378,8 @@ static void expert_gateup_rows(const ora_layer *L, int e, const int8_t *xq, cons
   int H = L->hidden;
   size_t rb = row_bytes(X.fmt, H);
   for (int j = r0; j < r1; j++) {
-    float gj = ora_row(X.fmt, X.gate + (size_t)j * rb, H, xq, dx, gs, X.S);
-    float uj = ora_row(X.fmt, X.up + (size_t)j * rb, H, xq, dx, gs, X.S);
+    float gj = ora_row(X.fmt, X.gate + (size_t)j * rb, H, xq, dx, gs, expert_segs(X.fmt, H));
+    float uj = ora_row(X.fmt, X.up + (size_t)j * rb, H, xq, dx, gs, expert_segs(X.fmt, H));
     if (g) g[j] = gj;
     if (u) u[j] = uj;
     h[j] = ora_silu(gj) * uj;
@@ -384,7 +391,7 @@ static void expert_down_rows(const ora_layer *L, int e, const int8_t *hq, const 
   expert_w X = expert_of(L, e);
   int F = L->ffn;
   size_t rb = row_bytes(X.fmt, F);
-  for (int r = r0; r < r1; r++) a[r] = ora_row(X.fmt, X.down + (size_t)r * rb, F, hq, dh, gsh, X.S);
+  for (int r = r0; r < r1; r++) a[r] = ora_row(X.fmt, X.down + (size_t)r * rb, F, hq, dh, gsh, expert_segs(X.fmt, F));
 }
 
 /* Full single expert for one token, exposing every intermediate. */

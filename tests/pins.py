@@ -173,46 +173,50 @@ def check_row_sum_f64(ora, seed=11):
             assert abs(got - ref) <= _sum_bound(terms) + 1e-30, (fmt, K, S, got, ref)
 
 
-def _segment_row():
-    blk = R.parse_golden(os.path.join(GOLDEN, "cas_segments.txt"))[0]
+def _segment_row(name="cas_segments.txt"):
+    """(row bytes, x, expected sums by S) of a hand-worked Q8_0 row."""
+    blk = R.parse_golden(os.path.join(GOLDEN, name))[0]
     rows = dict(blk["_rows"])
     d = [int(v, 16) for v in rows["d"]]
     w = [int(v) for v in rows["w"]]
-    row = np.zeros(8 * 34, np.uint8)
-    for b in range(8):
+    nb = len(d)
+    row = np.zeros(nb * 34, np.uint8)
+    for b in range(nb):
         row[34 * b:34 * b + 2] = np.frombuffer(d[b].to_bytes(2, "little"), np.uint8)
         row[34 * b + 2] = np.uint8(w[b] & 0xFF)
-    x = np.zeros(256, np.float32)
+    x = np.zeros(32 * nb, np.float32)
     x[::32] = 127.0
     return row, x, {k: float(rows[k][0]) for k in ("S1", "S4", "S8")}
 
 
 def check_cas_segment_order(ora):
-    """The segment structure of the row sum, on a row whose orders round
-    differently (hand-worked in golden/cas_segments.txt)."""
-    row, x, want = _segment_row()
-    xq, dx, gs = ora.quantize(x)
-    assert np.all(dx == 1.0)
-    for S in (1, 4, 8):
-        assert float(ora.row("q8_0", row, 256, xq, dx, gs, S)) == want[f"S{S}"], S
+    """The segment structure of the row sum, on rows whose orders round
+    differently (hand-worked in golden/cas_segments.txt, cas_segments16.txt)."""
+    for name in ("cas_segments.txt", "cas_segments16.txt"):
+        row, x, want = _segment_row(name)
+        xq, dx, gs = ora.quantize(x)
+        assert np.all(dx == 1.0)
+        for S in (1, 4, 8):
+            assert float(ora.row("q8_0", row, x.size, xq, dx, gs, S)) == want[f"S{S}"], (name, S)
 
 
-def check_shared_expert_uses_four_segments(ora):
-    """The shared expert's rows are summed in 4 segments, the routed experts'
-    in 1: the same hand-worked row as gate row 0 of each."""
-    row, x, want = _segment_row()
-    spec = synth.LayerSpec("seg", 256, 2, 1, 64, 1, "learned", 0, "f32", "q8_0", "q8_0",
+def check_expert_rows_use_eight_segments(ora):
+    """Routed and shared expert rows are summed in 8 segments: the hand-worked
+    16-block row as gate row 0 of a routed expert and of the shared expert."""
+    row, x, want = _segment_row("cas_segments16.txt")
+    H, F, rb, rbd = 512, 64, 16 * 34, 2 * 34
+    spec = synth.LayerSpec("seg", H, 2, 1, F, 1, "learned", 0, "f32", "q8_0", "q8_0",
                            router_sigma=0.0, bias="none")
-    gate = np.zeros(2 * 64 * 8 * 34, np.uint8)
-    gate[:8 * 34] = row                            # routed expert 0, row 0
-    sh_gate = np.zeros(64 * 8 * 34, np.uint8)
-    sh_gate[:8 * 34] = row                         # shared expert, row 0
-    w = {"router_w": np.zeros((2, 256), np.float32), "router_bias": np.zeros(2, np.float32),
-         "gate": gate, "up": np.zeros_like(gate), "down": np.zeros(2 * 256 * 2 * 34, np.uint8),
-         "sh_gate": sh_gate, "sh_up": np.zeros_like(sh_gate), "sh_down": np.zeros(256 * 2 * 34, np.uint8)}
+    gate = np.zeros(2 * F * rb, np.uint8)
+    gate[:rb] = row                                # routed expert 0, row 0
+    sh_gate = np.zeros(F * rb, np.uint8)
+    sh_gate[:rb] = row                             # shared expert, row 0
+    w = {"router_w": np.zeros((2, H), np.float32), "router_bias": np.zeros(2, np.float32),
+         "gate": gate, "up": np.zeros_like(gate), "down": np.zeros(2 * H * rbd, np.uint8),
+         "sh_gate": sh_gate, "sh_up": np.zeros_like(sh_gate), "sh_down": np.zeros(H * rbd, np.uint8)}
     L = ora.layer(spec, w)
-    assert float(L.expert(0, x)["g"][0]) == want["S1"]
-    assert float(L.expert(2, x)["g"][0]) == want["S4"]
+    assert float(L.expert(0, x)["g"][0]) == want["S8"]
+    assert float(L.expert(2, x)["g"][0]) == want["S8"]
 
 
 # ----------------------------------------------------------- exp / sigmoid --
@@ -498,7 +502,7 @@ def check_combine_linearity(ora, spec=synth.MICRO, seed=37):
 ALL_CHECKS = [
     check_binary16, check_q2s_dequant_golden, check_q8_dequant_golden, check_quantize_golden,
     check_quantize_vs_f64, check_block_dots_exact, check_row_sum_f64, check_cas_segment_order,
-    check_shared_expert_uses_four_segments, check_exp, check_sigmoid_silu,
+    check_expert_rows_use_eight_segments, check_exp, check_sigmoid_silu,
     check_rmsnorm, check_topk_golden, check_route_invariants, check_route_k_equals_E, check_hash_route,
     check_expert_stages, check_shared_is_swiglu_mlp, check_layer_vs_textbook, check_combine_linearity,
 ]

@@ -42,8 +42,8 @@ PLANTS = [
     ("down_uses_x", "expert_down_rows(L, e, c->hq + ts * F, c->dh + ts * (F / 32), c->gsh + ts * (F / 16), ch * CHUNK,",
      "expert_down_rows(L, e, c->xq + (size_t)t * H, c->dh + ts * (F / 32), c->gsh + ts * (F / 16), ch * CHUNK,"),
     ("bias_ignored", "key[e] = s[e] + L->router_bias[e];", "key[e] = s[e];"),
-    ("shared_one_segment", "x.fmt = L->shared_fmt, x.S = 4;", "x.fmt = L->shared_fmt, x.S = 1;"),
-    ("routed_four_segments", "x.fmt = L->routed_fmt, x.S = 1;", "x.fmt = L->routed_fmt, x.S = 4;"),
+    ("expert_one_segment", "return units < 8 ? units : 8;", "return 1;"),
+    ("expert_four_segments", "return units < 8 ? units : 8;", "return units < 4 ? units : 4;"),
     ("segments_merged", "    tot = tot + acc;\n  }\n  return tot;\n}\n\nstatic float row_q2s",
      "    tot = acc;\n  }\n  return tot;\n}\n\nstatic float row_q2s"),
 ]
