@@ -29,8 +29,9 @@ bool is_dev_ptr(const void *p) {
 
 bool fmt_ok(int f) { return f == DS4MOE_Q8_0 || f == DS4MOE_Q2S; }
 
-// K must be a whole number of K-steps of the format.
-bool k_ok(int fmt, int K) { return K > 0 && K % kstep(fmt) == 0; }
+// K must be a whole number of K-steps of the format, split evenly into the
+// row-sum segments of an expert row.
+bool k_ok(int fmt, int K) { return K > 0 && K % kstep(fmt) == 0 && (K / kstep(fmt)) % expert_segs(fmt, K) == 0; }
 
 ds4moe_status validate_desc(const ds4moe_layer_desc *d) {
   if (!d || d->abi_version != DS4MOE_ABI_VERSION) return DS4MOE_ERR_INVALID_ARG;
@@ -43,10 +44,7 @@ ds4moe_status validate_desc(const ds4moe_layer_desc *d) {
   if (!fmt_ok(d->routed_fmt)) return DS4MOE_ERR_INVALID_ARG;
   if (d->n_shared && !fmt_ok(d->shared_fmt)) return DS4MOE_ERR_INVALID_ARG;
   if (!k_ok(d->routed_fmt, d->hidden) || !k_ok(d->routed_fmt, d->ffn)) return DS4MOE_ERR_INVALID_ARG;
-  // the shared expert's rows are summed in SHARED_SEGS segments of whole K-steps
-  if (d->n_shared && (!k_ok(d->shared_fmt, d->hidden / SHARED_SEGS) || !k_ok(d->shared_fmt, d->ffn / SHARED_SEGS) ||
-                      d->hidden % SHARED_SEGS || d->ffn % SHARED_SEGS))
-    return DS4MOE_ERR_INVALID_ARG;
+  if (d->n_shared && (!k_ok(d->shared_fmt, d->hidden) || !k_ok(d->shared_fmt, d->ffn))) return DS4MOE_ERR_INVALID_ARG;
   if (d->route == DS4MOE_ROUTE_LEARNED) {
     if (d->router_fmt != DS4MOE_F32 && d->router_fmt != DS4MOE_Q8_0) return DS4MOE_ERR_INVALID_ARG;
   } else if (d->route == DS4MOE_ROUTE_HASH) {
@@ -165,25 +163,14 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   if ((st = alloc(h, &h->hbuf, (size_t)(Tc * NS) * F * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->err, 64)) != DS4MOE_OK) return st;
   if ((st = cuda_status(cudaMemsetAsync(h->err, 0, 64, s))) != DS4MOE_OK) return st;
-  {  // tickets and queues start at zero and reset themselves
-    const size_t n_sp = (size_t)Tc * SHARED_SEGS * 2 * F * 4, n_spd = (size_t)Tc * SHARED_SEGS * H * 4;
-    const size_t n_ht = (size_t)(Tc * NS) * (F / 32) * 4;
-    const size_t n_st = (size_t)Tc * (F / TILE_ROWS) * 4, n_std = (size_t)Tc * (H / TILE_ROWS) * 4;
-    const size_t n_ct = (size_t)Tc * (H / 32) * 4, n_q = 16 * 4;
-    if ((st = alloc(h, &h->spart, n_sp)) != DS4MOE_OK) return st;
-    if ((st = alloc(h, &h->spart_dn, n_spd)) != DS4MOE_OK) return st;
+  {  // tickets start at zero and reset themselves
+    const size_t n_ht = (size_t)(Tc * NS) * (F / 32) * 4, n_ct = (size_t)Tc * (H / 32) * 4;
     if ((st = alloc(h, &h->hticket, n_ht)) != DS4MOE_OK) return st;
-    if ((st = alloc(h, &h->sticket, n_st)) != DS4MOE_OK) return st;
-    if ((st = alloc(h, &h->sticket_dn, n_std)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->cticket, n_ct)) != DS4MOE_OK) return st;
-    if ((st = alloc(h, &h->queue, n_q)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->rticket, 16)) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->rticket, 0, 16, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->hticket, 0, n_ht, s))) != DS4MOE_OK) return st;
-    if ((st = cuda_status(cudaMemsetAsync(h->sticket, 0, n_st, s))) != DS4MOE_OK) return st;
-    if ((st = cuda_status(cudaMemsetAsync(h->sticket_dn, 0, n_std, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->cticket, 0, n_ct, s))) != DS4MOE_OK) return st;
-    if ((st = cuda_status(cudaMemsetAsync(h->queue, 0, n_q, s))) != DS4MOE_OK) return st;
   }
 
   if (d.route == DS4MOE_ROUTE_HASH) {
@@ -326,9 +313,9 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
     e = launch_dec_route(h, xc, tc, nc, h->ids, h->wts, true, s);
     mark(2);
     mark(3);
-    if (e == cudaSuccess) e = launch_dec_expert(h, tc, nc, yc, 0, s);
+    if (e == cudaSuccess) e = launch_experts(h, xc, nc, yc, 0, s);
     mark(4);
-    if (e == cudaSuccess) e = launch_dec_expert(h, tc, nc, yc, 1, s);
+    if (e == cudaSuccess) e = launch_experts(h, xc, nc, yc, 1, s);
     mark(5);
     mark(6);
     h->launches += 3;

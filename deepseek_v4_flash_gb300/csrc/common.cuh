@@ -24,13 +24,15 @@ namespace ds4 {
 // contiguous bytes per 16-byte load and the two lanes of a row add their
 // exact integer partial dots with one shuffle).
 //
-// Q2S RG16 tile = 16 rows x one superblock (256 K), 1344 bytes:
-//   [0,256)     sm8: lane l -> 8 bytes: the scale/min nibbles of the groups
-//               of parity h (groups h, h+2, ..., h+14), i.e. of blocks 0..7
+// Q2S RG16 tile = 16 rows x one superblock (256 K), 1344 bytes. Lane
+// l = 2r + h owns blocks h, h+2, h+4, h+6 of row r (both 16-weight groups of
+// each block):
+//   [0,256)     sm8: lane l -> 8 bytes: the scale/min nibble bytes of groups
+//               2b, 2b+1 for b = h, h+2, h+4, h+6, in that order
 //   [256,320)   dd:  row r -> 4 bytes at 4r (fp16 d, fp16 dmin)
-//   [320,1344)  qs:  2 chunks j x 32 lanes x 16 bytes: lane l, chunk j holds
-//               the group words of blocks 4j..4j+3 (group 2b+h of block b),
-//               each word's 2-bit fields transposed so that
+//   [320,1344)  qs:  2 chunks c x 32 lanes x 16 bytes: lane l, chunk c holds
+//               the group words of its blocks h+4c and h+4c+2 (groups 2b,
+//               2b+1 each), each word's 2-bit fields transposed so that
 //               ((W >> 2s) & 0x03030303) yields q[4s .. 4s+3] of the group
 //               in element order (one dp4a against 4 consecutive int8 x).
 // Q8 RG16 tile = 16 rows x one Q8_0 block (32 K), 544 bytes:
@@ -50,10 +52,14 @@ constexpr int RQ8_TILE = 2176, RQ8_Q = 128, RQ8_KSTEP = 64;
 __host__ __device__ constexpr int tile_bytes(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_TILE : Q8_TILE; }
 __host__ __device__ constexpr int kstep(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_KSTEP : Q8_KSTEP; }
 
-// Row-sum segments (CAS step 4): router rows 8, shared expert rows 4,
-// routed expert rows 1.
+// Row-sum segments (CAS step 4): router rows 8; expert rows
+// min(EXPERT_SEGS, K-steps of the row), a K-step being one superblock (Q2S)
+// or one block (Q8_0).
 constexpr int ROUTER_SEGS = 8;
-constexpr int SHARED_SEGS = 4;
+constexpr int EXPERT_SEGS = 8;
+__host__ __device__ constexpr int expert_segs(int fmt, int K) {
+  return K / kstep(fmt) < EXPERT_SEGS ? K / kstep(fmt) : EXPERT_SEGS;
+}
 
 // ---------------------------------------------------------------------------
 // CAS device math.
@@ -187,6 +193,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     if (clock64() - t0 > (1ll << 31)) return false;
   }
   return true;
+}
+
+// Programmatic dependent launch: wait for the previous kernel's completion
+// (and memory), and let the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void raise_flag(uint32_t *err, uint32_t bits) {

@@ -37,12 +37,7 @@ struct ds4moe_layer {
   uint32_t *err;         // device error flags
   float *hbuf;           // [Tc*NS][F] SwiGLU values before requant
   int32_t *hticket;      // [Tc*NS][F/32] requant tickets (self-resetting)
-  float *spart;          // [Tc][4][2F] shared-expert gate/up segment sums
-  float *spart_dn;       // [Tc][4][H] shared-expert down segment sums
-  int32_t *sticket;      // [Tc][F/16] shared gate/up merge tickets (self-resetting)
-  int32_t *sticket_dn;   // [Tc][H/16] shared down merge tickets (self-resetting)
   int32_t *cticket;      // [Tc][H/32] combine tickets (self-resetting)
-  int32_t *queue;        // work queues of the persistent kernels (self-resetting)
   int32_t *rticket;      // router-kernel ticket of the call (self-resetting)
 
   // Staging for ds4moe_forward_host.
@@ -80,7 +75,12 @@ constexpr int DEC_MAX_T = 64;  // largest n_tok served by the decode path
 size_t route_dec_smem(const ds4moe_layer *h);
 cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
                              float *w, bool bucket, cudaStream_t s);
-cudaError_t launch_dec_expert(const ds4moe_layer *h, const int32_t *tok, int T, float *y, int down, cudaStream_t s);
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args, bool pdl);
+
+// experts.cu
+size_t experts_smem(const ds4moe_layer *h);
+cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *y, int down, cudaStream_t s);
+cudaError_t experts_set_attributes();
 cudaError_t decode_set_attributes();
 constexpr size_t DEC_SMEM_LIMIT = 227 * 1024;
 

@@ -7,8 +7,9 @@
 namespace ds4 {
 
 // One thread per canonical Q2S superblock (84 bytes) -> its two lanes'
-// slices of an RG16 tile. The 2-bit fields of each 16-weight group are
-// transposed: canonical element 4*s+j of the group (byte s of the group,
+// slices of an RG16 tile (common.cuh). Lane 2r + h owns blocks h + 2j
+// (j = 0..3), both groups of each. The 2-bit fields of each 16-weight group
+// are transposed: canonical element 4*s+j of the group (byte s of the group,
 // bits 2j) moves to byte j, bits 2s of the group word, so (W >> 2s) &
 // 0x03030303 gives 4 consecutive elements in byte order.
 __global__ void k_repack_q2s(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
@@ -25,16 +26,19 @@ __global__ void k_repack_q2s(const uint8_t *__restrict__ src, uint8_t *__restric
   for (int j = 0; j < 4; j++) tile[Q2S_DD + 4 * rr + j] = sb[80 + j];
   for (int h = 0; h < 2; h++) {
     const int lane = 2 * rr + h;
-    for (int b = 0; b < 8; b++) {
-      const int g = 2 * b + h;
-      tile[Q2S_SM + 8 * lane + b] = sb[g];
-      uint32_t W = 0;
-      for (int sbyte = 0; sbyte < 4; sbyte++) {
-        const uint32_t v = sb[16 + 4 * g + sbyte];
-        for (int j = 0; j < 4; j++) W |= ((v >> (2 * j)) & 3u) << (8 * j + 2 * sbyte);
+    for (int j = 0; j < 4; j++) {
+      const int b = h + 2 * j;
+      for (int gi = 0; gi < 2; gi++) {
+        const int g = 2 * b + gi;
+        tile[Q2S_SM + 8 * lane + 2 * j + gi] = sb[g];
+        uint32_t W = 0;
+        for (int sbyte = 0; sbyte < 4; sbyte++) {
+          const uint32_t v = sb[16 + 4 * g + sbyte];
+          for (int e = 0; e < 4; e++) W |= ((v >> (2 * e)) & 3u) << (8 * e + 2 * sbyte);
+        }
+        uint8_t *o = tile + Q2S_QS + 512 * (j >> 1) + 16 * lane + 4 * (2 * (j & 1) + gi);
+        o[0] = (uint8_t)W, o[1] = (uint8_t)(W >> 8), o[2] = (uint8_t)(W >> 16), o[3] = (uint8_t)(W >> 24);
       }
-      uint8_t *o = tile + Q2S_QS + 512 * (b >> 2) + 16 * lane + 4 * (b & 3);
-      o[0] = (uint8_t)W, o[1] = (uint8_t)(W >> 8), o[2] = (uint8_t)(W >> 16), o[3] = (uint8_t)(W >> 24);
     }
   }
 }
