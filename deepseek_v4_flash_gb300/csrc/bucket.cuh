@@ -5,8 +5,8 @@
 //   int4  act[A_cap]   {expert, pair count, offset into list, 0}: the shared
 //                      expert first (expert = E, all tokens), then the routed
 //                      experts with at least one pair in ascending id
-//   int32 list[T*NS]   slot rows t*NS + j, grouped by expert in act order;
-//                      within an expert in (token, slot) order
+//   int32 list[T*NS]   (token t << 5) | slot j, grouped by expert in act
+//                      order; within an expert in (token, slot) order
 //
 // Every position is a rank count (how many pairs sort before this one), so
 // the table is the same on every run. The order of pairs within an expert
@@ -48,7 +48,7 @@ __device__ inline void bucket_rank(const int32_t *ids, int T, int E, int k, int 
         c += ej == e ? 1 : 0;
         f &= (ej == e && j < i) ? 0 : 1;
       }
-      list[r] = (i / k) * NS + (i % k);
+      list[r] = ((i / k) << 5) | (i % k);
       atomicAdd(&tot[0], 1);
       if (f) atomicAdd(&tot[1], 1);
     }
@@ -66,7 +66,7 @@ __device__ inline void bucket_rank(const int32_t *ids, int T, int E, int k, int 
     act[n_shared + d] = make_int4(e, count[i], rank[i], 0);
   }
   if (n_shared) {
-    for (int t = tid; t < T; t += nth) list[n_pairs + t] = t * NS + k;
+    for (int t = tid; t < T; t += nth) list[n_pairs + t] = (t << 5) | k;
     if (tid == 0) act[0] = make_int4(E, T, n_pairs, 0);
   }
   if (tid == 0) {

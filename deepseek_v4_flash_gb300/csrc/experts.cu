@@ -29,7 +29,7 @@
 namespace ds4 {
 
 constexpr int XC = EXPERT_SEGS;  // compute warps, one K-segment each
-constexpr int XE = 2;            // epilogue warps
+constexpr int XE = 4;            // epilogue warps
 constexpr int X_WARPS = XC + XE;
 constexpr int X_NST = 4;         // ring stages per compute warp
 constexpr int X_STRIDE = 2688;   // ring slot bytes: one gate+up Q2S K-step
@@ -37,6 +37,7 @@ constexpr int X_STRIDE = 2688;   // ring slot bytes: one gate+up Q2S K-step
 struct XArgs {
   int H, F, E, k, NS, n_shared, T, A_cap;
   int rf, sf, down, K, rows;
+  int maxj;                      // item-table entries per block
   const uint8_t *w_r, *w_s;      // routed / shared weights (RG16)
   const float *x;                // layer input (gate/up, quantised here when staged)
   const int8_t *aq;              // activations in global memory: xq or hq
@@ -83,55 +84,35 @@ __device__ __forceinline__ XKind x_kind(const XArgs &a, int fmt, int warp) {
   return k;
 }
 
-// Walks this block's items (c, c + G, c + 2G, ...; shared expert items
-// first, then the routed experts' in bucket order), their token passes and
-// this warp's stages, without divisions after the first routed item.
-struct XCursor {
-  int i;          // item index
-  int routed;     // 0: shared item (rg = i), 1: routed
-  int aj, rg;     // routed: act index (after the shared entry) and 16-row group
-  int e, n_tok, list_off, npass;
-  int pass, stage, unit;
-  const uint8_t *src;  // this warp's segment of the item
-};
-
-// Sets up the item at c->i; false when the block has no more items. Routed
-// items need the bucket (act, n_routed = active routed experts).
-template <int TT>
-__device__ __forceinline__ bool x_item_at(const XArgs &a, XCursor *c, int nsh, int RG, const int4 *act,
-                                          int n_routed, const XKind &ks, const XKind &kr) {
-  if (c->i < nsh) {
-    c->routed = 0, c->rg = c->i, c->e = a.E, c->n_tok = a.T, c->list_off = -1;
-    c->src = a.w_s + (size_t)c->rg * ks.item_bytes + (size_t)ks.ks0 * ks.kb;
+// This block's items are c, c + G, c + 2G, ... of the fixed order (shared
+// expert items first, then the routed experts' in bucket order). Entry j of
+// the block's item table: {byte offset (lo, hi) into the routed or shared
+// weights, tokens, list offset (-1: the shared expert, tokens 0..T-1)} and
+// {routed, 16-row group, -, -}.
+__device__ __forceinline__ void x_table_entry(const XArgs &a, int i, int nsh, int RG, const int4 *act,
+                                              size_t ib_s, size_t ib_r, int4 *tab) {
+  size_t off;
+  int n_tok, list_off, routed, rg;
+  if (i < nsh) {
+    routed = 0, rg = i, n_tok = a.T, list_off = -1;
+    off = (size_t)rg * ib_s;
   } else {
-    if (!c->routed) {  // first routed item of this block
-      const int j = c->i - nsh;
-      c->aj = j / RG, c->rg = j % RG, c->routed = 1;
-    }
-    if (c->aj >= n_routed) return false;
-    const int4 en = act[a.n_shared + c->aj];
-    c->e = en.x, c->n_tok = en.y, c->list_off = en.z;
-    c->src = a.w_r + ((size_t)c->e * RG + c->rg) * kr.item_bytes + (size_t)kr.ks0 * kr.kb;
+    const int j = i - nsh, aj = j / RG;
+    const int4 en = act[a.n_shared + aj];
+    routed = 1, rg = j % RG, n_tok = en.y, list_off = en.z;
+    off = ((size_t)en.x * RG + rg) * ib_r;
   }
-  c->npass = (c->n_tok + TT - 1) / TT;
-  c->pass = 0, c->stage = 0;
-  return true;
+  tab[0] = make_int4((int)(off & 0xFFFFFFFFu), (int)(off >> 32), n_tok, list_off);
+  tab[1] = make_int4(routed, rg, 0, 0);
 }
 
-__device__ __forceinline__ void x_next_item(XCursor *c, int G, int RG) {
-  c->i += G;
-  if (c->routed) {
-    c->rg += G;
-    while (c->rg >= RG) c->rg -= RG, c->aj++;
-  }
-}
-
-// Slot row and activation row of token index idx of the cursor's item.
-__device__ __forceinline__ void x_token(const XArgs &a, const XCursor &c, const int32_t *list, int idx, int *sr,
+// Slot row and activation row of token index idx of an item.
+__device__ __forceinline__ void x_token(const XArgs &a, int list_off, const int32_t *list, int idx, int *sr,
                                         int *arow) {
-  const int s = c.list_off < 0 ? idx * a.NS + a.k : list[c.list_off + idx];
-  *sr = s;
-  *arow = a.down ? s : s / a.NS;
+  const int code = list_off < 0 ? (idx << 5) | a.k : list[list_off + idx];
+  const int t = code >> 5;
+  *sr = t * a.NS + (code & 31);
+  *arow = a.down ? *sr : t;
 }
 
 // CAS step 1 over 32 values held one per lane, written as the SwiGLU codes
@@ -176,18 +157,21 @@ __device__ __forceinline__ void x_combine(const XArgs &a, int t, int rg, int lan
   *yp = __fadd_rn(*yp, acc);
 }
 
-// Shared-memory layout (bytes) for TT, staged activations of `act_bytes`.
+// Shared-memory layout (bytes) for TT, staged activations of `act_bytes`,
+// an item table of `maxj` entries.
 struct XSmem {
-  int ring, bars, ctrl, part, bkt, act, total;
+  int ring, bars, ctrl, part, tab, valid, bkt, act, total;
 };
 
-__host__ __device__ inline XSmem x_smem(int TT, int mats, int nbk, int act_bytes) {
+__host__ __device__ inline XSmem x_smem(int TT, int mats, int nbk, int act_bytes, int maxj, int T) {
   XSmem s;
   s.ring = 0;
   s.bars = XC * X_NST * X_STRIDE;
   s.ctrl = s.bars + XC * X_NST * 8;
-  s.part = s.ctrl + 256;  // bucket barrier, then full[8] and empty[8] slot barriers
-  s.bkt = s.part + x_slots(TT) * XC * mats * TT * TILE_ROWS * 4;
+  s.part = s.ctrl + 256;  // bucket barrier, item count, then full[8] and empty[8] slot barriers
+  s.tab = s.part + x_slots(TT) * XC * mats * TT * TILE_ROWS * 4;
+  s.valid = s.tab + maxj * 32;
+  s.bkt = s.valid + ((T * 4 + 127) & ~127);
   s.act = s.bkt + ((nbk * 4 + 127) & ~127);
   s.total = s.act + act_bytes;
   return s;
@@ -221,10 +205,13 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   const int nbk = bucket_table_ints(a.A_cap, a.T, a.NS);
   const int act_rows = a.down ? a.T * a.NS : a.T;
   const int act_bytes = AS ? act_rows * (a.K + (a.K >> 5) * 4 + (a.K >> 4) * 2) : 0;
-  const XSmem L = x_smem(TT, mats, nbk, act_bytes);
+  const XSmem L = x_smem(TT, mats, nbk, act_bytes, a.maxj, a.T);
   const uint32_t bkt_bar = smem_u32(smem + L.ctrl);
-  const uint32_t full0 = bkt_bar + 64, empty0 = bkt_bar + 128;  // slot barriers, 8 bytes apart
+  volatile int *s_nitems = (volatile int *)(smem + L.ctrl + 8);  // items of this block (after the bucket)
+  const uint32_t full0 = bkt_bar + 64, empty0 = bkt_bar + 128;    // slot barriers, 8 bytes apart
   float *part = (float *)(smem + L.part);  // [PS][XC][mats][TT][16]
+  int4 *tab = (int4 *)(smem + L.tab);      // [maxj][2]
+  int *valid = (int *)(smem + L.valid);    // down: routed slots with an expert, per token
   int32_t *bks = (int32_t *)(smem + L.bkt);
   const int4 *act = (const int4 *)(bks + BKT_HDR);
   const int32_t *list = bks + BKT_HDR + 4 * a.A_cap;
@@ -239,6 +226,10 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   pdl_launch_dependents();
   const uint32_t ring = smem_u32(smem + L.ring + warp * X_NST * X_STRIDE);
   const uint32_t bar = smem_u32(smem + L.bars + warp * X_NST * 8);
+  const int nsh = a.n_shared ? a.rows / TILE_ROWS : 0, RG = a.rows / TILE_ROWS;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int n_sh_items = c < nsh ? (nsh - 1 - c) / G + 1 : 0;  // this block's shared items
+  const XKind ks = x_kind(a, a.sf, warp < XC ? warp : 0), kr = x_kind(a, a.rf, warp < XC ? warp : 0);
   if (threadIdx.x == 0) {
     mbar_init(bkt_bar, 1);
     for (int i = 0; i < PS; i++) mbar_init(full0 + 8 * i, XC), mbar_init(empty0 + 8 * i, 1);
@@ -246,61 +237,66 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   if (warp < XC && lane == 0)
     for (int i = 0; i < X_NST; i++) mbar_init(bar + 8 * i, 1);
   if (lane == 0) fence_mbar_init();
-  const int nsh = a.n_shared ? a.rows / TILE_ROWS : 0, RG = a.rows / TILE_ROWS;
-  const int G = gridDim.x;
-  const XKind ks = x_kind(a, a.sf, warp < XC ? warp : 0), kr = x_kind(a, a.rf, warp < XC ? warp : 0);
-  int n_routed = -1;  // active routed experts, once the bucket is known
+  // the shared-expert entries of the item table need no routing
+  for (int j = threadIdx.x; j < n_sh_items; j += blockDim.x)
+    x_table_entry(a, c + j * G, nsh, RG, act, ks.item_bytes, kr.item_bytes, tab + 2 * j);
+  int n_items = -1;  // this block's items, once the bucket is known
   bool failed = false;
-  __syncthreads();  // barriers initialised
+  __syncthreads();  // barriers and shared entries ready
 
-  // ---- compute warps: producer cursor; request shared-expert stages now
-  XCursor P;
-  P.i = blockIdx.x, P.routed = 0, P.unit = 0;
-  bool p_ok = false, p_done = false;
-  uint32_t g_prod = 0, g_cons = 0;
-  // Next (item, pass, stage) of this warp after the current one.
-  auto p_advance = [&](const XKind &k) {
-    if (++P.stage < k.nst) return;
-    P.stage = 0, P.unit++;
-    if (++P.pass < P.npass) return;
-    x_next_item(&P, G, RG);
-    p_ok = false;
+  // Routed entries (after the bucket is in shared memory), by one warp.
+  auto build_routed = [&]() {
+    const int n_all = nsh + (bks[0] - a.n_shared) * RG;
+    const int n = c < n_all ? (n_all - 1 - c) / G + 1 : 0;
+    for (int j = n_sh_items + lane; j < n; j += 32)
+      x_table_entry(a, c + j * G, nsh, RG, act, ks.item_bytes, kr.item_bytes, tab + 2 * j);
+    if (lane == 0) *s_nitems = n;
   };
-  // Fill the ring; stops early when the next item needs the bucket.
+
+  // ---- compute warps: producer (ring) cursor
+  int pj = 0, ppass = 0, pstage = 0, pnpass = 0, pnst = 0, psb = 0;
+  bool p_ok = false, p_done = false;
+  const uint8_t *psrc = nullptr;
+  uint32_t g_prod = 0, g_cons = 0;
   auto fill = [&]() {
     while (!p_done && g_prod - g_cons < X_NST) {
       if (!p_ok) {
-        if (P.i >= nsh && n_routed < 0) {
+        if (pj >= n_sh_items && n_items < 0) {
           if (!mbar_test(bkt_bar, 0)) return;
-          n_routed = bks[0] - a.n_shared;
+          n_items = *s_nitems;
         }
-        if (!x_item_at<TT>(a, &P, nsh, RG, act, n_routed, ks, kr)) {
+        if (pj >= (pj < n_sh_items ? n_sh_items : n_items)) {
           p_done = true;
           return;
         }
-        p_ok = true;
-        const XKind &k = P.routed ? kr : ks;
-        if (k.nst == 0) {  // no segment of this item for this warp
-          P.unit += P.npass;
-          x_next_item(&P, G, RG);
-          p_ok = false;
+        const int4 e0 = tab[2 * pj], e1 = tab[2 * pj + 1];
+        const bool rt = e1.x != 0;
+        pnst = rt ? kr.nst : ks.nst, psb = rt ? kr.sbytes : ks.sbytes;
+        pnpass = (e0.z + TT - 1) / TT, ppass = 0, pstage = 0;
+        psrc = (rt ? a.w_r : a.w_s) + ((size_t)(uint32_t)e0.x | ((size_t)(uint32_t)e0.y << 32)) +
+               (size_t)(rt ? kr.ks0 * kr.kb : ks.ks0 * ks.kb);
+        if (pnst == 0 || pnpass == 0) {  // no segment of this item for this warp
+          pj++;
           continue;
         }
+        p_ok = true;
       }
-      const XKind &k = P.routed ? kr : ks;
       const uint32_t slot = g_prod % X_NST;
       if (lane == 0) {
         if (g_prod >= X_NST) fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar + 8 * slot, k.sbytes);
-        bulk_g2s(ring + slot * X_STRIDE, P.src + (size_t)P.stage * k.sbytes, k.sbytes, bar + 8 * slot);
+        mbar_arrive_expect_tx(bar + 8 * slot, psb);
+        bulk_g2s(ring + slot * X_STRIDE, psrc + (size_t)pstage * psb, psb, bar + 8 * slot);
       }
       g_prod++;
-      p_advance(k);
+      if (++pstage == pnst) {
+        pstage = 0;
+        if (++ppass == pnpass) pj++, p_ok = false;
+      }
     }
   };
   if (warp < XC) {
     __syncwarp();
-    if (EARLY || P.i < nsh) fill();  // (not early: only shared items, which need no bucket)
+    if (EARLY || n_sh_items > 0) fill();  // (not early: shared items only, before the wait)
   }
 
   // ---- activations (and, unless early, the bucket)
@@ -334,9 +330,11 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
       }
     }
     __syncthreads();
-    if (warp == XC) {  // epilogue warp 0: the bucket, once the router kernel is done
+    if (warp == XC) {  // epilogue warp 0: the bucket and the routed entries, once the router kernel is done
       pdl_wait();
       for (int i = lane; i < nbk; i += 32) bks[i] = __ldcg(a.bucket + i);
+      __syncwarp();
+      build_routed();
       __syncwarp();
       if (lane == 0) mbar_arrive(bkt_bar);
     }
@@ -353,40 +351,56 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
       for (size_t i = threadIdx.x; i < ng / 16; i += blockDim.x)
         ((uint4 *)(dst + nq + nd))[i] = __ldcg((const uint4 *)a.ag + i);
     }
+    if (a.down)  // routed slots with an expert, per token (the combine's arrival count)
+      for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
+        int n = 0;
+        for (int j = 0; j < a.k; j++) n += __ldg(a.ids + (size_t)t * a.k + j) >= 0;
+        valid[t] = n;
+      }
     __syncthreads();
-    n_routed = bks[0] - a.n_shared;
+    if (warp == 0) build_routed();
+    __syncthreads();
+    n_items = *s_nitems;
   }
 
   if (warp < XC) {
     // ================= compute warp: segment `warp` of every unit
-    XCursor C;
-    C.i = blockIdx.x, C.routed = 0, C.unit = 0;
+    int cj = 0, cpass = 0, cstage = 0, cnpass = 0, unit = 0, list_off = 0, n_tok = 0;
+    int c_nst = 0, c_ksps = 1, c_kb = 0, c_ks0 = 0, c_fmt = 0;
     bool c_ok = false;
     int arow[TT], nt = 0;
     float acc[2][TT];
     for (;;) {
       if (!c_ok) {  // the consumer's next item
-        if (C.i >= nsh && n_routed < 0) {
+        if (cj >= n_sh_items && n_items < 0) {
           if (!mbar_wait_bounded(bkt_bar, 0)) {
             failed = true;
             break;
           }
-          n_routed = bks[0] - a.n_shared;
+          n_items = *s_nitems;
         }
-        if (!x_item_at<TT>(a, &C, nsh, RG, act, n_routed, ks, kr)) break;
+        if (cj >= (cj < n_sh_items ? n_sh_items : n_items)) break;
+        const int4 e0 = tab[2 * cj], e1 = tab[2 * cj + 1];
+        const bool rt = e1.x != 0;
+        c_nst = rt ? kr.nst : ks.nst, c_ksps = rt ? kr.ksps : ks.ksps, c_kb = rt ? kr.kb : ks.kb;
+        c_ks0 = rt ? kr.ks0 : ks.ks0, c_fmt = rt ? kr.fmt : ks.fmt;
+        n_tok = e0.z, list_off = e0.w, cnpass = (n_tok + TT - 1) / TT, cpass = 0, cstage = 0;
         c_ok = true;
+        if (cnpass == 0) {
+          cj++, c_ok = false;
+          continue;
+        }
       }
-      const XKind &k = C.routed ? kr : ks;
-      if (C.stage == 0) {  // a new unit: its tokens
-        nt = min(TT, C.n_tok - C.pass * TT);
+      if (cstage == 0) {  // a new unit: its tokens
+        nt = min(TT, n_tok - cpass * TT);
 #pragma unroll
         for (int i = 0; i < TT; i++) {
           int sr;
-          x_token(a, C, list, min(C.pass * TT + i, C.n_tok - 1), &sr, &arow[i]);
+          x_token(a, list_off, list, min(cpass * TT + i, n_tok - 1), &sr, &arow[i]);
           acc[0][i] = 0.0f, acc[1][i] = 0.0f;
         }
       }
-      if (k.nst > 0) {
+      if (c_nst > 0) {
         fill();
         const uint32_t slot = g_cons % X_NST;
         if (!mbar_wait_bounded(bar + 8 * slot, (g_cons / X_NST) & 1)) {
@@ -395,10 +409,10 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
         }
         __syncwarp();
         const uint32_t st = ring + slot * X_STRIDE;
-        const int s0 = k.ks0 + C.stage * k.ksps;
-        for (int j = 0; j < k.ksps; j++) {
-          const uint32_t t = st + j * k.kb;
-          if (k.fmt == DS4MOE_Q2S) {
+        const int s0 = c_ks0 + cstage * c_ksps;
+        for (int j = 0; j < c_ksps; j++) {
+          const uint32_t t = st + j * c_kb;
+          if (c_fmt == DS4MOE_Q2S) {
             if (a.down) q2s_step<TT, 1, AS>(t, lane, s0 + j, a.K, arow, aq, ad, ag, *(float(*)[1][TT])acc);
             else q2s_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, ag, acc);
           } else {
@@ -409,14 +423,14 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
         __syncwarp();
         g_cons++;
       }
-      if (k.nst == 0 || C.stage == k.nst - 1) {
+      if (c_nst == 0 || cstage == c_nst - 1) {
         // the unit's segment is done: partial sums into slot unit % PS
-        const int ps = C.unit % PS, ph = C.unit / PS;
+        const int ps = unit % PS, ph = unit / PS;
         if (ph > 0 && !mbar_wait_bounded(empty0 + 8 * ps, (ph - 1) & 1)) {
           failed = true;
           break;
         }
-        if (k.nst > 0 && (lane & 1) == 0) {
+        if (c_nst > 0 && (lane & 1) == 0) {
           float *dst = part + (size_t)(ps * XC + warp) * mats * TT * TILE_ROWS;
 #pragma unroll
           for (int i = 0; i < TT; i++) {
@@ -428,10 +442,10 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(full0 + 8 * ps);
-        C.stage = 0, C.unit++;
-        if (++C.pass == C.npass) x_next_item(&C, G, RG), c_ok = false;
+        cstage = 0, unit++;
+        if (++cpass == cnpass) cj++, c_ok = false;
       } else {
-        C.stage++;
+        cstage++;
       }
     }
     if (failed) {
@@ -441,28 +455,31 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
     return;
   }
 
-  // ================= epilogue warps: units u with u % XE == ew
+  // ================= epilogue warps: units u whose slot u % PS maps to this
+  // warp ((u % PS) % XE == ew), so the units of one slot, which wait on the
+  // same barriers in alternating phases, are always taken by the same warp
   const int ew = warp - XC;
-  XCursor E;
-  E.i = blockIdx.x, E.routed = 0, E.unit = 0;
-  for (;;) {
-    if (E.i >= nsh && n_routed < 0) {  // routed units need the bucket
+  int unit = 0;
+  for (int j = 0;; j++) {
+    if (j >= n_sh_items && n_items < 0) {  // routed units need the bucket
       if (!mbar_wait_bounded(bkt_bar, 0)) {
         if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
         return;
       }
-      n_routed = bks[0] - a.n_shared;
+      n_items = *s_nitems;
     }
-    if (!x_item_at<TT>(a, &E, nsh, RG, act, n_routed, ks, kr)) break;
-    const int S = E.routed ? kr.S : ks.S;
-    for (; E.pass < E.npass; E.pass++, E.unit++) {
-      if (E.unit % XE != ew) continue;
-      const int ps = E.unit % PS;
-      if (!mbar_wait_bounded(full0 + 8 * ps, (E.unit / PS) & 1)) {
+    if (j >= (j < n_sh_items ? n_sh_items : n_items)) break;
+    const int4 e0 = tab[2 * j], e1 = tab[2 * j + 1];
+    const int S = e1.x ? kr.S : ks.S, rg = e1.y, n_tok = e0.z, list_off = e0.w;
+    const int npass = (n_tok + TT - 1) / TT;
+    for (int p = 0; p < npass; p++, unit++) {
+      if ((unit % PS) % XE != ew) continue;
+      const int ps = unit % PS;
+      if (!mbar_wait_bounded(full0 + 8 * ps, (unit / PS) & 1)) {
         if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
         return;
       }
-      const int nt = min(TT, E.n_tok - E.pass * TT);
+      const int nt = min(TT, n_tok - p * TT);
       const float *src = part + (size_t)ps * XC * mats * TT * TILE_ROWS;
       const int r = lane & 15;
       for (int i0 = 0; i0 < nt; i0 += 2) {
@@ -470,39 +487,33 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
         if (i < nt) {
           float g = 0.0f, uu = 0.0f;  // segment sums in order (CAS step 4)
           for (int sg = 0; sg < S; sg++) {
-            const float *p = src + (size_t)sg * mats * TT * TILE_ROWS;
-            g = __fadd_rn(g, p[i * TILE_ROWS + r]);
-            if (!a.down) uu = __fadd_rn(uu, p[(TT + i) * TILE_ROWS + r]);
+            const float *pp = src + (size_t)sg * mats * TT * TILE_ROWS;
+            g = __fadd_rn(g, pp[i * TILE_ROWS + r]);
+            if (!a.down) uu = __fadd_rn(uu, pp[(TT + i) * TILE_ROWS + r]);
           }
           int sr, arow;
-          x_token(a, E, list, E.pass * TT + i, &sr, &arow);
-          if (!a.down) a.hbuf[(size_t)sr * a.F + TILE_ROWS * E.rg + r] = __fmul_rn(cas_silu(g), uu);
-          else a.apart[(size_t)sr * a.H + TILE_ROWS * E.rg + r] = g;
+          x_token(a, list_off, list, p * TT + i, &sr, &arow);
+          if (!a.down) a.hbuf[(size_t)sr * a.F + TILE_ROWS * rg + r] = __fmul_rn(cas_silu(g), uu);
+          else a.apart[(size_t)sr * a.H + TILE_ROWS * rg + r] = g;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * ps);  // the slot is free again
       // completion of 32-row blocks across the two items that cover them
-      const int blk = E.rg >> 1;
+      const int blk = rg >> 1;
       for (int i = 0; i < nt; i++) {
         int sr, arow;
-        x_token(a, E, list, E.pass * TT + i, &sr, &arow);
+        x_token(a, list_off, list, p * TT + i, &sr, &arow);
         if (!a.down) {
           if (x_ticket_last(a.hticket + (size_t)sr * (a.F >> 5) + blk, 2, lane))
             x_requant(a, __ldcg(a.hbuf + (size_t)sr * a.F + 32 * blk + lane), sr, blk, lane);
         } else {
           const int t = sr / a.NS;
-          int expect = 0;
-          if (lane == 0) {
-            for (int jj = 0; jj < a.k; jj++) expect += __ldg(a.ids + (size_t)t * a.k + jj) >= 0;
-            expect = 2 * (expect + a.n_shared);
-          }
-          expect = __shfl_sync(0xffffffffu, expect, 0);
+          const int expect = 2 * (valid[t] + a.n_shared);
           if (x_ticket_last(a.cticket + (size_t)t * (a.H >> 5) + blk, expect, lane)) x_combine(a, t, blk, lane);
         }
       }
     }
-    x_next_item(&E, G, RG);
   }
 }
 
@@ -518,9 +529,19 @@ static size_t x_act_bytes(const ds4moe_layer *h, int T, bool down) {
 
 static int x_tt(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
 
+// Item-table entries per block: the call's items over the blocks.
+static int x_maxj(const ds4moe_layer *h, int T, bool down) {
+  const ds4moe_layer_desc &d = h->d;
+  const int RG = (down ? d.hidden : d.ffn) / TILE_ROWS;
+  const long long routed = (long long)T * d.top_k < d.n_experts ? (long long)T * d.top_k : d.n_experts;
+  const long long n = (d.n_shared ? RG : 0) + routed * RG;
+  return (int)((n + h->n_sm - 1) / h->n_sm);
+}
+
 static size_t x_smem_bytes(const ds4moe_layer *h, int T, bool down, bool as) {
   const int nbk = bucket_table_ints(h->A_max, T, h->NS);
-  return (size_t)x_smem(x_tt(T), down ? 1 : 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0).total;
+  return (size_t)x_smem(x_tt(T), down ? 1 : 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0, x_maxj(h, T, down), T)
+      .total;
 }
 
 size_t experts_smem(const ds4moe_layer *h) {
@@ -544,6 +565,7 @@ cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *
   a.bucket = h->bucket, a.ids = h->ids, a.w = h->wts;
   a.hq = h->hq, a.dh = h->dh, a.gsh = h->gsh, a.hbuf = h->hbuf, a.hticket = h->hticket;
   a.apart = h->apart, a.cticket = h->cticket, a.y = y, a.err = h->err, a.x = x;
+  a.maxj = x_maxj(h, T, down != 0);
   if (!down) {
     a.K = d.hidden, a.rows = d.ffn, a.w_r = h->gu, a.w_s = h->sgu, a.aq = h->xq, a.ad = h->dx, a.ag = h->gs;
   } else {
