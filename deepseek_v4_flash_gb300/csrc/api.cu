@@ -87,7 +87,9 @@ ds4moe_status cuda_status(cudaError_t e) {
   return e == cudaErrorMemoryAllocation ? DS4MOE_ERR_OOM : DS4MOE_ERR_CUDA;
 }
 
-// Re-lay out a [n_mat][rows][K] expert tensor into the RG16 layout.
+// Re-lay out a [n_mat][rows][K] expert tensor into the RG16 layout. pair 0:
+// alone; 1: interleaved per K-step with a second tensor (which = 0, 1);
+// 2: the two 16-row groups of every 32 rows interleaved per K-step.
 cudaError_t repack(int fmt, const void *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
                    cudaStream_t s) {
   if (fmt == DS4MOE_Q2S) return repack_q2s((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
@@ -137,7 +139,7 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
   if ((st = alloc(h, &h->dn, rg16_bytes(rf, E, H, F))) != DS4MOE_OK) return st;
   if ((st = cuda_status(repack(rf, w->gate, h->gu, E, F, H, 1, 0, s))) != DS4MOE_OK) return st;
   if ((st = cuda_status(repack(rf, w->up, h->gu, E, F, H, 1, 1, s))) != DS4MOE_OK) return st;
-  if ((st = cuda_status(repack(rf, w->down, h->dn, E, H, F, 0, 0, s))) != DS4MOE_OK) return st;
+  if ((st = cuda_status(repack(rf, w->down, h->dn, E, H, F, 2, 0, s))) != DS4MOE_OK) return st;
   if (d.n_shared) {
     if (!is_dev_ptr(w->sh_gate) || !is_dev_ptr(w->sh_up) || !is_dev_ptr(w->sh_down)) return DS4MOE_ERR_INVALID_ARG;
     const int sf = d.shared_fmt;
@@ -145,7 +147,7 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
     if ((st = alloc(h, &h->sdn, rg16_bytes(sf, 1, H, F))) != DS4MOE_OK) return st;
     if ((st = cuda_status(repack(sf, w->sh_gate, h->sgu, 1, F, H, 1, 0, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(repack(sf, w->sh_up, h->sgu, 1, F, H, 1, 1, s))) != DS4MOE_OK) return st;
-    if ((st = cuda_status(repack(sf, w->sh_down, h->sdn, 1, H, F, 0, 0, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(repack(sf, w->sh_down, h->sdn, 1, H, F, 2, 0, s))) != DS4MOE_OK) return st;
   }
 
   // ---- scratch, sized for one chunk of at most DEC_MAX_T tokens

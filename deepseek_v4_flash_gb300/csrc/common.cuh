@@ -42,8 +42,10 @@ namespace ds4 {
 // bytes: [0,128) d: lane l -> 4 bytes (fp16 d of block 0, block 1);
 // [128,2176) q: 4 pieces m x 32 lanes x 16 bytes; piece m = block m/2,
 // elements 16*(m%2) .. 16*(m%2)+15.
-// A matrix [R][K] becomes [R/16][K/KSTEP][tile]; gate and up of the same
-// expert are interleaved per K-step: [R/16][K/KSTEP][2][tile].
+// Gate and up of the same expert are interleaved per K-step:
+// [F/16][H/KSTEP][2][tile]; a down matrix interleaves the two 16-row halves
+// of every 32 rows per K-step: [H/32][F/KSTEP][2][tile]. Either way one
+// K-step of a work item is two consecutive tiles.
 constexpr int TILE_ROWS = 16;
 constexpr int Q2S_TILE = 1344, Q2S_SM = 0, Q2S_DD = 256, Q2S_QS = 320, Q2S_KSTEP = 256;
 constexpr int Q8_TILE = 544, Q8_Q = 32, Q8_KSTEP = 32;
@@ -172,14 +174,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
+// try_wait with a suspend-time hint (nanoseconds): the waiting warp sleeps
+// until the phase completes or the hint expires instead of spinning, so it
+// takes no issue slots from the warps that do the work.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }

@@ -31,8 +31,12 @@ namespace ds4 {
 constexpr int XC = EXPERT_SEGS;  // compute warps, one K-segment each
 constexpr int XE = 4;            // epilogue warps
 constexpr int X_WARPS = XC + XE;
-constexpr int X_NST = 4;         // ring stages per compute warp
-constexpr int X_STRIDE = 2688;   // ring slot bytes: one gate+up Q2S K-step
+// Ring per compute warp: 4 slots of 2688 bytes (one K-step of a work item:
+// two Q2S tiles), 10.75 KB in flight per warp and 86 KB per SM, which covers
+// the loaded HBM latency at full bandwidth.
+constexpr int X_NST = 4;
+constexpr int X_STRIDE = 2688;
+constexpr int X_RING_BYTES = X_NST * X_STRIDE;
 
 struct XArgs {
   int H, F, E, k, NS, n_shared, T, A_cap;
@@ -65,15 +69,14 @@ struct XKind {
   size_t item_bytes;  // one 16-row item over the whole K
 };
 
-__device__ __forceinline__ XKind x_kind(const XArgs &a, int fmt, int warp) {
+__device__ __forceinline__ XKind x_kind(const XArgs &a, int fmt, int warp, int stride) {
   XKind k;
-  const int mats = a.down ? 1 : 2;
   k.fmt = fmt;
-  k.kb = mats * tile_bytes(fmt);
+  k.kb = 2 * tile_bytes(fmt);  // a K-step of an item: two tiles
   k.nks = a.K / kstep(fmt);
   k.S = expert_segs(fmt, a.K);
   const int nseg = k.nks / k.S;
-  int ks = X_STRIDE / k.kb;  // K-steps per ring stage: as many as fit, dividing the segment
+  int ks = stride / k.kb;  // K-steps per ring stage: as many as fit, dividing the segment
   if (ks > nseg) ks = nseg;
   while (ks > 1 && nseg % ks) ks--;
   k.ksps = ks < 1 ? 1 : ks;
@@ -166,8 +169,8 @@ struct XSmem {
 __host__ __device__ inline XSmem x_smem(int TT, int mats, int nbk, int act_bytes, int maxj, int T) {
   XSmem s;
   s.ring = 0;
-  s.bars = XC * X_NST * X_STRIDE;
-  s.ctrl = s.bars + XC * X_NST * 8;
+  s.bars = XC * X_RING_BYTES;
+  s.ctrl = s.bars + XC * 8 * 8;
   s.part = s.ctrl + 256;  // bucket barrier, item count, then full[8] and empty[8] slot barriers
   s.tab = s.part + x_slots(TT) * XC * mats * TT * TILE_ROWS * 4;
   s.valid = s.tab + maxj * 32;
@@ -196,14 +199,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 // early: gate/up with staged activations quantised here; the bucket comes
 // later (epilogue warp 0 waits for the router kernel). Otherwise every
 // thread waits for the previous kernel first.
-template <int TT, bool AS, bool EARLY>
+template <int TT, bool AS, bool EARLY, bool DOWN>
 __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int PS = x_slots(TT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mats = a.down ? 1 : 2;
+  constexpr int mats = 2;       // gate and up (16 rows), or the two 16-row halves of 32 rows (down)
+  constexpr int ROWS = DOWN ? 32 : 16;  // output rows of a work item
   const int nbk = bucket_table_ints(a.A_cap, a.T, a.NS);
-  const int act_rows = a.down ? a.T * a.NS : a.T;
+  const int act_rows = DOWN ? a.T * a.NS : a.T;
   const int act_bytes = AS ? act_rows * (a.K + (a.K >> 5) * 4 + (a.K >> 4) * 2) : 0;
   const XSmem L = x_smem(TT, mats, nbk, act_bytes, a.maxj, a.T);
   const uint32_t bkt_bar = smem_u32(smem + L.ctrl);
@@ -224,12 +228,12 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
     ag = (const int16_t *)(smem + L.act + act_rows * a.K + act_rows * (a.K >> 5) * 4);
   }
   pdl_launch_dependents();
-  const uint32_t ring = smem_u32(smem + L.ring + warp * X_NST * X_STRIDE);
-  const uint32_t bar = smem_u32(smem + L.bars + warp * X_NST * 8);
-  const int nsh = a.n_shared ? a.rows / TILE_ROWS : 0, RG = a.rows / TILE_ROWS;
+  const uint32_t ring = smem_u32(smem + L.ring + warp * X_RING_BYTES);
+  const uint32_t bar = smem_u32(smem + L.bars + warp * 8 * 8);
+  const int nsh = a.n_shared ? a.rows / ROWS : 0, RG = a.rows / ROWS;
   const int G = gridDim.x, c = blockIdx.x;
   const int n_sh_items = c < nsh ? (nsh - 1 - c) / G + 1 : 0;  // this block's shared items
-  const XKind ks = x_kind(a, a.sf, warp < XC ? warp : 0), kr = x_kind(a, a.rf, warp < XC ? warp : 0);
+  const XKind ks = x_kind(a, a.sf, warp < XC ? warp : 0, X_STRIDE), kr = x_kind(a, a.rf, warp < XC ? warp : 0, X_STRIDE);
   if (threadIdx.x == 0) {
     mbar_init(bkt_bar, 1);
     for (int i = 0; i < PS; i++) mbar_init(full0 + 8 * i, XC), mbar_init(empty0 + 8 * i, 1);
@@ -302,34 +306,67 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   // ---- activations (and, unless early, the bucket)
   if (EARLY) {
     // CAS step 1 on x into shared memory (the router kernel publishes the same
-    // codes); every warp's loads are issued before any of its blocks is done
+    // codes). When every item's rows have XC segments, compute warp w reads
+    // only the blocks of K-segment w, so it quantises just those, on its own;
+    // otherwise all warps quantise everything and meet at a barrier.
     int8_t *xq_s = (int8_t *)(smem + L.act);
     float *dx_s = (float *)(smem + L.act + act_rows * a.K);
     int16_t *gs_s = (int16_t *)(smem + L.act + act_rows * a.K + act_rows * (a.K >> 5) * 4);
-    const int nb = a.K >> 5, nblk = a.T * nb;
-    constexpr int QB = 8;
-    for (int p0 = warp; p0 < nblk; p0 += X_WARPS * QB) {
-      float v[QB];
+    const int nb = a.K >> 5;
+    const bool local = ks.S == XC && kr.S == XC;
+    int p_begin, p_step, n_blk;  // blocks p = p_begin + i*p_step of a token-major numbering
+    if (local) {
+      p_begin = warp * (nb / XC), p_step = 1, n_blk = warp < XC ? a.T * (nb / XC) : 0;
+    } else {
+      p_begin = warp, p_step = X_WARPS, n_blk = (a.T * nb - warp + X_WARPS - 1) / X_WARPS;
+    }
+    // QB blocks at a time in phases, so their latency chains overlap
+    constexpr int QB = 16;
+    for (int i0 = 0; i0 < n_blk; i0 += QB) {
+      int tb[QB];
+      float v[QB], m[QB], d[QB];
+      int q[QB];
 #pragma unroll
-      for (int j = 0; j < QB; j++) {
-        const int p = p0 + j * X_WARPS;
-        v[j] = p < nblk ? __ldg(a.x + (size_t)(p / nb) * a.K + 32 * (p % nb) + lane) : 0.0f;
+      for (int j = 0; j < QB; j++) {  // all loads first
+        int p = -1;
+        if (i0 + j < n_blk) {
+          if (local) {
+            const int per = nb / XC, ii = i0 + j;
+            p = (ii / per) * nb + p_begin + ii % per;
+          } else {
+            p = p_begin + (i0 + j) * p_step;
+          }
+        }
+        tb[j] = p;
+        v[j] = p >= 0 ? __ldg(a.x + (size_t)(p / nb) * a.K + 32 * (p % nb) + lane) : 0.0f;
+        m[j] = fabsf(v[j]);
       }
 #pragma unroll
+      for (int o = 16; o; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < QB; j++) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], o));
+#pragma unroll
+      for (int j = 0; j < QB; j++) d[j] = __fdiv_rn(m[j], 127.0f), q[j] = cas_code(v[j], d[j]);
+      int g[QB];
+#pragma unroll
+      for (int j = 0; j < QB; j++) g[j] = q[j];
+#pragma unroll
+      for (int o = 8; o; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < QB; j++) g[j] += __shfl_xor_sync(0xffffffffu, g[j], o);
+#pragma unroll
       for (int j = 0; j < QB; j++) {
-        const int p = p0 + j * X_WARPS;
-        if (p < nblk) {
+        const int p = tb[j];
+        if (p >= 0) {
           const int t = p / nb, b = p % nb;
-          const float d = __fdiv_rn(warp_max(fabsf(v[j])), 127.0f);
-          const int q = cas_code(v[j], d);
-          const int gsum = half_warp_sum(q);
-          xq_s[(size_t)t * a.K + 32 * b + lane] = (int8_t)q;
-          if (lane == 0) dx_s[(size_t)t * nb + b] = d;
-          if ((lane & 15) == 0) gs_s[(size_t)t * (a.K >> 4) + 2 * b + (lane >> 4)] = (int16_t)gsum;
+          xq_s[(size_t)t * a.K + 32 * b + lane] = (int8_t)q[j];
+          if (lane == 0) dx_s[(size_t)t * nb + b] = d[j];
+          if ((lane & 15) == 0) gs_s[(size_t)t * (a.K >> 4) + 2 * b + (lane >> 4)] = (int16_t)g[j];
         }
       }
     }
-    __syncthreads();
+    if (local) __syncwarp();
+    else __syncthreads();
     if (warp == XC) {  // epilogue warp 0: the bucket and the routed entries, once the router kernel is done
       pdl_wait();
       for (int i = lane; i < nbk; i += 32) bks[i] = __ldcg(a.bucket + i);
@@ -351,7 +388,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
       for (size_t i = threadIdx.x; i < ng / 16; i += blockDim.x)
         ((uint4 *)(dst + nq + nd))[i] = __ldcg((const uint4 *)a.ag + i);
     }
-    if (a.down)  // routed slots with an expert, per token (the combine's arrival count)
+    if (DOWN)  // routed slots with an expert, per token (the combine's arrival count)
       for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
         int n = 0;
         for (int j = 0; j < a.k; j++) n += __ldg(a.ids + (size_t)t * a.k + j) >= 0;
@@ -412,13 +449,8 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
         const int s0 = c_ks0 + cstage * c_ksps;
         for (int j = 0; j < c_ksps; j++) {
           const uint32_t t = st + j * c_kb;
-          if (c_fmt == DS4MOE_Q2S) {
-            if (a.down) q2s_step<TT, 1, AS>(t, lane, s0 + j, a.K, arow, aq, ad, ag, *(float(*)[1][TT])acc);
-            else q2s_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, ag, acc);
-          } else {
-            if (a.down) q8_step<TT, 1, AS>(t, lane, s0 + j, a.K, arow, aq, ad, *(float(*)[1][TT])acc);
-            else q8_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, acc);
-          }
+          if (c_fmt == DS4MOE_Q2S) q2s_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, ag, acc);
+          else q8_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, acc);
         }
         __syncwarp();
         g_cons++;
@@ -436,7 +468,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
           for (int i = 0; i < TT; i++) {
             if (i < nt) {
               dst[i * TILE_ROWS + (lane >> 1)] = acc[0][i];
-              if (!a.down) dst[(TT + i) * TILE_ROWS + (lane >> 1)] = acc[1][i];
+              dst[(TT + i) * TILE_ROWS + (lane >> 1)] = acc[1][i];
             }
           }
         }
@@ -482,35 +514,44 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
       const int nt = min(TT, n_tok - p * TT);
       const float *src = part + (size_t)ps * XC * mats * TT * TILE_ROWS;
       const int r = lane & 15;
-      for (int i0 = 0; i0 < nt; i0 += 2) {
-        const int i = i0 + (lane >> 4);
-        if (i < nt) {
-          float g = 0.0f, uu = 0.0f;  // segment sums in order (CAS step 4)
-          for (int sg = 0; sg < S; sg++) {
-            const float *pp = src + (size_t)sg * mats * TT * TILE_ROWS;
-            g = __fadd_rn(g, pp[i * TILE_ROWS + r]);
-            if (!a.down) uu = __fadd_rn(uu, pp[(TT + i) * TILE_ROWS + r]);
+      if (!DOWN) {  // 16 rows of gate and up: lanes 0-15 token i, 16-31 token i+1
+        for (int i0 = 0; i0 < nt; i0 += 2) {
+          const int i = i0 + (lane >> 4);
+          if (i < nt) {
+            float g = 0.0f, uu = 0.0f;  // segment sums in order (CAS step 4)
+            for (int sg = 0; sg < S; sg++) {
+              const float *pp = src + (size_t)sg * mats * TT * TILE_ROWS;
+              g = __fadd_rn(g, pp[i * TILE_ROWS + r]);
+              uu = __fadd_rn(uu, pp[(TT + i) * TILE_ROWS + r]);
+            }
+            int sr, arow;
+            x_token(a, list_off, list, p * TT + i, &sr, &arow);
+            a.hbuf[(size_t)sr * a.F + TILE_ROWS * rg + r] = __fmul_rn(cas_silu(g), uu);
           }
+        }
+      } else {  // 32 rows (lane = row) of each token
+        const int m = lane >> 4;
+        for (int i = 0; i < nt; i++) {
+          float g = 0.0f;
+          for (int sg = 0; sg < S; sg++) g = __fadd_rn(g, src[(size_t)sg * mats * TT * TILE_ROWS + (m * TT + i) * TILE_ROWS + r]);
           int sr, arow;
           x_token(a, list_off, list, p * TT + i, &sr, &arow);
-          if (!a.down) a.hbuf[(size_t)sr * a.F + TILE_ROWS * rg + r] = __fmul_rn(cas_silu(g), uu);
-          else a.apart[(size_t)sr * a.H + TILE_ROWS * rg + r] = g;
+          a.apart[(size_t)sr * a.H + 32 * rg + lane] = g;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * ps);  // the slot is free again
-      // completion of 32-row blocks across the two items that cover them
-      const int blk = rg >> 1;
       for (int i = 0; i < nt; i++) {
         int sr, arow;
         x_token(a, list_off, list, p * TT + i, &sr, &arow);
-        if (!a.down) {
+        if (!DOWN) {  // a 32-row block of h spans two items: requant when both are in
+          const int blk = rg >> 1;
           if (x_ticket_last(a.hticket + (size_t)sr * (a.F >> 5) + blk, 2, lane))
             x_requant(a, __ldcg(a.hbuf + (size_t)sr * a.F + 32 * blk + lane), sr, blk, lane);
-        } else {
+        } else {  // combine once every slot of the token has these 32 rows
           const int t = sr / a.NS;
-          const int expect = 2 * (valid[t] + a.n_shared);
-          if (x_ticket_last(a.cticket + (size_t)t * (a.H >> 5) + blk, expect, lane)) x_combine(a, t, blk, lane);
+          if (x_ticket_last(a.cticket + (size_t)t * (a.H >> 5) + rg, valid[t] + a.n_shared, lane))
+            x_combine(a, t, rg, lane);
         }
       }
     }
@@ -532,7 +573,7 @@ static int x_tt(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
 // Item-table entries per block: the call's items over the blocks.
 static int x_maxj(const ds4moe_layer *h, int T, bool down) {
   const ds4moe_layer_desc &d = h->d;
-  const int RG = (down ? d.hidden : d.ffn) / TILE_ROWS;
+  const int RG = down ? d.hidden / 32 : d.ffn / TILE_ROWS;
   const long long routed = (long long)T * d.top_k < d.n_experts ? (long long)T * d.top_k : d.n_experts;
   const long long n = (d.n_shared ? RG : 0) + routed * RG;
   return (int)((n + h->n_sm - 1) / h->n_sm);
@@ -540,7 +581,7 @@ static int x_maxj(const ds4moe_layer *h, int T, bool down) {
 
 static size_t x_smem_bytes(const ds4moe_layer *h, int T, bool down, bool as) {
   const int nbk = bucket_table_ints(h->A_max, T, h->NS);
-  return (size_t)x_smem(x_tt(T), down ? 1 : 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0, x_maxj(h, T, down), T)
+  return (size_t)x_smem(x_tt(T), 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0, x_maxj(h, T, down), T)
       .total;
 }
 
@@ -550,11 +591,11 @@ size_t experts_smem(const ds4moe_layer *h) {
   return a > b ? a : b;
 }
 
-template <bool AS, bool EARLY>
+template <bool AS, bool EARLY, bool DOWN>
 static const void *x_fn(int T) {
-  return T <= 1 ? (const void *)k_experts<1, AS, EARLY>
-       : T <= 2 ? (const void *)k_experts<2, AS, EARLY>
-       : T <= 4 ? (const void *)k_experts<4, AS, EARLY> : (const void *)k_experts<8, AS, EARLY>;
+  return T <= 1 ? (const void *)k_experts<1, AS, EARLY, DOWN>
+       : T <= 2 ? (const void *)k_experts<2, AS, EARLY, DOWN>
+       : T <= 4 ? (const void *)k_experts<4, AS, EARLY, DOWN> : (const void *)k_experts<8, AS, EARLY, DOWN>;
 }
 
 cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *y, int down, cudaStream_t s) {
@@ -572,15 +613,18 @@ cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *
     a.K = d.ffn, a.rows = d.hidden, a.w_r = h->dn, a.w_s = h->sdn, a.aq = h->hq, a.ad = h->dh, a.ag = h->gsh;
   }
   const bool as = x_smem_bytes(h, T, down != 0, true) <= DEC_SMEM_LIMIT;
-  const void *fn = as ? (down ? x_fn<true, false>(T) : x_fn<true, true>(T)) : x_fn<false, false>(T);
+  const void *fn = down ? (as ? x_fn<true, false, true>(T) : x_fn<false, false, true>(T))
+                        : (as ? x_fn<true, true, false>(T) : x_fn<false, false, false>(T));
   void *args[] = {&a};
   return launch_pdl(fn, dim3(h->n_sm), dim3(X_WARPS * 32), x_smem_bytes(h, T, down != 0, as), s, args, true);
 }
 
 cudaError_t experts_set_attributes() {
-  const void *fns[] = {x_fn<true, true>(1),  x_fn<true, true>(2),  x_fn<true, true>(4),  x_fn<true, true>(8),
-                       x_fn<true, false>(1), x_fn<true, false>(2), x_fn<true, false>(4), x_fn<true, false>(8),
-                       x_fn<false, false>(1), x_fn<false, false>(2), x_fn<false, false>(4), x_fn<false, false>(8)};
+  const void *fns[] = {
+      x_fn<true, true, false>(1),  x_fn<true, true, false>(2),  x_fn<true, true, false>(4),  x_fn<true, true, false>(8),
+      x_fn<false, false, false>(1), x_fn<false, false, false>(2), x_fn<false, false, false>(4), x_fn<false, false, false>(8),
+      x_fn<true, false, true>(1),  x_fn<true, false, true>(2),  x_fn<true, false, true>(4),  x_fn<true, false, true>(8),
+      x_fn<false, false, true>(1), x_fn<false, false, true>(2), x_fn<false, false, true>(4), x_fn<false, false, true>(8)};
   cudaError_t e = cudaSuccess;
   for (const void *f : fns)
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM_LIMIT);

@@ -20,7 +20,7 @@ struct ds4moe_layer {
   float *bias;           // [E]
   int32_t *hash;         // [vocab][k]
   uint8_t *gu;           // routed gate+up [E][F/32][H/KSTEP][2][tile]
-  uint8_t *dn;           // routed down    [E][H/32][F/KSTEP][tile]
+  uint8_t *dn;           // routed down    [E][H/32][F/KSTEP][2][tile] (16-row halves)
   uint8_t *sgu, *sdn;    // shared, same layouts with E = 1
 
   // Scratch for max_tokens tokens.

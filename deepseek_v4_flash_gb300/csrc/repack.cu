@@ -6,6 +6,15 @@
 
 namespace ds4 {
 
+// Tile of 16-row group rg, K-step s of matrix m. npair 1: one matrix;
+// npair 2: two matrices interleaved per K-step (gate, up: which = 0, 1);
+// npair 3: the two 16-row groups of each 32-row group interleaved per K-step
+// (which = rg & 1).
+__device__ __forceinline__ int64_t tile_index(int m, int rows, int rg, int KS, int s, int npair, int which) {
+  if (npair == 3) return ((((int64_t)m * (rows >> 5) + (rg >> 1)) * KS + s) * 2 + (rg & 1));
+  return (((int64_t)m * (rows >> 4) + rg) * KS + s) * npair + which;
+}
+
 // One thread per canonical Q2S superblock (84 bytes) -> its two lanes'
 // slices of an RG16 tile (common.cuh). Lane 2r + h owns blocks h + 2j
 // (j = 0..3), both groups of each. The 2-bit fields of each 16-weight group
@@ -22,7 +31,7 @@ __global__ void k_repack_q2s(const uint8_t *__restrict__ src, uint8_t *__restric
   const int r = (int)(mr % rows), m = (int)(mr / rows);
   const uint8_t *sb = src + i * 84;
   const int rg = r >> 4, rr = r & 15;
-  uint8_t *tile = dst + ((((int64_t)m * (rows >> 4) + rg) * KS + s) * npair + which) * Q2S_TILE;
+  uint8_t *tile = dst + tile_index(m, rows, rg, KS, s, npair, which) * Q2S_TILE;
   for (int j = 0; j < 4; j++) tile[Q2S_DD + 4 * rr + j] = sb[80 + j];
   for (int h = 0; h < 2; h++) {
     const int lane = 2 * rr + h;
@@ -54,7 +63,7 @@ __global__ void k_repack_q8(const uint8_t *__restrict__ src, uint8_t *__restrict
   const int r = (int)(mr % rows), m = (int)(mr / rows);
   const uint8_t *b = src + i * 34;
   const int rg = r >> 4, rr = r & 15;
-  uint8_t *tile = dst + ((((int64_t)m * (rows >> 4) + rg) * KS + c) * npair + which) * Q8_TILE;
+  uint8_t *tile = dst + tile_index(m, rows, rg, KS, c, npair, which) * Q8_TILE;
   tile[2 * rr + 0] = b[0], tile[2 * rr + 1] = b[1];
   for (int h = 0; h < 2; h++)
     for (int j = 0; j < 16; j++) tile[Q8_Q + 16 * (2 * rr + h) + j] = b[2 + 16 * h + j];
@@ -95,7 +104,7 @@ cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, in
   const int KS = K / Q2S_KSTEP;
   const int64_t n = (int64_t)n_mat * rows * KS;
   if (n == 0) return cudaSuccess;
-  k_repack_q2s<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair ? 2 : 1, which);
+  k_repack_q2s<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair == 2 ? 3 : pair ? 2 : 1, which);
   return cudaGetLastError();
 }
 
@@ -104,7 +113,7 @@ cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int
   const int KS = K / Q8_KSTEP;
   const int64_t n = (int64_t)n_mat * rows * KS;
   if (n == 0) return cudaSuccess;
-  k_repack_q8<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair ? 2 : 1, which);
+  k_repack_q8<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair == 2 ? 3 : pair ? 2 : 1, which);
   return cudaGetLastError();
 }
 
