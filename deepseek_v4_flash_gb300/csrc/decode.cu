@@ -123,7 +123,6 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   float *dx_s = (float *)(smem + rc_dx_off(a.E_pad));
   int8_t *xq_s = (int8_t *)(smem + rc_xq_off(a.E_pad, per));
   uint8_t *work = smem + rc_work_off(a.E_pad, per);
-  pdl_launch_dependents();
   const uint32_t bar = smem_u32(&bars[warp]);
   const uint32_t wbuf = smem_u32(work + warp * seg_bytes);
   const size_t rg_stride = (size_t)(a.H / RQ8_KSTEP) * RQ8_TILE;
@@ -196,11 +195,15 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
     lgp[r] = acc;
     __syncwarp();  // every lane is done with the tiles before the next copy
   }
+  // the next kernel may launch now: its weight prefetch no longer competes
+  // with this kernel's router loads
+  pdl_launch_dependents();
   cluster_sync_all();
   // ---- routing of token t by block 0 of its cluster
+  const RouteScratch rs = route_scratch(work, a.E_pad, a.k);
+  int32_t *hash_ids = (int32_t *)(work + route_block_smem(a.E_pad, a.k));  // hash routing: this token's ids
   if (seg == 0) {
     if (a.learned) {
-      const RouteScratch rs = route_scratch(work, a.E_pad, a.k);
 #pragma unroll
       for (int i = 0; i < RC_MAX_E / (RC_WARPS * 32); i++) {
         const int e = threadIdx.x + i * RC_WARPS * 32;
@@ -216,16 +219,24 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
       const int v = __ldg(a.tok + t);
       const bool okv = v >= 0 && v < a.vocab;
       if (!okv && threadIdx.x == 0) raise_flag(a.err, DS4MOE_DEVERR_TOKEN_ID);
-      a.ids[(size_t)t * a.k + threadIdx.x] = okv ? __ldg(a.hash + (size_t)v * a.k + threadIdx.x) : -1;
+      const int e = okv ? __ldg(a.hash + (size_t)v * a.k + threadIdx.x) : -1;
+      hash_ids[threadIdx.x] = e;
+      a.ids[(size_t)t * a.k + threadIdx.x] = e;
       a.w[(size_t)t * a.k + threadIdx.x] = okv ? __fmul_rn(__fdiv_rn(1.0f, (float)a.k), a.scale) : 0.0f;
     }
   }
   cluster_sync_all();  // the other blocks' segment sums stay until block 0 has read them
   if (seg != 0 || !a.bucket) return;
-  // ---- bucketing of the call by the block that routed its last token
-  if (a.T > 1 && !block_ticket_last(a.rticket, a.T, s_flag)) return;
-  __syncthreads();
-  int32_t *ids_s = (int32_t *)work;
+  // ---- bucketing of the call by the block that routed its last token (a
+  // single token: from this block's own selection, still in shared memory)
+  int32_t *scr = hash_ids + 16;
+  if (a.T == 1) {
+    __syncthreads();
+    bucket_rank(a.learned ? rs.sel : hash_ids, 1, a.E, a.k, a.NS, a.n_shared, scr, a.bucket, a.A_cap, a.err);
+    return;
+  }
+  if (!block_ticket_last(a.rticket, a.T, s_flag)) return;
+  int32_t *ids_s = scr;
   for (int i = threadIdx.x; i < a.T * a.k; i += blockDim.x) ids_s[i] = __ldcg(a.ids + i);
   __syncthreads();
   bucket_rank(ids_s, a.T, a.E, a.k, a.NS, a.n_shared, ids_s + ((a.T * a.k + 3) & ~3), a.bucket, a.A_cap, a.err);
@@ -254,11 +265,10 @@ static size_t router_dec_smem(const ds4moe_layer *h) {
   const int H = d.hidden, nb = H / 32, per = nb / ROUTER_SEGS;
   const bool q8 = d.route == DS4MOE_ROUTE_LEARNED && d.router_fmt == DS4MOE_Q8_0;
   size_t work = q8 ? (size_t)RC_WARPS * ((per + 1) / 2 + 1) * RQ8_TILE : 0;
-  const size_t route = route_block_smem(h->E_pad, d.top_k);
   const int n = h->Tc * d.top_k;
-  const size_t bucket = (size_t)(((n + 3) & ~3) + bucket_rank_smem_ints(n)) * 4;
+  const size_t route = route_block_smem(h->E_pad, d.top_k) + 64 +
+                       (size_t)(((n + 3) & ~3) + bucket_rank_smem_ints(n)) * 4;
   if (route > work) work = route;
-  if (bucket > work) work = bucket;
   return rc_work_off(h->E_pad, per) + work;
 }
 

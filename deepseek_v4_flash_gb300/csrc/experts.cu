@@ -1,26 +1,26 @@
 // experts.cu -- gate/up and down of the routed and shared experts for a
 // decode-sized call (n_tok <= DEC_MAX_T).
 //
-// Persistent: one block per SM, XC = 8 compute warps and XE = 2 epilogue
-// warps. A work item is 16 rows of one expert matrix (gate and up
-// interleaved, or down) for the tokens routed to that expert; a unit is an
-// item together with one pass over up to TT of those tokens. Every expert
-// row is summed in S = 8 K-segments (CAS step 4), and compute warp w owns
-// segment w of every unit: it streams that segment's tiles through a private
-// ring of 1-D bulk async copies (mbarrier completion, bounded waits), keeps
-// the segment chain of the 16 rows for each token in registers, and leaves
-// it in a shared-memory slot. The epilogue warps add the S segment sums in
-// order and finish the unit: SwiGLU, then the int8 requant of each 32-row
-// block of h (gate/up); or the down output and the fixed-order combine into
-// y (down). A 32-row block spans two items, so its completion across blocks
-// uses self-resetting tickets.
+// Persistent: one block per SM, XC = 8 compute warps and XE = 4 epilogue
+// warps. A work item is 16 rows of gate and up (interleaved per K-step) or
+// 32 rows of down (two 16-row tiles per K-step) of one expert, for the
+// tokens routed to that expert; a unit is an item with one pass over up to
+// TT of those tokens. Every expert row is summed in 8 K-segments (CAS step
+// 4), and compute warp w owns segment w of every unit: it streams that
+// segment's tiles through a private ring of 1-D bulk async copies (mbarrier
+// completion, bounded waits), keeps the segment chains for each token in
+// registers, and leaves them in a shared-memory slot. An epilogue warp adds
+// the segment sums in order and finishes the unit: SwiGLU and the int8
+// requant of each 32-row block of h (gate/up), or the down output and the
+// fixed-order combine into y (down). A 32-row block of h spans two gate/up
+// items and the combine spans every slot of a token, so completion across
+// blocks uses self-resetting tickets.
 //
 // Items are dealt to blocks round-robin in a fixed order (shared expert
-// first, then the routed experts in bucket order), so every warp of a block
-// walks the same unit sequence without any queue. The gate/up kernel
-// quantises x itself (when the activations fit shared memory), so the
-// shared expert's units stream and compute before the router kernel ends;
-// the routed units wait for its bucket table.
+// first, then the routed experts in bucket order); each block lists its items
+// once in shared memory, so every warp walks the same unit sequence without
+// any queue. The shared expert's weights are requested before the wait for
+// the previous kernel; the routed items and the activations come after it.
 #include "bucket.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -43,7 +43,6 @@ struct XArgs {
   int rf, sf, down, K, rows;
   int maxj;                      // item-table entries per block
   const uint8_t *w_r, *w_s;      // routed / shared weights (RG16)
-  const float *x;                // layer input (gate/up, quantised here when staged)
   const int8_t *aq;              // activations in global memory: xq or hq
   const float *ad;
   const int16_t *ag;
@@ -196,10 +195,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// early: gate/up with staged activations quantised here; the bucket comes
-// later (epilogue warp 0 waits for the router kernel). Otherwise every
-// thread waits for the previous kernel first.
-template <int TT, bool AS, bool EARLY, bool DOWN>
+// AS: activations staged in shared memory. DOWN: the down kernel (items of
+// 32 rows), else gate/up (items of 16 rows, gate and up).
+template <int TT, bool AS, bool DOWN>
 __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int PS = x_slots(TT);
@@ -210,9 +208,8 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   const int act_rows = DOWN ? a.T * a.NS : a.T;
   const int act_bytes = AS ? act_rows * (a.K + (a.K >> 5) * 4 + (a.K >> 4) * 2) : 0;
   const XSmem L = x_smem(TT, mats, nbk, act_bytes, a.maxj, a.T);
-  const uint32_t bkt_bar = smem_u32(smem + L.ctrl);
   volatile int *s_nitems = (volatile int *)(smem + L.ctrl + 8);  // items of this block (after the bucket)
-  const uint32_t full0 = bkt_bar + 64, empty0 = bkt_bar + 128;    // slot barriers, 8 bytes apart
+  const uint32_t full0 = smem_u32(smem + L.ctrl) + 64, empty0 = full0 + 64;  // slot barriers, 8 bytes apart
   float *part = (float *)(smem + L.part);  // [PS][XC][mats][TT][16]
   int4 *tab = (int4 *)(smem + L.tab);      // [maxj][2]
   int *valid = (int *)(smem + L.valid);    // down: routed slots with an expert, per token
@@ -235,7 +232,6 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   const int n_sh_items = c < nsh ? (nsh - 1 - c) / G + 1 : 0;  // this block's shared items
   const XKind ks = x_kind(a, a.sf, warp < XC ? warp : 0, X_STRIDE), kr = x_kind(a, a.rf, warp < XC ? warp : 0, X_STRIDE);
   if (threadIdx.x == 0) {
-    mbar_init(bkt_bar, 1);
     for (int i = 0; i < PS; i++) mbar_init(full0 + 8 * i, XC), mbar_init(empty0 + 8 * i, 1);
   }
   if (warp < XC && lane == 0)
@@ -265,10 +261,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   auto fill = [&]() {
     while (!p_done && g_prod - g_cons < X_NST) {
       if (!p_ok) {
-        if (pj >= n_sh_items && n_items < 0) {
-          if (!mbar_test(bkt_bar, 0)) return;
-          n_items = *s_nitems;
-        }
+        if (pj >= n_sh_items && n_items < 0) return;  // routed items: after the previous kernel
         if (pj >= (pj < n_sh_items ? n_sh_items : n_items)) {
           p_done = true;
           return;
@@ -300,82 +293,11 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   };
   if (warp < XC) {
     __syncwarp();
-    if (EARLY || n_sh_items > 0) fill();  // (not early: shared items only, before the wait)
+    if (n_sh_items > 0) fill();  // shared-expert items need no routing: request them before the wait
   }
 
-  // ---- activations (and, unless early, the bucket)
-  if (EARLY) {
-    // CAS step 1 on x into shared memory (the router kernel publishes the same
-    // codes). When every item's rows have XC segments, compute warp w reads
-    // only the blocks of K-segment w, so it quantises just those, on its own;
-    // otherwise all warps quantise everything and meet at a barrier.
-    int8_t *xq_s = (int8_t *)(smem + L.act);
-    float *dx_s = (float *)(smem + L.act + act_rows * a.K);
-    int16_t *gs_s = (int16_t *)(smem + L.act + act_rows * a.K + act_rows * (a.K >> 5) * 4);
-    const int nb = a.K >> 5;
-    const bool local = ks.S == XC && kr.S == XC;
-    int p_begin, p_step, n_blk;  // blocks p = p_begin + i*p_step of a token-major numbering
-    if (local) {
-      p_begin = warp * (nb / XC), p_step = 1, n_blk = warp < XC ? a.T * (nb / XC) : 0;
-    } else {
-      p_begin = warp, p_step = X_WARPS, n_blk = (a.T * nb - warp + X_WARPS - 1) / X_WARPS;
-    }
-    // QB blocks at a time in phases, so their latency chains overlap
-    constexpr int QB = 16;
-    for (int i0 = 0; i0 < n_blk; i0 += QB) {
-      int tb[QB];
-      float v[QB], m[QB], d[QB];
-      int q[QB];
-#pragma unroll
-      for (int j = 0; j < QB; j++) {  // all loads first
-        int p = -1;
-        if (i0 + j < n_blk) {
-          if (local) {
-            const int per = nb / XC, ii = i0 + j;
-            p = (ii / per) * nb + p_begin + ii % per;
-          } else {
-            p = p_begin + (i0 + j) * p_step;
-          }
-        }
-        tb[j] = p;
-        v[j] = p >= 0 ? __ldg(a.x + (size_t)(p / nb) * a.K + 32 * (p % nb) + lane) : 0.0f;
-        m[j] = fabsf(v[j]);
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1)
-#pragma unroll
-        for (int j = 0; j < QB; j++) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], o));
-#pragma unroll
-      for (int j = 0; j < QB; j++) d[j] = __fdiv_rn(m[j], 127.0f), q[j] = cas_code(v[j], d[j]);
-      int g[QB];
-#pragma unroll
-      for (int j = 0; j < QB; j++) g[j] = q[j];
-#pragma unroll
-      for (int o = 8; o; o >>= 1)
-#pragma unroll
-        for (int j = 0; j < QB; j++) g[j] += __shfl_xor_sync(0xffffffffu, g[j], o);
-#pragma unroll
-      for (int j = 0; j < QB; j++) {
-        const int p = tb[j];
-        if (p >= 0) {
-          const int t = p / nb, b = p % nb;
-          xq_s[(size_t)t * a.K + 32 * b + lane] = (int8_t)q[j];
-          if (lane == 0) dx_s[(size_t)t * nb + b] = d[j];
-          if ((lane & 15) == 0) gs_s[(size_t)t * (a.K >> 4) + 2 * b + (lane >> 4)] = (int16_t)g[j];
-        }
-      }
-    }
-    if (local) __syncwarp();
-    else __syncthreads();
-    if (warp == XC) {  // epilogue warp 0: the bucket and the routed entries, once the router kernel is done
-      pdl_wait();
-      for (int i = lane; i < nbk; i += 32) bks[i] = __ldcg(a.bucket + i);
-      __syncwarp();
-      build_routed();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bkt_bar);
-    }
-  } else {
+  // ---- once the previous kernel is done: the bucket and the staged activations
+  {
     pdl_wait();
     for (int i = threadIdx.x; i < nbk; i += blockDim.x) bks[i] = __ldcg(a.bucket + i);
     if (AS) {
@@ -409,13 +331,6 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
     float acc[2][TT];
     for (;;) {
       if (!c_ok) {  // the consumer's next item
-        if (cj >= n_sh_items && n_items < 0) {
-          if (!mbar_wait_bounded(bkt_bar, 0)) {
-            failed = true;
-            break;
-          }
-          n_items = *s_nitems;
-        }
         if (cj >= (cj < n_sh_items ? n_sh_items : n_items)) break;
         const int4 e0 = tab[2 * cj], e1 = tab[2 * cj + 1];
         const bool rt = e1.x != 0;
@@ -493,13 +408,6 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   const int ew = warp - XC;
   int unit = 0;
   for (int j = 0;; j++) {
-    if (j >= n_sh_items && n_items < 0) {  // routed units need the bucket
-      if (!mbar_wait_bounded(bkt_bar, 0)) {
-        if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
-        return;
-      }
-      n_items = *s_nitems;
-    }
     if (j >= (j < n_sh_items ? n_sh_items : n_items)) break;
     const int4 e0 = tab[2 * j], e1 = tab[2 * j + 1];
     const int S = e1.x ? kr.S : ks.S, rg = e1.y, n_tok = e0.z, list_off = e0.w;
@@ -591,11 +499,11 @@ size_t experts_smem(const ds4moe_layer *h) {
   return a > b ? a : b;
 }
 
-template <bool AS, bool EARLY, bool DOWN>
+template <bool AS, bool DOWN>
 static const void *x_fn(int T) {
-  return T <= 1 ? (const void *)k_experts<1, AS, EARLY, DOWN>
-       : T <= 2 ? (const void *)k_experts<2, AS, EARLY, DOWN>
-       : T <= 4 ? (const void *)k_experts<4, AS, EARLY, DOWN> : (const void *)k_experts<8, AS, EARLY, DOWN>;
+  return T <= 1 ? (const void *)k_experts<1, AS, DOWN>
+       : T <= 2 ? (const void *)k_experts<2, AS, DOWN>
+       : T <= 4 ? (const void *)k_experts<4, AS, DOWN> : (const void *)k_experts<8, AS, DOWN>;
 }
 
 cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *y, int down, cudaStream_t s) {
@@ -605,7 +513,7 @@ cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *
   a.A_cap = h->A_max, a.rf = d.routed_fmt, a.sf = d.n_shared ? d.shared_fmt : d.routed_fmt, a.down = down;
   a.bucket = h->bucket, a.ids = h->ids, a.w = h->wts;
   a.hq = h->hq, a.dh = h->dh, a.gsh = h->gsh, a.hbuf = h->hbuf, a.hticket = h->hticket;
-  a.apart = h->apart, a.cticket = h->cticket, a.y = y, a.err = h->err, a.x = x;
+  a.apart = h->apart, a.cticket = h->cticket, a.y = y, a.err = h->err;
   a.maxj = x_maxj(h, T, down != 0);
   if (!down) {
     a.K = d.hidden, a.rows = d.ffn, a.w_r = h->gu, a.w_s = h->sgu, a.aq = h->xq, a.ad = h->dx, a.ag = h->gs;
@@ -613,18 +521,16 @@ cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *
     a.K = d.ffn, a.rows = d.hidden, a.w_r = h->dn, a.w_s = h->sdn, a.aq = h->hq, a.ad = h->dh, a.ag = h->gsh;
   }
   const bool as = x_smem_bytes(h, T, down != 0, true) <= DEC_SMEM_LIMIT;
-  const void *fn = down ? (as ? x_fn<true, false, true>(T) : x_fn<false, false, true>(T))
-                        : (as ? x_fn<true, true, false>(T) : x_fn<false, false, false>(T));
+  const void *fn = down ? (as ? x_fn<true, true>(T) : x_fn<false, true>(T)) : (as ? x_fn<true, false>(T) : x_fn<false, false>(T));
   void *args[] = {&a};
   return launch_pdl(fn, dim3(h->n_sm), dim3(X_WARPS * 32), x_smem_bytes(h, T, down != 0, as), s, args, true);
 }
 
 cudaError_t experts_set_attributes() {
-  const void *fns[] = {
-      x_fn<true, true, false>(1),  x_fn<true, true, false>(2),  x_fn<true, true, false>(4),  x_fn<true, true, false>(8),
-      x_fn<false, false, false>(1), x_fn<false, false, false>(2), x_fn<false, false, false>(4), x_fn<false, false, false>(8),
-      x_fn<true, false, true>(1),  x_fn<true, false, true>(2),  x_fn<true, false, true>(4),  x_fn<true, false, true>(8),
-      x_fn<false, false, true>(1), x_fn<false, false, true>(2), x_fn<false, false, true>(4), x_fn<false, false, true>(8)};
+  const void *fns[] = {x_fn<true, false>(1),  x_fn<true, false>(2),  x_fn<true, false>(4),  x_fn<true, false>(8),
+                       x_fn<false, false>(1), x_fn<false, false>(2), x_fn<false, false>(4), x_fn<false, false>(8),
+                       x_fn<true, true>(1),   x_fn<true, true>(2),   x_fn<true, true>(4),   x_fn<true, true>(8),
+                       x_fn<false, true>(1),  x_fn<false, true>(2),  x_fn<false, true>(4),  x_fn<false, true>(8)};
   cudaError_t e = cudaSuccess;
   for (const void *f : fns)
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM_LIMIT);
