@@ -31,12 +31,16 @@ namespace ds4 {
 constexpr int XC = EXPERT_SEGS;  // compute warps, one K-segment each
 constexpr int XE = 4;            // epilogue warps
 constexpr int X_WARPS = XC + XE;
-// Ring per compute warp: 4 slots of 2688 bytes (one K-step of a work item:
-// two Q2S tiles), 10.75 KB in flight per warp and 86 KB per SM, which covers
-// the loaded HBM latency at full bandwidth.
-constexpr int X_NST = 4;
-constexpr int X_STRIDE = 2688;
-constexpr int X_RING_BYTES = X_NST * X_STRIDE;
+// Ring per compute warp, 10.75 KB in flight per warp and 86 KB per SM, which
+// covers the loaded HBM latency at full bandwidth: gate/up 2 slots of 5376
+// bytes (two K-steps of a routed item, computed together for instruction-
+// level parallelism), down 4 slots of 2688 bytes (one K-step of a routed
+// 32-row item).
+template <bool DOWN> struct XRing {
+  static constexpr int NST = DOWN ? 4 : 2;
+  static constexpr int STRIDE = DOWN ? 2688 : 5376;
+};
+constexpr int X_RING_BYTES = 4 * 2688;
 
 struct XArgs {
   int H, F, E, k, NS, n_shared, T, A_cap;
@@ -200,6 +204,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 template <int TT, bool AS, bool DOWN>
 __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int X_NST = XRing<DOWN>::NST, X_STRIDE = XRing<DOWN>::STRIDE;
   constexpr int PS = x_slots(TT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int mats = 2;       // gate and up (16 rows), or the two 16-row halves of 32 rows (down)
@@ -362,10 +367,15 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
         __syncwarp();
         const uint32_t st = ring + slot * X_STRIDE;
         const int s0 = c_ks0 + cstage * c_ksps;
-        for (int j = 0; j < c_ksps; j++) {
-          const uint32_t t = st + j * c_kb;
-          if (c_fmt == DS4MOE_Q2S) q2s_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, ag, acc);
-          else q8_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, acc);
+        if (c_fmt == DS4MOE_Q2S && c_ksps == 2) {  // two K-steps in one block of code: their dots overlap
+          q2s_step<TT, 2, AS>(st, lane, s0, a.K, arow, aq, ad, ag, acc);
+          q2s_step<TT, 2, AS>(st + c_kb, lane, s0 + 1, a.K, arow, aq, ad, ag, acc);
+        } else {
+          for (int j = 0; j < c_ksps; j++) {
+            const uint32_t t = st + j * c_kb;
+            if (c_fmt == DS4MOE_Q2S) q2s_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, ag, acc);
+            else q8_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, acc);
+          }
         }
         __syncwarp();
         g_cons++;
