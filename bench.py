@@ -203,6 +203,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layer-copies", type=int, default=0,
+                    help="layer copies rotated across steps (0: enough that the working sets exceed L2)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     spec, T, desc = WORKLOADS[args.workload]
@@ -231,6 +233,8 @@ def main():
     # A layer small enough to sit in L2 uses one copy and an L2 flush instead.
     per_step = step_bytes(spec, T, min(spec.n_experts, T * spec.top_k))
     NL = 1 if per_step < (32 << 20) else max(2, min(8, int(np.ceil(4 * (128 << 20) / per_step))))
+    if args.layer_copies > 0:
+        NL = args.layer_copies
     use_flush = NL == 1
     layers, w = [], None
     for l in range(NL):
