@@ -150,19 +150,24 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
     if ((st = cuda_status(repack(sf, w->sh_down, h->sdn, 1, H, F, 2, 0, s))) != DS4MOE_OK) return st;
   }
 
-  // ---- scratch, sized for one chunk of at most DEC_MAX_T tokens
-  const long long Tc = h->Tc;
-  if ((st = alloc(h, &h->xq, (size_t)Tc * H)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->dx, (size_t)Tc * (H / 32) * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->gs, (size_t)Tc * (H / 16) * 2)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->ids, (size_t)Tc * k * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->wts, (size_t)Tc * k * 4)) != DS4MOE_OK) return st;
+  // ---- scratch, sized for one chunk of either path (Ts = max(Tc, Tp) tokens)
+  const long long Tc = h->Tc, Ts = h->Ts;
+  if ((st = alloc(h, &h->xq, (size_t)Ts * H)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->dx, (size_t)Ts * (H / 32) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->gs, (size_t)Ts * (H / 16) * 2)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->ids, (size_t)Ts * k * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->wts, (size_t)Ts * k * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->bucket, (size_t)bucket_table_ints(h->A_max, (int)Tc, (int)NS) * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->hq, (size_t)(Tc * NS) * F)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->dh, (size_t)(Tc * NS) * (F / 32) * 4)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->gsh, (size_t)(Tc * NS) * (F / 16) * 2)) != DS4MOE_OK) return st;
-  if ((st = alloc(h, &h->apart, (size_t)(Tc * NS) * H * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->hq, (size_t)(Ts * NS) * F)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->dh, (size_t)(Ts * NS) * (F / 32) * 4)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->gsh, (size_t)(Ts * NS) * (F / 16) * 2)) != DS4MOE_OK) return st;
+  if ((st = alloc(h, &h->apart, (size_t)(Ts * NS) * H * 4)) != DS4MOE_OK) return st;
   if ((st = alloc(h, &h->hbuf, (size_t)(Tc * NS) * F * 4)) != DS4MOE_OK) return st;
+  if (h->Tp > 0) {
+    if ((st = alloc(h, &h->pf_meta, (size_t)(E + 1) * 2 * 4)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->pf_pass, (size_t)(E + 2) * 4)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->pf_list, prefill_list_ints(h->Tp, k, d.n_shared) * 4)) != DS4MOE_OK) return st;
+  }
   if ((st = alloc(h, &h->err, 64)) != DS4MOE_OK) return st;
   if ((st = cuda_status(cudaMemsetAsync(h->err, 0, 64, s))) != DS4MOE_OK) return st;
   {  // tickets start at zero and reset themselves
@@ -222,6 +227,15 @@ ds4moe_status ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights 
   }
   h->E_pad = (desc->n_experts + 31) / 32 * 32;
   h->Tc = desc->max_tokens < DEC_MAX_T ? desc->max_tokens : DEC_MAX_T;
+  h->pf_min = PF_MIN_T_DEFAULT;
+  if (const char *v = getenv("DS4MOE_PREFILL_MIN_TOKENS")) {
+    const long m = strtol(v, nullptr, 10);
+    if (m >= 1 && m <= (1 << 20)) h->pf_min = (int)m;
+  }
+  h->Tp = 0;
+  if (prefill_supported(*desc) && desc->max_tokens >= h->pf_min)
+    h->Tp = desc->max_tokens < PF_MAX_T ? desc->max_tokens : PF_MAX_T;
+  h->Ts = h->Tp > h->Tc ? h->Tp : h->Tc;
   if (cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -236,7 +250,7 @@ ds4moe_status ds4moe_create(const ds4moe_layer_desc *desc, const ds4moe_weights 
     delete h;
     return DS4MOE_ERR_UNSUPPORTED;
   }
-  if (decode_set_attributes() != cudaSuccess) {
+  if (decode_set_attributes() != cudaSuccess || (h->Tp > 0 && prefill_set_attributes() != cudaSuccess)) {
     cudaGetLastError();
     delete h;
     return DS4MOE_ERR_CUDA;
@@ -303,8 +317,18 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
   auto mark = [&](int i) {
     if (prof) cudaEventRecord(h->ev[i], s);
   };
-  // Tokens are independent: run chunks of at most Tc tokens.
+  // Tokens are independent: a prefill-sized call runs in chunks of at most Tp
+  // tokens on the prefill path, anything else in chunks of at most Tc tokens
+  // on the decode path.
   cudaError_t e = cudaSuccess;
+  if (h->Tp > 0 && n_tok >= h->pf_min) {
+    for (int c0 = 0; c0 < n_tok && e == cudaSuccess; c0 += h->Tp) {
+      const int nc = n_tok - c0 < h->Tp ? n_tok - c0 : h->Tp;
+      e = launch_prefill(h, x + (size_t)c0 * H, token_ids ? token_ids + c0 : nullptr, nc, y + (size_t)c0 * H, s,
+                         prof ? h->ev : nullptr);
+    }
+    return cuda_status(e);
+  }
   for (int c0 = 0; c0 < n_tok && e == cudaSuccess; c0 += h->Tc) {
     const int nc = n_tok - c0 < h->Tc ? n_tok - c0 : h->Tc;
     const float *xc = x + (size_t)c0 * H;
@@ -416,7 +440,7 @@ ds4moe_status ds4moe_get_device_error(ds4moe_layer *h, void *stream, uint32_t *f
 // results of the last call (integer codes, ids, weights).
 ds4moe_status ds4moe_debug_scratch(ds4moe_layer *h, int32_t which, const void **ptr_out, uint64_t *bytes_out) {
   if (!h || !ptr_out || !bytes_out) return DS4MOE_ERR_INVALID_ARG;
-  const long long T = h->Tc, NS = h->NS, H = h->d.hidden, F = h->d.ffn, k = h->d.top_k;
+  const long long T = h->Ts, NS = h->NS, H = h->d.hidden, F = h->d.ffn, k = h->d.top_k;
   const void *p = nullptr;
   uint64_t n = 0;
   switch (which) {

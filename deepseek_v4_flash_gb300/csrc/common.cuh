@@ -174,6 +174,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // try_wait with a suspend-time hint (nanoseconds): the waiting warp sleeps
 // until the phase completes or the hint expires instead of spinning, so it
 // takes no issue slots from the warps that do the work.

@@ -195,10 +195,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 // AS: activations staged in shared memory. DOWN: the down kernel (items of
 // 32 rows), else gate/up (items of 16 rows, gate and up).
 template <int TT, bool AS, bool DOWN>

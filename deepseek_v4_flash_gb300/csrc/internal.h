@@ -13,7 +13,10 @@ struct ds4moe_layer {
   int NS;      // expert slots per token: top_k + n_shared
   int A_max;   // most active experts in one call: min(E, max_tokens*k) + n_shared
   int n_sm;    // streaming multiprocessors of the device
-  int Tc;      // tokens per chunk: min(max_tokens, DEC_MAX_T); scratch is sized for one chunk
+  int Tc;      // tokens per decode chunk: min(max_tokens, DEC_MAX_T)
+  int Tp;      // tokens per prefill chunk: min(max_tokens, PF_MAX_T), 0 without the prefill path
+  int Ts;      // scratch rows: max(Tc, Tp)
+  int pf_min;  // calls with at least this many tokens take the prefill path
 
   // Weights in the library's layout (see common.cuh).
   uint8_t *router;       // Q8 RG32 [E_pad/32][H/64][tile], or F32 [E][H]
@@ -23,7 +26,7 @@ struct ds4moe_layer {
   uint8_t *dn;           // routed down    [E][H/32][F/KSTEP][2][tile] (16-row halves)
   uint8_t *sgu, *sdn;    // shared, same layouts with E = 1
 
-  // Scratch for max_tokens tokens.
+  // Scratch for Ts tokens (one chunk of either path).
   int8_t *xq;            // [T][H]
   float *dx;             // [T][H/32]
   int16_t *gs;           // [T][H/16]
@@ -39,6 +42,9 @@ struct ds4moe_layer {
   int32_t *hticket;      // [Tc*NS][F/32] requant tickets (self-resetting)
   int32_t *cticket;      // [Tc][H/32] combine tickets (self-resetting)
   int32_t *rticket;      // router-kernel ticket of the call (self-resetting)
+  int32_t *pf_meta;      // prefill: [E+1][2] {pairs, list offset} per group (0 shared, 1+e routed)
+  int32_t *pf_pass;      // prefill: [E+2] first pass of each group, then the total
+  int32_t *pf_list;      // prefill: [Tp*k + Tp] pair codes (token << 5) | slot, grouped
 
   // Staging for ds4moe_forward_host.
   float *x_dev, *y_dev;
@@ -76,6 +82,15 @@ size_t route_dec_smem(const ds4moe_layer *h);
 cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
                              float *w, bool bucket, cudaStream_t s);
 cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args, bool pdl);
+
+// prefill.cu
+constexpr int PF_MAX_T = 4096;       // largest prefill chunk
+constexpr int PF_MIN_T_DEFAULT = 65; // smallest call that takes the prefill path
+bool prefill_supported(const ds4moe_layer_desc &d);
+cudaError_t prefill_set_attributes();
+size_t prefill_list_ints(int T, int k, int n_shared);
+cudaError_t launch_prefill(ds4moe_layer *h, const float *x, const int32_t *tok, int T, float *y, cudaStream_t s,
+                           cudaEvent_t *ev);
 
 // experts.cu
 size_t experts_smem(const ds4moe_layer *h);

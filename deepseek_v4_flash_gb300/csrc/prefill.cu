@@ -1,0 +1,677 @@
+// prefill.cu -- the path of a prefill-sized call: every expert of the layer
+// sees many tokens, so gate/up and down are grouped contractions and run on
+// the tensor cores (tcgen05, accumulators in tensor memory).
+//
+//   k_router_dec (decode.cu)  int8 quantisation of x and routing, all tokens
+//   k_pf_bucket               per-expert token lists, pass offsets
+//   k_pf_experts<0>           grouped gate/up + SwiGLU + int8 requant of h
+//   k_pf_experts<1>           grouped down -> per-slot outputs
+//   k_pf_combine              fixed-order combine into y
+//
+// The contraction: for every 32-block b of K the integer block dots of the
+// canonical arithmetic are exact products of small integers, so the kernel
+// feeds them to the tensor cores as fp16 values (sc*q in [0, 45] or int8 q,
+// against int8 activation codes; the min term as mn in [0, 15] against 16-
+// group sums in [-2032, 2032]): every product and every 32-term sum is an
+// integer below 2^24, which the fp32 accumulator holds exactly. Each block
+// gets its own accumulator (A_b, and B_b for the 2-bit format), and the
+// epilogue applies the block's float terms and the segment-ordered row sum
+// exactly as the decode path and the CPU evaluation do, so the results are
+// bit-identical to theirs.
+//
+// A work item is 128 rows (MMA M) of one expert matrix (gate/up: 128 rows of
+// gate and the same 128 rows of up) for one pass of up to 32 of the expert's
+// tokens (MMA N). A persistent block walks items c, c + G, ... with four
+// warp roles connected by mbarriers:
+//   producer   1-D bulk copies of the packed weight tiles (raw ring)
+//   converters expand one 32-block of weights into fp16 operand tiles in the
+//              canonical no-swizzle K-major layout, and the tokens' codes
+//              (fp16 ring), plus the epilogue's scales (side ring)
+//   MMA        one thread issues the block's MMAs into a TMEM stage and
+//              commits to the fp16 ring's and the TMEM stage's barriers
+//   epilogue   8 warps; warp w reads TMEM lanes 32*(w%4).. (rows) for one
+//              half of the pass's token columns, adds the block terms to the
+//              segment chains, and finishes the item.
+// Every wait is bounded; on a timeout the block raises DS4MOE_DEVERR_TIMEOUT,
+// drains what it has in flight and leaves.
+#include "common.cuh"
+#include "internal.h"
+#include "umma.cuh"
+
+namespace ds4 {
+
+constexpr int PF_NP = 32;  // tokens per pass (MMA N)
+constexpr int PF_M = 128;  // rows per item (MMA M)
+constexpr int PF_CW = 4;   // converter warps
+constexpr int PF_EW = 8;   // epilogue warps
+constexpr int PF_WARPS = 2 + PF_CW + PF_EW;
+constexpr int PF_RS = 4;                 // raw stages
+constexpr int PF_RAW = 16 * Q2S_TILE;    // 21504 bytes, the largest raw stage
+constexpr int PF_FS = 3;                 // fp16 operand stages, one 32-block each
+constexpr int PF_TS = 4;                 // TMEM stages of 128 columns
+constexpr int PF_XS = 8;                 // side-data stages, >= PF_FS + PF_TS + 1
+constexpr int PF_TMEM_COLS = PF_TS * 128;
+// fp16 stage: A main [2 mats][128 x 32] | A min [2][128 x 16] | B main [32 x 32] | B min [32 x 16]
+constexpr int PF_F_AMAIN = 0, PF_F_AMIN = 16384, PF_F_BMAIN = 24576, PF_F_BMIN = 26624, PF_F_BYTES = 27648;
+// side stage: dx [32 columns] f32 | (d, dmin) [2 mats][128 rows] float2
+constexpr int PF_X_DD = 128, PF_X_BYTES = 128 + 2 * 128 * 8;
+constexpr int PF_OFF_RAW = 0;
+constexpr int PF_OFF_F = PF_OFF_RAW + PF_RS * PF_RAW;
+constexpr int PF_OFF_X = PF_OFF_F + PF_FS * PF_F_BYTES;
+constexpr int PF_OFF_BAR = PF_OFF_X + PF_XS * PF_X_BYTES;
+constexpr int PF_NBARS = 2 * PF_RS + 2 * PF_FS + 2 * PF_TS + PF_XS;
+constexpr int PF_OFF_MISC = PF_OFF_BAR + PF_NBARS * 8;
+constexpr int PF_SMEM = PF_OFF_MISC + 64;
+static_assert(PF_XS >= PF_FS + PF_TS + 1, "side ring too short");
+static_assert(PF_SMEM <= 227 * 1024, "prefill kernel does not fit shared memory");
+
+struct PfArgs {
+  int H, F, k, NS, T, E;
+  int K, rows;           // contraction length and rows of one expert matrix
+  int rf, sf;            // routed / shared weight format
+  const uint8_t *w_r, *w_s;
+  const int8_t *aq;      // activation codes [rows of act][K]
+  const float *ad;       // [.][K/32]
+  const int16_t *ag;     // [.][K/16]
+  const int32_t *pass_off;  // [E+2]: first pass of group g (0 shared, 1+e routed e)
+  const int32_t *meta;      // [E+1][2]: {n, list offset}
+  const int32_t *list;      // pair codes (token << 5) | slot
+  int8_t *hq;
+  float *dh;
+  int16_t *gsh;
+  float *apart;
+  uint32_t *err;
+};
+
+// Item i -> group, pass, 128-row block, and what every role needs of it.
+struct PfItem {
+  int g, pass, rb, nv, list_off, fmt;
+  const uint8_t *base;  // the group's matrix
+};
+
+template <int MODE>
+__device__ __forceinline__ PfItem pf_item(const PfArgs &a, int i, int RB) {
+  PfItem it;
+  const int P = i / RB;
+  it.rb = i - P * RB;
+  int lo = 0, hi = a.E + 1;  // largest g with pass_off[g] <= P
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a.pass_off + mid) <= P) lo = mid;
+    else hi = mid;
+  }
+  it.g = lo;
+  it.pass = P - __ldg(a.pass_off + lo);
+  const int n = __ldg(a.meta + 2 * lo);
+  it.list_off = __ldg(a.meta + 2 * lo + 1) + it.pass * PF_NP;
+  it.nv = min(PF_NP, n - it.pass * PF_NP);
+  it.fmt = lo == 0 ? a.sf : a.rf;
+  const size_t mat = (size_t)(MODE == 0 ? 2 : 1) * (a.rows / TILE_ROWS) * (a.K / kstep(it.fmt)) * tile_bytes(it.fmt);
+  it.base = lo == 0 ? a.w_s : a.w_r + (size_t)(lo - 1) * mat;
+  return it;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// fp16 bit pattern of a small integer |v| < 2048 (exact).
+__device__ __forceinline__ uint32_t h_of_int(int v) { return (uint32_t)__half_as_ushort(__int2half_rn(v)); }
+
+// 8 int8 codes (two words) -> 8 fp16: (1024 + 128 + q) built from the byte
+// q ^ 0x80 under the exponent byte 0x64, minus 1152.
+__device__ __forceinline__ uint4 i8x8_to_h(uint32_t w0, uint32_t w1) {
+  const uint32_t E = 0x64646464u, C = 0x64806480u;  // C = (1152, 1152)
+  w0 ^= 0x80808080u, w1 ^= 0x80808080u;
+  uint4 o;
+  o.x = hsub2_u(prmt(w0, E, 0x4140), C);
+  o.y = hsub2_u(prmt(w0, E, 0x4342), C);
+  o.z = hsub2_u(prmt(w1, E, 0x4140), C);
+  o.w = hsub2_u(prmt(w1, E, 0x4342), C);
+  return o;
+}
+
+// One 16-weight group word of the packed 2-bit layout (element 4s+e at bits
+// 8e+2s) times its scale: 16 fp16 values sc*q in element order, as two
+// 16-byte core-matrix rows. (1024 + q) * sc - 1024 * sc = sc*q, one rounding.
+__device__ __forceinline__ void q2s_group_to_h(uint32_t W, uint32_t sc2, uint32_t nsc2, uint4 &lo, uint4 &hi) {
+  const uint32_t E = 0x64646464u;
+  uint32_t t = W & 0x03030303u;
+  lo.x = hfma2_u(prmt(t, E, 0x4140), sc2, nsc2);
+  lo.y = hfma2_u(prmt(t, E, 0x4342), sc2, nsc2);
+  t = (W >> 2) & 0x03030303u;
+  lo.z = hfma2_u(prmt(t, E, 0x4140), sc2, nsc2);
+  lo.w = hfma2_u(prmt(t, E, 0x4342), sc2, nsc2);
+  t = (W >> 4) & 0x03030303u;
+  hi.x = hfma2_u(prmt(t, E, 0x4140), sc2, nsc2);
+  hi.y = hfma2_u(prmt(t, E, 0x4342), sc2, nsc2);
+  t = (W >> 6) & 0x03030303u;
+  hi.z = hfma2_u(prmt(t, E, 0x4140), sc2, nsc2);
+  hi.w = hfma2_u(prmt(t, E, 0x4342), sc2, nsc2);
+}
+
+__device__ __forceinline__ uint32_t h2_of(int v) {
+  const uint32_t h = h_of_int(v);
+  return h | (h << 16);
+}
+
+struct PfBars {
+  uint32_t raw_full, raw_empty, f_full, f_empty, t_full, t_empty, x_full;
+};
+
+__device__ __forceinline__ PfBars pf_bars(uint8_t *smem) {
+  const uint32_t b = smem_u32(smem + PF_OFF_BAR);
+  PfBars p;
+  p.raw_full = b;
+  p.raw_empty = p.raw_full + 8 * PF_RS;
+  p.f_full = p.raw_empty + 8 * PF_RS;
+  p.f_empty = p.f_full + 8 * PF_FS;
+  p.t_full = p.f_empty + 8 * PF_FS;
+  p.t_empty = p.t_full + 8 * PF_TS;
+  p.x_full = p.t_empty + 8 * PF_TS;
+  return p;
+}
+
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > (1ll << 31)) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void pf_fail(volatile int *abort, uint32_t *err) {
+  if (!*abort) {
+    *abort = 1;
+    raise_flag(err, DS4MOE_DEVERR_TIMEOUT);
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int MATS = MODE == 0 ? 2 : 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const PfBars B = pf_bars(smem);
+  volatile int *abort = (volatile int *)(smem + PF_OFF_MISC);
+  uint32_t *tslot = (uint32_t *)(smem + PF_OFF_MISC + 16);
+  const int RB = a.rows / PF_M;
+  const int n_items = __ldg(a.pass_off + a.E + 1) * RB;
+  const int nb = a.K >> 5;
+  const uint32_t sm0 = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    for (int i = 0; i < PF_RS; i++) mbar_init(B.raw_full + 8 * i, 1), mbar_init(B.raw_empty + 8 * i, PF_CW);
+    for (int i = 0; i < PF_FS; i++) mbar_init(B.f_full + 8 * i, PF_CW), mbar_init(B.f_empty + 8 * i, 1);
+    for (int i = 0; i < PF_TS; i++) mbar_init(B.t_full + 8 * i, 1), mbar_init(B.t_empty + 8 * i, PF_EW);
+    for (int i = 0; i < PF_XS; i++) mbar_init(B.x_full + 8 * i, PF_CW);
+    fence_mbar_init();
+  }
+  // the parts of the min tiles that no block writes stay zero
+  for (int i = threadIdx.x; i < PF_FS * (PF_F_BYTES / 16); i += blockDim.x)
+    sts128(sm0 + PF_OFF_F + 16 * i, 0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 1) tmem_alloc(smem_u32(tslot), PF_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0) {
+    // ===================== producer: raw weight stages
+    uint32_t gst = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const PfItem it = pf_item<MODE>(a, i, RB);
+      if (it.nv <= 0) continue;
+      const bool q2 = it.fmt == DS4MOE_Q2S;
+      const int TB = tile_bytes(it.fmt), KS = a.K / kstep(it.fmt);
+      const int ks_per = q2 ? 1 : 2;                 // K-steps per stage
+      const int nchunk = MODE == 0 ? 8 : 4;          // 16-row groups (gate/up) or 32-row groups (down)
+      const int chunk = 2 * TB * ks_per;
+      const int nst = KS / ks_per;
+      for (int st = 0; st < nst; st++, gst++) {
+        const int rs = gst % PF_RS;
+        if (gst >= PF_RS && !pf_wait(B.raw_empty + 8 * rs, ((gst / PF_RS) - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(B.raw_full + 8 * rs, nchunk * chunk);
+        }
+        __syncwarp();
+        if (lane < nchunk) {
+          const int grp = it.rb * nchunk + lane;  // 16-row group (gate/up) or 32-row group (down)
+          const uint8_t *src = it.base + ((size_t)grp * KS + (size_t)st * ks_per) * 2 * TB;
+          bulk_g2s(sm0 + PF_OFF_RAW + rs * PF_RAW + lane * chunk, src, chunk, B.raw_full + 8 * rs);
+        }
+      }
+    }
+    if (!ok) pf_fail(abort, a.err);
+    // nothing may still be landing in shared memory when the block leaves:
+    // wait (bounded) for the stages nobody consumed
+    if (*abort) {
+      for (uint32_t g = gst > PF_RS ? gst - PF_RS : 0; g < gst; g++) (void)mbar_wait_bounded(B.raw_full + 8 * (g % PF_RS), (g / PF_RS) & 1);
+    }
+  } else if (warp == 1) {
+    // ===================== MMA issuer
+    uint32_t fc = 0;
+    bool ok = true;
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_f16(PF_M, PF_NP);
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        const PfItem it = pf_item<MODE>(a, i, RB);
+        if (it.nv <= 0) continue;
+        const bool q2 = it.fmt == DS4MOE_Q2S;
+        for (int b = 0; b < nb; b++, fc++) {
+          const int fs = fc % PF_FS, ts = fc % PF_TS;
+          if (!pf_wait(B.f_full + 8 * fs, (fc / PF_FS) & 1, abort) ||
+              (fc >= PF_TS && !pf_wait(B.t_empty + 8 * ts, ((fc / PF_TS) - 1) & 1, abort))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t f = sm0 + PF_OFF_F + fs * PF_F_BYTES;
+          const uint32_t d0 = tbase + ts * 128;
+#pragma unroll
+          for (int m = 0; m < MATS; m++) {
+            const uint32_t am = f + PF_F_AMAIN + m * 8192;
+            umma_f16(d0 + 32 * m, umma_desc(am, 128, 512), umma_desc(f + PF_F_BMAIN, 128, 512), idesc, 0);
+            umma_f16(d0 + 32 * m, umma_desc(am + 256, 128, 512), umma_desc(f + PF_F_BMAIN + 256, 128, 512), idesc, 1);
+            if (q2)
+              umma_f16(d0 + 64 + 32 * m, umma_desc(f + PF_F_AMIN + m * 4096, 128, 256),
+                       umma_desc(f + PF_F_BMIN, 128, 256), idesc, 0);
+          }
+          umma_commit(B.f_empty + 8 * fs);
+          umma_commit(B.t_full + 8 * ts);
+        }
+      }
+      if (!ok) pf_fail(abort, a.err);
+      // the last MMAs must be complete before TMEM is released
+      if (fc > 0) (void)mbar_wait_bounded(B.t_full + 8 * ((fc - 1) % PF_TS), ((fc - 1) / PF_TS) & 1);
+    }
+    __syncwarp();
+  } else if (warp < 2 + PF_CW) {
+    // ===================== converters (128 threads)
+    const int c = threadIdx.x - 64;
+    const int rr = c & 15, tau0 = c >> 4;      // weight rows: tiles tau0 (+8), row rr
+    const int col = c >> 2, kq = c & 3;        // token side: column col, elements 8kq..8kq+7
+    const int cw = warp - 2;
+    uint32_t fc = 0, gst = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const PfItem it = pf_item<MODE>(a, i, RB);
+      if (it.nv <= 0) continue;
+      const bool q2 = it.fmt == DS4MOE_Q2S;
+      const int TB = tile_bytes(it.fmt);
+      const int bpst = q2 ? 8 : 2;  // blocks per raw stage
+      // this thread's token column: pass token 2*(col%16) + col/16
+      const int pt = 2 * (col & 15) + (col >> 4);
+      int arow = -1;
+      if (pt < it.nv) {
+        const int code = __ldg(a.list + it.list_off + pt);
+        arow = MODE == 0 ? (code >> 5) : (code >> 5) * a.NS + (code & 31);
+      }
+      // software prefetch of the token data two blocks ahead
+      uint2 xv[2];
+      int gv[2];
+      float dv[2];
+      auto load_tok = [&](int b, uint2 &x, int &gsv, float &d) {
+        x = make_uint2(0, 0), gsv = 0, d = 0.0f;
+        if (arow >= 0 && b < nb) {
+          x = __ldg((const uint2 *)(a.aq + (size_t)arow * a.K + 32 * b + 8 * kq));
+          if (kq == 0) gsv = __ldg((const int *)(a.ag + (size_t)arow * (a.K >> 4) + 2 * b));
+          if (kq == 1) d = __ldg(a.ad + (size_t)arow * nb + b);
+        }
+      };
+      load_tok(0, xv[0], gv[0], dv[0]);
+      load_tok(1, xv[1], gv[1], dv[1]);
+      float dd_d[2] = {0.0f, 0.0f}, dd_m[2] = {0.0f, 0.0f};
+      for (int b = 0; b < nb; b += 2) {
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+          const int bb = b + u;
+          const int bin = bb % bpst;
+          const int rs = gst % PF_RS;
+          if (bin == 0 && !pf_wait(B.raw_full + 8 * rs, (gst / PF_RS) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          const int fs = fc % PF_FS, xs = fc % PF_XS;
+          if (fc >= PF_FS && !pf_wait(B.f_empty + 8 * fs, ((fc / PF_FS) - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t raw = sm0 + PF_OFF_RAW + rs * PF_RAW;
+          const uint32_t f = sm0 + PF_OFF_F + fs * PF_F_BYTES;
+          const uint32_t xsd = sm0 + PF_OFF_X + xs * PF_X_BYTES;
+          // ---- weights: tiles tau0 and (gate/up) tau0 + 8, row rr
+#pragma unroll
+          for (int h2 = 0; h2 < (MODE == 0 ? 2 : 1); h2++) {
+            const int tau = tau0 + 8 * h2;
+            const int m = MODE == 0 ? (tau & 1) : 0;
+            const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
+            const uint32_t arow_a = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
+            if (q2) {
+              const uint32_t tile = raw + tau * TB;
+              const int L = 2 * rr + (bin & 1), j = bin >> 1;
+              if (bin == 0) {
+                const uint32_t ddw = ld_shared_u32(tile + Q2S_DD + 4 * rr);
+                dd_d[h2] = half_bits_to_float(ddw), dd_m[h2] = half_bits_to_float(ddw >> 16);
+              }
+              const uint2 w = ld_shared_v2(tile + Q2S_QS + 512 * (j >> 1) + 16 * L + 8 * (j & 1));
+              const uint32_t smb = ld_shared_u32(tile + Q2S_SM + ((8 * L + 2 * j) & ~3)) >> (8 * ((2 * j) & 3));
+              const int sc0 = smb & 15, mn0 = (smb >> 4) & 15, sc1 = (smb >> 8) & 15, mn1 = (smb >> 12) & 15;
+              uint4 lo, hi;
+              q2s_group_to_h(w.x, h2_of(sc0), h2_of(-1024 * sc0), lo, hi);
+              sts128(arow_a, lo.x, lo.y, lo.z, lo.w);
+              sts128(arow_a + 128, hi.x, hi.y, hi.z, hi.w);
+              q2s_group_to_h(w.y, h2_of(sc1), h2_of(-1024 * sc1), lo, hi);
+              sts128(arow_a + 256, lo.x, lo.y, lo.z, lo.w);
+              sts128(arow_a + 384, hi.x, hi.y, hi.z, hi.w);
+              sts128(f + PF_F_AMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, h_of_int(mn0) | (h_of_int(mn1) << 16),
+                     0, 0, 0);
+              asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8),
+                           "f"(dd_d[h2]), "f"(dd_m[h2])
+                           : "memory");
+            } else {
+              const uint32_t tile = raw + (tau >> 1) * 4 * TB + bin * 2 * TB + (tau & 1) * TB;
+              const uint32_t dw = ld_shared_u32(tile + 4 * (rr >> 1));
+              const float d = half_bits_to_float((rr & 1) ? dw >> 16 : dw);
+              const uint4 q0 = ld_shared_v4(tile + Q8_Q + 32 * rr), q1 = ld_shared_v4(tile + Q8_Q + 32 * rr + 16);
+              uint4 o = i8x8_to_h(q0.x, q0.y);
+              sts128(arow_a, o.x, o.y, o.z, o.w);
+              o = i8x8_to_h(q0.z, q0.w);
+              sts128(arow_a + 128, o.x, o.y, o.z, o.w);
+              o = i8x8_to_h(q1.x, q1.y);
+              sts128(arow_a + 256, o.x, o.y, o.z, o.w);
+              o = i8x8_to_h(q1.z, q1.w);
+              sts128(arow_a + 384, o.x, o.y, o.z, o.w);
+              asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8), "f"(d),
+                           "f"(0.0f)
+                           : "memory");
+            }
+          }
+          // ---- tokens: B main (codes), B min (group sums), dx
+          {
+            const uint4 o = i8x8_to_h(xv[u].x, xv[u].y);
+            sts128(f + PF_F_BMAIN + ((col >> 3) * 4 + kq) * 128 + (col & 7) * 16, o.x, o.y, o.z, o.w);
+            if (kq == 0 && q2)
+              sts128(f + PF_F_BMIN + (col >> 3) * 256 + (col & 7) * 16,
+                     h_of_int((int)(int16_t)(gv[u] & 0xFFFF)) | (h_of_int(gv[u] >> 16) << 16), 0, 0, 0);
+            if (kq == 1) asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsd + 4 * col), "f"(dv[u]) : "memory");
+          }
+          load_tok(bb + 2, xv[u], gv[u], dv[u]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(B.f_full + 8 * fs);
+            mbar_arrive(B.x_full + 8 * xs);
+          }
+          fc++;
+          if (bin == bpst - 1) {
+            if (lane == 0) mbar_arrive(B.raw_empty + 8 * rs);
+            gst++;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+    (void)cw;
+    if (!ok) pf_fail(abort, a.err);
+  } else {
+    // ===================== epilogue (8 warps)
+    const int q = warp & 3, p = (warp - 2 - PF_CW) >> 2;  // TMEM lane quadrant, token half
+    const int row = 32 * q + lane;
+    uint32_t fc = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const PfItem it = pf_item<MODE>(a, i, RB);
+      if (it.nv <= 0) continue;
+      const bool q2 = it.fmt == DS4MOE_Q2S;
+      const int nvp = (it.nv - p + 1) >> 1;  // valid columns 16p + j, j < nvp
+      const int S = expert_segs(it.fmt, a.K), bseg = nb / S;
+      float seg[MATS][16], tot[MATS][16];
+#pragma unroll
+      for (int m = 0; m < MATS; m++)
+#pragma unroll
+        for (int j = 0; j < 16; j++) seg[m][j] = 0.0f, tot[m][j] = 0.0f;
+      for (int b = 0; b < nb; b++, fc++) {
+        const int ts = fc % PF_TS, xs = fc % PF_XS;
+        if (!pf_wait(B.t_full + 8 * ts, (fc / PF_TS) & 1, abort) ||
+            !pf_wait(B.x_full + 8 * xs, (fc / PF_XS) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t xsd = sm0 + PF_OFF_X + xs * PF_X_BYTES;
+        const uint32_t t0 = tbase + ((uint32_t)(32 * q) << 16) + ts * 128 + 16 * p;
+#pragma unroll
+        for (int m = 0; m < MATS; m++) {
+          float A[16], Bm[16];
+          tmem_ld16x2(t0 + 32 * m, t0 + 64 + 32 * m, A, Bm);
+          if (m == MATS - 1) {  // every load of the stage is done: release it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.t_empty + 8 * ts);
+          }
+          const uint2 ddv = ld_shared_v2(xsd + PF_X_DD + (m * 128 + row) * 8);
+          const float d = __uint_as_float(ddv.x), dmin = __uint_as_float(ddv.y);
+#pragma unroll
+          for (int j4 = 0; j4 < 4; j4++) {
+            if (4 * j4 < nvp) {
+              const uint4 v = ld_shared_v4(xsd + 4 * (16 * p + 4 * j4));
+              const float dxs[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                                    __uint_as_float(v.w)};
+#pragma unroll
+              for (int jj = 0; jj < 4; jj++) {
+                const int j = 4 * j4 + jj;
+                float term;
+                if (q2) term = __fmul_rn(dxs[jj], __fmaf_rn(d, A[j], -__fmul_rn(dmin, Bm[j])));
+                else term = __fmul_rn(__fmul_rn(d, dxs[jj]), A[j]);
+                seg[m][j] = __fadd_rn(seg[m][j], term);
+              }
+            }
+          }
+        }
+        if ((b + 1) % bseg == 0) {
+#pragma unroll
+          for (int m = 0; m < MATS; m++)
+#pragma unroll
+            for (int j = 0; j < 16; j++) tot[m][j] = __fadd_rn(tot[m][j], seg[m][j]), seg[m][j] = 0.0f;
+        }
+      }
+      if (!ok) break;
+      // ---- finish the item
+#pragma unroll
+      for (int j = 0; j < 16; j++) {
+        if (j < nvp) {
+          const int code = __ldg(a.list + it.list_off + 2 * j + p);
+          const int sr = (code >> 5) * a.NS + (code & 31);
+          if (MODE == 0) {
+            const float hv = __fmul_rn(cas_silu(tot[0][j]), tot[MATS - 1][j]);
+            const int blk = it.rb * 4 + q;
+            const float amax = warp_max(fabsf(hv));
+            const float dq = __fdiv_rn(amax, 127.0f);
+            const int cq = cas_code(hv, dq);
+            const int gsum = half_warp_sum(cq);
+            a.hq[(size_t)sr * a.F + 32 * blk + lane] = (int8_t)cq;
+            if (lane == 0) a.dh[(size_t)sr * (a.F >> 5) + blk] = dq;
+            if ((lane & 15) == 0) a.gsh[(size_t)sr * (a.F >> 4) + 2 * blk + (lane >> 4)] = (int16_t)gsum;
+          } else {
+            a.apart[(size_t)sr * a.H + it.rb * PF_M + row] = tot[0][j];
+          }
+        }
+      }
+    }
+    if (!ok) pf_fail(abort, a.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, PF_TMEM_COLS);
+  }
+}
+
+// ===========================================================================
+// Bucketing: one block per group g (0 = the shared expert, 1 + e = routed
+// expert e). Every block histograms all routed pairs, derives the groups'
+// list offsets and pass offsets (prefix sums in group order), and lists its
+// own pairs in (token, slot) order: (t << 5) | slot.
+__global__ void __launch_bounds__(512) k_pf_bucket(const int32_t *__restrict__ ids, int T, int k, int E,
+                                                   int n_shared, int32_t *meta, int32_t *pass_off,
+                                                   int32_t *list) {
+  extern __shared__ int32_t bsm[];
+  int32_t *cnt = bsm;                  // [E+1]
+  int32_t *wsum = bsm + E + 1;         // [32]
+  const int g = blockIdx.x, tid = threadIdx.x, nth = blockDim.x;
+  const int n = T * k;
+  for (int i = tid; i <= E; i += nth) cnt[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += nth) {
+    const int e = __ldg(ids + i);
+    if (e >= 0 && e < E) atomicAdd(&cnt[1 + e], 1);
+  }
+  if (tid == 0) cnt[0] = n_shared ? T : 0;
+  __syncthreads();
+  if (tid == 0) {
+    int lo = 0, po = 0, my_lo = 0, my_po = 0;
+    for (int j = 0; j <= E; j++) {
+      if (j == g) my_lo = lo, my_po = po;
+      lo += cnt[j];
+      po += (cnt[j] + PF_NP - 1) / PF_NP;
+    }
+    meta[2 * g] = cnt[g];
+    meta[2 * g + 1] = my_lo;
+    pass_off[g] = my_po;
+    if (g == 0) pass_off[E + 1] = po;
+    wsum[31] = my_lo;
+  }
+  __syncthreads();
+  const int base = wsum[31];
+  __syncthreads();
+  if (g == 0) {
+    for (int t = tid; t < (n_shared ? T : 0); t += nth) list[base + t] = (t << 5) | k;
+    return;
+  }
+  const int e = g - 1, warp = tid >> 5, lane = tid & 31, nw = nth >> 5;
+  int run = 0;
+  for (int i0 = 0; i0 < n; i0 += nth) {
+    const int i = i0 + tid;
+    const bool f = i < n && __ldg(ids + i) == e;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) wsum[warp] = __popc(bal);
+    __syncthreads();
+    int before = run;
+    for (int w = 0; w < warp; w++) before += wsum[w];
+    if (f) list[base + before + __popc(bal & ((1u << lane) - 1))] = ((i / k) << 5) | (i % k);
+    int tot = 0;
+    for (int w = 0; w < nw; w++) tot += wsum[w];
+    run += tot;
+    __syncthreads();
+  }
+}
+
+// y[t] += sum_j w_j * a_j + a_shared (CAS step 7), one thread per element.
+__global__ void k_pf_combine(const int32_t *__restrict__ ids, const float *__restrict__ w,
+                             const float *__restrict__ apart, float *y, int T, int H, int k, int NS, int n_shared) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)T * H) return;
+  const int t = (int)(idx / H), r = (int)(idx % H);
+  if (__ldg(ids + (size_t)t * k) < 0) return;
+  float acc = 0.0f;
+  for (int j = 0; j < k; j++)
+    acc = __fadd_rn(acc, __fmul_rn(__ldg(w + (size_t)t * k + j), __ldcg(apart + ((size_t)t * NS + j) * H + r)));
+  if (n_shared) acc = __fadd_rn(acc, __ldcg(apart + ((size_t)t * NS + k) * H + r));
+  y[idx] = __fadd_rn(y[idx], acc);
+}
+
+// ===========================================================================
+// Host side.
+
+bool prefill_supported(const ds4moe_layer_desc &d) {
+  // 128-row items of every matrix; gate/up rows = ffn, down rows = hidden
+  return d.ffn % PF_M == 0 && d.hidden % PF_M == 0;
+}
+
+cudaError_t prefill_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(k_pf_experts<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_pf_experts<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+  return e;
+}
+
+size_t prefill_list_ints(int T, int k, int n_shared) { return (size_t)T * k + (size_t)(n_shared ? T : 0); }
+
+cudaError_t launch_prefill(ds4moe_layer *h, const float *x, const int32_t *tok, int T, float *y, cudaStream_t s,
+                           cudaEvent_t *ev) {
+  const ds4moe_layer_desc &d = h->d;
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], s);
+  };
+  const int E = d.n_experts, k = d.top_k;
+  mark(0);
+  mark(1);
+  cudaError_t e = launch_dec_route(h, x, tok, T, h->ids, h->wts, false, s);
+  mark(2);
+  if (e == cudaSuccess) {
+    const size_t smem = (size_t)(E + 1 + 32) * 4;
+    k_pf_bucket<<<E + 1, 512, smem, s>>>(h->ids, T, k, E, d.n_shared, h->pf_meta, h->pf_pass, h->pf_list);
+    e = cudaGetLastError();
+  }
+  mark(3);
+  PfArgs a = {};
+  a.H = d.hidden, a.F = d.ffn, a.k = k, a.NS = h->NS, a.T = T, a.E = E;
+  a.rf = d.routed_fmt, a.sf = d.n_shared ? d.shared_fmt : d.routed_fmt;
+  a.pass_off = h->pf_pass, a.meta = h->pf_meta, a.list = h->pf_list;
+  a.hq = h->hq, a.dh = h->dh, a.gsh = h->gsh, a.apart = h->apart, a.err = h->err;
+  const int grid = h->n_sm;
+  if (e == cudaSuccess) {
+    PfArgs g = a;
+    g.K = d.hidden, g.rows = d.ffn, g.w_r = h->gu, g.w_s = h->sgu, g.aq = h->xq, g.ad = h->dx, g.ag = h->gs;
+    k_pf_experts<0><<<grid, PF_WARPS * 32, PF_SMEM, s>>>(g);
+    e = cudaGetLastError();
+  }
+  mark(4);
+  if (e == cudaSuccess) {
+    PfArgs g = a;
+    g.K = d.ffn, g.rows = d.hidden, g.w_r = h->dn, g.w_s = h->sdn, g.aq = h->hq, g.ad = h->dh, g.ag = h->gsh;
+    k_pf_experts<1><<<grid, PF_WARPS * 32, PF_SMEM, s>>>(g);
+    e = cudaGetLastError();
+  }
+  mark(5);
+  if (e == cudaSuccess) {
+    const long long n = (long long)T * d.hidden;
+    k_pf_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(h->ids, h->wts, h->apart, y, T, d.hidden, k, h->NS,
+                                                            d.n_shared);
+    e = cudaGetLastError();
+  }
+  mark(6);
+  h->launches += 5;
+  return e;
+}
+
+}  // namespace ds4

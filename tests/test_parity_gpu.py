@@ -234,3 +234,66 @@ def test_empty_and_too_many_tokens(ora):
         layer.forward(x, y, n_tok=66)
     with pytest.raises(ds4.Ds4MoeError):
         layer.forward(x, x, n_tok=3)  # y must not alias x
+
+
+# ---- the prefill path (tensor-core grouped GEMM), forced onto small calls
+# by lowering the token threshold before the layer is created
+
+@pytest.fixture
+def prefill_always(monkeypatch):
+    monkeypatch.setenv("DS4MOE_PREFILL_MIN_TOKENS", "1")
+
+
+@pytest.mark.parametrize("spec,seed,T", [
+    (synth.MICRO, 51, 1), (synth.MICRO, 51, 2), (synth.MICRO, 51, 7), (synth.MICRO, 51, 16),
+    (synth.MICRO, 51, 33), (synth.MICRO, 51, 64),
+    (synth.TINY, 53, 4),                 # Q8_0 routed experts, fp32 router
+    (synth.MICRO_HASH, 55, 130),         # hash routing
+])
+def test_prefill_path_bit_exact(ora, prefill_always, spec, seed, T):
+    run_case(ora, spec, seed, T, max_tokens=max(T, 64))
+
+
+def test_prefill_multi_pass_experts(ora, prefill_always):
+    """300 tokens over 8 experts (top-3): every expert sees more than one pass
+    of 32 tokens, the shared expert ten."""
+    run_case(ora, synth.MICRO, 57, 300, max_tokens=300)
+
+
+def test_prefill_chunks(ora, monkeypatch):
+    """A call larger than the prefill chunk runs chunk by chunk."""
+    monkeypatch.setenv("DS4MOE_PREFILL_MIN_TOKENS", "65")
+    run_case(ora, synth.MICRO_HASH, 59, 200, max_tokens=200)
+
+
+def test_ds4_prefill_small(ora, prefill_always):
+    run_case(ora, synth.DS4, 61, 5)
+
+
+def test_ds4_zipf_prefill_256(ora):
+    """Zipf(1.1) expert popularity over 256 tokens: hot experts take several
+    passes on the prefill path."""
+    run_case(ora, synth.DS4_ZIPF, 63, 256)
+
+
+def test_decode_and_prefill_paths_agree(ora, monkeypatch):
+    """The same tokens through the decode kernels and through the prefill
+    kernels give the same bits."""
+    import torch
+    spec, T = synth.MICRO, 40
+    w = synth.gen_layer(spec, 65, 0)
+    ol = ora.layer(spec, w)
+    x = torch.from_numpy(margin_inputs(ol, spec, 65, T)).cuda()
+    monkeypatch.setenv("DS4MOE_PREFILL_MIN_TOKENS", "1")
+    lp = make_layer(spec, w, T)
+    monkeypatch.setenv("DS4MOE_PREFILL_MIN_TOKENS", "100000")
+    ld = make_layer(spec, w, T)
+    yp = torch.zeros(T, spec.hidden, device="cuda")
+    yd = torch.zeros_like(yp)
+    lp.forward(x, yp)
+    ld.forward(x, yd)
+    torch.cuda.synchronize()
+    assert lp.device_error() == 0 and ld.device_error() == 0
+    assert torch.equal(yp, yd)
+    lp.close()
+    ld.close()
