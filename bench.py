@@ -144,6 +144,23 @@ def dist_setup():
     return world, rank, local
 
 
+def reduce_max(value: float, device) -> float:
+    """The largest `value` over the ranks of the job (the value itself when
+    there is one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, max_seconds: float, world: int) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / max_seconds
+
+
 def run_reference(args, spec, T, desc):
     """The reference arm: the CPU oracle, as it stands, on the host cores."""
     world, rank, _ = dist_setup()
@@ -313,12 +330,8 @@ def main():
     clk = clocks.stop()
     launches = launches_per_step * args.steps
     step_ms = np.array([a.elapsed_time(b) for a, b in ev])
-    total_s = float(step_ms.sum()) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = world * args.steps * T / total_s
+    total_s = reduce_max(float(step_ms.sum()) / 1e3, dev)
+    value = job_throughput(args.steps * T, total_s, world)
 
     # Stage times: events recorded by the library around each kernel of a
     # forward (no graph), same layer rotation.

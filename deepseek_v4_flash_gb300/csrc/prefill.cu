@@ -168,9 +168,16 @@ __device__ __forceinline__ void q2s_group_to_h(uint32_t W, uint32_t sc2, uint32_
   hi.w = hfma2_u(prmt(t, E, 0x4342), sc2, nsc2);
 }
 
-__device__ __forceinline__ uint32_t h2_of(int v) {
-  const uint32_t h = h_of_int(v);
-  return h | (h << 16);
+// fp16x2 bit pattern of two small integers 0 <= a, b < 1024 (exact):
+// (1024 + v) from the exponent pattern 0x6400, minus 1024.
+__device__ __forceinline__ uint32_t h2_small(uint32_t a, uint32_t b) {
+  return hsub2_u(0x64006400u | a | (b << 16), 0x64006400u);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 struct PfBars {
@@ -368,48 +375,78 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
           const uint32_t raw = sm0 + PF_OFF_RAW + rs * PF_RAW;
           const uint32_t f = sm0 + PF_OFF_F + fs * PF_F_BYTES;
           const uint32_t xsd = sm0 + PF_OFF_X + xs * PF_X_BYTES;
-          // ---- weights: tiles tau0 and (gate/up) tau0 + 8, row rr
+          // ---- weights: tiles tau0 and (gate/up) tau0 + 8, row rr. All shared
+          // loads first, then the conversions (independent chains), then the
+          // stores, so that the ordered shared-memory accesses do not
+          // serialise the arithmetic.
+          constexpr int NH = MODE == 0 ? 2 : 1;
+          if (q2) {
+            const int L = 2 * rr + (bin & 1), j = bin >> 1;
+            uint2 w[NH];
+            uint32_t smb[NH];
 #pragma unroll
-          for (int h2 = 0; h2 < (MODE == 0 ? 2 : 1); h2++) {
-            const int tau = tau0 + 8 * h2;
-            const int m = MODE == 0 ? (tau & 1) : 0;
-            const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
-            const uint32_t arow_a = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
-            if (q2) {
-              const uint32_t tile = raw + tau * TB;
-              const int L = 2 * rr + (bin & 1), j = bin >> 1;
+            for (int h2 = 0; h2 < NH; h2++) {
+              const uint32_t tile = raw + (tau0 + 8 * h2) * TB;
               if (bin == 0) {
                 const uint32_t ddw = ld_shared_u32(tile + Q2S_DD + 4 * rr);
                 dd_d[h2] = half_bits_to_float(ddw), dd_m[h2] = half_bits_to_float(ddw >> 16);
               }
-              const uint2 w = ld_shared_v2(tile + Q2S_QS + 512 * (j >> 1) + 16 * L + 8 * (j & 1));
-              const uint32_t smb = ld_shared_u32(tile + Q2S_SM + ((8 * L + 2 * j) & ~3)) >> (8 * ((2 * j) & 3));
-              const int sc0 = smb & 15, mn0 = (smb >> 4) & 15, sc1 = (smb >> 8) & 15, mn1 = (smb >> 12) & 15;
-              uint4 lo, hi;
-              q2s_group_to_h(w.x, h2_of(sc0), h2_of(-1024 * sc0), lo, hi);
-              sts128(arow_a, lo.x, lo.y, lo.z, lo.w);
-              sts128(arow_a + 128, hi.x, hi.y, hi.z, hi.w);
-              q2s_group_to_h(w.y, h2_of(sc1), h2_of(-1024 * sc1), lo, hi);
-              sts128(arow_a + 256, lo.x, lo.y, lo.z, lo.w);
-              sts128(arow_a + 384, hi.x, hi.y, hi.z, hi.w);
-              sts128(f + PF_F_AMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, h_of_int(mn0) | (h_of_int(mn1) << 16),
-                     0, 0, 0);
+              w[h2] = ld_shared_v2(tile + Q2S_QS + 512 * (j >> 1) + 16 * L + 8 * (j & 1));
+              smb[h2] = ld_shared_u32(tile + Q2S_SM + ((8 * L + 2 * j) & ~3)) >> (8 * ((2 * j) & 3));
+            }
+            uint4 lo[NH][2], hi[NH][2];
+            uint32_t mnw[NH];
+#pragma unroll
+            for (int h2 = 0; h2 < NH; h2++) {
+              const uint32_t sm = smb[h2];
+              const uint32_t sc2a = h2_small(sm & 15, sm & 15), sc2b = h2_small((sm >> 8) & 15, (sm >> 8) & 15);
+              q2s_group_to_h(w[h2].x, sc2a, hmul2_u(sc2a, 0xE400E400u), lo[h2][0], hi[h2][0]);
+              q2s_group_to_h(w[h2].y, sc2b, hmul2_u(sc2b, 0xE400E400u), lo[h2][1], hi[h2][1]);
+              mnw[h2] = h2_small((sm >> 4) & 15, (sm >> 12) & 15);
+            }
+#pragma unroll
+            for (int h2 = 0; h2 < NH; h2++) {
+              const int tau = tau0 + 8 * h2;
+              const int m = MODE == 0 ? (tau & 1) : 0;
+              const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
+              const uint32_t ar = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
+              sts128(ar, lo[h2][0].x, lo[h2][0].y, lo[h2][0].z, lo[h2][0].w);
+              sts128(ar + 128, hi[h2][0].x, hi[h2][0].y, hi[h2][0].z, hi[h2][0].w);
+              sts128(ar + 256, lo[h2][1].x, lo[h2][1].y, lo[h2][1].z, lo[h2][1].w);
+              sts128(ar + 384, hi[h2][1].x, hi[h2][1].y, hi[h2][1].z, hi[h2][1].w);
+              sts128(f + PF_F_AMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, mnw[h2], 0, 0, 0);
               asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8),
                            "f"(dd_d[h2]), "f"(dd_m[h2])
                            : "memory");
-            } else {
+            }
+          } else {
+            uint4 q0[NH], q1[NH];
+            uint32_t dw[NH];
+#pragma unroll
+            for (int h2 = 0; h2 < NH; h2++) {
+              const int tau = tau0 + 8 * h2;
               const uint32_t tile = raw + (tau >> 1) * 4 * TB + bin * 2 * TB + (tau & 1) * TB;
-              const uint32_t dw = ld_shared_u32(tile + 4 * (rr >> 1));
-              const float d = half_bits_to_float((rr & 1) ? dw >> 16 : dw);
-              const uint4 q0 = ld_shared_v4(tile + Q8_Q + 32 * rr), q1 = ld_shared_v4(tile + Q8_Q + 32 * rr + 16);
-              uint4 o = i8x8_to_h(q0.x, q0.y);
-              sts128(arow_a, o.x, o.y, o.z, o.w);
-              o = i8x8_to_h(q0.z, q0.w);
-              sts128(arow_a + 128, o.x, o.y, o.z, o.w);
-              o = i8x8_to_h(q1.x, q1.y);
-              sts128(arow_a + 256, o.x, o.y, o.z, o.w);
-              o = i8x8_to_h(q1.z, q1.w);
-              sts128(arow_a + 384, o.x, o.y, o.z, o.w);
+              dw[h2] = ld_shared_u32(tile + 4 * (rr >> 1));
+              q0[h2] = ld_shared_v4(tile + Q8_Q + 32 * rr);
+              q1[h2] = ld_shared_v4(tile + Q8_Q + 32 * rr + 16);
+            }
+            uint4 o[NH][4];
+#pragma unroll
+            for (int h2 = 0; h2 < NH; h2++) {
+              o[h2][0] = i8x8_to_h(q0[h2].x, q0[h2].y);
+              o[h2][1] = i8x8_to_h(q0[h2].z, q0[h2].w);
+              o[h2][2] = i8x8_to_h(q1[h2].x, q1[h2].y);
+              o[h2][3] = i8x8_to_h(q1[h2].z, q1[h2].w);
+            }
+#pragma unroll
+            for (int h2 = 0; h2 < NH; h2++) {
+              const int tau = tau0 + 8 * h2;
+              const int m = MODE == 0 ? (tau & 1) : 0;
+              const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
+              const uint32_t ar = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
+#pragma unroll
+              for (int kc = 0; kc < 4; kc++) sts128(ar + 128 * kc, o[h2][kc].x, o[h2][kc].y, o[h2][kc].z, o[h2][kc].w);
+              const float d = half_bits_to_float((rr & 1) ? dw[h2] >> 16 : dw[h2]);
               asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8), "f"(d),
                            "f"(0.0f)
                            : "memory");
