@@ -178,28 +178,32 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// try_wait with a suspend-time hint (nanoseconds): the waiting warp sleeps
-// until the phase completes or the hint expires instead of spinning, so it
-// takes no issue slots from the warps that do the work.
+// One bounded test of the phase: try_wait without a suspend-time hint lets
+// the hardware suspend the warp for its own short default interval only.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
 // Bounded wait: gives up after ~2^31 SM cycles (about a second) and returns
-// false; callers then raise DS4MOE_DEVERR_TIMEOUT and leave.
+// false; callers then raise DS4MOE_DEVERR_TIMEOUT and leave. Between tests
+// the warp sleeps (growing to 256 ns), so waiting warps leave the issue
+// slots to the warps that do the work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
+  unsigned ns = 32;
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > (1ll << 31)) return false;
+    __nanosleep(ns);
+    ns = ns < 256 ? 2 * ns : 256;
   }
   return true;
 }

@@ -141,6 +141,13 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
     const int e = threadIdx.x + i * RC_WARPS * 32;
     bias_r[i] = (seg == 0 && a.learned && e < a.E) ? __ldg(a.bias + e) : 0.0f;
   }
+  // The router tiles and the bias above are constant: they are requested
+  // before the previous kernel of the stream is done. Everything after reads
+  // the call's inputs or writes scratch that kernel may still use.
+  pdl_wait();
+  // the gate/up kernel may launch now: it quantises x itself and runs the
+  // shared expert while this kernel routes
+  pdl_launch_dependents();
   // quantise the segment's blocks (warp w: blocks b0 + w + RC_WARPS*j), all
   // loads first
   if (a.x) {
@@ -195,9 +202,6 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
     lgp[r] = acc;
     __syncwarp();  // every lane is done with the tiles before the next copy
   }
-  // the next kernel may launch now: its weight prefetch no longer competes
-  // with this kernel's router loads
-  pdl_launch_dependents();
   cluster_sync_all();
   // ---- routing of token t by block 0 of its cluster
   const RouteScratch rs = route_scratch(work, a.E_pad, a.k);
@@ -292,7 +296,7 @@ cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_
   r.bucket = bucket ? h->bucket : nullptr;
   void *args[] = {&r};
   return launch_pdl((const void *)k_router_dec, dim3(ROUTER_SEGS, T), dim3(RC_WARPS * 32), router_dec_smem(h), s,
-                    args, false);
+                    args, true);
 }
 
 cudaError_t decode_set_attributes() {

@@ -43,6 +43,7 @@ template <bool DOWN> struct XRing {
 constexpr int X_RING_BYTES = 4 * 2688;
 
 struct XArgs {
+  const float *x;                // the call's activations (gate/up quantises them itself when staged)
   int H, F, E, k, NS, n_shared, T, A_cap;
   int rf, sf, down, K, rows;
   int maxj;                      // item-table entries per block
@@ -197,8 +198,14 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 // AS: activations staged in shared memory. DOWN: the down kernel (items of
 // 32 rows), else gate/up (items of 16 rows, gate and up).
+// Gate/up with staged activations quantises x itself (CAS step 1, the same
+// operations as the router kernel), so its shared-expert items run while the
+// routing is still in flight. In every variant the bucket table is loaded by
+// one warp (the last epilogue warp, at its start, unless another gets there
+// first), which publishes the routed items to the others; the compute warps
+// meanwhile run the shared expert's items, which need no routing.
 template <int TT, bool AS, bool DOWN>
-__global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
+__global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int X_NST = XRing<DOWN>::NST, X_STRIDE = XRing<DOWN>::STRIDE;
   constexpr int PS = x_slots(TT);
@@ -209,7 +216,9 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   const int act_rows = DOWN ? a.T * a.NS : a.T;
   const int act_bytes = AS ? act_rows * (a.K + (a.K >> 5) * 4 + (a.K >> 4) * 2) : 0;
   const XSmem L = x_smem(TT, mats, nbk, act_bytes, a.maxj, a.T);
+  constexpr bool EARLY = AS && !DOWN;
   volatile int *s_nitems = (volatile int *)(smem + L.ctrl + 8);  // items of this block (after the bucket)
+  int *s_claim = (int *)(smem + L.ctrl + 12);                     // EARLY: the warp that loads the bucket
   const uint32_t full0 = smem_u32(smem + L.ctrl) + 64, empty0 = full0 + 64;  // slot barriers, 8 bytes apart
   float *part = (float *)(smem + L.part);  // [PS][XC][mats][TT][16]
   int4 *tab = (int4 *)(smem + L.tab);      // [maxj][2]
@@ -234,6 +243,8 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   const XKind ks = x_kind(a, a.sf, warp < XC ? warp : 0, X_STRIDE), kr = x_kind(a, a.rf, warp < XC ? warp : 0, X_STRIDE);
   if (threadIdx.x == 0) {
     for (int i = 0; i < PS; i++) mbar_init(full0 + 8 * i, XC), mbar_init(empty0 + 8 * i, 1);
+    *s_nitems = -1;  // no routed items known yet (read by the first prefetch pass)
+    *s_claim = 0;
   }
   if (warp < XC && lane == 0)
     for (int i = 0; i < X_NST; i++) mbar_init(bar + 8 * i, 1);
@@ -251,7 +262,43 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
     const int n = c < n_all ? (n_all - 1 - c) / G + 1 : 0;
     for (int j = n_sh_items + lane; j < n; j += 32)
       x_table_entry(a, c + j * G, nsh, RG, act, ks.item_bytes, kr.item_bytes, tab + 2 * j);
+    __syncwarp();
+    __threadfence_block();
     if (lane == 0) *s_nitems = n;
+  };
+  // EARLY: the routed item count once published (n_items stays -1 before)
+  auto poll_items = [&]() {
+    if (n_items < 0) {
+      const int v = *s_nitems;
+      if (v >= 0) {
+        __threadfence_block();
+        n_items = v;
+      }
+    }
+  };
+  auto wait_items = [&]() -> bool {
+    poll_items();
+    if (n_items >= 0) return true;
+    int mine = 0;
+    if (lane == 0) mine = atomicCAS(s_claim, 0, 1) == 0;
+    if (__shfl_sync(0xffffffffu, mine, 0)) {  // this warp loads the bucket for the block
+      pdl_wait();
+      for (int i = lane; i < nbk; i += 32) bks[i] = __ldcg(a.bucket + i);
+      if (DOWN)  // routed slots with an expert, per token (the combine's arrival count)
+        for (int t = lane; t < a.T; t += 32) {
+          int n = 0;
+          for (int j = 0; j < a.k; j++) n += __ldg(a.ids + (size_t)t * a.k + j) >= 0;
+          valid[t] = n;
+        }
+      __syncwarp();
+      build_routed();
+    }
+    const long long t0 = clock64();
+    for (poll_items(); n_items < 0; poll_items()) {
+      if (clock64() - t0 > (1ll << 31)) return false;
+      __nanosleep(64);
+    }
+    return true;
   };
 
   // ---- compute warps: producer (ring) cursor
@@ -262,6 +309,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   auto fill = [&]() {
     while (!p_done && g_prod - g_cons < X_NST) {
       if (!p_ok) {
+        if (pj >= n_sh_items) poll_items();
         if (pj >= n_sh_items && n_items < 0) return;  // routed items: after the previous kernel
         if (pj >= (pj < n_sh_items ? n_sh_items : n_items)) {
           p_done = true;
@@ -297,10 +345,40 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
     if (n_sh_items > 0) fill();  // shared-expert items need no routing: request them before the wait
   }
 
-  // ---- once the previous kernel is done: the bucket and the staged activations
-  {
+  if (EARLY) {
+    // ---- quantise x into the staged activation area (every warp), then the
+    // control warp takes the bucket once the router kernel is done
+    int8_t *xs = (int8_t *)(smem + L.act);
+    float *dxs = (float *)(smem + L.act + act_rows * a.K);
+    int16_t *gss = (int16_t *)(smem + L.act + act_rows * a.K + act_rows * (a.K >> 5) * 4);
+    const int nb = a.K >> 5, nw = blockDim.x >> 5;
+    constexpr int QB = 8;  // loads in batches ahead of the arithmetic
+    for (int u0 = warp; u0 < a.T * nb; u0 += QB * nw) {
+      float v[QB];
+#pragma unroll
+      for (int j = 0; j < QB; j++) {
+        const int u = u0 + j * nw;
+        v[j] = u < a.T * nb ? __ldg(a.x + (size_t)(u / nb) * a.K + 32 * (u % nb) + lane) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < QB; j++) {
+        const int u = u0 + j * nw;
+        if (u >= a.T * nb) break;
+        const int t = u / nb, b = u - t * nb;
+        const float amax = warp_max(fabsf(v[j]));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const int q = cas_code(v[j], d);
+        const int s16 = half_warp_sum(q);
+        xs[(size_t)t * a.K + 32 * b + lane] = (int8_t)q;
+        if (lane == 0) dxs[t * nb + b] = d;
+        if ((lane & 15) == 0) gss[t * (a.K >> 4) + 2 * b + (lane >> 4)] = (int16_t)s16;
+      }
+    }
+    __syncthreads();
+  } else {
+    // ---- once the previous kernel is done: the staged activations (the
+    // bucket table is loaded by the first warp that needs it, see wait_items)
     pdl_wait();
-    for (int i = threadIdx.x; i < nbk; i += blockDim.x) bks[i] = __ldcg(a.bucket + i);
     if (AS) {
       uint8_t *dst = smem + L.act;
       const size_t nq = (size_t)act_rows * a.K, nd = (size_t)act_rows * (a.K >> 5) * 4,
@@ -311,16 +389,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
       for (size_t i = threadIdx.x; i < ng / 16; i += blockDim.x)
         ((uint4 *)(dst + nq + nd))[i] = __ldcg((const uint4 *)a.ag + i);
     }
-    if (DOWN)  // routed slots with an expert, per token (the combine's arrival count)
-      for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
-        int n = 0;
-        for (int j = 0; j < a.k; j++) n += __ldg(a.ids + (size_t)t * a.k + j) >= 0;
-        valid[t] = n;
-      }
     __syncthreads();
-    if (warp == 0) build_routed();
-    __syncthreads();
-    n_items = *s_nitems;
   }
 
   if (warp < XC) {
@@ -332,6 +401,10 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
     float acc[2][TT];
     for (;;) {
       if (!c_ok) {  // the consumer's next item
+        if (cj >= n_sh_items && !wait_items()) {
+          failed = true;
+          break;
+        }
         if (cj >= (cj < n_sh_items ? n_sh_items : n_items)) break;
         const int4 e0 = tab[2 * cj], e1 = tab[2 * cj + 1];
         const bool rt = e1.x != 0;
@@ -412,8 +485,18 @@ __global__ void __launch_bounds__(X_WARPS * 32, 1) k_experts(XArgs a) {
   // warp ((u % PS) % XE == ew), so the units of one slot, which wait on the
   // same barriers in alternating phases, are always taken by the same warp
   const int ew = warp - XC;
+  // the last epilogue warp loads the bucket table at once; in the down kernel
+  // every epilogue warp needs it (arrival counts) before its first unit
+  if ((ew == XE - 1 || DOWN) && !wait_items()) {
+    if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
+    return;
+  }
   int unit = 0;
   for (int j = 0;; j++) {
+    if (j >= n_sh_items && !wait_items()) {
+      if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
+      return;
+    }
     if (j >= (j < n_sh_items ? n_sh_items : n_items)) break;
     const int4 e0 = tab[2 * j], e1 = tab[2 * j + 1];
     const int S = e1.x ? kr.S : ks.S, rg = e1.y, n_tok = e0.z, list_off = e0.w;
@@ -485,12 +568,17 @@ static size_t x_act_bytes(const ds4moe_layer *h, int T, bool down) {
 static int x_tt(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
 
 // Item-table entries per block: the call's items over the blocks.
+// Blocks per SM: two for single-token calls (registers capped to fit), so
+// twice the warps hide the latency of the short per-item chains.
+static int x_blocks(const ds4moe_layer *h, int T) { return (T <= 1 ? 2 : 1) * h->n_sm; }
+
 static int x_maxj(const ds4moe_layer *h, int T, bool down) {
   const ds4moe_layer_desc &d = h->d;
   const int RG = down ? d.hidden / 32 : d.ffn / TILE_ROWS;
   const long long routed = (long long)T * d.top_k < d.n_experts ? (long long)T * d.top_k : d.n_experts;
   const long long n = (d.n_shared ? RG : 0) + routed * RG;
-  return (int)((n + h->n_sm - 1) / h->n_sm);
+  const int G = x_blocks(h, T);
+  return (int)((n + G - 1) / G);
 }
 
 static size_t x_smem_bytes(const ds4moe_layer *h, int T, bool down, bool as) {
@@ -526,10 +614,15 @@ cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *
   } else {
     a.K = d.ffn, a.rows = d.hidden, a.w_r = h->dn, a.w_s = h->sdn, a.aq = h->hq, a.ad = h->dh, a.ag = h->gsh;
   }
-  const bool as = x_smem_bytes(h, T, down != 0, true) <= DEC_SMEM_LIMIT;
+  a.x = x;
+  // activations staged in shared memory when they fit beside the rest (for
+  // single-token calls: in half an SM, two blocks per SM)
+  const size_t lim = T <= 1 ? (size_t)(228 * 1024 / 2 - 1024) : DEC_SMEM_LIMIT;
+  const bool as = x_smem_bytes(h, T, down != 0, true) <= lim;
+
   const void *fn = down ? (as ? x_fn<true, true>(T) : x_fn<false, true>(T)) : (as ? x_fn<true, false>(T) : x_fn<false, false>(T));
   void *args[] = {&a};
-  return launch_pdl(fn, dim3(h->n_sm), dim3(X_WARPS * 32), x_smem_bytes(h, T, down != 0, as), s, args, true);
+  return launch_pdl(fn, dim3(x_blocks(h, T)), dim3(X_WARPS * 32), x_smem_bytes(h, T, down != 0, as), s, args, true);
 }
 
 cudaError_t experts_set_attributes() {

@@ -45,11 +45,11 @@ constexpr int PF_M = 128;  // rows per item (MMA M)
 constexpr int PF_CW = 4;   // converter warps
 constexpr int PF_EW = 8;   // epilogue warps
 constexpr int PF_WARPS = 2 + PF_CW + PF_EW;
-constexpr int PF_RS = 4;                 // raw stages
+constexpr int PF_RS = 2;                 // raw stages
 constexpr int PF_RAW = 16 * Q2S_TILE;    // 21504 bytes, the largest raw stage
-constexpr int PF_FS = 3;                 // fp16 operand stages, one 32-block each
+constexpr int PF_FS = 4;                 // fp16 operand stages, one 32-block each
 constexpr int PF_TS = 4;                 // TMEM stages of 128 columns
-constexpr int PF_XS = 8;                 // side-data stages, >= PF_FS + PF_TS + 1
+constexpr int PF_XS = 9;                 // side-data stages, >= PF_FS + PF_TS + 1
 constexpr int PF_TMEM_COLS = PF_TS * 128;
 // fp16 stage: A main [2 mats][128 x 32] | A min [2][128 x 16] | B main [32 x 32] | B min [32 x 16]
 constexpr int PF_F_AMAIN = 0, PF_F_AMIN = 16384, PF_F_BMAIN = 24576, PF_F_BMIN = 26624, PF_F_BYTES = 27648;
@@ -197,13 +197,18 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *smem) {
   return p;
 }
 
-// Bounded wait that also gives up once another role has aborted.
+// Bounded wait that also gives up once another role has aborted; sleeps
+// between tests (growing to 256 ns) so that waiting roles do not take issue
+// slots from the working ones.
 __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
+  unsigned ns = 32;
   while (!mbar_try_wait(bar, parity)) {
     if (*abort) return false;
     if (clock64() - t0 > (1ll << 31)) return false;
+    __nanosleep(ns);
+    ns = ns < 256 ? 2 * ns : 256;
   }
   return true;
 }
