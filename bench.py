@@ -42,6 +42,15 @@ WORKLOADS = {
                                                "Zipf(1.1) expert popularity"),
     "ds4-hash-prefill-512": (synth.DS4_HASH, 512, "hash-routed layer (vocab 129280), prefill chunk of 512 tokens"),
     "tiny-4": (synth.TINY, 4, "tiny layer H 256, E 16 top-2 + 1 shared, F 128, all Q8_0, fp32 router, 4 tokens"),
+    "ds4-prefill-4096": (synth.DS4, 4096, "prefill chunk of 4096 tokens on the learned-routing DeepSeek-V4-Flash-shaped "
+                                          "layer"),
+}
+# The 43-layer stack (layers 0-2 hash routed, 3-42 learned): a residual
+# stream h passes through every layer as h <- h + MoE_l(RMSNorm(h)).
+STACK_WORKLOADS = {
+    "ds4-stack-43-decode-1": (1, "43-layer stack of DeepSeek-V4-Flash-shaped MoE FFN layers, decode batch 1"),
+    "ds4-stack-43-decode-8": (8, "43-layer stack, decode batch 8"),
+    "ds4-stack-43-prefill-4096": (4096, "43-layer stack, prefill of 4096 tokens"),
 }
 DEFAULT_WORKLOAD = "ds4-decode-1"
 SEED = 2026
@@ -193,6 +202,45 @@ def run_reference(args, spec, T, desc):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_stack(args):
+    """The reference arm for the 43-layer stack: the CPU oracle carries one
+    token of the workload through all 43 layers (each layer's weights are
+    generated, used and dropped in turn; only the oracle's forward calls are
+    timed), once per step."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    T, desc = STACK_WORKLOADS[args.workload]
+    ora = oracle.get()
+    cores = os.cpu_count() or 1
+    n_tok = 1
+    h0 = synth.gen_x(synth.DS4, SEED, n_tok)
+    tok = synth.gen_token_ids(synth.DS4_HASH, SEED, n_tok)
+    hs = [h0.copy() for _ in range(args.steps)]
+    dt = 0.0
+    for l in range(synth.N_STACK_LAYERS):
+        spec = synth.stack_layer_spec(l)
+        ol = ora.layer(spec, synth.gen_layer(spec, SEED, l))
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            xr = ora.rmsnorm(hs[i], 1e-6)
+            hs[i], _, _, _ = ol.forward(xr, hs[i], tok if spec.route == "hash" else None, nthreads=cores)
+        dt += time.perf_counter() - t0
+    value = args.steps * n_tok / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32+f32",
+        "data": "synthetic", "config": {"workload": args.workload, "description": desc, "n_tok": T},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} step(s) of 1 token through all 43 layers (of the workload's {T}), "
+                                   f"scalar C oracle with {cores} threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def cpu_baseline(spec, T, w, budget_s=12.0):
     """The oracle as it stands, on this host's cores, on a bounded sample."""
     import oracle
@@ -211,19 +259,133 @@ def cpu_baseline(spec, T, w, budget_s=12.0):
             "sample": f"{n} forward(s) of {T} token(s) of the same workload ({dt:.1f} s of CPU work)"}
 
 
+def run_stack(args):
+    """The 43-layer stack: every layer's weights resident (about 92 GB), one
+    step = T tokens through all 43 layers (RMSNorm, then the MoE FFN added to
+    the residual stream), captured as one CUDA graph."""
+    import torch
+
+    import deepseek_v4_flash_gb300 as ds4
+
+    T, desc = STACK_WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda")
+    L = synth.N_STACK_LAYERS
+    layers, specs = [], []
+    for l in range(L):
+        spec = synth.stack_layer_spec(l)
+        wl = synth.gen_layer(spec, SEED, l)
+        wd = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in wl.items()}
+        layers.append(ds4.Layer(desc_from_spec(ds4, spec, T), wd))
+        specs.append(spec)
+        del wd, wl
+        torch.cuda.empty_cache()
+    NX = int(max(2, min(16, (1 << 26) // (T * synth.DS4.hidden))))
+    xs = torch.from_numpy(np.stack([synth.gen_x(synth.DS4, SEED + 7 * i + rank, T) for i in range(NX)])).to(dev)
+    tok = torch.from_numpy(synth.gen_token_ids(synth.DS4_HASH, SEED + rank, T)).to(dev)
+    x_in = xs[0].clone()
+    h = torch.empty_like(x_in)
+    xn = torch.empty_like(x_in)
+
+    def step():
+        h.copy_(x_in)
+        for l in range(L):
+            ds4.rmsnorm(h, xn, 1e-6)
+            layers[l].forward(xn, h, tok if specs[l].route == "hash" else None)
+
+    # unique routed experts per layer for the first input batch (algorithmic bytes)
+    uniq = []
+    h.copy_(x_in)
+    for l in range(L):
+        ds4.rmsnorm(h, xn, 1e-6)
+        ids, _ = layers[l].route(xn, tok if specs[l].route == "hash" else None)
+        v = ids.cpu().numpy()
+        uniq.append(len(np.unique(v[v >= 0])))
+        layers[l].forward(xn, h, tok if specs[l].route == "hash" else None)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    n0 = sum(Ly.launch_count() for Ly in layers)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    launches_per_step = sum(Ly.launch_count() for Ly in layers) - n0 + L  # + the RMSNorm launches
+    for i in range(args.warmup):
+        x_in.copy_(xs[i % NX])
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        x_in.copy_(xs[i % NX])
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_s = reduce_max(float(sum(a.elapsed_time(b) for a, b in ev)) / 1e3, dev)
+    value = job_throughput(args.steps * T, total_s, world)
+    hbm_peak, _, peak_kind = peaks()
+    bytes_step = float(sum(step_bytes(specs[l], T, uniq[l]) for l in range(L)) + L * 2 * T * synth.DS4.hidden * 4)
+    gbs = bytes_step * world * args.steps / total_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32+f32", "data": "synthetic",
+        "config": {"workload": args.workload, "description": desc, "n_tok": T, "layers": L,
+                   "l2": "not flushed: 43 layers, about 92 GB of weights, far above L2",
+                   "inputs": f"{NX} seeded batches resident in HBM, cycled"},
+        "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "bytes_per_step": bytes_step,
+        "unique_experts_per_layer": float(np.mean(uniq)),
+        "roofline": {"kernel": "whole 43-layer step", "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind, "traffic": None},
+        "timing": "one CUDA graph of the 43 layers per step, CUDA events around each replay",
+        "gpu_launches": int(launches_per_step * args.steps),
+    }
+    if clk:
+        line["clocks"] = clk
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(STACK_WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layer-copies", type=int, default=0,
                     help="layer copies rotated across steps (0: enough that the working sets exceed L2)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.workload in STACK_WORKLOADS:
+        if args.impl == "reference":
+            run_reference_stack(args)
+        else:
+            run_stack(args)
+        return
     spec, T, desc = WORKLOADS[args.workload]
 
     if args.impl == "reference":
@@ -264,8 +426,9 @@ def main():
         torch.cuda.empty_cache()
     layer = layers[0]
 
-    # Inputs resident in HBM: NX distinct batches, cycled.
-    NX = 64
+    # Inputs resident in HBM: NX distinct batches (64, fewer for large
+    # batches), cycled.
+    NX = int(max(2, min(64, (1 << 26) // (T * spec.hidden))))
     xs = torch.from_numpy(np.stack([synth.gen_x(spec, SEED + 7 * i + rank, T) for i in range(NX)])).to(dev)
     tok = torch.from_numpy(synth.gen_token_ids(spec, SEED + rank, T)).to(dev) if spec.route == "hash" else None
     ys = [torch.zeros(T, spec.hidden, device=dev) for _ in range(NL)]

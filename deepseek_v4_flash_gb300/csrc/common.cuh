@@ -193,17 +193,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: gives up after ~2^31 SM cycles (about a second) and returns
-// false; callers then raise DS4MOE_DEVERR_TIMEOUT and leave. Between tests
-// the warp sleeps (growing to 256 ns), so waiting warps leave the issue
-// slots to the warps that do the work.
+// false; callers then raise DS4MOE_DEVERR_TIMEOUT and leave. No sleep
+// between tests: these waits sit on the decode path's latency chain.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  unsigned ns = 32;
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > (1ll << 31)) return false;
-    __nanosleep(ns);
-    ns = ns < 256 ? 2 * ns : 256;
   }
   return true;
 }

@@ -65,7 +65,7 @@ struct XArgs {
   uint32_t *err;
 };
 
-__host__ __device__ constexpr int x_slots(int TT) { return TT <= 1 ? 8 : TT <= 2 ? 4 : 2; }
+__host__ __device__ constexpr int x_slots(int TT) { return 8 + 0 * TT; }
 
 // Invariants of the items of one kind (shared or routed) for one warp.
 struct XKind {
@@ -132,23 +132,6 @@ __device__ __forceinline__ void x_requant(const XArgs &a, float h, int sr, int b
   a.hq[(size_t)sr * a.F + 32 * blk + lane] = (int8_t)q;
   if (lane == 0) a.dh[(size_t)sr * (a.F >> 5) + blk] = d;
   if ((lane & 15) == 0) a.gsh[(size_t)sr * (a.F >> 4) + 2 * blk + (lane >> 4)] = (int16_t)gsum;
-}
-
-// Count one arrival on a ticket; true (on every lane) for the caller that
-// completes it. The acquire-release atomic orders this warp's earlier global
-// writes before the completer's later reads; the completer resets it.
-__device__ __forceinline__ bool x_ticket_last(int32_t *tk, int expect, int lane) {
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(tk) : "memory");
-    last = old == expect - 1;
-    if (last) *tk = 0;
-  }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  __syncwarp();
-  return last != 0;
 }
 
 // CAS step 8 for rows 32*rg .. +31 of token t (lane = row).
@@ -437,13 +420,13 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
         const uint32_t st = ring + slot * X_STRIDE;
         const int s0 = c_ks0 + cstage * c_ksps;
         if (c_fmt == DS4MOE_Q2S && c_ksps == 2) {  // two K-steps in one block of code: their dots overlap
-          q2s_step<TT, 2, AS>(st, lane, s0, a.K, arow, aq, ad, ag, acc);
-          q2s_step<TT, 2, AS>(st + c_kb, lane, s0 + 1, a.K, arow, aq, ad, ag, acc);
+          q2s_step<TT, 2, AS>(st, lane, s0, a.K, arow, nt, aq, ad, ag, acc);
+          q2s_step<TT, 2, AS>(st + c_kb, lane, s0 + 1, a.K, arow, nt, aq, ad, ag, acc);
         } else {
           for (int j = 0; j < c_ksps; j++) {
             const uint32_t t = st + j * c_kb;
-            if (c_fmt == DS4MOE_Q2S) q2s_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, ag, acc);
-            else q8_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, aq, ad, acc);
+            if (c_fmt == DS4MOE_Q2S) q2s_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, nt, aq, ad, ag, acc);
+            else q8_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, nt, aq, ad, acc);
           }
         }
         __syncwarp();
@@ -538,17 +521,45 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * ps);  // the slot is free again
-      for (int i = 0; i < nt; i++) {
-        int sr, arow;
-        x_token(a, list_off, list, p * TT + i, &sr, &arow);
-        if (!DOWN) {  // a 32-row block of h spans two items: requant when both are in
-          const int blk = rg >> 1;
-          if (x_ticket_last(a.hticket + (size_t)sr * (a.F >> 5) + blk, 2, lane))
+      // One ticket per token (lane i takes token i, all in flight at once):
+      // gate/up: a 32-row block of h spans two items, requantised once both
+      // are in; down: the fixed-order combine once every slot of the token
+      // has these 32 rows. The acquire-release atomics order the other
+      // item's (slot's) writes before this warp's reads; the completer resets
+      // the ticket.
+      {
+        int last = 0;
+        if (lane < nt) {
+          int sr, arow;
+          x_token(a, list_off, list, p * TT + lane, &sr, &arow);
+          int32_t *tk;
+          int expect;
+          if (!DOWN) {
+            tk = a.hticket + (size_t)sr * (a.F >> 5) + (rg >> 1);
+            expect = 2;
+          } else {
+            const int t = sr / a.NS;
+            tk = a.cticket + (size_t)t * (a.H >> 5) + rg;
+            expect = valid[t] + a.n_shared;
+          }
+          int old;
+          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(tk) : "memory");
+          last = old == expect - 1;
+          if (last) *tk = 0;
+        }
+        unsigned done = __ballot_sync(0xffffffffu, last);
+        __syncwarp();
+        while (done) {
+          const int i = __ffs(done) - 1;
+          done &= done - 1;
+          int sr, arow;
+          x_token(a, list_off, list, p * TT + i, &sr, &arow);
+          if (!DOWN) {
+            const int blk = rg >> 1;
             x_requant(a, __ldcg(a.hbuf + (size_t)sr * a.F + 32 * blk + lane), sr, blk, lane);
-        } else {  // combine once every slot of the token has these 32 rows
-          const int t = sr / a.NS;
-          if (x_ticket_last(a.cticket + (size_t)t * (a.H >> 5) + rg, valid[t] + a.n_shared, lane))
-            x_combine(a, t, rg, lane);
+          } else {
+            x_combine(a, sr / a.NS, rg, lane);
+          }
         }
       }
     }

@@ -41,7 +41,7 @@ __device__ __forceinline__ int dp2a_su(uint32_t a, uint32_t b, int c) {
 // trades them with its partner, so lane h = 0 adds all eight terms to the
 // row chain in block order (CAS step 4). acc of lanes with h = 1 is not used.
 template <int TT, int MATS, bool ACT_SMEM>
-__device__ __forceinline__ void q2s_step(uint32_t t0, int lane, int s, int K, const int *arow,
+__device__ __forceinline__ void q2s_step(uint32_t t0, int lane, int s, int K, const int *arow, int nt,
                                          const int8_t *__restrict__ aq, const float *__restrict__ ad,
                                          const int16_t *__restrict__ ag, float (&acc)[MATS][TT]) {
   const int h = lane & 1, r = lane >> 1;
@@ -67,6 +67,7 @@ __device__ __forceinline__ void q2s_step(uint32_t t0, int lane, int s, int K, co
       const int blk = 8 * s + h + 4 * c + 2 * jj;
 #pragma unroll
       for (int t = 0; t < TT; t++) {
+        if (t >= nt) break;  // warp-uniform: only the unit's valid tokens
         const int8_t *xr = aq + (size_t)arow[t] * K + 32 * blk;
         const uint4 x0 = act_load<ACT_SMEM>((const uint4 *)xr);
         const uint4 x1 = act_load<ACT_SMEM>((const uint4 *)(xr + 16));
@@ -97,7 +98,7 @@ __device__ __forceinline__ void q2s_step(uint32_t t0, int lane, int s, int K, co
 // Lane 2r + h takes elements 16h .. 16h+15 of row r; the partner lane
 // completes I exactly and both lanes add the same term.
 template <int TT, int MATS, bool ACT_SMEM>
-__device__ __forceinline__ void q8_step(uint32_t t0, int lane, int s, int K, const int *arow,
+__device__ __forceinline__ void q8_step(uint32_t t0, int lane, int s, int K, const int *arow, int nt,
                                         const int8_t *__restrict__ aq, const float *__restrict__ ad,
                                         float (&acc)[MATS][TT]) {
   const int h = lane & 1, r = lane >> 1;
@@ -113,6 +114,7 @@ __device__ __forceinline__ void q8_step(uint32_t t0, int lane, int s, int K, con
   const int nb = K >> 5;
 #pragma unroll
   for (int t = 0; t < TT; t++) {
+    if (t >= nt) break;  // warp-uniform: only the unit's valid tokens
     const uint4 x = act_load<ACT_SMEM>((const uint4 *)(aq + (size_t)arow[t] * K + 32 * s + 16 * h));
     const float dxv = act_load<ACT_SMEM>(ad + (size_t)arow[t] * nb + s);
 #pragma unroll
