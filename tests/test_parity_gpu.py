@@ -297,3 +297,74 @@ def test_decode_and_prefill_paths_agree(ora, monkeypatch):
     assert torch.equal(yp, yd)
     lp.close()
     ld.close()
+
+
+def test_prefill_bad_token_ids(ora, prefill_always):
+    """Hash token ids outside the table on the prefill path: the flag is set
+    and those tokens add nothing, the others are exact."""
+    import torch
+    spec, T = synth.MICRO_HASH, 150
+    w = synth.gen_layer(spec, 67, 0)
+    ol = ora.layer(spec, w)
+    layer = make_layer(spec, w, T)
+    x = synth.gen_x(spec, 67, T)
+    tok = synth.gen_token_ids(spec, 67, T)
+    tok[3] = spec.vocab
+    tok[77] = -1
+    tok[149] = 1 << 30
+    ref, _, _, bad = ol.forward(x, None, tok)
+    assert bad == 3
+    yd = torch.zeros(T, spec.hidden, device="cuda")
+    layer.forward(torch.from_numpy(x).cuda(), yd, torch.from_numpy(tok).cuda())
+    assert layer.device_error() & 1
+    got = yd.cpu().numpy()
+    assert np.all(got[[3, 77, 149]] == 0)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    layer.close()
+
+
+def test_prefill_more_tokens_than_one_chunk(ora):
+    """4100 tokens: one prefill chunk of 4096 and a second of 4."""
+    import torch
+    spec, T = synth.MICRO, 4100
+    w = synth.gen_layer(spec, 69, 0)
+    ol = ora.layer(spec, w)
+    layer = make_layer(spec, w, T)
+    x = synth.gen_x(spec, 69, T)
+    ref, _, _, _ = ol.forward(x, None, None)
+    yd = torch.zeros(T, spec.hidden, device="cuda")
+    layer.forward(torch.from_numpy(x).cuda(), yd)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    got = yd.cpu().numpy()
+    assert within_tolerance(got, ref)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    layer.close()
+
+
+def test_prefill_forward_host(ora, prefill_always):
+    import torch
+    spec, T = synth.MICRO, 70
+    w = synth.gen_layer(spec, 71, 0)
+    ol = ora.layer(spec, w)
+    layer = make_layer(spec, w, T)
+    x = synth.gen_x(spec, 71, T)
+    y0 = (np.random.default_rng(71).standard_normal(x.shape) * 3).astype(np.float32)
+    ref, _, _, _ = ol.forward(x, y0, None)
+    yh = torch.from_numpy(y0.copy()).pin_memory()
+    layer.forward_host(torch.from_numpy(x).pin_memory(), yh)
+    assert np.array_equal(yh.numpy().view(np.uint32), ref.view(np.uint32))
+    layer.close()
+
+
+def test_prefill_nonfinite_input_sets_flag(ora, prefill_always):
+    import torch
+    spec = synth.MICRO
+    w = synth.gen_layer(spec, 73, 0)
+    layer = make_layer(spec, w, 80)
+    x = torch.randn(80, spec.hidden, device="cuda")
+    x[40, 3] = float("nan")
+    y = torch.zeros_like(x)
+    layer.forward(x, y)
+    assert layer.device_error() & 2
+    layer.close()
