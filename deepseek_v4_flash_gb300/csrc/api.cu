@@ -340,9 +340,9 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
     e = launch_dec_route(h, xc, tc, nc, h->ids, h->wts, true, s);
     mark(2);
     mark(3);
-    if (e == cudaSuccess) e = launch_experts(h, xc, nc, yc, 0, s);
+    if (e == cudaSuccess) e = launch_experts(h, nc, yc, 0, s);
     mark(4);
-    if (e == cudaSuccess) e = launch_experts(h, xc, nc, yc, 1, s);
+    if (e == cudaSuccess) e = launch_experts(h, nc, yc, 1, s);
     mark(5);
     mark(6);
     h->launches += 3;

@@ -145,8 +145,8 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   // before the previous kernel of the stream is done. Everything after reads
   // the call's inputs or writes scratch that kernel may still use.
   pdl_wait();
-  // the gate/up kernel may launch now: it quantises x itself and runs the
-  // shared expert while this kernel routes
+  // the gate/up kernel may launch now: it requests the shared expert's
+  // weights while this kernel routes
   pdl_launch_dependents();
   // quantise the segment's blocks (warp w: blocks b0 + w + RC_WARPS*j), all
   // loads first

@@ -43,7 +43,6 @@ template <bool DOWN> struct XRing {
 constexpr int X_RING_BYTES = 4 * 2688;
 
 struct XArgs {
-  const float *x;                // the call's activations (gate/up quantises them itself when staged)
   int H, F, E, k, NS, n_shared, T, A_cap;
   int rf, sf, down, K, rows;
   int maxj;                      // item-table entries per block
@@ -181,12 +180,11 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 // AS: activations staged in shared memory. DOWN: the down kernel (items of
 // 32 rows), else gate/up (items of 16 rows, gate and up).
-// Gate/up with staged activations quantises x itself (CAS step 1, the same
-// operations as the router kernel), so its shared-expert items run while the
-// routing is still in flight. In every variant the bucket table is loaded by
-// one warp (the last epilogue warp, at its start, unless another gets there
-// first), which publishes the routed items to the others; the compute warps
-// meanwhile run the shared expert's items, which need no routing.
+// The bucket table is loaded by one warp (the last epilogue warp, at its
+// start, unless another gets there first), which publishes the routed items
+// to the others; the compute warps meanwhile run the shared expert's items,
+// which need no routing. The shared expert's weights are requested before
+// the wait for the previous kernel.
 template <int TT, bool AS, bool DOWN>
 __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -199,9 +197,8 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
   const int act_rows = DOWN ? a.T * a.NS : a.T;
   const int act_bytes = AS ? act_rows * (a.K + (a.K >> 5) * 4 + (a.K >> 4) * 2) : 0;
   const XSmem L = x_smem(TT, mats, nbk, act_bytes, a.maxj, a.T);
-  constexpr bool EARLY = AS && !DOWN;
   volatile int *s_nitems = (volatile int *)(smem + L.ctrl + 8);  // items of this block (after the bucket)
-  int *s_claim = (int *)(smem + L.ctrl + 12);                     // EARLY: the warp that loads the bucket
+  int *s_claim = (int *)(smem + L.ctrl + 12);                     // the warp that loads the bucket
   const uint32_t full0 = smem_u32(smem + L.ctrl) + 64, empty0 = full0 + 64;  // slot barriers, 8 bytes apart
   float *part = (float *)(smem + L.part);  // [PS][XC][mats][TT][16]
   int4 *tab = (int4 *)(smem + L.tab);      // [maxj][2]
@@ -249,7 +246,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
     __threadfence_block();
     if (lane == 0) *s_nitems = n;
   };
-  // EARLY: the routed item count once published (n_items stays -1 before)
+  // the routed item count once published (n_items stays -1 before)
   auto poll_items = [&]() {
     if (n_items < 0) {
       const int v = *s_nitems;
@@ -328,37 +325,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
     if (n_sh_items > 0) fill();  // shared-expert items need no routing: request them before the wait
   }
 
-  if (EARLY) {
-    // ---- quantise x into the staged activation area (every warp), then the
-    // control warp takes the bucket once the router kernel is done
-    int8_t *xs = (int8_t *)(smem + L.act);
-    float *dxs = (float *)(smem + L.act + act_rows * a.K);
-    int16_t *gss = (int16_t *)(smem + L.act + act_rows * a.K + act_rows * (a.K >> 5) * 4);
-    const int nb = a.K >> 5, nw = blockDim.x >> 5;
-    constexpr int QB = 8;  // loads in batches ahead of the arithmetic
-    for (int u0 = warp; u0 < a.T * nb; u0 += QB * nw) {
-      float v[QB];
-#pragma unroll
-      for (int j = 0; j < QB; j++) {
-        const int u = u0 + j * nw;
-        v[j] = u < a.T * nb ? __ldg(a.x + (size_t)(u / nb) * a.K + 32 * (u % nb) + lane) : 0.0f;
-      }
-#pragma unroll
-      for (int j = 0; j < QB; j++) {
-        const int u = u0 + j * nw;
-        if (u >= a.T * nb) break;
-        const int t = u / nb, b = u - t * nb;
-        const float amax = warp_max(fabsf(v[j]));
-        const float d = __fdiv_rn(amax, 127.0f);
-        const int q = cas_code(v[j], d);
-        const int s16 = half_warp_sum(q);
-        xs[(size_t)t * a.K + 32 * b + lane] = (int8_t)q;
-        if (lane == 0) dxs[t * nb + b] = d;
-        if ((lane & 15) == 0) gss[t * (a.K >> 4) + 2 * b + (lane >> 4)] = (int16_t)s16;
-      }
-    }
-    __syncthreads();
-  } else {
+  {
     // ---- once the previous kernel is done: the staged activations (the
     // bucket table is loaded by the first warp that needs it, see wait_items)
     pdl_wait();
@@ -611,7 +578,7 @@ static const void *x_fn(int T) {
        : T <= 4 ? (const void *)k_experts<4, AS, DOWN> : (const void *)k_experts<8, AS, DOWN>;
 }
 
-cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *y, int down, cudaStream_t s) {
+cudaError_t launch_experts(const ds4moe_layer *h, int T, float *y, int down, cudaStream_t s) {
   const ds4moe_layer_desc &d = h->d;
   XArgs a = {};
   a.H = d.hidden, a.F = d.ffn, a.E = d.n_experts, a.k = d.top_k, a.NS = h->NS, a.n_shared = d.n_shared, a.T = T;
@@ -625,7 +592,6 @@ cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *
   } else {
     a.K = d.ffn, a.rows = d.hidden, a.w_r = h->dn, a.w_s = h->sdn, a.aq = h->hq, a.ad = h->dh, a.ag = h->gsh;
   }
-  a.x = x;
   // activations staged in shared memory when they fit beside the rest (for
   // single-token calls: in half an SM, two blocks per SM)
   const size_t lim = T <= 1 ? (size_t)(228 * 1024 / 2 - 1024) : DEC_SMEM_LIMIT;

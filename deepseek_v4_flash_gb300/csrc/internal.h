@@ -94,7 +94,7 @@ cudaError_t launch_prefill(ds4moe_layer *h, const float *x, const int32_t *tok, 
 
 // experts.cu
 size_t experts_smem(const ds4moe_layer *h);
-cudaError_t launch_experts(const ds4moe_layer *h, const float *x, int T, float *y, int down, cudaStream_t s);
+cudaError_t launch_experts(const ds4moe_layer *h, int T, float *y, int down, cudaStream_t s);
 cudaError_t experts_set_attributes();
 cudaError_t decode_set_attributes();
 constexpr size_t DEC_SMEM_LIMIT = 227 * 1024;
