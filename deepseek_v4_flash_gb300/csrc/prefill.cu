@@ -362,87 +362,107 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
       load_tok(0, xv[0], gv[0], dv[0]);
       load_tok(1, xv[1], gv[1], dv[1]);
       float dd_d[2] = {0.0f, 0.0f}, dd_m[2] = {0.0f, 0.0f};
+      // Two 32-blocks per step (b, b + 1: always in the same raw stage), each
+      // phase for both at once, so that the loads, conversions and stores of
+      // the two blocks overlap.
+      constexpr int NH = MODE == 0 ? 2 : 1;
       for (int b = 0; b < nb; b += 2) {
+        const int bin0 = b % bpst;
+        const int rs = gst % PF_RS;
+        if (bin0 == 0 && !pf_wait(B.raw_full + 8 * rs, (gst / PF_RS) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        int fsu[2], xsu[2];
+        bool waited = true;
 #pragma unroll
         for (int u = 0; u < 2; u++) {
-          const int bb = b + u;
-          const int bin = bb % bpst;
-          const int rs = gst % PF_RS;
-          if (bin == 0 && !pf_wait(B.raw_full + 8 * rs, (gst / PF_RS) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          const int fs = fc % PF_FS, xs = fc % PF_XS;
-          if (fc >= PF_FS && !pf_wait(B.f_empty + 8 * fs, ((fc / PF_FS) - 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          const uint32_t raw = sm0 + PF_OFF_RAW + rs * PF_RAW;
-          const uint32_t f = sm0 + PF_OFF_F + fs * PF_F_BYTES;
-          const uint32_t xsd = sm0 + PF_OFF_X + xs * PF_X_BYTES;
-          // ---- weights: tiles tau0 and (gate/up) tau0 + 8, row rr. All shared
-          // loads first, then the conversions (independent chains), then the
-          // stores, so that the ordered shared-memory accesses do not
-          // serialise the arithmetic.
-          constexpr int NH = MODE == 0 ? 2 : 1;
-          if (q2) {
-            const int L = 2 * rr + (bin & 1), j = bin >> 1;
-            uint2 w[NH];
-            uint32_t smb[NH];
+          const uint32_t fcu = fc + u;
+          fsu[u] = fcu % PF_FS, xsu[u] = fcu % PF_XS;
+          if (fcu >= PF_FS && !pf_wait(B.f_empty + 8 * fsu[u], ((fcu / PF_FS) - 1) & 1, abort)) waited = false;
+        }
+        if (!waited) {
+          ok = false;
+          break;
+        }
+        const uint32_t raw = sm0 + PF_OFF_RAW + rs * PF_RAW;
+        // ---- weights: tiles tau0 and (gate/up) tau0 + 8, row rr
+        if (q2) {
+          uint2 w[2][NH];
+          uint32_t smb[2][NH];
 #pragma unroll
-            for (int h2 = 0; h2 < NH; h2++) {
-              const uint32_t tile = raw + (tau0 + 8 * h2) * TB;
-              if (bin == 0) {
-                const uint32_t ddw = ld_shared_u32(tile + Q2S_DD + 4 * rr);
-                dd_d[h2] = half_bits_to_float(ddw), dd_m[h2] = half_bits_to_float(ddw >> 16);
-              }
-              w[h2] = ld_shared_v2(tile + Q2S_QS + 512 * (j >> 1) + 16 * L + 8 * (j & 1));
-              smb[h2] = ld_shared_u32(tile + Q2S_SM + ((8 * L + 2 * j) & ~3)) >> (8 * ((2 * j) & 3));
+          for (int h2 = 0; h2 < NH; h2++) {
+            const uint32_t tile = raw + (tau0 + 8 * h2) * TB;
+            if (bin0 == 0) {
+              const uint32_t ddw = ld_shared_u32(tile + Q2S_DD + 4 * rr);
+              dd_d[h2] = half_bits_to_float(ddw), dd_m[h2] = half_bits_to_float(ddw >> 16);
             }
-            uint4 lo[NH][2], hi[NH][2];
-            uint32_t mnw[NH];
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+              const int bin = bin0 + u, L = 2 * rr + (bin & 1), j = bin >> 1;
+              w[u][h2] = ld_shared_v2(tile + Q2S_QS + 512 * (j >> 1) + 16 * L + 8 * (j & 1));
+              smb[u][h2] = ld_shared_u32(tile + Q2S_SM + ((8 * L + 2 * j) & ~3)) >> (8 * ((2 * j) & 3));
+            }
+          }
+          uint4 lo[2][NH][2], hi[2][NH][2];
+          uint32_t mnw[2][NH];
+#pragma unroll
+          for (int u = 0; u < 2; u++)
 #pragma unroll
             for (int h2 = 0; h2 < NH; h2++) {
-              const uint32_t sm = smb[h2];
+              const uint32_t sm = smb[u][h2];
               const uint32_t sc2a = h2_small(sm & 15, sm & 15), sc2b = h2_small((sm >> 8) & 15, (sm >> 8) & 15);
-              q2s_group_to_h(w[h2].x, sc2a, hmul2_u(sc2a, 0xE400E400u), lo[h2][0], hi[h2][0]);
-              q2s_group_to_h(w[h2].y, sc2b, hmul2_u(sc2b, 0xE400E400u), lo[h2][1], hi[h2][1]);
-              mnw[h2] = h2_small((sm >> 4) & 15, (sm >> 12) & 15);
+              q2s_group_to_h(w[u][h2].x, sc2a, hmul2_u(sc2a, 0xE400E400u), lo[u][h2][0], hi[u][h2][0]);
+              q2s_group_to_h(w[u][h2].y, sc2b, hmul2_u(sc2b, 0xE400E400u), lo[u][h2][1], hi[u][h2][1]);
+              mnw[u][h2] = h2_small((sm >> 4) & 15, (sm >> 12) & 15);
             }
+#pragma unroll
+          for (int u = 0; u < 2; u++) {
+            const uint32_t f = sm0 + PF_OFF_F + fsu[u] * PF_F_BYTES;
+            const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
 #pragma unroll
             for (int h2 = 0; h2 < NH; h2++) {
               const int tau = tau0 + 8 * h2;
               const int m = MODE == 0 ? (tau & 1) : 0;
               const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
               const uint32_t ar = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
-              sts128(ar, lo[h2][0].x, lo[h2][0].y, lo[h2][0].z, lo[h2][0].w);
-              sts128(ar + 128, hi[h2][0].x, hi[h2][0].y, hi[h2][0].z, hi[h2][0].w);
-              sts128(ar + 256, lo[h2][1].x, lo[h2][1].y, lo[h2][1].z, lo[h2][1].w);
-              sts128(ar + 384, hi[h2][1].x, hi[h2][1].y, hi[h2][1].z, hi[h2][1].w);
-              sts128(f + PF_F_AMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, mnw[h2], 0, 0, 0);
+              sts128(ar, lo[u][h2][0].x, lo[u][h2][0].y, lo[u][h2][0].z, lo[u][h2][0].w);
+              sts128(ar + 128, hi[u][h2][0].x, hi[u][h2][0].y, hi[u][h2][0].z, hi[u][h2][0].w);
+              sts128(ar + 256, lo[u][h2][1].x, lo[u][h2][1].y, lo[u][h2][1].z, lo[u][h2][1].w);
+              sts128(ar + 384, hi[u][h2][1].x, hi[u][h2][1].y, hi[u][h2][1].z, hi[u][h2][1].w);
+              sts128(f + PF_F_AMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, mnw[u][h2], 0, 0, 0);
               asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8),
                            "f"(dd_d[h2]), "f"(dd_m[h2])
                            : "memory");
             }
-          } else {
-            uint4 q0[NH], q1[NH];
-            uint32_t dw[NH];
+          }
+        } else {
+          uint4 q0[2][NH], q1[2][NH];
+          uint32_t dw[2][NH];
+#pragma unroll
+          for (int u = 0; u < 2; u++)
 #pragma unroll
             for (int h2 = 0; h2 < NH; h2++) {
               const int tau = tau0 + 8 * h2;
-              const uint32_t tile = raw + (tau >> 1) * 4 * TB + bin * 2 * TB + (tau & 1) * TB;
-              dw[h2] = ld_shared_u32(tile + 4 * (rr >> 1));
-              q0[h2] = ld_shared_v4(tile + Q8_Q + 32 * rr);
-              q1[h2] = ld_shared_v4(tile + Q8_Q + 32 * rr + 16);
+              const uint32_t tile = raw + (tau >> 1) * 4 * TB + (bin0 + u) * 2 * TB + (tau & 1) * TB;
+              dw[u][h2] = ld_shared_u32(tile + 4 * (rr >> 1));
+              q0[u][h2] = ld_shared_v4(tile + Q8_Q + 32 * rr);
+              q1[u][h2] = ld_shared_v4(tile + Q8_Q + 32 * rr + 16);
             }
-            uint4 o[NH][4];
+          uint4 o[2][NH][4];
+#pragma unroll
+          for (int u = 0; u < 2; u++)
 #pragma unroll
             for (int h2 = 0; h2 < NH; h2++) {
-              o[h2][0] = i8x8_to_h(q0[h2].x, q0[h2].y);
-              o[h2][1] = i8x8_to_h(q0[h2].z, q0[h2].w);
-              o[h2][2] = i8x8_to_h(q1[h2].x, q1[h2].y);
-              o[h2][3] = i8x8_to_h(q1[h2].z, q1[h2].w);
+              o[u][h2][0] = i8x8_to_h(q0[u][h2].x, q0[u][h2].y);
+              o[u][h2][1] = i8x8_to_h(q0[u][h2].z, q0[u][h2].w);
+              o[u][h2][2] = i8x8_to_h(q1[u][h2].x, q1[u][h2].y);
+              o[u][h2][3] = i8x8_to_h(q1[u][h2].z, q1[u][h2].w);
             }
+#pragma unroll
+          for (int u = 0; u < 2; u++) {
+            const uint32_t f = sm0 + PF_OFF_F + fsu[u] * PF_F_BYTES;
+            const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
 #pragma unroll
             for (int h2 = 0; h2 < NH; h2++) {
               const int tau = tau0 + 8 * h2;
@@ -450,36 +470,40 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
               const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
               const uint32_t ar = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
 #pragma unroll
-              for (int kc = 0; kc < 4; kc++) sts128(ar + 128 * kc, o[h2][kc].x, o[h2][kc].y, o[h2][kc].z, o[h2][kc].w);
-              const float d = half_bits_to_float((rr & 1) ? dw[h2] >> 16 : dw[h2]);
+              for (int kc = 0; kc < 4; kc++)
+                sts128(ar + 128 * kc, o[u][h2][kc].x, o[u][h2][kc].y, o[u][h2][kc].z, o[u][h2][kc].w);
+              const float d = half_bits_to_float((rr & 1) ? dw[u][h2] >> 16 : dw[u][h2]);
               asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8), "f"(d),
                            "f"(0.0f)
                            : "memory");
             }
           }
-          // ---- tokens: B main (codes), B min (group sums), dx
-          {
-            const uint4 o = i8x8_to_h(xv[u].x, xv[u].y);
-            sts128(f + PF_F_BMAIN + ((col >> 3) * 4 + kq) * 128 + (col & 7) * 16, o.x, o.y, o.z, o.w);
-            if (kq == 0 && q2)
-              sts128(f + PF_F_BMIN + (col >> 3) * 256 + (col & 7) * 16,
-                     h_of_int((int)(int16_t)(gv[u] & 0xFFFF)) | (h_of_int(gv[u] >> 16) << 16), 0, 0, 0);
-            if (kq == 1) asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsd + 4 * col), "f"(dv[u]) : "memory");
-          }
-          load_tok(bb + 2, xv[u], gv[u], dv[u]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(B.f_full + 8 * fs);
-            mbar_arrive(B.x_full + 8 * xs);
-          }
-          fc++;
-          if (bin == bpst - 1) {
-            if (lane == 0) mbar_arrive(B.raw_empty + 8 * rs);
-            gst++;
-          }
         }
-        if (!ok) break;
+        // ---- tokens: B main (codes), B min (group sums), dx
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+          const uint32_t f = sm0 + PF_OFF_F + fsu[u] * PF_F_BYTES;
+          const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
+          const uint4 o = i8x8_to_h(xv[u].x, xv[u].y);
+          sts128(f + PF_F_BMAIN + ((col >> 3) * 4 + kq) * 128 + (col & 7) * 16, o.x, o.y, o.z, o.w);
+          if (kq == 0 && q2)
+            sts128(f + PF_F_BMIN + (col >> 3) * 256 + (col & 7) * 16,
+                   h_of_int((int)(int16_t)(gv[u] & 0xFFFF)) | (h_of_int(gv[u] >> 16) << 16), 0, 0, 0);
+          if (kq == 1) asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsd + 4 * col), "f"(dv[u]) : "memory");
+        }
+        load_tok(b + 2, xv[0], gv[0], dv[0]);
+        load_tok(b + 3, xv[1], gv[1], dv[1]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int u = 0; u < 2; u++) mbar_arrive(B.f_full + 8 * fsu[u]), mbar_arrive(B.x_full + 8 * xsu[u]);
+        }
+        fc += 2;
+        if (bin0 + 1 == bpst - 1) {
+          if (lane == 0) mbar_arrive(B.raw_empty + 8 * rs);
+          gst++;
+        }
       }
     }
     (void)cw;
