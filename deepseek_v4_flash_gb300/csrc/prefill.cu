@@ -180,6 +180,34 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Two binary32 lanes per instruction (sm_100+ packed forms). Each lane is
+// one correctly rounded operation, exactly as the scalar form: the packed
+// forms change the instruction count, not the arithmetic.
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float &lo, float &hi) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 struct PfBars {
   uint32_t raw_full, raw_empty, f_full, f_empty, t_full, t_empty, x_full;
 };
@@ -519,12 +547,16 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
       if (it.nv <= 0) continue;
       const bool q2 = it.fmt == DS4MOE_Q2S;
       const int nvp = (it.nv - p + 1) >> 1;  // valid columns 16p + j, j < nvp
+      // the pair code of column 16p + lane, loaded now so that finishing the
+      // item does not wait on it
+      const int my_code = lane < nvp ? __ldg(a.list + it.list_off + 2 * lane + p) : 0;
       const int S = expert_segs(it.fmt, a.K), bseg = nb / S;
-      float seg[MATS][16], tot[MATS][16];
+      // segment and row sums of columns (2k, 2k+1) as packed pairs
+      unsigned long long seg[MATS][8], tot[MATS][8];
 #pragma unroll
       for (int m = 0; m < MATS; m++)
 #pragma unroll
-        for (int j = 0; j < 16; j++) seg[m][j] = 0.0f, tot[m][j] = 0.0f;
+        for (int k = 0; k < 8; k++) seg[m][k] = 0ull, tot[m][k] = 0ull;
       for (int b = 0; b < nb; b++, fc++) {
         const int ts = fc % PF_TS, xs = fc % PF_XS;
         if (!pf_wait(B.t_full + 8 * ts, (fc / PF_TS) & 1, abort) ||
@@ -546,19 +578,24 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
           }
           const uint2 ddv = ld_shared_v2(xsd + PF_X_DD + (m * 128 + row) * 8);
           const float d = __uint_as_float(ddv.x), dmin = __uint_as_float(ddv.y);
+          // (-dmin) * B is exactly -(dmin * B): the block term is
+          // dx * fma(d, A, -(dmin * B)) (2-bit) or (d * dx) * I (Q8_0)
+          const unsigned long long d2 = f2_pack(d, d), nm2 = f2_pack(-dmin, -dmin);
 #pragma unroll
           for (int j4 = 0; j4 < 4; j4++) {
             if (4 * j4 < nvp) {
               const uint4 v = ld_shared_v4(xsd + 4 * (16 * p + 4 * j4));
-              const float dxs[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                                    __uint_as_float(v.w)};
 #pragma unroll
-              for (int jj = 0; jj < 4; jj++) {
-                const int j = 4 * j4 + jj;
-                float term;
-                if (q2) term = __fmul_rn(dxs[jj], __fmaf_rn(d, A[j], -__fmul_rn(dmin, Bm[j])));
-                else term = __fmul_rn(__fmul_rn(d, dxs[jj]), A[j]);
-                seg[m][j] = __fadd_rn(seg[m][j], term);
+              for (int jp = 0; jp < 2; jp++) {
+                const int j = 4 * j4 + 2 * jp, k = j >> 1;
+                const unsigned long long dx2 =
+                    jp ? f2_pack(__uint_as_float(v.z), __uint_as_float(v.w))
+                       : f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
+                const unsigned long long a2 = f2_pack(A[j], A[j + 1]);
+                unsigned long long term;
+                if (q2) term = f2_mul(dx2, f2_fma(d2, a2, f2_mul(nm2, f2_pack(Bm[j], Bm[j + 1]))));
+                else term = f2_mul(f2_mul(d2, dx2), a2);
+                seg[m][k] = f2_add(seg[m][k], term);
               }
             }
           }
@@ -567,7 +604,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
 #pragma unroll
           for (int m = 0; m < MATS; m++)
 #pragma unroll
-            for (int j = 0; j < 16; j++) tot[m][j] = __fadd_rn(tot[m][j], seg[m][j]), seg[m][j] = 0.0f;
+            for (int k = 0; k < 8; k++) tot[m][k] = f2_add(tot[m][k], seg[m][k]), seg[m][k] = 0ull;
         }
       }
       if (!ok) break;
@@ -575,10 +612,13 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
 #pragma unroll
       for (int j = 0; j < 16; j++) {
         if (j < nvp) {
-          const int code = __ldg(a.list + it.list_off + 2 * j + p);
+          const int code = __shfl_sync(0xffffffffu, my_code, j);
           const int sr = (code >> 5) * a.NS + (code & 31);
+          float t0v[2], t1v[2];
+          f2_unpack(tot[0][j >> 1], t0v[0], t0v[1]);
+          f2_unpack(tot[MATS - 1][j >> 1], t1v[0], t1v[1]);
           if (MODE == 0) {
-            const float hv = __fmul_rn(cas_silu(tot[0][j]), tot[MATS - 1][j]);
+            const float hv = __fmul_rn(cas_silu(t0v[j & 1]), t1v[j & 1]);
             const int blk = it.rb * 4 + q;
             const float amax = warp_max(fabsf(hv));
             const float dq = __fdiv_rn(amax, 127.0f);
@@ -588,7 +628,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
             if (lane == 0) a.dh[(size_t)sr * (a.F >> 5) + blk] = dq;
             if ((lane & 15) == 0) a.gsh[(size_t)sr * (a.F >> 4) + 2 * blk + (lane >> 4)] = (int16_t)gsum;
           } else {
-            a.apart[(size_t)sr * a.H + it.rb * PF_M + row] = tot[0][j];
+            a.apart[(size_t)sr * a.H + it.rb * PF_M + row] = t0v[j & 1];
           }
         }
       }
