@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
     int c_nst = 0, c_ksps = 1, c_kb = 0, c_ks0 = 0, c_fmt = 0;
     bool c_ok = false;
     int arow[TT], nt = 0;
-    float acc[2][TT];
+    Chains<(TT > 1)> acc[TT];  // per token: the two tiles' row chains
     for (;;) {
       if (!c_ok) {  // the consumer's next item
         if (cj >= n_sh_items && !wait_items()) {
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
         for (int i = 0; i < TT; i++) {
           int sr;
           x_token(a, list_off, list, min(cpass * TT + i, n_tok - 1), &sr, &arow[i]);
-          acc[0][i] = 0.0f, acc[1][i] = 0.0f;
+          chains_zero(acc[i]);
         }
       }
       if (c_nst > 0) {
@@ -387,13 +387,13 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
         const uint32_t st = ring + slot * X_STRIDE;
         const int s0 = c_ks0 + cstage * c_ksps;
         if (c_fmt == DS4MOE_Q2S && c_ksps == 2) {  // two K-steps in one block of code: their dots overlap
-          q2s_step<TT, 2, AS>(st, lane, s0, a.K, arow, nt, aq, ad, ag, acc);
-          q2s_step<TT, 2, AS>(st + c_kb, lane, s0 + 1, a.K, arow, nt, aq, ad, ag, acc);
+          q2s_step<TT, AS, (TT > 1)>(st, lane, s0, a.K, arow, nt, aq, ad, ag, acc);
+          q2s_step<TT, AS, (TT > 1)>(st + c_kb, lane, s0 + 1, a.K, arow, nt, aq, ad, ag, acc);
         } else {
           for (int j = 0; j < c_ksps; j++) {
             const uint32_t t = st + j * c_kb;
-            if (c_fmt == DS4MOE_Q2S) q2s_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, nt, aq, ad, ag, acc);
-            else q8_step<TT, 2, AS>(t, lane, s0 + j, a.K, arow, nt, aq, ad, acc);
+            if (c_fmt == DS4MOE_Q2S) q2s_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, ag, acc);
+            else q8_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, acc);
           }
         }
         __syncwarp();
@@ -411,8 +411,10 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
 #pragma unroll
           for (int i = 0; i < TT; i++) {
             if (i < nt) {
-              dst[i * TILE_ROWS + (lane >> 1)] = acc[0][i];
-              dst[(TT + i) * TILE_ROWS + (lane >> 1)] = acc[1][i];
+              float a0, a1;
+              chains_get(acc[i], a0, a1);
+              dst[i * TILE_ROWS + (lane >> 1)] = a0;
+              dst[(TT + i) * TILE_ROWS + (lane >> 1)] = a1;
             }
           }
         }
