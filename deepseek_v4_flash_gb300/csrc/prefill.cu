@@ -564,6 +564,12 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
                     jp ? f2_pack(__uint_as_float(v.z), __uint_as_float(v.w))
                        : f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
                 const unsigned long long a2 = f2_pack(A[j], A[j + 1]);
+                // ptxas merges a packed product whose only use is a packed
+                // add into one single-rounding multiply-add (.rn or not);
+                // here the add takes one of two products chosen at run time
+                // and stays separate (the parity tests hold it to the bit).
+                // A rewrite without the run-time choice must round the
+                // product on its own (a scalar product, or a second use).
                 unsigned long long term;
                 if (q2) term = f2_mul(dx2, f2_fma(d2, a2, f2_mul(nm2, f2_pack(Bm[j], Bm[j + 1]))));
                 else term = f2_mul(f2_mul(d2, dx2), a2);
