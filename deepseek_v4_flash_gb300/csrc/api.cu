@@ -175,8 +175,9 @@ ds4moe_status build(ds4moe_layer *h, const ds4moe_weights *w) {
     if ((st = alloc(h, &h->hticket, n_ht)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->cticket, n_ct)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->rticket, 16)) != DS4MOE_OK) return st;
-
+    if ((st = alloc(h, &h->xq_ready, 16)) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->rticket, 0, 16, s))) != DS4MOE_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(h->xq_ready, 0, 16, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->hticket, 0, n_ht, s))) != DS4MOE_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(h->cticket, 0, n_ct, s))) != DS4MOE_OK) return st;
   }

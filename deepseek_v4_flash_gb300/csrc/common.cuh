@@ -239,6 +239,26 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// A count in global memory shared by the kernels of one call: arrivals with
+// release semantics, a bounded wait with acquire semantics.
+__device__ __forceinline__ void red_release_gpu_add(int32_t *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits until *p >= target; false after ~2^31 cycles.
+__device__ __forceinline__ bool wait_count(const int32_t *p, int target) {
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(p) < target) {
+    if (clock64() - t0 > (1ll << 31)) return false;
+    __nanosleep(32);
+  }
+  return true;
+}
+
 __device__ __forceinline__ void raise_flag(uint32_t *err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }

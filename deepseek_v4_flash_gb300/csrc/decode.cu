@@ -50,6 +50,7 @@ struct RouteDecArgs {
   int32_t *ids;         // [T][k] routing outputs
   float *w;
   int32_t *rticket;     // the call's ticket (self-resetting)
+  int32_t *xq_ready;    // decode forward: count of blocks whose codes of x are written, else null
   int32_t *bucket;      // bucket table (null: no bucketing)
   uint32_t *err;
 };
@@ -168,6 +169,12 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
     }
   }
   __syncthreads();
+  // The block's codes of x are written: the gate/up kernel starts the shared
+  // expert on them while this kernel routes.
+  if (a.xq_ready && threadIdx.x == 0) {
+    __threadfence();
+    red_release_gpu_add(a.xq_ready, 1);
+  }
   // segment sums of router rows 32*rg + lane
   for (int rg = warp, round = 0; rg < nrg; rg += RC_WARPS, round++) {
     float acc = 0.0f;
@@ -294,6 +301,7 @@ cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_
   r.xq = h->xq, r.dx = h->dx, r.gs = h->gs, r.err = h->err;
   r.ids = ids, r.w = w, r.rticket = h->rticket;
   r.bucket = bucket ? h->bucket : nullptr;
+  r.xq_ready = bucket && x ? h->xq_ready : nullptr;
   void *args[] = {&r};
   return launch_pdl((const void *)k_router_dec, dim3(ROUTER_SEGS, T), dim3(RC_WARPS * 32), router_dec_smem(h), s,
                     args, true);

@@ -20,7 +20,10 @@
 // first, then the routed experts in bucket order); each block lists its items
 // once in shared memory, so every warp walks the same unit sequence without
 // any queue. The shared expert's weights are requested before the wait for
-// the previous kernel; the routed items and the activations come after it.
+// the previous kernel; the routed items come after it. Gate/up with staged
+// activations starts the shared expert's items as soon as the router blocks
+// have written the codes of x (a release/acquire count), before the router
+// has finished routing.
 #include "bucket.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -51,6 +54,8 @@ struct XArgs {
   const float *ad;
   const int16_t *ag;
   const int32_t *bucket;         // bucket table (bucket.cuh)
+  int32_t *xq_ready;             // router blocks whose codes of x are written
+  int xq_parts;                  // ... of this many (all of the call's)
   const int32_t *ids;            // routing [T][k]
   const float *w;
   int8_t *hq;                    // gate/up outputs
@@ -326,9 +331,20 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
   }
 
   {
-    // ---- once the previous kernel is done: the staged activations (the
-    // bucket table is loaded by the first warp that needs it, see wait_items)
-    pdl_wait();
+    // ---- the staged activations (the bucket table is loaded by the first
+    // warp that needs it, see wait_items). Gate/up with staged activations
+    // waits only for the router blocks' codes of x (count with acquire
+    // semantics, read through L2), so the shared expert runs while the
+    // router is still routing; otherwise wait for the previous kernel. Down
+    // clears the count: the gate/up grid, and with it the router grid (every
+    // gate/up block waits for it before its routed items), is complete.
+    if (!DOWN && AS) {
+      if (threadIdx.x == 0 && !wait_count(a.xq_ready, a.xq_parts)) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
+      __syncthreads();
+    } else {
+      pdl_wait();
+      if (DOWN && blockIdx.x == 0 && threadIdx.x == 0) a.xq_ready[0] = 0;
+    }
     if (AS) {
       uint8_t *dst = smem + L.act;
       const size_t nq = (size_t)act_rows * a.K, nd = (size_t)act_rows * (a.K >> 5) * 4,
@@ -586,6 +602,7 @@ cudaError_t launch_experts(const ds4moe_layer *h, int T, float *y, int down, cud
   a.H = d.hidden, a.F = d.ffn, a.E = d.n_experts, a.k = d.top_k, a.NS = h->NS, a.n_shared = d.n_shared, a.T = T;
   a.A_cap = h->A_max, a.rf = d.routed_fmt, a.sf = d.n_shared ? d.shared_fmt : d.routed_fmt, a.down = down;
   a.bucket = h->bucket, a.ids = h->ids, a.w = h->wts;
+  a.xq_ready = h->xq_ready, a.xq_parts = ROUTER_SEGS * T;
   a.hq = h->hq, a.dh = h->dh, a.gsh = h->gsh, a.hbuf = h->hbuf, a.hticket = h->hticket;
   a.apart = h->apart, a.cticket = h->cticket, a.y = y, a.err = h->err;
   a.maxj = x_maxj(h, T, down != 0);

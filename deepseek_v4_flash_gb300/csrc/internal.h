@@ -42,6 +42,7 @@ struct ds4moe_layer {
   int32_t *hticket;      // [Tc*NS][F/32] requant tickets (self-resetting)
   int32_t *cticket;      // [Tc][H/32] combine tickets (self-resetting)
   int32_t *rticket;      // router-kernel ticket of the call (self-resetting)
+  int32_t *xq_ready;     // decode: router blocks whose codes of x are written (cleared by down)
   int32_t *pf_meta;      // prefill: [E+1][2] {pairs, list offset} per group (0 shared, 1+e routed)
   int32_t *pf_pass;      // prefill: [E+2] first pass of each group, then the total
   int32_t *pf_list;      // prefill: [Tp*k + Tp] pair codes (token << 5) | slot, grouped
