@@ -26,9 +26,10 @@ namespace ds4 {
 // token t has one block per K segment. Block seg quantises the token's
 // 32-blocks of its segment (and publishes them), then sums every router row
 // over the segment (warp w: row groups w, w + RC_WARPS, ...; lane = row) into
-// its shared memory. After a cluster barrier, block 0 of the cluster adds the
-// eight segment sums of each row in segment order, reading the other blocks'
-// shared memory, and routes the token with all its threads (route.cuh; hash
+// block 0's shared memory (distributed shared memory stores). After one
+// cluster barrier the other blocks are done; block 0 adds the eight segment
+// sums of each row in segment order from its own shared memory and routes
+// the token with all its threads (route.cuh; hash
 // routing: the table lookup). When bucketing is asked for, the block that
 // routed the call's last token (a self-resetting ticket; none for one token)
 // buckets the call (bucket.cuh).
@@ -55,10 +56,11 @@ struct RouteDecArgs {
   uint32_t *err;
 };
 
-// Layout after the header: lgp [E_pad] f32 (this segment's row sums), dx_s
-// [per] f32, xq_s [per*32] int8, then the 128-aligned work area (router
-// tiles; afterwards the routing and bucketing scratch).
-__host__ __device__ constexpr int rc_dx_off(int E_pad) { return RC_HDR + 4 * E_pad; }
+// Layout after the header: lgp [ROUTER_SEGS][E_pad] f32 (in block 0: every
+// segment's row sums, stored there by the cluster's blocks), dx_s [per] f32,
+// xq_s [per*32] int8, then the 128-aligned work area (router tiles;
+// afterwards the routing and bucketing scratch).
+__host__ __device__ constexpr int rc_dx_off(int E_pad) { return RC_HDR + 4 * ROUTER_SEGS * E_pad; }
 __host__ __device__ constexpr int rc_xq_off(int E_pad, int per) { return rc_dx_off(E_pad) + ((4 * per + 15) & ~15); }
 __host__ __device__ constexpr int rc_work_off(int E_pad, int per) {
   return (rc_xq_off(E_pad, per) + 32 * per + 127) & ~127;
@@ -83,13 +85,12 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// A float in the shared memory of block `rank` of this cluster.
-__device__ __forceinline__ float ld_cluster_f32(const float *p, int rank) {
+// Stores v at the address of p in the shared memory of block `rank` of this
+// cluster.
+__device__ __forceinline__ void st_cluster_f32(float *p, int rank, float v) {
   uint32_t ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
 }
 
 // One arrival on a block-level ticket (thread 0); true in every thread of
@@ -206,14 +207,15 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
       const float *xv = a.x + (size_t)t * a.H;
       for (int j = j0; j < j1; j++) acc = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), acc);
     }
-    lgp[r] = acc;
+    st_cluster_f32(lgp + seg * a.E_pad + r, 0, acc);  // into block 0's table
     __syncwarp();  // every lane is done with the tiles before the next copy
   }
-  cluster_sync_all();
+  cluster_sync_all();  // block 0 has every segment's sums
+  if (seg != 0) return;
   // ---- routing of token t by block 0 of its cluster
   const RouteScratch rs = route_scratch(work, a.E_pad, a.k);
   int32_t *hash_ids = (int32_t *)(work + route_block_smem(a.E_pad, a.k));  // hash routing: this token's ids
-  if (seg == 0) {
+  {
     if (a.learned) {
 #pragma unroll
       for (int i = 0; i < RC_MAX_E / (RC_WARPS * 32); i++) {
@@ -221,7 +223,7 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
         if (e < a.E_pad) {
           float lg = 0.0f;
           if (e < a.E)
-            for (int g = 0; g < ROUTER_SEGS; g++) lg = __fadd_rn(lg, ld_cluster_f32(lgp + e, g));
+            for (int g = 0; g < ROUTER_SEGS; g++) lg = __fadd_rn(lg, lgp[g * a.E_pad + e]);
           route_score(rs, e, a.E, lg, bias_r[i]);
         }
       }
@@ -236,8 +238,7 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
       a.w[(size_t)t * a.k + threadIdx.x] = okv ? __fmul_rn(__fdiv_rn(1.0f, (float)a.k), a.scale) : 0.0f;
     }
   }
-  cluster_sync_all();  // the other blocks' segment sums stay until block 0 has read them
-  if (seg != 0 || !a.bucket) return;
+  if (!a.bucket) return;
   // ---- bucketing of the call by the block that routed its last token (a
   // single token: from this block's own selection, still in shared memory)
   int32_t *scr = hash_ids + 16;
