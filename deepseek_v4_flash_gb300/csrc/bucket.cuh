@@ -78,4 +78,46 @@ __device__ inline void bucket_rank(const int32_t *ids, int T, int E, int k, int 
   __syncthreads();
 }
 
+// The same table for a single token, by one warp (lane j < k: slot j); every
+// lane of the warp calls it. ids: the token's k routed ids (-1 = none; >= E
+// raises DS4MOE_DEVERR_INTERNAL and is dropped).
+__device__ inline void bucket_one_token(const int32_t *ids, int E, int k, int n_shared, int32_t *out, int A_cap,
+                                        uint32_t *err, int lane) {
+  const int e = lane < k ? ids[lane] : -1;
+  const bool ok = e >= 0 && e < E;
+  if (lane < k && e >= E) raise_flag(err, DS4MOE_DEVERR_INTERNAL);
+  int r = 0, c = 0, f = 1, d = 0;
+  for (int i = 0; i < k; i++) {
+    const int ei = __shfl_sync(0xffffffffu, e, i);
+    const bool oki = ei >= 0 && ei < E;
+    // is slot i the first of its expert?
+    int fi = oki;
+    for (int j = 0; j < i; j++) fi &= __shfl_sync(0xffffffffu, e, j) != ei;
+    if (oki) {
+      r += (ei < e || (ei == e && i < lane)) ? 1 : 0;
+      c += ei == e ? 1 : 0;
+      f &= (ei == e && i < lane) ? 0 : 1;
+      d += (fi && ei < e) ? 1 : 0;
+    }
+  }
+  const unsigned valid = __ballot_sync(0xffffffffu, ok), first = __ballot_sync(0xffffffffu, ok && f);
+  const int n_pairs = __popc(valid), n_exp = __popc(first);
+  int4 *act = (int4 *)(out + BKT_HDR);
+  int32_t *list = out + BKT_HDR + 4 * A_cap;
+  if (ok) {
+    list[r] = lane;  // token 0, slot lane
+    if (f) act[n_shared + d] = make_int4(e, c, r, 0);
+  }
+  if (lane == 0) {
+    if (n_shared) {
+      list[n_pairs] = k;
+      act[0] = make_int4(E, 1, n_pairs, 0);
+    }
+    out[0] = n_exp + n_shared;
+    out[1] = n_pairs;
+    out[2] = 0;
+    out[3] = 0;
+  }
+}
+
 }  // namespace ds4

@@ -244,7 +244,7 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   int32_t *scr = hash_ids + 16;
   if (a.T == 1) {
     __syncthreads();
-    bucket_rank(a.learned ? rs.sel : hash_ids, 1, a.E, a.k, a.NS, a.n_shared, scr, a.bucket, a.A_cap, a.err);
+    if (warp == 0) bucket_one_token(a.learned ? rs.sel : hash_ids, a.E, a.k, a.n_shared, a.bucket, a.A_cap, a.err, lane);
     return;
   }
   if (!block_ticket_last(a.rticket, a.T, s_flag)) return;

@@ -79,6 +79,7 @@ __device__ inline void route_select(const RouteScratch &r, int E_pad, int k, flo
   for (int i = tid; i < nc; i += nth) {
     const uint64_t me = r.cand[i];
     int n = 0;
+#pragma unroll 8
     for (int j = 0; j < nc; j++) n += r.cand[j] > me ? 1 : 0;
     if (n < k) r.sel[n] = (int)(~(uint32_t)me);
   }

@@ -196,6 +196,24 @@ def test_bad_token_id_sets_flag_and_skips_token(ora):
     assert layer.device_error() == 0  # cleared
 
 
+def test_bad_token_id_single_token(ora):
+    """One token (the single-token bucketing) whose id is out of range: the
+    flag is raised and the token adds nothing, not even the shared expert."""
+    import torch
+    spec = synth.MICRO_HASH
+    w, ol, layer = _layer_pair(ora, spec, 33, 130)
+    x = synth.gen_x(spec, 34, 1)
+    tok = np.array([spec.vocab + 5], dtype=np.int32)
+    y0 = np.random.default_rng(34).standard_normal(x.shape).astype(np.float32)
+    ref, _, _, bad = ol.forward(x, y0, tok)
+    assert bad == 1 and np.array_equal(ref.view(np.uint32), y0.view(np.uint32))
+    yd = torch.from_numpy(y0).cuda()
+    layer.forward(torch.from_numpy(x).cuda(), yd, torch.from_numpy(tok).cuda())
+    assert layer.device_error() & 1
+    assert np.array_equal(yd.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert layer.device_error() == 0
+
+
 def test_nonfinite_input_sets_flag(ora):
     import torch
     spec = synth.MICRO
