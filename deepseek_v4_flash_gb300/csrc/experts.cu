@@ -338,22 +338,43 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
     // router is still routing; otherwise wait for the previous kernel. Down
     // clears the count: the gate/up grid, and with it the router grid (every
     // gate/up block waits for it before its routed items), is complete.
-    if (!DOWN && AS) {
+    constexpr bool EARLY = !DOWN && AS;
+    if (EARLY) {
       if (threadIdx.x == 0 && !wait_count(a.xq_ready, a.xq_parts)) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
       __syncthreads();
     } else {
       pdl_wait();
       if (DOWN && blockIdx.x == 0 && threadIdx.x == 0) a.xq_ready[0] = 0;
     }
-    if (AS) {
-      uint8_t *dst = smem + L.act;
-      const size_t nq = (size_t)act_rows * a.K, nd = (size_t)act_rows * (a.K >> 5) * 4,
-                   ng = (size_t)act_rows * (a.K >> 4) * 2;
-      for (size_t i = threadIdx.x; i < nq / 16; i += blockDim.x) ((uint4 *)dst)[i] = __ldcg((const uint4 *)a.aq + i);
-      for (size_t i = threadIdx.x; i < nd / 16; i += blockDim.x)
-        ((uint4 *)(dst + nq))[i] = __ldcg((const uint4 *)a.ad + i);
-      for (size_t i = threadIdx.x; i < ng / 16; i += blockDim.x)
-        ((uint4 *)(dst + nq + nd))[i] = __ldcg((const uint4 *)a.ag + i);
+    // Down with staged activations: the last warp loads the routed table
+    // while the others stage (unstaged kernels load it after the barrier,
+    // measured faster there; EARLY gate/up must wait for the router first).
+    constexpr bool CLAIM = AS && !EARLY;
+    const int nstage = CLAIM ? blockDim.x - 32 : blockDim.x;
+    if (CLAIM && warp == X_WARPS - 1) {
+      (void)wait_items();
+    } else if (AS) {
+      // the three arrays as one run of 16-byte words, every load of a
+      // round issued before its stores
+      uint4 *dst = (uint4 *)(smem + L.act);
+      const size_t nq = (size_t)act_rows * a.K / 16, nd = (size_t)act_rows * (a.K >> 5) * 4 / 16,
+                   ng = (size_t)act_rows * (a.K >> 4) * 2 / 16, n = nq + nd + ng;
+      constexpr int SB = 4;
+      for (size_t b0 = 0; b0 < n; b0 += (size_t)SB * nstage) {
+        uint4 v[SB];
+#pragma unroll
+        for (int j = 0; j < SB; j++) {
+          const size_t i = b0 + threadIdx.x + (size_t)j * nstage;
+          if (i < n)
+            v[j] = __ldcg(i < nq ? (const uint4 *)a.aq + i
+                          : i < nq + nd ? (const uint4 *)a.ad + (i - nq) : (const uint4 *)a.ag + (i - nq - nd));
+        }
+#pragma unroll
+        for (int j = 0; j < SB; j++) {
+          const size_t i = b0 + threadIdx.x + (size_t)j * nstage;
+          if (i < n) dst[i] = v[j];
+        }
+      }
     }
     __syncthreads();
   }
