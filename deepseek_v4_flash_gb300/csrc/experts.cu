@@ -139,15 +139,37 @@ __device__ __forceinline__ void x_requant(const XArgs &a, float h, int sr, int b
 }
 
 // CAS step 8 for rows 32*rg .. +31 of token t (lane = row).
+// Every value is requested before the first is used (up to 8 routed slots;
+// more take the plain loop).
 __device__ __forceinline__ void x_combine(const XArgs &a, int t, int rg, int lane) {
-  if (__ldg(a.ids + (size_t)t * a.k) < 0) return;  // an out-of-range hash token adds nothing
   const int r = 32 * rg + lane;
-  float acc = 0.0f;
-  for (int j = 0; j < a.k; j++)
-    acc = __fadd_rn(acc, __fmul_rn(__ldg(a.w + (size_t)t * a.k + j),
-                                   __ldcg(a.apart + ((size_t)t * a.NS + j) * a.H + r)));
-  if (a.n_shared) acc = __fadd_rn(acc, __ldcg(a.apart + ((size_t)t * a.NS + a.k) * a.H + r));
+  const float *ap = a.apart + (size_t)t * a.NS * a.H + r;
+  const float *wp = a.w + (size_t)t * a.k;
   float *yp = a.y + (size_t)t * a.H + r;
+  constexpr int KF = 8;
+  if (a.k <= KF) {
+    const int id0 = __ldg(a.ids + (size_t)t * a.k);
+    float wv[KF], av[KF];
+#pragma unroll
+    for (int j = 0; j < KF; j++) {
+      wv[j] = j < a.k ? __ldg(wp + j) : 0.0f;
+      av[j] = j < a.k ? __ldcg(ap + (size_t)j * a.H) : 0.0f;
+    }
+    const float sh = a.n_shared ? __ldcg(ap + (size_t)a.k * a.H) : 0.0f;
+    const float y0 = *yp;
+    if (id0 < 0) return;  // an out-of-range hash token adds nothing
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < KF; j++)
+      if (j < a.k) acc = __fadd_rn(acc, __fmul_rn(wv[j], av[j]));
+    if (a.n_shared) acc = __fadd_rn(acc, sh);
+    *yp = __fadd_rn(y0, acc);
+    return;
+  }
+  if (__ldg(a.ids + (size_t)t * a.k) < 0) return;
+  float acc = 0.0f;
+  for (int j = 0; j < a.k; j++) acc = __fadd_rn(acc, __fmul_rn(__ldg(wp + j), __ldcg(ap + (size_t)j * a.H)));
+  if (a.n_shared) acc = __fadd_rn(acc, __ldcg(ap + (size_t)a.k * a.H));
   *yp = __fadd_rn(*yp, acc);
 }
 
@@ -268,11 +290,25 @@ __global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs
     if (lane == 0) mine = atomicCAS(s_claim, 0, 1) == 0;
     if (__shfl_sync(0xffffffffu, mine, 0)) {  // this warp loads the bucket for the block
       pdl_wait();
-      for (int i = lane; i < nbk; i += 32) bks[i] = __ldcg(a.bucket + i);
+      // (loads of a round issued before its stores)
+      for (int i0 = 0; i0 < nbk; i0 += 4 * 32) {
+        int v[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) v[j] = i0 + lane + 32 * j < nbk ? __ldcg(a.bucket + i0 + lane + 32 * j) : 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+          if (i0 + lane + 32 * j < nbk) bks[i0 + lane + 32 * j] = v[j];
+      }
       if (DOWN)  // routed slots with an expert, per token (the combine's arrival count)
         for (int t = lane; t < a.T; t += 32) {
           int n = 0;
-          for (int j = 0; j < a.k; j++) n += __ldg(a.ids + (size_t)t * a.k + j) >= 0;
+          for (int j0 = 0; j0 < a.k; j0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) v[j] = j0 + j < a.k ? __ldg(a.ids + (size_t)t * a.k + j0 + j) : -1;
+#pragma unroll
+            for (int j = 0; j < 8; j++) n += v[j] >= 0;
+          }
           valid[t] = n;
         }
       __syncwarp();
