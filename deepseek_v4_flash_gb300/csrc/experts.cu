@@ -1,9 +1,10 @@
 // experts.cu -- gate/up and down of the routed and shared experts for a
 // decode-sized call (n_tok <= DEC_MAX_T).
 //
-// Persistent: one block per SM, XC = 8 compute warps and XE = 4 epilogue
-// warps. A work item is 16 rows of gate and up (interleaved per K-step) or
-// 32 rows of down (two 16-row tiles per K-step) of one expert, for the
+// Persistent: one block per SM (two for single-token calls), XC = 8 compute
+// warps and XE = 4 epilogue warps (two for single-token calls). A work item
+// is 16 rows of gate and up (interleaved per K-step) or 32 rows of down (two
+// 16-row tiles per K-step) of one expert, for the
 // tokens routed to that expert; a unit is an item with one pass over up to
 // TT of those tokens. Every expert row is summed in 8 K-segments (CAS step
 // 4), and compute warp w owns segment w of every unit: it streams that
@@ -32,8 +33,11 @@
 namespace ds4 {
 
 constexpr int XC = EXPERT_SEGS;  // compute warps, one K-segment each
-constexpr int XE = 4;            // epilogue warps
-constexpr int X_WARPS = XC + XE;
+// Epilogue warps: 4, or 2 for single-token calls (a block has about three
+// units then; two blocks per SM, and 10 warps instead of 12 leave the
+// compute warps 96 registers instead of 80, with no spills).
+__host__ __device__ constexpr int x_epi_warps(int TT) { return TT == 1 ? 2 : 4; }
+__host__ __device__ constexpr int x_warps(int TT) { return XC + x_epi_warps(TT); }
 // Ring per compute warp, 10.75 KB in flight per warp and 86 KB per SM, which
 // covers the loaded HBM latency at full bandwidth: gate/up 2 slots of 5376
 // bytes (two K-steps of a routed item, computed together for instruction-
@@ -213,7 +217,8 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // which need no routing. The shared expert's weights are requested before
 // the wait for the previous kernel.
 template <int TT, bool AS, bool DOWN>
-__global__ void __launch_bounds__(X_WARPS * 32, TT == 1 ? 2 : 1) k_experts(XArgs a) {
+__global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(XArgs a) {
+  constexpr int XE = x_epi_warps(TT), X_WARPS = x_warps(TT);
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int X_NST = XRing<DOWN>::NST, X_STRIDE = XRing<DOWN>::STRIDE;
   constexpr int PS = x_slots(TT);
@@ -675,7 +680,8 @@ cudaError_t launch_experts(const ds4moe_layer *h, int T, float *y, int down, cud
 
   const void *fn = down ? (as ? x_fn<true, true>(T) : x_fn<false, true>(T)) : (as ? x_fn<true, false>(T) : x_fn<false, false>(T));
   void *args[] = {&a};
-  return launch_pdl(fn, dim3(x_blocks(h, T)), dim3(X_WARPS * 32), x_smem_bytes(h, T, down != 0, as), s, args, true);
+  return launch_pdl(fn, dim3(x_blocks(h, T)), dim3(x_warps(x_tt(T)) * 32), x_smem_bytes(h, T, down != 0, as), s, args,
+                    true);
 }
 
 cudaError_t experts_set_attributes() {
