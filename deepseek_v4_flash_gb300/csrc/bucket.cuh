@@ -86,27 +86,25 @@ __device__ inline void bucket_one_token(const int32_t *ids, int E, int k, int n_
   const int e = lane < k ? ids[lane] : -1;
   const bool ok = e >= 0 && e < E;
   if (lane < k && e >= E) raise_flag(err, DS4MOE_DEVERR_INTERNAL);
-  int r = 0, c = 0, f = 1, d = 0;
-  for (int i = 0; i < k; i++) {
+  const unsigned valid = __ballot_sync(0xffffffffu, ok);
+  const unsigned same = __match_any_sync(0xffffffffu, ok ? e : -1) & valid;  // this lane's expert
+  const bool f = ok && (same & ((1u << lane) - 1u)) == 0;                    // first slot of it
+  const unsigned first = __ballot_sync(0xffffffffu, f);
+  int below = 0, dbelow = 0;  // valid slots / distinct experts with a lower id
+#pragma unroll
+  for (int i = 0; i < 32; i++) {
+    if (i >= k) break;
     const int ei = __shfl_sync(0xffffffffu, e, i);
-    const bool oki = ei >= 0 && ei < E;
-    // is slot i the first of its expert?
-    int fi = oki;
-    for (int j = 0; j < i; j++) fi &= __shfl_sync(0xffffffffu, e, j) != ei;
-    if (oki) {
-      r += (ei < e || (ei == e && i < lane)) ? 1 : 0;
-      c += ei == e ? 1 : 0;
-      f &= (ei == e && i < lane) ? 0 : 1;
-      d += (fi && ei < e) ? 1 : 0;
-    }
+    below += ((valid >> i) & 1u) && ei < e;
+    dbelow += ((first >> i) & 1u) && ei < e;
   }
-  const unsigned valid = __ballot_sync(0xffffffffu, ok), first = __ballot_sync(0xffffffffu, ok && f);
+  const int r = below + __popc(same & ((1u << lane) - 1u)), c = __popc(same);
   const int n_pairs = __popc(valid), n_exp = __popc(first);
   int4 *act = (int4 *)(out + BKT_HDR);
   int32_t *list = out + BKT_HDR + 4 * A_cap;
   if (ok) {
     list[r] = lane;  // token 0, slot lane
-    if (f) act[n_shared + d] = make_int4(e, c, r, 0);
+    if (f) act[n_shared + dbelow] = make_int4(e, c, r, 0);
   }
   if (lane == 0) {
     if (n_shared) {
