@@ -38,6 +38,7 @@ METRIC = "MoE-FFN tokens/s (decode, prefill) and achieved HBM GB/s vs GB300 peak
 WORKLOADS = {
     "ds4-decode-1": (synth.DS4, 1, "single decode token, DeepSeek-V4-Flash-shaped layer (H 4096, E 256 top-6 + 1 "
                                    "shared, F 2048, Q2S routed, Q8_0 shared/router), learned routing"),
+    "ds4-decode-8": (synth.DS4, 8, "batched decode of 8 tokens on the same layer, learned routing"),
     "ds4-decode-32-zipf": (synth.DS4_ZIPF, 32, "batched decode of 32 tokens on the same layer, router bias with "
                                                "Zipf(1.1) expert popularity"),
     "ds4-hash-prefill-512": (synth.DS4_HASH, 512, "hash-routed layer (vocab 129280), prefill chunk of 512 tokens"),
