@@ -42,12 +42,11 @@ __host__ __device__ constexpr int x_warps(int TT) { return XC + x_epi_warps(TT);
 // covers the loaded HBM latency at full bandwidth: gate/up 2 slots of 5376
 // bytes (two K-steps of a routed item, computed together for instruction-
 // level parallelism), down 4 slots of 2688 bytes (one K-step of a routed
-// 32-row item).
-template <bool DOWN> struct XRing {
-  static constexpr int NST = DOWN ? 4 : 2;
-  static constexpr int STRIDE = DOWN ? 2688 : 5376;
-};
-constexpr int X_RING_BYTES = 4 * 2688;
+// 32-row item). Down at eight tokens: 2 slots, so that its activations
+// (8 tokens x every slot) fit in shared memory beside the ring.
+__host__ __device__ constexpr int x_ring_nst(int TT, bool down) { return down ? (TT >= 8 ? 2 : 4) : 2; }
+__host__ __device__ constexpr int x_ring_stride(bool down) { return down ? 2688 : 5376; }
+__host__ __device__ constexpr int x_ring_bytes(int TT, bool down) { return x_ring_nst(TT, down) * x_ring_stride(down); }
 
 struct XArgs {
   int H, F, E, k, NS, n_shared, T, A_cap;
@@ -73,7 +72,9 @@ struct XArgs {
   uint32_t *err;
 };
 
-__host__ __device__ constexpr int x_slots(int TT) { return 8 + 0 * TT; }
+// Partial-sum slots between the compute and the epilogue warps (down at
+// eight tokens: 4, for the same reason as its ring).
+__host__ __device__ constexpr int x_slots(int TT, bool down) { return down && TT >= 8 ? 4 : 8; }
 
 // Invariants of the items of one kind (shared or routed) for one warp.
 struct XKind {
@@ -183,13 +184,13 @@ struct XSmem {
   int ring, bars, ctrl, part, tab, valid, bkt, act, total;
 };
 
-__host__ __device__ inline XSmem x_smem(int TT, int mats, int nbk, int act_bytes, int maxj, int T) {
+__host__ __device__ inline XSmem x_smem(int TT, bool down, int mats, int nbk, int act_bytes, int maxj, int T) {
   XSmem s;
   s.ring = 0;
-  s.bars = XC * X_RING_BYTES;
+  s.bars = XC * x_ring_bytes(TT, down);
   s.ctrl = s.bars + XC * 8 * 8;
   s.part = s.ctrl + 256;  // bucket barrier, item count, then full[8] and empty[8] slot barriers
-  s.tab = s.part + x_slots(TT) * XC * mats * TT * TILE_ROWS * 4;
+  s.tab = s.part + x_slots(TT, down) * XC * mats * TT * TILE_ROWS * 4;
   s.valid = s.tab + maxj * 32;
   s.bkt = s.valid + ((T * 4 + 127) & ~127);
   s.act = s.bkt + ((nbk * 4 + 127) & ~127);
@@ -220,15 +221,15 @@ template <int TT, bool AS, bool DOWN>
 __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(XArgs a) {
   constexpr int XE = x_epi_warps(TT), X_WARPS = x_warps(TT);
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int X_NST = XRing<DOWN>::NST, X_STRIDE = XRing<DOWN>::STRIDE;
-  constexpr int PS = x_slots(TT);
+  constexpr int X_NST = x_ring_nst(TT, DOWN), X_STRIDE = x_ring_stride(DOWN);
+  constexpr int PS = x_slots(TT, DOWN);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int mats = 2;       // gate and up (16 rows), or the two 16-row halves of 32 rows (down)
   constexpr int ROWS = DOWN ? 32 : 16;  // output rows of a work item
   const int nbk = bucket_table_ints(a.A_cap, a.T, a.NS);
   const int act_rows = DOWN ? a.T * a.NS : a.T;
   const int act_bytes = AS ? act_rows * (a.K + (a.K >> 5) * 4 + (a.K >> 4) * 2) : 0;
-  const XSmem L = x_smem(TT, mats, nbk, act_bytes, a.maxj, a.T);
+  const XSmem L = x_smem(TT, DOWN, mats, nbk, act_bytes, a.maxj, a.T);
   volatile int *s_nitems = (volatile int *)(smem + L.ctrl + 8);  // items of this block (after the bucket)
   int *s_claim = (int *)(smem + L.ctrl + 12);                     // the warp that loads the bucket
   const uint32_t full0 = smem_u32(smem + L.ctrl) + 64, empty0 = full0 + 64;  // slot barriers, 8 bytes apart
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
     ag = (const int16_t *)(smem + L.act + act_rows * a.K + act_rows * (a.K >> 5) * 4);
   }
   pdl_launch_dependents();
-  const uint32_t ring = smem_u32(smem + L.ring + warp * X_RING_BYTES);
+  const uint32_t ring = smem_u32(smem + L.ring + warp * x_ring_bytes(TT, DOWN));
   const uint32_t bar = smem_u32(smem + L.bars + warp * 8 * 8);
   const int nsh = a.n_shared ? a.rows / ROWS : 0, RG = a.rows / ROWS;
   const int G = gridDim.x, c = blockIdx.x;
@@ -641,7 +642,7 @@ static int x_maxj(const ds4moe_layer *h, int T, bool down) {
 
 static size_t x_smem_bytes(const ds4moe_layer *h, int T, bool down, bool as) {
   const int nbk = bucket_table_ints(h->A_max, T, h->NS);
-  return (size_t)x_smem(x_tt(T), 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0, x_maxj(h, T, down), T)
+  return (size_t)x_smem(x_tt(T), down, 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0, x_maxj(h, T, down), T)
       .total;
 }
 
