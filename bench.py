@@ -571,8 +571,8 @@ def main():
         xh = [xs[i % NX].cpu().pin_memory() for i in range(min(args.e2e_steps, NX))]
         yh = torch.zeros(T, spec.hidden).pin_memory()
         th = tok.cpu().pin_memory() if tok is not None else None
-        for i in range(3):
-            layer.forward_host(xh[i % len(xh)], yh, th)
+        for i in range(max(3, NL)):  # every layer copy once (first calls set up its host path)
+            layers[i % NL].forward_host(xh[i % len(xh)], yh, th)
         tot = 0.0
         for i in range(args.e2e_steps):
             if use_flush:

@@ -274,6 +274,12 @@ void ds4moe_destroy(ds4moe_layer *h) {
   cudaDeviceSynchronize();
   if (h->ev_made)
     for (int i = 0; i < 8; i++) cudaEventDestroy(h->ev[i]);
+  for (int i = 0; i < DS4_HOST_GRAPHS; i++)
+    if (h->host_graph[i]) cudaGraphExecDestroy(h->host_graph[i]);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  if (h->x_pin) cudaFreeHost(h->x_pin);
+  if (h->y_pin) cudaFreeHost(h->y_pin);
+  if (h->tok_pin) cudaFreeHost(h->tok_pin);
   free_all(h);
   delete h;
 }
@@ -306,14 +312,9 @@ ds4moe_status ds4moe_route(ds4moe_layer *h, const float *x, const int32_t *token
   return cuda_status(e);
 }
 
-ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids, float *y,
-                             void *stream) {
-  ds4moe_status st = check_call(h, n_tok);
-  if (st != DS4MOE_OK) return st;
-  if (n_tok == 0) return DS4MOE_OK;
-  if (!is_dev_ptr(x) || !is_dev_ptr(y) || x == y) return DS4MOE_ERR_INVALID_ARG;
-  if (h->d.route == DS4MOE_ROUTE_HASH && !is_dev_ptr(token_ids)) return DS4MOE_ERR_INVALID_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
+// The launches of a forward call whose arguments are checked.
+static ds4moe_status forward_run(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids, float *y,
+                                 cudaStream_t s) {
   const int H = h->d.hidden;
   const bool prof = h->prof_on != 0;
   auto mark = [&](int i) {
@@ -349,6 +350,16 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
     h->launches += 3;
   }
   return cuda_status(e);
+}
+
+ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids, float *y,
+                             void *stream) {
+  ds4moe_status st = check_call(h, n_tok);
+  if (st != DS4MOE_OK) return st;
+  if (n_tok == 0) return DS4MOE_OK;
+  if (!is_dev_ptr(x) || !is_dev_ptr(y) || x == y) return DS4MOE_ERR_INVALID_ARG;
+  if (h->d.route == DS4MOE_ROUTE_HASH && !is_dev_ptr(token_ids)) return DS4MOE_ERR_INVALID_ARG;
+  return forward_run(h, x, n_tok, token_ids, y, (cudaStream_t)stream);
 }
 
 ds4moe_status ds4moe_profile_enable(ds4moe_layer *h, int32_t on) {
@@ -391,6 +402,53 @@ ds4moe_status ds4moe_profile_read(const ds4moe_layer *h, double *ms_out, int32_t
 
 uint64_t ds4moe_launch_count(const ds4moe_layer *h) { return h ? h->launches : 0; }
 
+// A decode-sized forward_host call (n_tok <= Tc) runs on the handle's
+// mapped pinned buffers: the kernels read x (and the token ids) and update y
+// in host memory directly over the coherent CPU-GPU link, so no copy
+// precedes or follows them; the launches are captured once per token count
+// into a CUDA graph.
+static cudaError_t host_sequence(ds4moe_layer *h, int n_tok, bool hash, cudaStream_t s) {
+  float *xm = nullptr, *ym = nullptr;
+  int32_t *tm = nullptr;
+  cudaError_t e = cudaHostGetDevicePointer((void **)&xm, h->x_pin, 0);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer((void **)&ym, h->y_pin, 0);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer((void **)&tm, h->tok_pin, 0);
+  if (e != cudaSuccess) return e;
+  return forward_run(h, xm, n_tok, hash ? tm : nullptr, ym, s) == DS4MOE_OK ? cudaSuccess : cudaErrorUnknown;
+}
+
+static cudaGraphExec_t host_graph(ds4moe_layer *h, int n_tok, bool hash) {
+  if (h->host_graph[n_tok]) return h->host_graph[n_tok];
+  if (h->host_graph_off) return nullptr;
+  if (!h->cap_stream && cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    h->cap_stream = nullptr;
+    h->host_graph_off = 1;
+    return nullptr;
+  }
+  const int64_t l0 = h->launches;
+  cudaGraph_t g = nullptr;
+  cudaGraphExec_t x = nullptr;
+  if (cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    cudaGetLastError();
+    h->host_graph_off = 1;
+    return nullptr;
+  }
+  const cudaError_t e = host_sequence(h, n_tok, hash, h->cap_stream);
+  const cudaError_t e2 = cudaStreamEndCapture(h->cap_stream, &g);
+  h->launches = l0;
+  if (e == cudaSuccess && e2 == cudaSuccess && g && cudaGraphInstantiate(&x, g, 0) == cudaSuccess) {
+    h->host_graph[n_tok] = x;
+    h->host_graph_launches[n_tok] = 3 * ((n_tok + h->Tc - 1) / h->Tc);
+  } else {  // not capturable here: the plain sequence from now on
+    cudaGetLastError();
+    h->host_graph_off = 1;
+    x = nullptr;
+  }
+  if (g) cudaGraphDestroy(g);
+  return x;
+}
+
 ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t n_tok, const int32_t *token_ids_host,
                                   float *y_host, void *stream) {
   ds4moe_status st = check_call(h, n_tok);
@@ -407,6 +465,29 @@ ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t 
   }
   cudaStream_t s = (cudaStream_t)stream;
   const size_t nb = (size_t)n_tok * h->d.hidden * 4;
+  // Decode-sized calls: the inputs into the handle's mapped pinned buffers,
+  // one graph replay of the forward on them, the result back.
+  if (n_tok <= h->Tc && !h->prof_on) {
+    const size_t pb = (size_t)h->Tc * h->d.hidden * 4;
+    if (!h->x_pin && (cudaHostAlloc(&h->x_pin, pb, cudaHostAllocMapped) != cudaSuccess ||
+                      cudaHostAlloc(&h->y_pin, pb, cudaHostAllocMapped) != cudaSuccess ||
+                      cudaHostAlloc(&h->tok_pin, (size_t)h->Tc * 4, cudaHostAllocMapped) != cudaSuccess)) {
+      cudaGetLastError();
+      return DS4MOE_ERR_OOM;
+    }
+    cudaGraphExec_t g = host_graph(h, n_tok, hash);
+    if (g) {
+      memcpy(h->x_pin, x_host, nb);
+      memcpy(h->y_pin, y_host, nb);
+      if (hash) memcpy(h->tok_pin, token_ids_host, (size_t)n_tok * 4);
+      cudaError_t e = cudaGraphLaunch(g, s);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+      if (e != cudaSuccess) return cuda_status(e);
+      h->launches += h->host_graph_launches[n_tok];
+      memcpy(y_host, h->y_pin, nb);
+      return DS4MOE_OK;
+    }
+  }
   cudaError_t e = cudaMemcpyAsync(h->x_dev, x_host, nb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(h->y_dev, y_host, nb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && hash)

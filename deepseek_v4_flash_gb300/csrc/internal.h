@@ -6,6 +6,8 @@
 
 #include "ds4moe.h"
 
+constexpr int DS4_HOST_GRAPHS = 65;  // decode chunk sizes 1..64 (DEC_MAX_T) + 1
+
 struct ds4moe_layer {
   ds4moe_layer_desc d;
   int device;
@@ -50,6 +52,15 @@ struct ds4moe_layer {
   // Staging for ds4moe_forward_host.
   float *x_dev, *y_dev;
   int32_t *tok_dev;
+  // Decode-sized ds4moe_forward_host calls replay one CUDA graph per token
+  // count (the copies through these pinned buffers and the forward's
+  // launches), captured on first use.
+  float *x_pin, *y_pin;
+  int32_t *tok_pin;
+  cudaStream_t cap_stream;
+  cudaGraphExec_t host_graph[DS4_HOST_GRAPHS];   // by token count, 1 .. decode chunk
+  int64_t host_graph_launches[DS4_HOST_GRAPHS];   // kernels one replay launches
+  int host_graph_off;                              // capture failed once: plain copies and launches
 
   // Profiling (ds4moe_profile_*) and launch counting.
   int prof_on;
@@ -79,6 +90,7 @@ cudaError_t launch_rmsnorm(const float *x, float *out, int T, int H, float eps, 
 
 // decode.cu
 constexpr int DEC_MAX_T = 64;  // largest n_tok served by the decode path
+static_assert(DS4_HOST_GRAPHS == DEC_MAX_T + 1, "one forward_host graph per decode chunk size");
 size_t route_dec_smem(const ds4moe_layer *h);
 cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
                              float *w, bool bucket, cudaStream_t s);

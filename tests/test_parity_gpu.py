@@ -360,6 +360,30 @@ def test_prefill_more_tokens_than_one_chunk(ora):
     layer.close()
 
 
+def test_forward_host_replays(ora):
+    """Decode-sized host calls replay one captured graph per token count:
+    repeated calls with new inputs, several counts (the first call of each
+    captures), pinned and pageable host tensors, learned and hash routing,
+    each bit-exact against the oracle."""
+    import torch
+    for spec, seed, mt in ((synth.MICRO, 41, 65), (synth.MICRO_HASH, 43, 130)):
+        w, ol, layer = _layer_pair(ora, spec, seed, mt)
+        for i, T in enumerate((1, 3, 1, 64, 3, 1)):
+            x = margin_inputs(ol, spec, seed + 7 * i, T)
+            tok = synth.gen_token_ids(spec, seed + 7 * i, T) if spec.route == "hash" else None
+            y0 = np.random.default_rng(seed + i).standard_normal(x.shape).astype(np.float32)
+            ref, *_ = ol.forward(x, y0, tok)
+            pin = i % 2 == 0
+            xh, yh = torch.from_numpy(x), torch.from_numpy(y0.copy())
+            th = torch.from_numpy(tok) if tok is not None else None
+            if pin:
+                xh, yh = xh.pin_memory(), yh.pin_memory()
+                th = th.pin_memory() if th is not None else None
+            layer.forward_host(xh, yh, th)
+            assert np.array_equal(yh.numpy().view(np.uint32), ref.view(np.uint32)), (spec.name, T, pin)
+        assert layer.device_error() == 0
+
+
 def test_prefill_forward_host(ora, prefill_always):
     import torch
     spec, T = synth.MICRO, 70
