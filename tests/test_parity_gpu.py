@@ -225,11 +225,14 @@ def test_nonfinite_input_sets_flag(ora):
     assert layer.device_error() & 2
 
 
-def test_rmsnorm_bit_exact(ora):
+@pytest.mark.parametrize("H", [4096, 416, 256, 16384])
+def test_rmsnorm_bit_exact(ora, H):
+    """Widths with segments of 128, 13 (a tail of the unrolled chain) and 8
+    words staged in shared memory, and a row too wide to stage."""
     import torch
     import deepseek_v4_flash_gb300 as ds4
-    rng = np.random.default_rng(37)
-    x = (rng.standard_normal((33, 4096)) * rng.uniform(0.01, 100, (33, 1))).astype(np.float32)
+    rng = np.random.default_rng(37 + H)
+    x = (rng.standard_normal((33, H)) * rng.uniform(0.01, 100, (33, 1))).astype(np.float32)
     ref = ora.rmsnorm(x, 1e-6)
     xd = torch.from_numpy(x).cuda()
     out = torch.empty_like(xd)
