@@ -349,6 +349,13 @@ static ds4moe_status forward_run(ds4moe_layer *h, const float *x, int32_t n_tok,
     mark(6);
     h->launches += 3;
   }
+  // A call stopped between its router and its down kernel leaves the count
+  // of quantised x that down clears; clear it here so that no later call
+  // starts on it.
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaMemsetAsync(h->xq_ready, 0, sizeof(int32_t), s);
+  }
   return cuda_status(e);
 }
 
