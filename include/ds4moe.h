@@ -48,7 +48,7 @@ extern "C" {
 typedef enum {
   DS4MOE_OK = 0,
   DS4MOE_ERR_INVALID_ARG = 1, /* bad pointer, shape, format or token count */
-  DS4MOE_ERR_UNSUPPORTED = 2, /* valid request this build does not handle  */
+  DS4MOE_ERR_UNSUPPORTED = 2, /* valid request the library does not handle */
   DS4MOE_ERR_OOM = 3,         /* device allocation failed                  */
   DS4MOE_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed      */
   DS4MOE_ERR_DEVICE = 5       /* the device error flag was set             */
