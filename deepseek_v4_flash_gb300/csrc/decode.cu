@@ -41,6 +41,7 @@ constexpr int RC_MAX_E = 1024;
 struct RouteDecArgs {
   const float *x;
   int T, H, E, E_pad, k, NS, n_shared, learned, q8, vocab, A_cap;
+  int tg;               // tokens per cluster (1, or ROUTER_SEGS: block r routes token r)
   float scale;
   const uint8_t *W;     // router (RQ8 or F32 [E][H])
   const float *bias;
@@ -61,9 +62,11 @@ struct RouteDecArgs {
 // xq_s [per*32] int8, then the 128-aligned work area (router tiles;
 // afterwards the routing and bucketing scratch).
 __host__ __device__ constexpr int rc_dx_off(int E_pad) { return RC_HDR + 4 * ROUTER_SEGS * E_pad; }
-__host__ __device__ constexpr int rc_xq_off(int E_pad, int per) { return rc_dx_off(E_pad) + ((4 * per + 15) & ~15); }
-__host__ __device__ constexpr int rc_work_off(int E_pad, int per) {
-  return (rc_xq_off(E_pad, per) + 32 * per + 127) & ~127;
+__host__ __device__ constexpr int rc_xq_off(int E_pad, int per, int tg) {
+  return rc_dx_off(E_pad) + ((4 * per * tg + 15) & ~15);
+}
+__host__ __device__ constexpr int rc_work_off(int E_pad, int per, int tg) {
+  return (rc_xq_off(E_pad, per, tg) + 32 * per * tg + 127) & ~127;
 }
 
 // CAS step 1 for one value per lane of block b of token t, already loaded.
@@ -114,7 +117,7 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
     k_router_dec(RouteDecArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = blockIdx.x, t = blockIdx.y;
+  const int seg = blockIdx.x, tg = a.tg, t0 = blockIdx.y * tg, ntg = min(tg, a.T - t0);
   const int nb = a.H >> 5, per = nb / ROUTER_SEGS, b0 = seg * per;
   const int c0 = b0 >> 1, c1 = (b0 + per + 1) >> 1;  // RQ8 2-block chunks covering the segment
   const int seg_bytes = a.q8 ? (c1 - c0) * RQ8_TILE : 0;
@@ -122,9 +125,9 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   int *s_flag = (int *)smem;
   uint64_t *bars = (uint64_t *)(smem + 64);
   float *lgp = (float *)(smem + RC_HDR);
-  float *dx_s = (float *)(smem + rc_dx_off(a.E_pad));
-  int8_t *xq_s = (int8_t *)(smem + rc_xq_off(a.E_pad, per));
-  uint8_t *work = smem + rc_work_off(a.E_pad, per);
+  float *dx_s = (float *)(smem + rc_dx_off(a.E_pad));                  // [tg][per]
+  int8_t *xq_s = (int8_t *)(smem + rc_xq_off(a.E_pad, per, tg));       // [tg][per * 32]
+  uint8_t *work = smem + rc_work_off(a.E_pad, per, tg);
   const uint32_t bar = smem_u32(&bars[warp]);
   const uint32_t wbuf = smem_u32(work + warp * seg_bytes);
   const size_t rg_stride = (size_t)(a.H / RQ8_KSTEP) * RQ8_TILE;
@@ -136,12 +139,12 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
       bulk_g2s(wbuf, a.W + (size_t)warp * rg_stride + (size_t)c0 * RQ8_TILE, seg_bytes, bar);
     }
   }
-  // the routing block's bias values, requested early
+  // the routing blocks' bias values, requested early
   float bias_r[RC_MAX_E / (RC_WARPS * 32)];
 #pragma unroll
   for (int i = 0; i < RC_MAX_E / (RC_WARPS * 32); i++) {
     const int e = threadIdx.x + i * RC_WARPS * 32;
-    bias_r[i] = (seg == 0 && a.learned && e < a.E) ? __ldg(a.bias + e) : 0.0f;
+    bias_r[i] = (seg < ntg && a.learned && e < a.E) ? __ldg(a.bias + e) : 0.0f;
   }
   // The router tiles and the bias above are constant: they are requested
   // before the previous kernel of the stream is done. Everything after reads
@@ -150,22 +153,23 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   // the gate/up kernel may launch now: it requests the shared expert's
   // weights while this kernel routes
   pdl_launch_dependents();
-  // quantise the segment's blocks (warp w: blocks b0 + w + RC_WARPS*j), all
-  // loads first
+  // quantise the segment's blocks of the cluster's tokens (warp w: pairs
+  // (token, block) w, w + RC_WARPS, ...), all loads of a round first
   if (a.x) {
     constexpr int QB = 4;
-    for (int bb = warp; bb < per; bb += RC_WARPS * QB) {
+    const int np = ntg * per;
+    for (int pp = warp; pp < np; pp += RC_WARPS * QB) {
       float v[QB];
 #pragma unroll
       for (int j = 0; j < QB; j++) {
-        const int b = bb + j * RC_WARPS;
-        v[j] = b < per ? __ldg(a.x + (size_t)t * a.H + 32 * (b0 + b) + lane) : 0.0f;
+        const int p = pp + j * RC_WARPS, i = p / per, b = p - i * per;
+        v[j] = p < np ? __ldg(a.x + (size_t)(t0 + i) * a.H + 32 * (b0 + b) + lane) : 0.0f;
       }
 #pragma unroll
       for (int j = 0; j < QB; j++) {
-        const int b = bb + j * RC_WARPS;
-        if (b < per)
-          quant_value(v[j], a.H, t, b0 + b, lane, xq_s + 32 * b, dx_s + b, a.xq, a.dx, a.gs, a.err);
+        const int p = pp + j * RC_WARPS, i = p / per, b = p - i * per;
+        if (p < np)
+          quant_value(v[j], a.H, t0 + i, b0 + b, lane, xq_s + 32 * p, dx_s + p, a.xq, a.dx, a.gs, a.err);
       }
     }
   }
@@ -176,9 +180,10 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
     __threadfence();
     red_release_gpu_add(a.xq_ready, 1);
   }
-  // segment sums of router rows 32*rg + lane
+  // segment sums of router rows 32*rg + lane, for each of the cluster's
+  // tokens (the row group's tiles once), into the table of the block that
+  // routes the token
   for (int rg = warp, round = 0; rg < nrg; rg += RC_WARPS, round++) {
-    float acc = 0.0f;
     const int r = 32 * rg + lane;
     if (a.q8) {
       if (round > 0 && lane == 0) {
@@ -191,28 +196,38 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
         if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
         break;
       }
-      for (int b = b0; b < b0 + per; b++) {
-        const uint32_t tile = wbuf + ((b >> 1) - c0) * RQ8_TILE;
-        const uint32_t dd = ld_shared_u32(tile + 4 * lane);
-        const float d = half_bits_to_float((b & 1) ? dd >> 16 : dd);
-        const uint4 w0 = ld_shared_v4(tile + RQ8_Q + 512 * (2 * (b & 1)) + 16 * lane);
-        const uint4 w1 = ld_shared_v4(tile + RQ8_Q + 512 * (2 * (b & 1) + 1) + 16 * lane);
-        const uint4 *xv = (const uint4 *)(xq_s + (b - b0) * 32);
-        const int I = dot16(w1, xv[1], dot16(w0, xv[0], 0));
-        acc = __fadd_rn(acc, q8_term(d, dx_s[b - b0], I));
+      for (int i = 0; i < ntg; i++) {
+        float acc = 0.0f;
+        for (int b = b0; b < b0 + per; b++) {
+          const uint32_t tile = wbuf + ((b >> 1) - c0) * RQ8_TILE;
+          const uint32_t dd = ld_shared_u32(tile + 4 * lane);
+          const float d = half_bits_to_float((b & 1) ? dd >> 16 : dd);
+          const uint4 w0 = ld_shared_v4(tile + RQ8_Q + 512 * (2 * (b & 1)) + 16 * lane);
+          const uint4 w1 = ld_shared_v4(tile + RQ8_Q + 512 * (2 * (b & 1) + 1) + 16 * lane);
+          const uint4 *xv = (const uint4 *)(xq_s + (i * per + b - b0) * 32);
+          const int I = dot16(w1, xv[1], dot16(w0, xv[0], 0));
+          acc = __fadd_rn(acc, q8_term(d, dx_s[i * per + b - b0], I));
+        }
+        st_cluster_f32(lgp + seg * a.E_pad + r, i, acc);
       }
-    } else if (r < a.E) {  // fp32 router rows: fma chain over the segment (x unquantised)
-      const int j0 = seg * (a.H / ROUTER_SEGS), j1 = j0 + a.H / ROUTER_SEGS;
-      const float *wr = (const float *)a.W + (size_t)r * a.H;
-      const float *xv = a.x + (size_t)t * a.H;
-      for (int j = j0; j < j1; j++) acc = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), acc);
+    } else {
+      for (int i = 0; i < ntg; i++) {
+        float acc = 0.0f;
+        if (r < a.E) {  // fp32 router rows: fma chain over the segment (x unquantised)
+          const int j0 = seg * (a.H / ROUTER_SEGS), j1 = j0 + a.H / ROUTER_SEGS;
+          const float *wr = (const float *)a.W + (size_t)r * a.H;
+          const float *xv = a.x + (size_t)(t0 + i) * a.H;
+          for (int j = j0; j < j1; j++) acc = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), acc);
+        }
+        st_cluster_f32(lgp + seg * a.E_pad + r, i, acc);
+      }
     }
-    st_cluster_f32(lgp + seg * a.E_pad + r, 0, acc);  // into block 0's table
     __syncwarp();  // every lane is done with the tiles before the next copy
   }
-  cluster_sync_all();  // block 0 has every segment's sums
-  if (seg != 0) return;
-  // ---- routing of token t by block 0 of its cluster
+  cluster_sync_all();  // block i has every segment's sums of token i
+  if (seg >= ntg) return;
+  const int t = t0 + seg;
+  // ---- routing of token t by block seg of its cluster
   const RouteScratch rs = route_scratch(work, a.E_pad, a.k);
   int32_t *hash_ids = (int32_t *)(work + route_block_smem(a.E_pad, a.k));  // hash routing: this token's ids
   {
@@ -281,7 +296,7 @@ static size_t router_dec_smem(const ds4moe_layer *h) {
   const size_t route = route_block_smem(h->E_pad, d.top_k) + 64 +
                        (size_t)(((n + 3) & ~3) + bucket_rank_smem_ints(n)) * 4;
   if (route > work) work = route;
-  return rc_work_off(h->E_pad, per) + work;
+  return rc_work_off(h->E_pad, per, ROUTER_SEGS) + work;
 }
 
 size_t route_dec_smem(const ds4moe_layer *h) {
@@ -304,7 +319,11 @@ cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_
   r.bucket = bucket ? h->bucket : nullptr;
   r.xq_ready = bucket && x ? h->xq_ready : nullptr;
   void *args[] = {&r};
-  return launch_pdl((const void *)k_router_dec, dim3(ROUTER_SEGS, T), dim3(RC_WARPS * 32), router_dec_smem(h), s,
+  // without bucketing (prefill, ds4moe_route) and from 16 tokens on, a
+  // cluster takes 8 tokens: its router tiles are read once for all of them
+  r.tg = (!bucket && T >= 2 * ROUTER_SEGS) ? ROUTER_SEGS : 1;
+  return launch_pdl((const void *)k_router_dec, dim3(ROUTER_SEGS, (T + r.tg - 1) / r.tg), dim3(RC_WARPS * 32),
+                    router_dec_smem(h), s,
                     args, true);
 }
 
