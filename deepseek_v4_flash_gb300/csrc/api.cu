@@ -424,6 +424,16 @@ static cudaError_t host_sequence(ds4moe_layer *h, int n_tok, bool hash, cudaStre
   return forward_run(h, xm, n_tok, hash ? tm : nullptr, ym, s) == DS4MOE_OK ? cudaSuccess : cudaErrorUnknown;
 }
 
+// The device address of pinned (page-locked, mapped) host memory, else null.
+static void *mapped_ptr(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 static cudaGraphExec_t host_graph(ds4moe_layer *h, int n_tok, bool hash) {
   if (h->host_graph[n_tok]) return h->host_graph[n_tok];
   if (h->host_graph_off) return nullptr;
@@ -472,8 +482,19 @@ ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t 
   }
   cudaStream_t s = (cudaStream_t)stream;
   const size_t nb = (size_t)n_tok * h->d.hidden * 4;
-  // Decode-sized calls: the inputs into the handle's mapped pinned buffers,
-  // one graph replay of the forward on them, the result back.
+  // Decode-sized calls on pinned caller buffers: the kernels read x (and the
+  // token ids) and update y in them directly.
+  if (n_tok <= h->Tc && !h->prof_on) {
+    float *xm = (float *)mapped_ptr(x_host), *ym = (float *)mapped_ptr(y_host);
+    int32_t *tm = hash ? (int32_t *)mapped_ptr(token_ids_host) : nullptr;
+    if (xm && ym && xm != ym && (!hash || tm)) {
+      st = forward_run(h, xm, n_tok, tm, ym, s);
+      if (st != DS4MOE_OK) return st;
+      return cuda_status(cudaStreamSynchronize(s));
+    }
+  }
+  // Other decode-sized calls: the inputs into the handle's mapped pinned
+  // buffers, one graph replay of the forward on them, the result back.
   if (n_tok <= h->Tc && !h->prof_on) {
     const size_t pb = (size_t)h->Tc * h->d.hidden * 4;
     if (!h->x_pin && (cudaHostAlloc(&h->x_pin, pb, cudaHostAllocMapped) != cudaSuccess ||
