@@ -182,12 +182,13 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
 
 /* ds4moe_forward on HOST buffers (pinned or pageable): y_host += MoE(x_host),
  * synchronising `stream` before it returns. Decode-sized calls (n_tok up to
- * min(max_tokens, 64)) copy x, token_ids and y into mapped pinned buffers
- * owned by the handle, which the kernels read and update in place over the
- * CPU-GPU link, and replay one CUDA graph per token count (captured on the
- * first call of that count; the handle keeps it until ds4moe_destroy).
- * Larger calls copy to device buffers, run the layer and copy y back. Not
- * reentrant on one handle. Same arguments otherwise. */
+ * min(max_tokens, 64)) on pinned buffers: the kernels read x and token_ids
+ * and update y in them directly over the CPU-GPU link. Decode-sized calls on
+ * pageable buffers copy them into mapped pinned buffers owned by the handle
+ * and replay one CUDA graph per token count (captured on the first call of
+ * that count; kept until ds4moe_destroy). Larger calls copy to device
+ * buffers, run the layer and copy y back. Not reentrant on one handle. Same
+ * arguments otherwise. */
 ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t n_tok,
                                   const int32_t *token_ids_host, float *y_host, void *stream);
 
