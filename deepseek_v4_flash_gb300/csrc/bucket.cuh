@@ -81,9 +81,16 @@ __device__ inline void bucket_rank(const int32_t *ids, int T, int E, int k, int 
 // The same table for a single token, by one warp (lane j < k: slot j); every
 // lane of the warp calls it. ids: the token's k routed ids (-1 = none; >= E
 // raises DS4MOE_DEVERR_INTERNAL and is dropped).
+__device__ inline void bucket_one_token_ids(int e, int E, int k, int n_shared, int32_t *out, int A_cap,
+                                            uint32_t *err, int lane);
 __device__ inline void bucket_one_token(const int32_t *ids, int E, int k, int n_shared, int32_t *out, int A_cap,
                                         uint32_t *err, int lane) {
-  const int e = lane < k ? ids[lane] : -1;
+  bucket_one_token_ids(lane < k ? ids[lane] : -1, E, k, n_shared, out, A_cap, err, lane);
+}
+// The same with lane j < k holding slot j's id e (others: -1); `out` may be
+// shared memory.
+__device__ inline void bucket_one_token_ids(int e, int E, int k, int n_shared, int32_t *out, int A_cap,
+                                            uint32_t *err, int lane) {
   const bool ok = e >= 0 && e < E;
   if (lane < k && e >= E) raise_flag(err, DS4MOE_DEVERR_INTERNAL);
   const unsigned valid = __ballot_sync(0xffffffffu, ok);

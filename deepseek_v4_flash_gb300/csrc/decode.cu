@@ -257,9 +257,11 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   // ---- bucketing of the call by the block that routed its last token (a
   // single token: from this block's own selection, still in shared memory)
   int32_t *scr = hash_ids + 16;
-  if (a.T == 1) {
-    __syncthreads();
-    if (warp == 0) bucket_one_token(a.learned ? rs.sel : hash_ids, a.E, a.k, a.n_shared, a.bucket, a.A_cap, a.err, lane);
+  if (a.T == 1) {  // the expert kernels build a single token's table from its ids
+    if (threadIdx.x < a.k) {
+      const int e = a.learned ? rs.sel[threadIdx.x] : hash_ids[threadIdx.x];
+      if (e >= a.E) raise_flag(a.err, DS4MOE_DEVERR_INTERNAL);
+    }
     return;
   }
   if (!block_ticket_last(a.rticket, a.T, s_flag)) return;

@@ -296,6 +296,10 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
     if (lane == 0) mine = atomicCAS(s_claim, 0, 1) == 0;
     if (__shfl_sync(0xffffffffu, mine, 0)) {  // this warp loads the bucket for the block
       pdl_wait();
+      if (a.T == 1) {  // a single token: the table from its routed ids
+        const int e = lane < a.k ? __ldcg(a.ids + lane) : -1;
+        bucket_one_token_ids(e, a.E, a.k, a.n_shared, bks, a.A_cap, nullptr, lane);
+      } else
       // (loads of a round issued before its stores)
       for (int i0 = 0; i0 < nbk; i0 += 4 * 32) {
         int v[4];
