@@ -214,6 +214,32 @@ def test_bad_token_id_single_token(ora):
     assert layer.device_error() == 0
 
 
+@pytest.mark.parametrize("T", [1, 5, 130])
+def test_hash_rows_with_repeated_experts(ora, T):
+    """Hash-table rows that name one expert twice or thrice: the expert's
+    group holds several slots of the same token (single-token and batched
+    decode bucketing, and the prefill path at 130 tokens), bit-exact against
+    the oracle."""
+    import torch
+    spec, seed = synth.MICRO_HASH, 51
+    w = synth.gen_layer(spec, seed, 0)
+    tok = synth.gen_token_ids(spec, seed, T)
+    rows = [[3, 3, 5], [6, 6, 6], [1, 2, 1], [7, 0, 7], [4, 4, 2]]
+    for i, t in enumerate(tok):
+        w["hash_table"][t] = rows[i % len(rows)]
+    ol = ora.layer(spec, w)
+    layer = make_layer(spec, w, max(65, T))
+    x = synth.gen_x(spec, seed, T)
+    y0 = np.random.default_rng(seed).standard_normal(x.shape).astype(np.float32)
+    ref, ids_ref, _, bad = ol.forward(x, y0, tok)
+    assert bad == 0
+    yd = torch.from_numpy(y0).cuda()
+    layer.forward(torch.from_numpy(x).cuda(), yd, torch.from_numpy(tok).cuda())
+    assert layer.device_error() == 0
+    assert np.array_equal(yd.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    layer.close()
+
+
 def test_nonfinite_input_sets_flag(ora):
     import torch
     spec = synth.MICRO
