@@ -78,6 +78,8 @@ def lib():
             "ds4moe_profile_read": (i32, [vp, ctypes.POINTER(ctypes.c_double), i32,
                                           ctypes.POINTER(ctypes.c_int64)]),
             "ds4moe_launch_count": (ctypes.c_uint64, [vp]),
+            "ds4moe_debug_set_wait_limit": (i32, [vp, ctypes.c_int64]),
+            "ds4moe_debug_fail_alloc": (i32, [i32]),
             "ds4moe_status_string": (ctypes.c_char_p, [i32]),
             "ds4moe_abi_version": (u32, []),
         }
@@ -212,6 +214,11 @@ class Layer:
                                   _stream(stream)), "ds4moe_route")
         return ids_out, w_out
 
+    def set_wait_limit(self, cycles: int):
+        """Bound of the decode expert kernels' hand-off waits, in SM cycles
+        (0: the default); a test hook (ds4moe_debug_set_wait_limit)."""
+        _check(lib().ds4moe_debug_set_wait_limit(self._h, int(cycles)), "ds4moe_debug_set_wait_limit")
+
     def device_error(self, stream=None) -> int:
         """Synchronise, read and clear the device error flags (0 = none)."""
         f = ctypes.c_uint32(0)
@@ -260,6 +267,12 @@ def route_noalloc(desc: LayerDesc, weights: dict, x=None, token_ids=None, ids_ou
                                       _ptr(ids_out), _ptr(w_out), _ptr(err_flags), _stream(stream)),
            "ds4moe_route_noalloc")
     return ids_out, w_out
+
+
+def fail_alloc(n: int):
+    """Make the n-th device allocation the library makes from now on fail as
+    if out of memory (0: off); a test hook (ds4moe_debug_fail_alloc)."""
+    _check(lib().ds4moe_debug_fail_alloc(int(n)), "ds4moe_debug_fail_alloc")
 
 
 def status_string(status: int) -> str:

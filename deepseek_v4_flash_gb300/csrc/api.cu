@@ -7,6 +7,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <new>
 
 #include "bucket.cuh"
@@ -60,6 +61,11 @@ ds4moe_status validate_desc(const ds4moe_layer_desc *d) {
   return DS4MOE_OK;
 }
 
+// Allocation-failure injection for tests: the n-th device allocation made by
+// ds4moe_create after ds4moe_debug_fail_alloc(n) fails as if the device were
+// out of memory (0: off). One process-wide countdown.
+std::atomic<int> g_fail_alloc{0};
+
 void free_all(ds4moe_layer *h) {
   for (int i = 0; i < h->n_allocs; i++) cudaFree(h->allocs[i]);
   h->n_allocs = 0;
@@ -71,6 +77,10 @@ ds4moe_status alloc(ds4moe_layer *h, T **p, size_t bytes) {
   if (bytes == 0) return DS4MOE_OK;
   if (h->n_allocs >= (int)(sizeof(h->allocs) / sizeof(h->allocs[0]))) return DS4MOE_ERR_OOM;
   void *q = nullptr;
+  int n = g_fail_alloc.load();
+  while (n > 0 && !g_fail_alloc.compare_exchange_weak(n, n - 1)) {
+  }
+  if (n == 1) return DS4MOE_ERR_OOM;  // the injected failure
   if (cudaMalloc(&q, bytes) != cudaSuccess) {
     cudaGetLastError();
     return DS4MOE_ERR_OOM;
@@ -474,11 +484,12 @@ ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t 
   if (!x_host || !y_host) return DS4MOE_ERR_INVALID_ARG;
   const bool hash = h->d.route == DS4MOE_ROUTE_HASH;
   if (hash && !token_ids_host) return DS4MOE_ERR_INVALID_ARG;
-  const size_t xb = (size_t)h->d.max_tokens * h->d.hidden * 4;
+  // device staging of one chunk (Ts tokens) for the copy path, on first use
+  const size_t xb = (size_t)h->Ts * h->d.hidden * 4;
   if (!h->x_dev) {
     if ((st = alloc(h, &h->x_dev, xb)) != DS4MOE_OK) return st;
     if ((st = alloc(h, &h->y_dev, xb)) != DS4MOE_OK) return st;
-    if ((st = alloc(h, &h->tok_dev, (size_t)h->d.max_tokens * 4)) != DS4MOE_OK) return st;
+    if ((st = alloc(h, &h->tok_dev, (size_t)h->Ts * 4)) != DS4MOE_OK) return st;
   }
   cudaStream_t s = (cudaStream_t)stream;
   const size_t nb = (size_t)n_tok * h->d.hidden * 4;
@@ -516,14 +527,20 @@ ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t 
       return DS4MOE_OK;
     }
   }
-  cudaError_t e = cudaMemcpyAsync(h->x_dev, x_host, nb, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(h->y_dev, y_host, nb, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && hash)
-    e = cudaMemcpyAsync(h->tok_dev, token_ids_host, (size_t)n_tok * 4, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_status(e);
-  st = ds4moe_forward(h, h->x_dev, n_tok, hash ? h->tok_dev : nullptr, h->y_dev, stream);
-  if (st != DS4MOE_OK) return st;
-  e = cudaMemcpyAsync(y_host, h->y_dev, nb, cudaMemcpyDeviceToHost, s);
+  // Anything else: chunk by chunk through the device staging buffers.
+  cudaError_t e = cudaSuccess;
+  for (int c0 = 0; c0 < n_tok && e == cudaSuccess; c0 += h->Ts) {
+    const int nc = n_tok - c0 < h->Ts ? n_tok - c0 : h->Ts;
+    const size_t cb = (size_t)nc * h->d.hidden * 4, off = (size_t)c0 * h->d.hidden;
+    e = cudaMemcpyAsync(h->x_dev, x_host + off, cb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->y_dev, y_host + off, cb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && hash)
+      e = cudaMemcpyAsync(h->tok_dev, token_ids_host + c0, (size_t)nc * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) break;
+    st = ds4moe_forward(h, h->x_dev, nc, hash ? h->tok_dev : nullptr, h->y_dev, stream);
+    if (st != DS4MOE_OK) return st;
+    e = cudaMemcpyAsync(y_host + off, h->y_dev, cb, cudaMemcpyDeviceToHost, s);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return cuda_status(e);
 }
@@ -542,9 +559,32 @@ ds4moe_status ds4moe_get_device_error(ds4moe_layer *h, void *stream, uint32_t *f
   cudaError_t e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemcpy(&f, h->err, 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4);
+  // A block that gave up a wait left without its arrivals on the self-
+  // resetting completion counters; zero them so that the next call starts
+  // from a clean state.
+  if (e == cudaSuccess && (f & DS4MOE_DEVERR_TIMEOUT)) {
+    const long long Tc = h->Tc, NS = h->NS;
+    e = cudaMemset(h->hticket, 0, (size_t)(Tc * NS) * (h->d.ffn / 32) * 4);
+    if (e == cudaSuccess) e = cudaMemset(h->cticket, 0, (size_t)Tc * (h->d.hidden / 32) * 4);
+    if (e == cudaSuccess) e = cudaMemset(h->rticket, 0, 16);
+    if (e == cudaSuccess) e = cudaMemset(h->xq_ready, 0, 16);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  }
   if (e != cudaSuccess) return cuda_status(e);
   if (flags_out) *flags_out = f;
   return f ? DS4MOE_ERR_DEVICE : DS4MOE_OK;
+}
+
+ds4moe_status ds4moe_debug_set_wait_limit(ds4moe_layer *h, int64_t cycles) {
+  if (!h || cycles < 0) return DS4MOE_ERR_INVALID_ARG;
+  h->wait_limit = cycles;
+  return DS4MOE_OK;
+}
+
+ds4moe_status ds4moe_debug_fail_alloc(int32_t n) {
+  if (n < 0) return DS4MOE_ERR_INVALID_ARG;
+  g_fail_alloc.store(n);
+  return DS4MOE_OK;
 }
 
 // Read-only views of the handle's scratch, for inspecting the intermediate

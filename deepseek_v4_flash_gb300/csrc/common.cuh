@@ -220,14 +220,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^31 SM cycles (about a second) and returns
-// false; callers then raise DS4MOE_DEVERR_TIMEOUT and leave. No sleep
-// between tests: these waits sit on the decode path's latency chain.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// The bound of every on-chip wait: ~2^31 SM cycles (about a second).
+constexpr long long WAIT_LIMIT = 1ll << 31;
+
+// Bounded wait: gives up after `limit` SM cycles and returns false; callers
+// then raise DS4MOE_DEVERR_TIMEOUT and leave. No sleep between tests: these
+// waits sit on the decode path's latency chain.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit = WAIT_LIMIT) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > (1ll << 31)) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }
@@ -249,11 +252,11 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-// Waits until *p >= target; false after ~2^31 cycles.
-__device__ __forceinline__ bool wait_count(const int32_t *p, int target) {
+// Waits until *p >= target; false after `limit` cycles.
+__device__ __forceinline__ bool wait_count(const int32_t *p, int target, long long limit = WAIT_LIMIT) {
   const long long t0 = clock64();
   while (ld_acquire_gpu(p) < target) {
-    if (clock64() - t0 > (1ll << 31)) return false;
+    if (clock64() - t0 > limit) return false;
     __nanosleep(32);
   }
   return true;

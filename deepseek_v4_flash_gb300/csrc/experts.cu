@@ -70,6 +70,10 @@ struct XArgs {
   int32_t *cticket;              // [T][H/32]
   float *y;
   uint32_t *err;
+  // bound of the hand-off waits (between the block's warps, and on the
+  // router's count of quantised x); waits on the block's own copies keep
+  // WAIT_LIMIT, so a block that gives up never leaves a copy in flight
+  long long hlimit;
 };
 
 // Partial-sum slots between the compute and the epilogue warps (down at
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
     }
     const long long t0 = clock64();
     for (poll_items(); n_items < 0; poll_items()) {
-      if (clock64() - t0 > (1ll << 31)) return false;
+      if (clock64() - t0 > a.hlimit) return false;
       __nanosleep(64);
     }
     return true;
@@ -386,7 +390,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
     // gate/up block waits for it before its routed items), is complete.
     constexpr bool EARLY = !DOWN && AS;
     if (EARLY) {
-      if (threadIdx.x == 0 && !wait_count(a.xq_ready, a.xq_parts)) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
+      if (threadIdx.x == 0 && !wait_count(a.xq_ready, a.xq_parts, a.hlimit)) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
       __syncthreads();
     } else {
       pdl_wait();
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
       if (c_nst == 0 || cstage == c_nst - 1) {
         // the unit's segment is done: partial sums into slot unit % PS
         const int ps = unit % PS, ph = unit / PS;
-        if (ph > 0 && !mbar_wait_bounded(empty0 + 8 * ps, (ph - 1) & 1)) {
+        if (ph > 0 && !mbar_wait_bounded(empty0 + 8 * ps, (ph - 1) & 1, a.hlimit)) {
           failed = true;
           break;
         }
@@ -539,7 +543,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
     for (int p = 0; p < npass; p++, unit++) {
       if ((unit % PS) % XE != ew) continue;
       const int ps = unit % PS;
-      if (!mbar_wait_bounded(full0 + 8 * ps, (unit / PS) & 1)) {
+      if (!mbar_wait_bounded(full0 + 8 * ps, (unit / PS) & 1, a.hlimit)) {
         if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
         return;
       }
@@ -676,6 +680,7 @@ cudaError_t launch_experts(const ds4moe_layer *h, int T, float *y, int down, cud
   a.hq = h->hq, a.dh = h->dh, a.gsh = h->gsh, a.hbuf = h->hbuf, a.hticket = h->hticket;
   a.apart = h->apart, a.cticket = h->cticket, a.y = y, a.err = h->err;
   a.maxj = x_maxj(h, T, down != 0);
+  a.hlimit = h->wait_limit > 0 ? h->wait_limit : WAIT_LIMIT;
   if (!down) {
     a.K = d.hidden, a.rows = d.ffn, a.w_r = h->gu, a.w_s = h->sgu, a.aq = h->xq, a.ad = h->dx, a.ag = h->gs;
   } else {

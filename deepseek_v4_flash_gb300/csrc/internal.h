@@ -70,6 +70,8 @@ struct ds4moe_layer {
   int64_t prof_calls;
   uint64_t launches;
 
+  long long wait_limit;  // hand-off wait bound of the decode expert kernels (0: WAIT_LIMIT)
+
   uint64_t bytes;        // total device bytes owned
   void *allocs[32];
   int n_allocs;

@@ -8,7 +8,7 @@
 //   k_na_router_part : int8 quantisation of each token's 32-blocks in one K
 //                      segment (in shared memory) and that segment's sum of
 //                      every router row, read from the canonical Q8_0 (or
-//                      F32) rows, written to the array;
+//                      F32) rows with coalesced loads, written to the array;
 //   k_na_route       : one block per token: logits, sigmoid, bias top-k and
 //                      renormalisation from the segment sums (route.cuh);
 //                      hash routing instead looks the table up.
@@ -28,7 +28,7 @@ static __device__ __align__(256) uint8_t na_scratch[DS4MOE_NOALLOC_SCRATCH_BYTES
 namespace {
 
 constexpr int NA_RT = 8;      // tokens per token tile of k_na_router_part
-constexpr int NA_WARPS = 4;   // router row groups of 32 per block
+constexpr int NA_WARPS = 4;   // warps per block of k_na_router_part (32 router rows)
 constexpr int NA_MAX_DEVICES = 64;
 constexpr int NA_ROUTE_THREADS = 256;
 
@@ -46,9 +46,14 @@ struct NaArgs {
   uint32_t *err;           // may be null
 };
 
-// grid (ceil(E_pad/32 / NA_WARPS), ROUTER_SEGS, ceil(T / NA_RT)); warp w of
-// block x handles router rows 32*(x*NA_WARPS + w) + lane over K segment y for
-// the tokens of tile z.
+// grid (ceil(E_pad/32), ROUTER_SEGS, ceil(T / NA_RT)); block x handles
+// router rows 32x .. 32x+31 over K segment y for the tokens of tile z, warp w
+// the rows 32x + w, 32x + w + NA_WARPS, ... one at a time.
+//
+// A row's segment is `per` contiguous canonical Q8_0 blocks (34 bytes each,
+// 2-byte aligned): the warp reads it with consecutive 16-bit loads into its
+// shared-memory buffer (coalesced), then lane j computes the term of block j
+// and the terms are added in block order (CAS step 4) by shuffles.
 __global__ void __launch_bounds__(NA_WARPS * 32) k_na_router_part(NaArgs a) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -56,6 +61,7 @@ __global__ void __launch_bounds__(NA_WARPS * 32) k_na_router_part(NaArgs a) {
   const int nb = a.H >> 5, per = nb / ROUTER_SEGS, b0 = seg * per;
   int8_t *xq_s = (int8_t *)sm;                         // [NA_RT][per * 32]
   float *dx_s = (float *)(sm + NA_RT * per * 32);      // [NA_RT][per]
+  uint16_t *row_s = (uint16_t *)(sm + NA_RT * per * 36) + warp * (per * 17);  // this warp's row segment
   // CAS step 1 on the segment's blocks (lane = element); the F32 router uses
   // x unquantised and only needs the finiteness check
   for (int p = warp; p < nt * per; p += NA_WARPS) {
@@ -70,45 +76,44 @@ __global__ void __launch_bounds__(NA_WARPS * 32) k_na_router_part(NaArgs a) {
     }
   }
   __syncthreads();
-  const int r = (blockIdx.x * NA_WARPS + warp) * 32 + lane;
-  if (r >= a.E) return;
-  float acc[NA_RT];
+  for (int rr = warp; rr < 32; rr += NA_WARPS) {
+    const int r = blockIdx.x * 32 + rr;
+    if (r >= a.E) break;  // warp-uniform
+    if (a.q8) {
+      const uint16_t *src = (const uint16_t *)(a.W + ((size_t)r * nb + b0) * 34);
+      for (int j = lane; j < per * 17; j += 32) row_s[j] = __ldg(src + j);
+      __syncwarp();
+      for (int i = 0; i < nt; i++) {
+        float s = 0.0f;
+        for (int c0 = 0; c0 < per; c0 += 32) {  // 32 blocks per round, lane = block
+          const int bb = c0 + lane;
+          float p = 0.0f;
+          if (bb < per) {
+            const uint16_t *blk = row_s + 17 * bb;
+            const int *xv = (const int *)(xq_s + i * per * 32 + bb * 32);
+            int I = 0;
 #pragma unroll
-  for (int i = 0; i < NA_RT; i++) acc[i] = 0.0f;
-  if (a.q8) {
-    // row r, blocks b0 .. b0+per-1: 34 bytes each (fp16 d, int8 q[32]),
-    // 2-byte aligned
-    const uint16_t *row = (const uint16_t *)(a.W + ((size_t)r * nb + b0) * 34);
-    for (int bb = 0; bb < per; bb++) {
-      const uint16_t *blk = row + 17 * bb;
-      const float d = half_bits_to_float(__ldg(blk));
-      uint32_t q[8];
-#pragma unroll
-      for (int m = 0; m < 8; m++) q[m] = (uint32_t)__ldg(blk + 1 + 2 * m) | ((uint32_t)__ldg(blk + 2 + 2 * m) << 16);
-#pragma unroll
-      for (int i = 0; i < NA_RT; i++) {
-        if (i < nt) {
-          const int *xv = (const int *)(xq_s + i * per * 32 + bb * 32);
-          int I = 0;
-#pragma unroll
-          for (int m = 0; m < 8; m++) I = __dp4a((int)q[m], xv[m], I);
-          acc[i] = __fadd_rn(acc[i], q8_term(d, dx_s[i * per + bb], I));
+            for (int m = 0; m < 8; m++)
+              I = __dp4a((int)((uint32_t)blk[1 + 2 * m] | ((uint32_t)blk[2 + 2 * m] << 16)), xv[m], I);
+            p = q8_term(half_bits_to_float(blk[0]), dx_s[i * per + bb], I);
+          }
+          const int nr = min(32, per - c0);
+          for (int j = 0; j < nr; j++) s = __fadd_rn(s, __shfl_sync(0xffffffffu, p, j));
         }
+        if (lane == 0) a.part[((size_t)(t0 + i) * ROUTER_SEGS + seg) * a.E_pad + r] = s;
+      }
+      __syncwarp();  // the buffer is read before the next row overwrites it
+    } else {  // fp32 rows: lane i runs token i's fma chain over the segment
+      const int j0 = seg * (a.H / ROUTER_SEGS), j1 = j0 + a.H / ROUTER_SEGS;
+      const float *wr = (const float *)a.W + (size_t)r * a.H;
+      if (lane < nt) {
+        const float *xv = a.x + (size_t)(t0 + lane) * a.H;
+        float s = 0.0f;
+        for (int j = j0; j < j1; j++) s = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), s);
+        a.part[((size_t)(t0 + lane) * ROUTER_SEGS + seg) * a.E_pad + r] = s;
       }
     }
-  } else {  // fp32 rows: one fma chain over the segment
-    const int j0 = seg * (a.H / ROUTER_SEGS), j1 = j0 + a.H / ROUTER_SEGS;
-    const float *wr = (const float *)a.W + (size_t)r * a.H;
-    for (int i = 0; i < nt; i++) {
-      const float *xv = a.x + (size_t)(t0 + i) * a.H;
-      float s = 0.0f;
-      for (int j = j0; j < j1; j++) s = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), s);
-      acc[i] = s;
-    }
   }
-#pragma unroll
-  for (int i = 0; i < NA_RT; i++)
-    if (i < nt) a.part[((size_t)(t0 + i) * ROUTER_SEGS + seg) * a.E_pad + r] = acc[i];
 }
 
 // Learned routing: block t routes token t.
@@ -135,6 +140,10 @@ __global__ void k_na_hash(NaArgs a) {
   a.ids[i] = e;
   a.w[i] = e >= 0 ? __fmul_rn(__fdiv_rn(1.0f, (float)a.k), a.scale) : 0.0f;
 }
+
+// Shared memory of k_na_router_part: codes and scales of the token tile's
+// segment blocks, and one row segment (per * 34 bytes) per warp.
+size_t na_router_smem(int per) { return (size_t)NA_RT * per * 36 + (size_t)NA_WARPS * per * 34; }
 
 bool na_dev_ptr(const void *p) {
   if (!p) return false;
@@ -201,15 +210,22 @@ extern "C" ds4moe_status ds4moe_route_noalloc(const ds4moe_layer_desc *d, const 
   a.vocab = d->vocab, a.q8 = d->router_fmt == DS4MOE_Q8_0, a.scale = d->route_scale;
   a.part = (float *)scratch, a.ids = ids_out, a.w = w_out, a.err = err_flags;
   cudaStream_t s = (cudaStream_t)stream;
+  // Each launch's own result decides the status (cudaLaunchKernel returns
+  // it); an error left pending by unrelated earlier work is neither reported
+  // as this call's nor cleared.
+  void *args[] = {&a};
+  cudaError_t e;
   if (hash) {
     const long long n = (long long)n_tok * a.k;
-    k_na_hash<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a);
+    e = cudaLaunchKernel((const void *)k_na_hash, dim3((unsigned)((n + 255) / 256)), dim3(256), args, 0, s);
   } else {
     const int per = (a.H >> 5) / ROUTER_SEGS;
-    const dim3 grid((E_pad / 32 + NA_WARPS - 1) / NA_WARPS, ROUTER_SEGS, (n_tok + NA_RT - 1) / NA_RT);
-    k_na_router_part<<<grid, NA_WARPS * 32, NA_RT * per * 36, s>>>(a);
-    if (cudaPeekAtLastError() == cudaSuccess)
-      k_na_route<<<n_tok, NA_ROUTE_THREADS, route_block_smem(E_pad, a.k), s>>>(a);
+    const dim3 grid(E_pad / 32, ROUTER_SEGS, (n_tok + NA_RT - 1) / NA_RT);
+    e = cudaLaunchKernel((const void *)k_na_router_part, grid, dim3(NA_WARPS * 32), args,
+                         na_router_smem(per), s);
+    if (e == cudaSuccess)
+      e = cudaLaunchKernel((const void *)k_na_route, dim3(n_tok), dim3(NA_ROUTE_THREADS), args,
+                           route_block_smem(E_pad, a.k), s);
   }
-  return cudaGetLastError() == cudaSuccess ? DS4MOE_OK : DS4MOE_ERR_CUDA;
+  return e == cudaSuccess ? DS4MOE_OK : DS4MOE_ERR_CUDA;
 }

@@ -88,9 +88,13 @@ typedef struct {
   int32_t routed_fmt;   /* DS4MOE_Q8_0 or DS4MOE_Q2S                                */
   int32_t shared_fmt;   /* DS4MOE_Q8_0 or DS4MOE_Q2S                                */
   float route_scale;    /* multiplies the renormalised routed weights (1.0)         */
-  int32_t max_tokens;   /* largest n_tok of any later call, 1..1048576; calls run in */
-                        /* chunks of at most 64 tokens, so scratch is sized for    */
-                        /* min(max_tokens, 64) tokens                               */
+  int32_t max_tokens;   /* largest n_tok of any later call, 1..1048576. A call of   */
+                        /* fewer than 65 tokens runs on the decode path in chunks  */
+                        /* of at most 64 tokens; a larger one (when the layer's    */
+                        /* formats allow it) on the prefill path in chunks of at   */
+                        /* most 4096 tokens. Scratch is sized at create for        */
+                        /* Ts = max(min(max_tokens, 64), min(max_tokens, 4096))    */
+                        /* tokens: about 560 MB at 4096 tokens and the DS4 shape   */
 } ds4moe_layer_desc;
 
 /* Canonical weight buffers, DEVICE memory, read only during ds4moe_create
@@ -123,6 +127,10 @@ void ds4moe_destroy(ds4moe_layer *h);
 
 /* Routing only (steps: int8 quantisation of x, router GEMV, sigmoid,
  * bias-for-selection top-k, renormalisation; or the hash-table lookup).
+ * Passages: "DeepSeek V4 Flash -- DFlash Integration", Model Architecture
+ * (routed experts chosen by top-k over a learned router plus an optional
+ * bias; the first layers route by a token-ID table) and Execution Modes
+ * (--ds4-expert-top-k: the kept experts' weights are renormalised).
  *   x        [n_tok][H] fp32 (learned routing; may be NULL for hash)
  *   token_ids[n_tok] int32 (hash routing; may be NULL for learned)
  *   ids_out  [n_tok][k] int32: expert ids in descending key order
@@ -171,12 +179,21 @@ ds4moe_status ds4moe_route_noalloc(const ds4moe_layer_desc *desc, const ds4moe_w
                                    uint32_t *err_flags, void *stream);
 
 /* The whole layer: y[t] += MoE(x[t]) for t < n_tok, i.e.
+ * Passages: "DeepSeek V4 Flash -- DFlash Integration", Model Architecture
+ * (256 routed experts top-6 plus 1 shared, expert FFN 2048) and Forward Pass
+ * (the MoE FFN adds its output to the residual stream); "Baekpica/ds4 dfm
+ * Edition" README, two-bank batching notes (router -> top-k -> gate/up ->
+ * weighted SwiGLU -> expert down, plus the shared expert).
  *   y[t] += sum_j w_j * down_j(hq_j) + shared(x[t])
  * with hq_j the int8-requantised silu(gate_j x) * (up_j x).
  *   x         [n_tok][H] fp32, read only
  *   token_ids [n_tok] int32, required for hash routing, else may be NULL
  *   y         [n_tok][H] fp32, read and written (must not alias x)
- * n_tok in 0..max_tokens. Enqueued on `stream`; no host synchronisation. */
+ * n_tok in 0..max_tokens. Enqueued on `stream`; no host synchronisation.
+ * Calls of fewer than 65 tokens take the decode path (router, gate/up and
+ * down kernels, chunks of at most 64 tokens); larger calls the prefill path
+ * (tensor-core grouped GEMMs, chunks of at most 4096 tokens). Both give the
+ * same bits. */
 ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids,
                              float *y, void *stream);
 
@@ -186,9 +203,14 @@ ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, con
  * and update y in them directly over the CPU-GPU link. Decode-sized calls on
  * pageable buffers copy them into mapped pinned buffers owned by the handle
  * and replay one CUDA graph per token count (captured on the first call of
- * that count; kept until ds4moe_destroy). Larger calls copy to device
- * buffers, run the layer and copy y back. Not reentrant on one handle. Same
- * arguments otherwise. */
+ * that count; kept until ds4moe_destroy). Larger calls copy x, the token
+ * ids and y to device staging buffers chunk by chunk (Ts tokens at a time,
+ * see max_tokens), run the layer on each chunk and copy y back.
+ * Memory: the first call allocates, and keeps until ds4moe_destroy, device
+ * staging of 2 * Ts * hidden * 4 + Ts * 4 bytes (about 128 MB at Ts = 4096,
+ * hidden 4096) and, for pageable callers, 2 * min(max_tokens, 64) * hidden * 4
+ * + min(max_tokens, 64) * 4 bytes of mapped pinned host memory. Not reentrant
+ * on one handle. Same arguments otherwise. */
 ds4moe_status ds4moe_forward_host(ds4moe_layer *h, const float *x_host, int32_t n_tok,
                                   const int32_t *token_ids_host, float *y_host, void *stream);
 
@@ -201,11 +223,16 @@ ds4moe_status ds4moe_rmsnorm(const float *x, float *out, int32_t n_tok, int32_t 
 
 /* Synchronise `stream`, read and clear the handle's device error flag.
  * *flags_out (may be NULL) receives the DS4MOE_DEVERR_* bits.
+ * When DS4MOE_DEVERR_TIMEOUT is among them, a kernel gave up a bounded wait
+ * and left some cross-block completion counters unfinished: this call also
+ * zeroes them (and synchronises the device), so the next call starts from a
+ * clean state. Outputs of calls made between the timeout and this call are
+ * undefined.
  * Returns DS4MOE_ERR_DEVICE when any bit was set, else DS4MOE_OK. */
 ds4moe_status ds4moe_get_device_error(ds4moe_layer *h, void *stream, uint32_t *flags_out);
 
 /* Read-only device view of the handle's scratch after the last forward call,
- * for inspecting intermediate results. With C = min(max_tokens, 64) and
+ * for inspecting intermediate results. With C = Ts (see max_tokens) and
  * NS = k + n_shared, `which`:
  *   0 xq  int8  [C][H]        activation codes (CAS step 1)
  *   1 dx  fp32  [C][H/32]     activation scales
@@ -215,8 +242,8 @@ ds4moe_status ds4moe_get_device_error(ds4moe_layer *h, void *stream, uint32_t *f
  *   5 hq  int8  [C*NS][F]     SwiGLU codes, row t*NS+slot (slot k = shared)
  *   6 dh  fp32  [C*NS][F/32]  SwiGLU scales
  *   7 a   fp32  [C*NS][H]     per-slot down-projection outputs
- * Rows refer to the tokens of the last chunk of that call (a call runs in
- * chunks of at most 64 tokens); other rows are undefined.
+ * Rows refer to the tokens of the last chunk of that call (64 tokens at most
+ * on the decode path, 4096 on the prefill path); other rows are undefined.
  * Errors: INVALID_ARG for an unknown `which`. */
 ds4moe_status ds4moe_debug_scratch(ds4moe_layer *h, int32_t which, const void **ptr_out, uint64_t *bytes_out);
 
@@ -235,6 +262,22 @@ ds4moe_status ds4moe_debug_scratch(ds4moe_layer *h, int32_t which, const void **
 ds4moe_status ds4moe_profile_enable(ds4moe_layer *h, int32_t on);
 ds4moe_status ds4moe_profile_collect(ds4moe_layer *h);
 ds4moe_status ds4moe_profile_read(const ds4moe_layer *h, double *ms_out, int32_t n, int64_t *calls);
+
+/* Test hooks for failure detection (no counterpart in the pages; they make
+ * failures happen on the host side or through a short wait bound, never by
+ * faulting the GPU).
+ * ds4moe_debug_set_wait_limit: bound, in SM cycles, of the hand-off waits of
+ *   the decode path's expert kernels (a warp waiting for another warp of its
+ *   block, or for the router's count of quantised x); 0 restores the default
+ *   (about 2^31 cycles). A wait that runs out raises DS4MOE_DEVERR_TIMEOUT
+ *   and its block leaves; waits for the block's own copies keep the default
+ *   bound, so no copy is left in flight. Errors: INVALID_ARG (NULL, < 0).
+ * ds4moe_debug_fail_alloc: the n-th device allocation the library makes
+ *   from now on (in ds4moe_create, or the first ds4moe_forward_host) fails
+ *   as if the device were out of memory; 0 turns it off. Process-wide.
+ *   Errors: INVALID_ARG (n < 0). */
+ds4moe_status ds4moe_debug_set_wait_limit(ds4moe_layer *h, int64_t cycles);
+ds4moe_status ds4moe_debug_fail_alloc(int32_t n);
 
 /* Number of kernels this handle has launched since create. */
 uint64_t ds4moe_launch_count(const ds4moe_layer *h);

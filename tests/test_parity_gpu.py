@@ -88,6 +88,52 @@ def test_ds4_batched_decode_32_zipf(ora):
     run_case(ora, synth.DS4_ZIPF, 11, 32)
 
 
+# The decode dispatcher picks the tokens per unit, the blocks per SM and
+# whether activations are staged in shared memory from the token count and
+# the shared-memory footprint at the full DeepSeek-V4-Flash shape (the
+# handle's max_tokens sizes the bucket table that shares that space), so
+# every width class runs at that shape: one-token units (1-2 tokens), four-
+# token units (3-4), eight-token units with staged (5-8) and unstaged
+# (9-64) activations, a ragged last unit, and max_tokens both equal to the
+# call and larger.
+@pytest.mark.parametrize("T", [2, 3, 4, 5, 7, 9, 16, 33, 64])
+def test_ds4_decode_widths(ora, T):
+    run_case(ora, synth.DS4, 81, T)
+
+
+@pytest.mark.parametrize("T", [2, 5, 9])
+def test_ds4_decode_widths_larger_handle(ora, T):
+    run_case(ora, synth.DS4, 83, T, max_tokens=64)
+
+
+@pytest.mark.parametrize("T", [12, 48])
+def test_ds4_zipf_decode_hot_experts(ora, T):
+    """Zipf(1.1) popularity: hot experts hold more tokens than one unit, so
+    they run several passes of eight tokens."""
+    run_case(ora, synth.DS4_ZIPF, 85, T)
+
+
+def test_ds4_batch_invariance(ora):
+    """At the full shape, each of five tokens routed one by one gives the same
+    bits as the five in one call (batched routing and expert units against
+    single-token ones)."""
+    import torch
+    spec, T = synth.DS4, 5
+    w, ol, layer = _layer_pair(ora, spec, 87, T)
+    x = torch.from_numpy(margin_inputs(ol, spec, 87, T)).cuda()
+    yb = torch.zeros(T, spec.hidden, device="cuda")
+    layer.forward(x, yb)
+    ids_b, w_b = layer.route(x)
+    for t in range(T):
+        y1 = torch.zeros(1, spec.hidden, device="cuda")
+        layer.forward(x[t:t + 1].contiguous(), y1)
+        ids1, w1 = layer.route(x[t:t + 1].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(y1[0], yb[t])
+        assert torch.equal(ids1[0], ids_b[t]) and torch.equal(w1[0], w_b[t])
+    assert layer.device_error() == 0
+
+
 def test_ds4_hash_prefill_512(ora):
     run_case(ora, synth.DS4_HASH, 13, 512)
 
