@@ -1,12 +1,15 @@
 #!/usr/bin/env python3
-"""Benchmark of the routed MoE FFN of a DeepSeek-V4-Flash-shaped layer on GB300.
+"""Benchmark of the routed MoE FFN of DeepSeek-V4-Flash-shaped layers on GB300.
 
-Default workload: one decode token through one layer with hidden 4096, 256
-routed experts top-6 + 1 shared, FFN width 2048, 2-bit superblock routed
-experts and Q8_0 shared expert and router (about 2.1 GB of routed weights
-resident in HBM). A step is one ds4moe_forward over one batch of synthetic
-input; inputs are resident in HBM before the timed region; L2 is flushed by a
-512 MiB write between timed steps (outside the timed kernels).
+Default workload: the 43-layer stack (layers 0-2 hash routed, 3-42 learned;
+each layer hidden 4096, 256 routed experts top-6 + 1 shared, FFN width 2048,
+2-bit superblock routed experts and Q8_0 shared expert and router; about 92 GB
+of weights resident in HBM) at decode batch 1: a step carries one token
+through all 43 layers (RMSNorm, then the MoE FFN added to the residual
+stream). The same line carries the stack at decode batch 8 and at a prefill of
+4096 tokens as extra keys. Inputs are resident in HBM before the timed region;
+every step reads gigabytes of weights, far above L2, so no flush is needed.
+Single-layer workloads (--workload) rotate layer copies or flush L2 instead.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME]
@@ -53,7 +56,7 @@ STACK_WORKLOADS = {
     "ds4-stack-43-decode-8": (8, "43-layer stack, decode batch 8"),
     "ds4-stack-43-prefill-4096": (4096, "43-layer stack, prefill of 4096 tokens"),
 }
-DEFAULT_WORKLOAD = "ds4-decode-1"
+DEFAULT_WORKLOAD = "ds4-stack-43-decode-1"
 SEED = 2026
 
 
@@ -277,13 +280,178 @@ def cpu_baseline(spec, T, w, budget_s=12.0):
             "sample": f"{n} forward(s) of {T} token(s) of the same workload ({dt:.1f} s of CPU work)"}
 
 
-def run_stack(args):
-    """The 43-layer stack: every layer's weights resident (about 92 GB), one
-    step = T tokens through all 43 layers (RMSNorm, then the MoE FFN added to
-    the residual stream), captured as one CUDA graph."""
-    import torch
+def stack_cpu_baseline(w_hash, w_learned, budget_s=15.0):
+    """The oracle as it stands on this host's cores, on a bounded sample of
+    the stack workload: one token through a hash-routed layer (0) and a
+    learned one (3), RMSNorm before each, repeated for about `budget_s`; the
+    per-token time of the 43-layer step is 3 x the hash layer's + 40 x the
+    learned layer's."""
+    import oracle
+    ora = oracle.get()
+    cores = os.cpu_count() or 1
+    ol_h = ora.layer(synth.DS4_HASH, w_hash)
+    ol_l = ora.layer(synth.DS4, w_learned)
+    tok = synth.gen_token_ids(synth.DS4_HASH, SEED, 1)
+    th = tl = 0.0
+    n = 0
+    t_start = time.perf_counter()
+    while n < 4096 and (n < 2 or time.perf_counter() - t_start < budget_s):
+        h = synth.gen_x(synth.DS4, SEED + 3000 + n, 1)
+        t0 = time.perf_counter()
+        h, _, _, _ = ol_h.forward(ora.rmsnorm(h, 1e-6), h, tok, nthreads=cores)
+        t1 = time.perf_counter()
+        h, _, _, _ = ol_l.forward(ora.rmsnorm(h, 1e-6), h, None, nthreads=cores)
+        t2 = time.perf_counter()
+        th += t1 - t0
+        tl += t2 - t1
+        n += 1
+    per_tok = (synth.N_HASH_LAYERS * th + (synth.N_STACK_LAYERS - synth.N_HASH_LAYERS) * tl) / n
+    return {"value": 1.0 / per_tok, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} token(s) through one hash-routed and one learned layer (RMSNorm + MoE FFN each, "
+                      f"{th + tl:.1f} s of CPU work); 43-layer time = 3 x hash + 40 x learned"}
 
-    import deepseek_v4_flash_gb300 as ds4
+
+class Stack:
+    """The 43-layer stack: every layer's weights resident (about 92 GB), each
+    handle sized for `max_tokens`. A step carries T tokens through all 43
+    layers (RMSNorm, then the MoE FFN added to the residual stream)."""
+
+    def __init__(self, max_tokens, dev, keep=()):
+        import deepseek_v4_flash_gb300 as ds4
+        import torch
+        self.ds4, self.dev = ds4, dev
+        self.L = synth.N_STACK_LAYERS
+        self.layers, self.specs, self.host = [], [], {}
+        for l in range(self.L):
+            spec = synth.stack_layer_spec(l)
+            wl = synth.gen_layer(spec, SEED, l)
+            if l in keep:
+                self.host[l] = wl
+            wd = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in wl.items()}
+            self.layers.append(ds4.Layer(desc_from_spec(ds4, spec, max_tokens), wd))
+            self.specs.append(spec)
+            del wd, wl
+            torch.cuda.empty_cache()
+        self.tok = torch.from_numpy(synth.gen_token_ids(synth.DS4_HASH, SEED, max_tokens)).to(dev)
+
+    def step(self, h, xn, T):
+        ds4 = self.ds4
+        for l in range(self.L):
+            ds4.rmsnorm(h[:T], xn[:T], 1e-6)
+            self.layers[l].forward(xn[:T], h[:T], self.tok[:T] if self.specs[l].route == "hash" else None)
+
+    def unique_experts(self, x0, T):
+        """Routed experts each layer touches when x0 passes through the stack."""
+        import torch
+        h, xn = x0.clone(), torch.empty_like(x0)
+        uniq = []
+        for l in range(self.L):
+            self.ds4.rmsnorm(h, xn, 1e-6)
+            tk = self.tok[:T] if self.specs[l].route == "hash" else None
+            ids, _ = self.layers[l].route(xn, tk)
+            v = ids.cpu().numpy()
+            uniq.append(len(np.unique(v[v >= 0])))
+            self.layers[l].forward(xn, h, tk)
+        torch.cuda.synchronize()
+        return uniq
+
+    def time(self, T, steps, warmup, rank, clocks=None, world=1):
+        """Graph replays of whole steps timed with CUDA events; returns
+        (seconds over all steps, max over ranks, unique experts per layer,
+        launches per step)."""
+        import torch
+        dev = self.dev
+        NX = int(max(2, min(16, (1 << 26) // (T * synth.DS4.hidden))))
+        xs = torch.from_numpy(np.stack([synth.gen_x(synth.DS4, SEED + 7 * i + rank, T) for i in range(NX)])).to(dev)
+        uniq = self.unique_experts(xs[0], T)
+        x_in = xs[0].clone()
+        h, xn = torch.empty_like(x_in), torch.empty_like(x_in)
+
+        def step():
+            h.copy_(x_in)
+            self.step(h, xn, T)
+
+        stream = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        n0 = sum(Ly.launch_count() for Ly in self.layers)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        launches = sum(Ly.launch_count() for Ly in self.layers) - n0 + self.L  # + the RMSNorm launches
+        for i in range(warmup):
+            x_in.copy_(xs[i % NX])
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if clocks:
+            clocks.start()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            x_in.copy_(xs[i % NX])
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        clk = clocks.stop() if clocks else None
+        total_s = reduce_max(float(sum(a.elapsed_time(b) for a, b in ev)) / 1e3, dev)
+        del g
+        return total_s, uniq, launches, clk, xs
+
+    def stage_ms(self, xs, T, reps=3):
+        """Per-kernel CUDA-event times (the library's profiling events on the
+        call's stream), averaged over layers and `reps` eager steps: returns
+        {stage: ms per layer call} per routing kind."""
+        import torch
+        h, xn = torch.empty_like(xs[0]), torch.empty_like(xs[0])
+        for Ly in self.layers:
+            Ly.profile(True)
+        for r in range(reps):
+            h.copy_(xs[r % len(xs)])
+            for l in range(self.L):
+                self.ds4.rmsnorm(h, xn, 1e-6)
+                self.layers[l].forward(xn, h, self.tok[:T] if self.specs[l].route == "hash" else None)
+                self.layers[l].profile_collect()
+        per = {"hash": {}, "learned": {}}
+        cnt = {"hash": 0, "learned": 0}
+        for l, Ly in enumerate(self.layers):
+            sm, nc = Ly.profile_read()
+            kind = self.specs[l].route
+            cnt[kind] += nc
+            for k2, v2 in sm.items():
+                per[kind][k2] = per[kind].get(k2, 0.0) + v2
+            Ly.profile(False)
+        return {kind: {k2: v2 / max(cnt[kind], 1) for k2, v2 in d.items()} for kind, d in per.items()}
+
+    def bytes_per_step(self, T, uniq):
+        return float(sum(step_bytes(self.specs[l], T, uniq[l]) for l in range(self.L)) +
+                     self.L * 2 * T * synth.DS4.hidden * 4)
+
+    def gateup_roofline(self, T, uniq, stages, hbm_peak, peak_kind):
+        """The gate/up kernel (the dominant one): algorithmic bytes per launch
+        (averaged over the 43 layers' launches) over its average CUDA-event
+        duration (hash and learned layers weighted 3 : 40)."""
+        nh, nl = synth.N_HASH_LAYERS, self.L - synth.N_HASH_LAYERS
+        b = float(np.mean([gateup_bytes(self.specs[l], T, uniq[l]) for l in range(self.L)]))
+        ms = (nh * stages["hash"]["gateup"] + nl * stages["learned"]["gateup"]) / self.L
+        gbs = b / (ms / 1e3) / 1e9
+        return {"kernel": "gate/up", "bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gbs / hbm_peak, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": b,
+                "launch_ms": ms}
+
+
+def run_stack(args):
+    """The 43-layer stack (configs: decode at batch 1 and 8, prefill of 4096
+    tokens), one CUDA graph per step."""
+    import torch
 
     T, desc = STACK_WORKLOADS[args.workload]
     world, rank, local = dist_setup()
@@ -294,91 +462,80 @@ def run_stack(args):
     else:
         torch.cuda.set_device(0)
     dev = torch.device("cuda")
-    L = synth.N_STACK_LAYERS
-    layers, specs = [], []
-    for l in range(L):
-        spec = synth.stack_layer_spec(l)
-        wl = synth.gen_layer(spec, SEED, l)
-        wd = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in wl.items()}
-        layers.append(ds4.Layer(desc_from_spec(ds4, spec, T), wd))
-        specs.append(spec)
-        del wd, wl
-        torch.cuda.empty_cache()
-    NX = int(max(2, min(16, (1 << 26) // (T * synth.DS4.hidden))))
-    xs = torch.from_numpy(np.stack([synth.gen_x(synth.DS4, SEED + 7 * i + rank, T) for i in range(NX)])).to(dev)
-    tok = torch.from_numpy(synth.gen_token_ids(synth.DS4_HASH, SEED + rank, T)).to(dev)
-    x_in = xs[0].clone()
-    h = torch.empty_like(x_in)
-    xn = torch.empty_like(x_in)
-
-    def step():
-        h.copy_(x_in)
-        for l in range(L):
-            ds4.rmsnorm(h, xn, 1e-6)
-            layers[l].forward(xn, h, tok if specs[l].route == "hash" else None)
-
-    # unique routed experts per layer for the first input batch (algorithmic bytes)
-    uniq = []
-    h.copy_(x_in)
-    for l in range(L):
-        ds4.rmsnorm(h, xn, 1e-6)
-        ids, _ = layers[l].route(xn, tok if specs[l].route == "hash" else None)
-        v = ids.cpu().numpy()
-        uniq.append(len(np.unique(v[v >= 0])))
-        layers[l].forward(xn, h, tok if specs[l].route == "hash" else None)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    side = torch.cuda.Stream()
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        step()
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
-    n0 = sum(Ly.launch_count() for Ly in layers)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        step()
-    launches_per_step = sum(Ly.launch_count() for Ly in layers) - n0 + L  # + the RMSNorm launches
-    for i in range(args.warmup):
-        x_in.copy_(xs[i % NX])
-        g.replay()
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        x_in.copy_(xs[i % NX])
-        ev[i][0].record(stream)
-        g.replay()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    total_s = reduce_max(float(sum(a.elapsed_time(b) for a, b in ev)) / 1e3, dev)
-    value = job_throughput(args.steps * T, total_s, world)
+    extras = [] if args.no_extras or args.workload != DEFAULT_WORKLOAD else \
+        ["ds4-stack-43-decode-8", "ds4-stack-43-prefill-4096"]
+    max_t = max([T] + [STACK_WORKLOADS[w][0] for w in extras])
+    want_cpu = rank == 0 and not args.no_cpu_baseline
+    stack = Stack(max_t, dev, keep=(0, synth.N_HASH_LAYERS) if want_cpu else ())
     hbm_peak, _, peak_kind = peaks()
-    bytes_step = float(sum(step_bytes(specs[l], T, uniq[l]) for l in range(L)) + L * 2 * T * synth.DS4.hidden * 4)
+
+    clocks = ClockSampler(local)
+    total_s, uniq, launches, clk, xs = stack.time(T, args.steps, args.warmup, rank, clocks, world)
+    value = job_throughput(args.steps * T, total_s, world)
+    bytes_step = stack.bytes_per_step(T, uniq)
     gbs = bytes_step * world * args.steps / total_s / 1e9
+    stages = stack.stage_ms(xs, T)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32+f32", "data": "synthetic",
-        "config": {"workload": args.workload, "description": desc, "n_tok": T, "layers": L,
-                   "l2": "not flushed: 43 layers, about 92 GB of weights, far above L2",
-                   "inputs": f"{NX} seeded batches resident in HBM, cycled"},
+        "config": {"workload": args.workload, "description": desc, "n_tok": T, "layers": stack.L,
+                   "l2": "not flushed: each step reads the touched weights of 43 layers (GBs), far above L2",
+                   "inputs": "seeded batches resident in HBM, cycled"},
         "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "bytes_per_step": bytes_step,
         "unique_experts_per_layer": float(np.mean(uniq)),
-        "roofline": {"kernel": "whole 43-layer step", "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind, "traffic": None},
-        "timing": "one CUDA graph of the 43 layers per step, CUDA events around each replay",
-        "gpu_launches": int(launches_per_step * args.steps),
+        "roofline": dict(stack.gateup_roofline(T, uniq, stages, hbm_peak, peak_kind), traffic=None),
+        "stages_ms_per_layer": stages,
+        "timing": "value: one CUDA graph of the 43 layers per step, CUDA events around each replay; "
+                  "roofline: the library's per-kernel events in a separate eager pass",
+        "gpu_launches": int(launches * args.steps),
     }
+    if T == 1:
+        line["roofline"]["traffic"] = recorded_traffic()
     if clk:
         line["clocks"] = clk
+
+    for wname in extras:
+        Tx = STACK_WORKLOADS[wname][0]
+        steps_x = args.steps if Tx <= 64 else max(1, min(args.steps, 3))
+        tx, ux, lx, _, xsx = stack.time(Tx, steps_x, args.warmup if Tx <= 64 else 1, rank, None, world)
+        bx = stack.bytes_per_step(Tx, ux)
+        gx = bx * world * steps_x / tx / 1e9
+        stx = stack.stage_ms(xsx, Tx, reps=3 if Tx <= 64 else 1)
+        ex = {"tokens_per_s": job_throughput(steps_x * Tx, tx, world), "ms_per_step": 1e3 * tx / steps_x,
+              "steps": steps_x, "hbm_gbs": gx, "hbm_frac": gx / hbm_peak, "bytes_per_step": bx,
+              "unique_experts_per_layer": float(np.mean(ux)),
+              "gate_up": stack.gateup_roofline(Tx, ux, stx, hbm_peak, peak_kind)}
+        if Tx > 64:  # the grouped GEMM: its integer MACs (2 ops each) per second as well
+            ops = 2.0 * 25165824 * Tx * (synth.DS4.top_k + 1) * 2 / 3
+            ex["gate_up"]["tera_ops_per_s"] = ops / (ex["gate_up"]["launch_ms"] / 1e3) / 1e12
+        line[wname.replace("ds4-stack-43-", "stack_").replace("-", "_")] = ex
+        line["gpu_launches"] += int(lx * steps_x)
+
+    if rank == 0 and args.e2e_steps > 0:
+        # through the public calls on host buffers: the input batch from pinned
+        # host memory, RMSNorm + MoE FFN of all 43 layers, the result back
+        xh = [xs[i % len(xs)].cpu().pin_memory() for i in range(min(args.e2e_steps, len(xs)))]
+        out = torch.empty(T, synth.DS4.hidden).pin_memory()
+        h, xn = torch.empty_like(xs[0]), torch.empty_like(xs[0])
+        for i in range(3):
+            h.copy_(xh[i % len(xh)], non_blocking=True)
+            stack.step(h, xn, T)
+            out.copy_(h)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.e2e_steps):
+            h.copy_(xh[i % len(xh)], non_blocking=True)
+            stack.step(h, xn, T)
+            out.copy_(h)  # synchronises
+        dt = time.perf_counter() - t0
+        line["e2e"] = {"value": args.e2e_steps * T / dt, "unit": "tokens/s",
+                       "h2d_bytes_per_step": T * synth.DS4.hidden * 4,
+                       "d2h_bytes_per_step": T * synth.DS4.hidden * 4, "steps": args.e2e_steps,
+                       "how": "pinned host input copied in, ds4moe_rmsnorm + ds4moe_forward per layer "
+                              "(eager), result copied out, wall clock"}
+    if want_cpu:
+        line["cpu_baseline"] = stack_cpu_baseline(stack.host[0], stack.host[synth.N_HASH_LAYERS])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -388,16 +545,21 @@ def run_stack(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 100 for the stack, 4000 for one layer)")
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(STACK_WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default workload only: skip the stack's batch-8 and prefill-4096 lines")
     ap.add_argument("--layer-copies", type=int, default=0,
                     help="layer copies rotated across steps (0: enough that the working sets exceed L2)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.steps is None:
+        args.steps = 100 if args.workload in STACK_WORKLOADS else 4000
     if args.workload in STACK_WORKLOADS:
         if args.impl == "reference":
             run_reference_stack(args)
@@ -557,7 +719,7 @@ def main():
         "roofline": {"kernel": "gate/up (k_experts, gate/up variant)", "bound": "hbm", "achieved": gu_gbs, "peak": hbm_peak,
                      "unit": "GB/s", "frac": gu_gbs / hbm_peak, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": float(gu_bytes.mean()), "launch_ms": gu_ms,
-                     "traffic": recorded_traffic() if (args.workload == DEFAULT_WORKLOAD) else None},
+                     "traffic": recorded_traffic() if (args.workload == "ds4-decode-1") else None},
         "stages_ms": {k: v / max(ncalls, 1) for k, v in stage_ms.items()},
         "timing": "value: CUDA-graph replays timed with events; stages_ms: per-kernel events, separate pass",
         "gpu_launches": int(launches),

@@ -22,6 +22,7 @@ def test_create_out_of_memory_at_every_allocation():
     spec = synth.MICRO
     w = to_device(synth.gen_layer(spec, 91, 0))
     desc = lib_desc(spec, 100)  # decode and prefill scratch
+    ds4.Layer(desc, w).close()  # the library's module (code, static data) is loaded once, here
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
     n = 1
