@@ -79,6 +79,7 @@ class Oracle:
             "ora_expert": (None, [vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp]),
             "ora_forward": (ctypes.c_int, [vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_int]),
             "ora_rmsnorm": (None, [vp, vp, ctypes.c_int, ctypes.c_int, f32]),
+            "ora_dense_q8": (None, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -140,6 +141,15 @@ class Oracle:
         out = np.empty_like(x)
         self.L.ora_rmsnorm(_ptr(x), _ptr(out), T, H, eps)
         return out
+
+    def dense_q8(self, w: np.ndarray, N: int, K: int, x: np.ndarray, nthreads: int = 0) -> np.ndarray:
+        """y[T][N] = W x for canonical Q8_0 rows w ([N][K]) and x [T][K] f32."""
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, K)
+        w = np.ascontiguousarray(w, dtype=np.uint8)
+        assert w.nbytes == N * (K // 32) * 34
+        y = np.empty((x.shape[0], N), np.float32)
+        self.L.ora_dense_q8(_ptr(w), N, K, _ptr(x), x.shape[0], _ptr(y), nthreads or (os.cpu_count() or 1))
+        return y
 
     # -- layer ---------------------------------------------------------------
     def layer(self, spec, w: dict) -> "BoundLayer":

@@ -25,6 +25,10 @@
  *  - Activations pre-quantised to int8 before the Q8_0 matmuls ("_preq"
  *    kernels): ds4-rocm fork README, __launch_bounds__ annotations list.
  *  - Final RMSNorm: DFlash Integration page, Forward Pass step 5.
+ *  - Dense Q8_0 products beside the MoE (output head "OutQ8", attention
+ *    projections) on pre-quantised int8 activations: ds4-rocm fork README,
+ *    Performance optimizations (the matmul_q8_0_preq_* kernels) and the
+ *    DwarfStar README, Model Weights (the OutQ8 model name).
  * The pages fix neither the bytes of the 2-bit format, nor the score
  * function, nor any float operation order. Those are fixed by the canonical
  * arithmetic spec (CAS) this file implements, stated at each function.
@@ -587,4 +591,55 @@ void ora_rmsnorm(const float *x, float *out, int T, int H, float eps) {
     float inv = 1.0f / sqrtf(ss / (float)H + eps);
     for (int i = 0; i < H; i++) out[(size_t)t * H + i] = v[i] * inv;
   }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dense Q8_0 product y = W x beside the MoE (output head, attention         */
+/* projections): x quantised per 32-block (CAS step 1); each output row is   */
+/* the CAS row sum (steps 2-4) of its Q8_0 blocks, with the row's blocks in  */
+/* S = min(8, K/32) contiguous segments, as for an expert row.               */
+/*   w [N][K] canonical Q8_0 rows, x [T][K] f32, y [T][N] f32 (overwritten). */
+/* Rows are independent: nthreads > 1 splits them across threads, each row's */
+/* arithmetic unchanged.                                                      */
+
+typedef struct {
+  const uint8_t *w;
+  int N, K, T, nthreads, tid;
+  const int8_t *xq;
+  const float *dx;
+  const int16_t *gs;
+  float *y;
+} dense_ctx;
+
+static void *dense_worker(void *p) {
+  dense_ctx *c = (dense_ctx *)p;
+  const size_t rb = row_bytes(FMT_Q8_0, c->K);
+  const int S = expert_segs(FMT_Q8_0, c->K);
+  for (int n = c->tid; n < c->N; n += c->nthreads)
+    for (int t = 0; t < c->T; t++)
+      c->y[(size_t)t * c->N + n] = ora_row(FMT_Q8_0, c->w + (size_t)n * rb, c->K, c->xq + (size_t)t * c->K,
+                                           c->dx + (size_t)t * (c->K / 32), c->gs + (size_t)t * (c->K / 16), S);
+  return NULL;
+}
+
+void ora_dense_q8(const uint8_t *w, int N, int K, const float *x, int T, float *y, int nthreads) {
+  int8_t *xq = (int8_t *)malloc((size_t)T * K);
+  float *dx = (float *)malloc((size_t)T * (K / 32) * sizeof(float));
+  int16_t *gs = (int16_t *)malloc((size_t)T * (K / 16) * sizeof(int16_t));
+  for (int t = 0; t < T; t++)
+    ora_quantize(x + (size_t)t * K, K, xq + (size_t)t * K, dx + (size_t)t * (K / 32), gs + (size_t)t * (K / 16));
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  dense_ctx cs[256];
+  for (int i = 0; i < nthreads; i++) {
+    cs[i] = (dense_ctx){w, N, K, T, nthreads, i, xq, dx, gs, y};
+    if (nthreads == 1) dense_worker(&cs[i]);
+    else pthread_create(&th[i], NULL, dense_worker, &cs[i]);
+  }
+  if (nthreads > 1)
+    for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
+  free(xq);
+  free(dx);
+  free(gs);
 }

@@ -499,10 +499,84 @@ def check_combine_linearity(ora, spec=synth.MICRO, seed=37):
     assert np.array_equal(z, z1)
 
 
+# ------------------------------------------------------------ dense Q8_0 --
+
+def _dense_golden():
+    blk = R.parse_golden(os.path.join(GOLDEN, "dense_q8.txt"))[0]
+    rows = dict(blk["_rows"])
+    K, N = 64, 2
+    x = np.zeros((2, K), np.float32)
+    x[0, :3] = [float(v) for v in rows["x0"]]
+    x[0, 32:35] = [float(v) for v in rows["x1"]]
+    x[1] = -x[0]
+    w = np.zeros((N, 2, 34), np.uint8)
+    for r in range(N):
+        for b, d in enumerate(rows[f"r{r}d"]):
+            w[r, b, :2] = np.frombuffer(int(d, 16).to_bytes(2, "little"), np.uint8)
+            q = [int(v) for v in rows[f"r{r}q{b}"]]
+            w[r, b, 2:2 + len(q)] = np.array(q, np.int8).view(np.uint8)
+    y = np.array([float(v) for v in rows["y"]], np.float32)
+    return w.reshape(-1), N, K, x, y
+
+
+def check_dense_golden(ora):
+    """Hand-worked dense product (golden/dense_q8.txt), two tokens."""
+    w, N, K, x, y = _dense_golden()
+    got = ora.dense_q8(w, N, K, x, nthreads=1)
+    assert got.tolist() == [y.tolist(), (-y).tolist()], got
+
+
+def check_dense_segments(ora):
+    """Dense rows are summed in min(8, blocks) segments like expert rows: the
+    hand-worked 16-block row of golden/cas_segments16.txt gives its S = 8 sum."""
+    row, x, want = _segment_row("cas_segments16.txt")
+    y = ora.dense_q8(row, 1, x.size, x[None, :], nthreads=1)
+    assert float(y[0, 0]) == want["S8"]
+
+
+def check_dense_identity(ora, seed=17):
+    """A closed form: W with one code 1 (scale 1) at column n of row n is the
+    identity on the quantised activations, so y[t][n] = dx_t(n) * xq_t[n]
+    (rows and columns, and tokens, kept apart)."""
+    rng = np.random.default_rng(seed)
+    K = N = 96
+    w = np.zeros((N, K // 32, 34), np.uint8)
+    for n in range(N):
+        w[n, n // 32, :2] = np.frombuffer((0x3C00).to_bytes(2, "little"), np.uint8)
+        w[n, n // 32, 2 + n % 32] = 1
+    x = (rng.standard_normal((3, K)) * 5).astype(np.float32)
+    y = ora.dense_q8(w.reshape(-1), N, K, x, nthreads=2)
+    for t in range(3):
+        q, dx, _ = ora.quantize(x[t])
+        assert np.array_equal(y[t], (np.repeat(dx, 32) * q.astype(np.float32)).astype(np.float32))
+
+
+def check_dense_vs_f64(ora, seed=19):
+    """Random rows against the float64 sum of the float64 block terms, within
+    the recursive-summation bound (nb + 3) * u * sum |p_b|."""
+    rng = np.random.default_rng(seed)
+    N, K, T = 40, 768, 2
+    blocks = rng.integers(-127, 128, (N, K // 32, 32)).astype(np.int8)
+    d = (rng.uniform(1e-3, 2e-2, (N, K // 32))).astype(np.float16)
+    w = np.zeros((N, K // 32, 34), np.uint8)
+    w[:, :, :2] = d.view(np.uint8).reshape(N, K // 32, 2)
+    w[:, :, 2:] = blocks.view(np.uint8)
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    y = ora.dense_q8(w.reshape(-1), N, K, x, nthreads=3)
+    for t in range(T):
+        q, dx, _ = ora.quantize(x[t])
+        I = (blocks.astype(np.int64) * q.astype(np.int64).reshape(1, K // 32, 32)).sum(-1)
+        terms = d.astype(np.float64) * dx.astype(np.float64)[None, :] * I
+        ref = terms.sum(1)
+        bound = (K // 32 + 3) * 2.0 ** -24 * np.abs(terms).sum(1) + 1e-30
+        assert np.all(np.abs(y[t].astype(np.float64) - ref) <= bound)
+
+
 ALL_CHECKS = [
     check_binary16, check_q2s_dequant_golden, check_q8_dequant_golden, check_quantize_golden,
     check_quantize_vs_f64, check_block_dots_exact, check_row_sum_f64, check_cas_segment_order,
     check_expert_rows_use_eight_segments, check_exp, check_sigmoid_silu,
     check_rmsnorm, check_topk_golden, check_route_invariants, check_route_k_equals_E, check_hash_route,
     check_expert_stages, check_shared_is_swiglu_mlp, check_layer_vs_textbook, check_combine_linearity,
+    check_dense_golden, check_dense_segments, check_dense_identity, check_dense_vs_f64,
 ]

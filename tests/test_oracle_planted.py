@@ -44,6 +44,9 @@ PLANTS = [
     ("bias_ignored", "key[e] = s[e] + L->router_bias[e];", "key[e] = s[e];"),
     ("expert_one_segment", "return units < 8 ? units : 8;", "return 1;"),
     ("expert_four_segments", "return units < 8 ? units : 8;", "return units < 4 ? units : 4;"),
+    ("dense_one_segment", "const int S = expert_segs(FMT_Q8_0, c->K);", "const int S = 1;"),
+    ("dense_token_stride", "c->xq + (size_t)t * c->K,\n", "c->xq,\n"),
+    ("dense_transposed", "c->y[(size_t)t * c->N + n] = ora_row(", "c->y[(size_t)n * c->T + t] = ora_row("),
     ("segments_merged", "    tot = tot + acc;\n  }\n  return tot;\n}\n\nstatic float row_q2s",
      "    tot = acc;\n  }\n  return tot;\n}\n\nstatic float row_q2s"),
 ]
