@@ -56,6 +56,12 @@ STACK_WORKLOADS = {
     "ds4-stack-43-decode-8": (8, "43-layer stack, decode batch 8"),
     "ds4-stack-43-prefill-4096": (4096, "43-layer stack, prefill of 4096 tokens"),
 }
+# Dense Q8_0 products beside the MoE: (n_out, n_in, tokens, description).
+DENSE_WORKLOADS = {
+    "ds4-out-head-decode-1": (129280, 4096, 1, "output head 129280 x 4096 Q8_0 (563 MB), one decode token"),
+    "ds4-out-head-decode-8": (129280, 4096, 8, "output head 129280 x 4096 Q8_0, eight decode tokens"),
+    "ds4-attn-proj-decode-1": (4096, 4096, 1, "a 4096 x 4096 Q8_0 projection (17.8 MB), one decode token"),
+}
 DEFAULT_WORKLOAD = "ds4-stack-43-decode-1"
 SEED = 2026
 
@@ -545,6 +551,122 @@ def run_stack(args):
         torch.distributed.destroy_process_group()
 
 
+def run_dense(args):
+    """A dense Q8_0 product y = W x (ds4moe_dense_forward): CUDA-graph replays
+    timed with events; matrices that fit L2 are rotated over copies."""
+    import torch
+
+    import deepseek_v4_flash_gb300 as ds4
+
+    N, K, T, desc = DENSE_WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda")
+    wbytes = N * (K // 32) * 34
+    NC = 1 if wbytes > (256 << 20) else int(np.ceil(4 * (128 << 20) / wbytes))
+    w_host = synth.gen_q8_matrix(SEED, N, K)
+    mats = []
+    for c in range(NC):
+        wd = torch.from_numpy(w_host if c == 0 else synth.gen_q8_matrix(SEED + c, N, K)).to(dev)
+        mats.append(ds4.Dense(N, K, wd, max_tokens=T))
+        del wd
+        torch.cuda.empty_cache()
+    xs = torch.from_numpy(synth.gen_dense_x(SEED + rank, T, K)).to(dev)
+    ys = [torch.empty(T, N, device=dev) for _ in range(NC)]
+    stream = torch.cuda.current_stream()
+    graphs = []
+    n0 = sum(m.launch_count() for m in mats)
+    for c in range(NC):
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            mats[c].forward(xs, ys[c])
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            mats[c].forward(xs, ys[c])
+        graphs.append(g)
+    launches_per_step = (sum(m.launch_count() for m in mats) - n0) // (2 * NC)
+    for i in range(max(args.warmup, NC)):
+        graphs[i % NC].replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        graphs[i % NC].replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    total_s = reduce_max(float(step_ms.sum()) / 1e3, dev)
+    value = job_throughput(args.steps * T, total_s, world)
+    hbm_peak, _, peak_kind = peaks()
+    bytes_step = wbytes + T * K * 4 + T * N * 4
+    gbs = bytes_step * world * args.steps / total_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8/int32+f32", "data": "synthetic",
+        "config": {"workload": args.workload, "description": desc, "n_out": N, "n_in": K, "n_tok": T,
+                   "l2": ("not flushed: the matrix (%d MB) is far above L2" % (wbytes >> 20)) if NC == 1 else
+                         f"not flushed: {NC} matrix copies rotated, {NC * wbytes >> 20} MB > L2"},
+        "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "bytes_per_step": float(bytes_step),
+        "roofline": {"kernel": "k_dense (quantise kernel before it included)", "bound": "hbm", "achieved": gbs,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": float(bytes_step), "launch_ms": 1e3 * total_s / args.steps,
+                     "traffic": None},
+        "timing": "CUDA-graph replays of ds4moe_dense_forward, CUDA events around each",
+        "gpu_launches": int(launches_per_step * args.steps),
+    }
+    if clk:
+        line["clocks"] = clk
+    if rank == 0 and args.e2e_steps > 0:
+        xh = torch.from_numpy(synth.gen_dense_x(SEED, T, K)).pin_memory()
+        yh = torch.empty(T, N).pin_memory()
+        xd = torch.empty(T, K, device=dev)
+        for _ in range(3):
+            xd.copy_(xh, non_blocking=True)
+            mats[0].forward(xd, ys[0])
+            yh.copy_(ys[0])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            xd.copy_(xh, non_blocking=True)
+            mats[0].forward(xd, ys[0])
+            yh.copy_(ys[0])  # synchronises
+        dt = time.perf_counter() - t0
+        line["e2e"] = {"value": args.e2e_steps * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": T * K * 4,
+                       "d2h_bytes_per_step": T * N * 4, "steps": args.e2e_steps}
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        ora = oracle.get()
+        cores = os.cpu_count() or 1
+        n, t0 = 0, time.perf_counter()
+        while n < 1000 and (n < 1 or time.perf_counter() - t0 < 10.0):
+            ora.dense_q8(w_host, N, K, synth.gen_dense_x(SEED + 100 + n, T, K), nthreads=cores)
+            n += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": n * T / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{n} product(s) of {T} token(s) on the same matrix ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -552,7 +674,8 @@ def main():
                     help="timed steps (default: 100 for the stack, 4000 for one layer)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(STACK_WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(WORKLOADS) + sorted(STACK_WORKLOADS) + sorted(DENSE_WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
@@ -563,6 +686,12 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.steps is None:
         args.steps = 100 if args.workload in STACK_WORKLOADS else 4000
+    if args.workload in DENSE_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the MoE workloads"}))
+        else:
+            run_dense(args)
+        return
     if args.workload in STACK_WORKLOADS:
         if args.impl == "reference":
             run_reference_stack(args)

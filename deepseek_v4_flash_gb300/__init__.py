@@ -9,7 +9,7 @@ Entry points mirror the C ABI in include/ds4moe.h:
 ``Layer(desc, weights)`` = ds4moe_create, ``Layer.route`` = ds4moe_route,
 ``Layer.forward`` = ds4moe_forward, ``Layer.forward_host`` =
 ds4moe_forward_host, ``rmsnorm`` = ds4moe_rmsnorm, ``route_noalloc`` =
-ds4moe_route_noalloc.
+ds4moe_route_noalloc, ``Dense`` = the ds4moe_dense_* calls.
 """
 from __future__ import annotations
 
@@ -82,6 +82,12 @@ def lib():
             "ds4moe_debug_fail_alloc": (i32, [i32]),
             "ds4moe_status_string": (ctypes.c_char_p, [i32]),
             "ds4moe_abi_version": (u32, []),
+            "ds4moe_dense_create": (i32, [i32, i32, i32, vp, ctypes.POINTER(vp)]),
+            "ds4moe_dense_forward": (i32, [vp, vp, i32, vp, vp]),
+            "ds4moe_dense_get_device_error": (i32, [vp, vp, ctypes.POINTER(u32)]),
+            "ds4moe_dense_destroy": (None, [vp]),
+            "ds4moe_dense_device_bytes": (ctypes.c_uint64, [vp]),
+            "ds4moe_dense_launch_count": (ctypes.c_uint64, [vp]),
         }
         for name, (res, args) in sigs.items():
             f = getattr(L, name)
@@ -238,6 +244,47 @@ class Layer:
         _check(lib().ds4moe_debug_scratch(self._h, which, ctypes.byref(p), ctypes.byref(n)), "ds4moe_debug_scratch")
         itemsize = int(typestr[2:])
         return torch.as_tensor(_CudaArray(p.value, (n.value // itemsize,), typestr), device="cuda")
+
+
+class Dense:
+    """A dense Q8_0 matrix beside the MoE (ds4moe_dense_create): `w` is the
+    canonical [n_out][n_in] Q8_0 matrix as a CUDA uint8 tensor."""
+
+    def __init__(self, n_out: int, n_in: int, w, max_tokens: int = 1):
+        L = lib()
+        h = ctypes.c_void_p()
+        _check(L.ds4moe_dense_create(n_out, n_in, max_tokens, _ptr(w), ctypes.byref(h)), "ds4moe_dense_create")
+        self._h, self.n_out, self.n_in = h, n_out, n_in
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().ds4moe_dense_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, x, y=None, stream=None, n_tok=None):
+        """y = W x (ds4moe_dense_forward); returns y."""
+        import torch
+        n = x.shape[0] if n_tok is None else n_tok
+        if y is None:
+            y = torch.empty((n, self.n_out), dtype=torch.float32, device=x.device)
+        _check(lib().ds4moe_dense_forward(self._h, _ptr(x), n, _ptr(y), _stream(stream)), "ds4moe_dense_forward")
+        return y
+
+    def device_error(self, stream=None) -> int:
+        f = ctypes.c_uint32(0)
+        st = lib().ds4moe_dense_get_device_error(self._h, _stream(stream), ctypes.byref(f))
+        if st not in (0, 5):
+            raise Ds4MoeError(st, "ds4moe_dense_get_device_error")
+        return int(f.value)
+
+    def launch_count(self) -> int:
+        return int(lib().ds4moe_dense_launch_count(self._h))
 
 
 def rmsnorm(x, out, eps: float = 1e-6, stream=None):

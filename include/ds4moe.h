@@ -263,6 +263,43 @@ ds4moe_status ds4moe_profile_enable(ds4moe_layer *h, int32_t on);
 ds4moe_status ds4moe_profile_collect(ds4moe_layer *h);
 ds4moe_status ds4moe_profile_read(const ds4moe_layer *h, double *ms_out, int32_t n, int64_t *calls);
 
+/* ---------------------------------------------------------------------------
+ * Dense Q8_0 product beside the MoE: y = W x for the output head (129280 x
+ * 4096, "OutQ8") and the attention projections, on activations pre-quantised
+ * to int8 per 32-block.
+ * Passages: ds4-rocm fork README, Performance optimizations (the
+ * matmul_q8_0_preq_* kernels: Q8_0 matmuls on pre-quantised activations, the
+ * largest share of decode time beside the MoE); DwarfStar README, Model
+ * Weights (the OutQ8 model name).
+ * Arithmetic (canonical spec): x quantised as for the MoE (CAS step 1); each
+ * output is the CAS row sum of its Q8_0 block terms (d * dx) * I over
+ * S = min(8, n_in/32) contiguous segments, as for an expert row.
+ *
+ * ds4moe_dense_create: w_q8 is the canonical [n_out][n_in] Q8_0 matrix (rows
+ *   of n_in/32 blocks of 34 bytes) in DEVICE memory, read only during the call
+ *   (re-laid out into a handle-owned copy; rows padded to a multiple of 32).
+ *   n_out 1..2^24; n_in a multiple of 32, up to 65536, with n_in/32 a multiple
+ *   of min(8, n_in/32); max_tokens 1..65536 sizes the activation scratch.
+ *   Synchronises. Errors: INVALID_ARG, UNSUPPORTED (n_in too wide for a
+ *   block's shared memory), OOM, CUDA; on error *out is NULL.
+ * ds4moe_dense_forward: y[t][n] = sum_k W[n][k] x[t][k] for t < n_tok
+ *   (x [n_tok][n_in] fp32, y [n_tok][n_out] fp32, overwritten; device
+ *   pointers), enqueued on `stream` (two launches, no allocation, no host
+ *   synchronisation). Built for decode-sized n_tok: the matrix is streamed
+ *   once per pass of up to 8 tokens (fewer for very wide n_in).
+ *   Errors: INVALID_ARG (pointers, n_tok outside 0..max_tokens), CUDA.
+ * ds4moe_dense_get_device_error: as ds4moe_get_device_error, for the dense
+ *   handle's flag (DS4MOE_DEVERR_NONFINITE, DS4MOE_DEVERR_TIMEOUT).
+ * ds4moe_dense_destroy: releases everything (synchronises); NULL is a no-op. */
+typedef struct ds4moe_dense ds4moe_dense;
+ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_tokens, const void *w_q8,
+                                  ds4moe_dense **out);
+ds4moe_status ds4moe_dense_forward(ds4moe_dense *h, const float *x, int32_t n_tok, float *y, void *stream);
+ds4moe_status ds4moe_dense_get_device_error(ds4moe_dense *h, void *stream, uint32_t *flags_out);
+void ds4moe_dense_destroy(ds4moe_dense *h);
+uint64_t ds4moe_dense_device_bytes(const ds4moe_dense *h);
+uint64_t ds4moe_dense_launch_count(const ds4moe_dense *h);
+
 /* Test hooks for failure detection (no counterpart in the pages; they make
  * failures happen on the host side or through a short wait bound, never by
  * faulting the GPU).

@@ -28,6 +28,7 @@ _LIB = os.path.join(_HERE, "libds4synth.so")
 # Tensor tags used to derive independent random streams.
 T_ROUTER, T_BIAS, T_HASH, T_GATE, T_UP, T_DOWN, T_SH_GATE, T_SH_UP, T_SH_DOWN = range(1, 10)
 T_X, T_TOK, T_PERM = 10, 11, 12
+T_DENSE = 13
 
 FMT_F32, FMT_Q8_0, FMT_Q2S = "f32", "q8_0", "q2s"
 
@@ -256,3 +257,20 @@ def gen_token_ids(spec: LayerSpec, seed: int, n_tok: int) -> np.ndarray:
     vocab = spec.vocab if spec.vocab > 0 else 129280
     lib().ds4s_token_ids(t.ctypes.data, n_tok, vocab, key(seed, 0, T_TOK))
     return t
+
+
+def gen_q8_matrix(seed: int, n_out: int, n_in: int, sigma: float = 0.02, nthreads: int = 0) -> np.ndarray:
+    """A dense [n_out][n_in] Q8_0 matrix (canonical bytes), weights ~ N(0, sigma)
+    quantised as the shared expert's are."""
+    assert n_in % 32 == 0
+    out = np.empty(n_out * (n_in // 32) * 34, dtype=np.uint8)
+    lib().ds4s_q8(out.ctypes.data, 0, n_out * (n_in // 32), key(seed, 0, T_DENSE), sigma, nthreads)
+    return out
+
+
+def gen_dense_x(seed: int, n_tok: int, n_in: int) -> np.ndarray:
+    """x[T][n_in] ~ N(0,1) fp32, one stream per token."""
+    x = np.empty((n_tok, n_in), dtype=np.float32)
+    for t in range(n_tok):
+        lib().ds4s_normal_f32(x[t].ctypes.data, n_in, key(seed, t, T_DENSE + 1), 1.0, 0.0, 1)
+    return x

@@ -1,0 +1,70 @@
+"""GPU parity of the dense Q8_0 product (output head, attention projections)
+through the C ABI against the CPU oracle: bit-exact (both sides follow the
+same binary32 order), and within the float tolerance of the MoE spec."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(n_out, n_in, T, seed, max_tokens=None, scale=1.0):
+    import torch
+    import deepseek_v4_flash_gb300 as ds4
+    w = synth.gen_q8_matrix(seed, n_out, n_in)
+    x = synth.gen_dense_x(seed, T, n_in) * np.float32(scale)
+    ref = oracle.get().dense_q8(w, n_out, n_in, x)
+    d = ds4.Dense(n_out, n_in, torch.from_numpy(w).cuda(), max_tokens=max_tokens or T)
+    y = d.forward(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert d.device_error() == 0
+    got = y.cpu().numpy()
+    assert within_tolerance(got, ref)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), \
+        f"not bit-exact: {np.count_nonzero(got != ref)} of {got.size} differ"
+    d.close()
+
+
+@pytest.mark.parametrize("n_out,n_in,T", [
+    (32, 32, 1),        # one item, one block (one segment)
+    (100, 512, 3),      # ragged rows (padding to 128), 16 blocks
+    (64, 96, 2),        # 3 blocks: three one-block segments
+    (96, 768, 9),       # 24 blocks (stages of 3), two passes of 8 tokens
+    (4096, 4096, 5),    # an attention-projection shape
+    (1000, 4096, 17),   # three passes, ragged last pass
+])
+def test_dense_shapes(n_out, n_in, T):
+    _run(n_out, n_in, T, seed=n_out + n_in + T)
+
+
+def test_dense_output_head_one_token():
+    """The output head at full size: 129280 x 4096 (563 MB of Q8_0)."""
+    _run(129280, 4096, 1, seed=777)
+
+
+def test_dense_wide_input():
+    """n_in 16384: passes of 2 tokens (the codes of a pass fit 64 KB)."""
+    _run(256, 16384, 3, seed=5)
+
+
+def test_dense_zero_and_bad_calls():
+    import torch
+    import deepseek_v4_flash_gb300 as ds4
+    w = torch.from_numpy(synth.gen_q8_matrix(1, 64, 256)).cuda()
+    d = ds4.Dense(64, 256, w, max_tokens=4)
+    x = torch.zeros(4, 256, device="cuda")
+    y = d.forward(x)  # all-zero activations: zero scales, zero codes, y = 0
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y) == 0
+    d.forward(x, n_tok=0)
+    with pytest.raises(ds4.Ds4MoeError):
+        d.forward(x, n_tok=5)
+    x[1, 3] = float("nan")
+    d.forward(x)
+    assert d.device_error() & 2
+    d.close()
+    with pytest.raises(ds4.Ds4MoeError):
+        ds4.Dense(64, 100, w)  # n_in not a multiple of 32
