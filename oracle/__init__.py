@@ -24,7 +24,7 @@ _SRC = os.path.join(_HERE, "ds4oracle.c")
 _LIB = os.path.join(_HERE, "libds4oracle.so")
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread"]
 
-FMT = {"f32": 0, "q8_0": 1, "q2s": 2}
+FMT = {"f32": 0, "q8_0": 1, "q2s": 2, "q4s": 3}
 ROUTE = {"learned": 0, "hash": 1}
 
 
@@ -70,6 +70,8 @@ class Oracle:
             "ora_quantize": (None, [vp, ctypes.c_int, vp, vp, vp]),
             "ora_q8_dot": (i32, [vp, vp]),
             "ora_q2s_dot": (None, [vp, ctypes.c_int, vp, vp, vp, vp]),
+            "ora_q4s_dequant_f64": (None, [vp, i64, vp]),
+            "ora_q4s_dot": (None, [vp, ctypes.c_int, vp, vp, vp, vp]),
             "ora_row": (f32, [ctypes.c_int, vp, ctypes.c_int, vp, vp, vp, ctypes.c_int]),
             "ora_exp": (f32, [f32]),
             "ora_sigmoid": (f32, [f32]),
@@ -103,6 +105,12 @@ class Oracle:
         self.L.ora_q2s_dequant_f64(_ptr(np.ascontiguousarray(sbs)), n, _ptr(out))
         return out
 
+    def q4s_dequant(self, sbs: np.ndarray) -> np.ndarray:
+        n = sbs.nbytes // 148
+        out = np.empty(n * 256, np.float64)
+        self.L.ora_q4s_dequant_f64(_ptr(np.ascontiguousarray(sbs)), n, _ptr(out))
+        return out
+
     # -- CAS steps ----------------------------------------------------------
     def quantize(self, v: np.ndarray):
         v = np.ascontiguousarray(v, dtype=np.float32)
@@ -119,6 +127,12 @@ class Oracle:
     def q2s_dot(self, sb: np.ndarray, j: int, xq32: np.ndarray, gs2: np.ndarray):
         A, B = ctypes.c_int32(), ctypes.c_int32()
         self.L.ora_q2s_dot(_ptr(np.ascontiguousarray(sb)), j, _ptr(np.ascontiguousarray(xq32)),
+                           _ptr(np.ascontiguousarray(gs2, dtype=np.int16)), ctypes.byref(A), ctypes.byref(B))
+        return A.value, B.value
+
+    def q4s_dot(self, sb: np.ndarray, j: int, xq32: np.ndarray, gs2: np.ndarray):
+        A, B = ctypes.c_int32(), ctypes.c_int32()
+        self.L.ora_q4s_dot(_ptr(np.ascontiguousarray(sb)), j, _ptr(np.ascontiguousarray(xq32)),
                            _ptr(np.ascontiguousarray(gs2, dtype=np.int16)), ctypes.byref(A), ctypes.byref(B))
         return A.value, B.value
 

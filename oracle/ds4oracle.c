@@ -43,6 +43,7 @@
 #define FMT_F32 0
 #define FMT_Q8_0 1
 #define FMT_Q2S 2
+#define FMT_Q4S 3
 #define ROUTE_LEARNED 0
 #define ROUTE_HASH 1
 
@@ -97,6 +98,25 @@ void ora_q2s_dequant_f64(const uint8_t *sbs, int64_t n_sb, double *out) {
     for (int i = 0; i < 256; i++) {
       int g = i >> 4, sc = p[g] & 15, mn = p[g] >> 4;
       int q = (p[16 + (i >> 2)] >> (2 * (i & 3))) & 3;
+      out[256 * s + i] = d * sc * q - dmin * mn;
+    }
+  }
+}
+
+/* Q4S superblock, 148 bytes: uint8 sm[16] | uint8 qs[128] | fp16 d | fp16
+ * dmin (this library's own 4-bit layout: the pages name a 4-bit variant of
+ * the routed experts, "q2 with the last 6 layers q4", without its bytes).
+ * Group g = i / 16: sc = sm[g] & 15, mn = sm[g] >> 4;
+ * q_i = (qs[i / 2] >> (4 * (i % 2))) & 15; w_i = d * sc * q_i - dmin * mn.
+ * Evaluated in float64 (exact: every product of binary16 values and small
+ * integers fits). */
+void ora_q4s_dequant_f64(const uint8_t *sbs, int64_t n_sb, double *out) {
+  for (int64_t s = 0; s < n_sb; s++) {
+    const uint8_t *sb = sbs + 148 * s;
+    double d = ora_half(rd16(sb + 144)), dmin = ora_half(rd16(sb + 146));
+    for (int i = 0; i < 256; i++) {
+      int g = i / 16, sc = sb[g] & 15, mn = sb[g] >> 4;
+      int q = (sb[16 + i / 2] >> (4 * (i % 2))) & 15;
       out[256 * s + i] = d * sc * q - dmin * mn;
     }
   }
@@ -168,10 +188,32 @@ void ora_q2s_dot(const uint8_t *sb, int j, const int8_t *xq, const int16_t *gs, 
   *B = b;
 }
 
+/* Q4S, 32-block j (0..7) of superblock sb: A and B as for Q2S, with 4-bit
+ * codes. */
+void ora_q4s_dot(const uint8_t *sb, int j, const int8_t *xq, const int16_t *gs, int32_t *A,
+                 int32_t *B) {
+  int32_t a = 0, b = 0;
+  for (int h = 0; h < 2; h++) {
+    int g = 2 * j + h;
+    int sc = sb[g] & 15, mn = sb[g] >> 4;
+    int32_t dot = 0;
+    for (int i = 0; i < 16; i++) {
+      int e = 16 * g + i; /* element index within the superblock */
+      int q = (sb[16 + (e >> 1)] >> (4 * (e & 1))) & 15;
+      dot += q * (int32_t)xq[16 * h + i];
+    }
+    a += sc * dot;
+    b += mn * (int32_t)gs[h];
+  }
+  *A = a;
+  *B = b;
+}
+
 /* ------------------------------------------------------------------------ */
 /* CAS steps 3-4: block float terms and the row sum.                         */
 /*   Q8_0: p_b = (d_b * dx_b) * (float)I_b                                   */
 /*   Q2S : p_b = dx_b * fmaf(d_s, (float)A_b, -(dmin_s * (float)B_b))       */
+/*   Q4S : the same, with A_b and B_b from the 4-bit codes                   */
 /*   Row sum over nb blocks in S equal contiguous segments: each segment is  */
 /*   acc = 0; acc = acc + p_b for increasing b; the segment sums are then    */
 /*   added the same way in increasing segment order. Router rows: S = 8.     */
@@ -217,6 +259,26 @@ static float row_q2s(const uint8_t *row, int K, const int8_t *xq, const float *d
   return tot;
 }
 
+static float row_q4s(const uint8_t *row, int K, const int8_t *xq, const float *dx,
+                     const int16_t *gs, int S) {
+  int nb = K / 32, per = nb / S;
+  float tot = 0.0f;
+  for (int s = 0; s < S; s++) {
+    float acc = 0.0f;
+    for (int b = s * per; b < (s + 1) * per; b++) {
+      const uint8_t *sb = row + 148 * (b / 8);
+      int32_t A, B;
+      ora_q4s_dot(sb, b % 8, xq + 32 * b, gs + 2 * b, &A, &B);
+      float d = ora_half(rd16(sb + 144)), dmin = ora_half(rd16(sb + 146));
+      float m = dmin * (float)B;
+      float p = dx[b] * fmaf(d, (float)A, -m);
+      acc = acc + p;
+    }
+    tot = tot + acc;
+  }
+  return tot;
+}
+
 static float row_f32(const float *w, int K, const float *x, int S) {
   int per = K / S;
   float tot = 0.0f;
@@ -229,13 +291,15 @@ static float row_f32(const float *w, int K, const float *x, int S) {
 }
 
 static size_t row_bytes(int fmt, int K) {
-  return fmt == FMT_Q2S ? (size_t)(K / 256) * 84 : fmt == FMT_Q8_0 ? (size_t)(K / 32) * 34 : (size_t)K * 4;
+  return fmt == FMT_Q2S ? (size_t)(K / 256) * 84 : fmt == FMT_Q4S ? (size_t)(K / 256) * 148
+       : fmt == FMT_Q8_0 ? (size_t)(K / 32) * 34 : (size_t)K * 4;
 }
 
 /* One matrix row against one quantised activation vector. */
 float ora_row(int fmt, const uint8_t *row, int K, const int8_t *xq, const float *dx,
               const int16_t *gs, int S) {
-  return fmt == FMT_Q2S ? row_q2s(row, K, xq, dx, gs, S) : row_q8(row, K, xq, dx, S);
+  return fmt == FMT_Q2S ? row_q2s(row, K, xq, dx, gs, S)
+       : fmt == FMT_Q4S ? row_q4s(row, K, xq, dx, gs, S) : row_q8(row, K, xq, dx, S);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -359,7 +423,7 @@ typedef struct {
 
 /* Row-sum segments of an expert row of K columns (CAS step 4). */
 static int expert_segs(int fmt, int K) {
-  int units = fmt == FMT_Q2S ? K / 256 : K / 32;
+  int units = (fmt == FMT_Q2S || fmt == FMT_Q4S) ? K / 256 : K / 32;
   return units < 8 ? units : 8;
 }
 

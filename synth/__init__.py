@@ -30,7 +30,7 @@ T_ROUTER, T_BIAS, T_HASH, T_GATE, T_UP, T_DOWN, T_SH_GATE, T_SH_UP, T_SH_DOWN = 
 T_X, T_TOK, T_PERM = 10, 11, 12
 T_DENSE = 13
 
-FMT_F32, FMT_Q8_0, FMT_Q2S = "f32", "q8_0", "q2s"
+FMT_F32, FMT_Q8_0, FMT_Q2S, FMT_Q4S = "f32", "q8_0", "q2s", "q4s"
 
 
 def build(force: bool = False) -> str:
@@ -54,13 +54,14 @@ def lib():
         L.ds4s_key.restype = ctypes.c_uint64
         L.ds4s_key.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32]
         L.ds4s_q2s.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_int]
+        L.ds4s_q4s.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_int]
         L.ds4s_q8.argtypes = [u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_int]
         L.ds4s_normal_f32.argtypes = [f32p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_float, ctypes.c_int]
         L.ds4s_uniform_f32.argtypes = [f32p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_float, ctypes.c_int]
         L.ds4s_token_ids.argtypes = [i32p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64]
         L.ds4s_hash_table.argtypes = [i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64, ctypes.c_int]
         L.ds4s_permutation.argtypes = [i32p, ctypes.c_int32, ctypes.c_uint64]
-        for f in ("ds4s_q2s", "ds4s_q8", "ds4s_normal_f32", "ds4s_uniform_f32", "ds4s_token_ids",
+        for f in ("ds4s_q2s", "ds4s_q4s", "ds4s_q8", "ds4s_normal_f32", "ds4s_uniform_f32", "ds4s_token_ids",
                   "ds4s_hash_table", "ds4s_permutation"):
             getattr(L, f).restype = None
         _lib = L
@@ -93,6 +94,7 @@ class LayerSpec:
     route_scale: float = 1.0
     q8_sigma: float = 0.02
     q2s_dsig: float = 0.01
+    q4s_dsig: float = 0.002  # 4-bit codes are 5x wider: about the 2-bit format's weight spread
 
 
 # Tiny layer: every weight Q8_0, fp32 router.
@@ -109,6 +111,11 @@ DS4_HASH = replace(DS4, name="ds4-hash", route="hash", vocab=129280, bias="none"
 MICRO = LayerSpec("micro", 512, 8, 3, 256, 1, "learned", 0, FMT_Q8_0, FMT_Q2S, FMT_Q8_0,
                   router_sigma=0.02, bias="uniform")
 MICRO_HASH = replace(MICRO, name="micro-hash", route="hash", vocab=1000, bias="none")
+# The same shapes with 4-bit routed experts (the "q2 with the last 6 layers
+# q4" variant of the DwarfStar model weights).
+DS4_Q4 = replace(DS4, name="ds4-q4", routed_fmt=FMT_Q4S)
+MICRO_Q4 = replace(MICRO, name="micro-q4", routed_fmt=FMT_Q4S)
+MICRO_Q4_HASH = replace(MICRO_HASH, name="micro-q4-hash", routed_fmt=FMT_Q4S)
 # DS4 router shapes with small experts, for router-only checks.
 DS4_ROUTER_ONLY = replace(DS4, name="ds4-router", ffn=256, routed_fmt=FMT_Q8_0, n_shared=0)
 
@@ -116,8 +123,14 @@ N_STACK_LAYERS = 43
 N_HASH_LAYERS = 3
 
 
-def stack_layer_spec(layer: int) -> LayerSpec:
-    """Layer l of the 43-layer stack: 0-2 hash routed, 3-42 learned."""
+N_Q4_LAYERS = 6
+
+
+def stack_layer_spec(layer: int, q4_tail: bool = False) -> LayerSpec:
+    """Layer l of the 43-layer stack: 0-2 hash routed, 3-42 learned; with
+    q4_tail the last 6 layers' routed experts are 4-bit."""
+    if q4_tail and layer >= N_STACK_LAYERS - N_Q4_LAYERS:
+        return DS4_Q4
     return DS4_HASH if layer < N_HASH_LAYERS else DS4
 
 
@@ -130,6 +143,9 @@ def row_bytes(fmt: str, k: int) -> int:
     if fmt == FMT_Q2S:
         assert k % 256 == 0
         return (k // 256) * 84
+    if fmt == FMT_Q4S:
+        assert k % 256 == 0
+        return (k // 256) * 148
     raise ValueError(fmt)
 
 
@@ -176,6 +192,9 @@ def gen_tensor_into(spec: LayerSpec, seed: int, layer: int, name: str, ptr: int,
     if fmt == FMT_Q2S:
         per = c // 256
         L.ds4s_q2s(ptr, first_row * per, n_rows * per, k, spec.q2s_dsig, nthreads)
+    elif fmt == FMT_Q4S:
+        per = c // 256
+        L.ds4s_q4s(ptr, first_row * per, n_rows * per, k, spec.q4s_dsig, nthreads)
     elif fmt == FMT_Q8_0:
         per = c // 32
         sigma = spec.router_sigma if name == "router_w" else spec.q8_sigma

@@ -163,6 +163,33 @@ void ds4s_q2s(uint8_t *out, int64_t first, int64_t n_superblocks, uint64_t key, 
 }
 
 /* ---------------------------------------------------------------------- */
+/* 4-bit superblock (148 bytes): sm[16] | qs[128] | fp16 d | fp16 dmin.     */
+
+static void q4s_range(int64_t lo, int64_t hi, void *p) {
+  q2s_ctx *c = (q2s_ctx *)p;
+  for (int64_t i = lo; i < hi; i++) {
+    uint64_t s = stream_for(c->key, (uint64_t)(c->first + i));
+    uint8_t *b = c->out + i * 148;
+    for (int w = 0; w < 18; w++) { /* 144 random bytes: sm[16] + qs[128] */
+      uint64_t r = sm_next(&s);
+      memcpy(b + 8 * w, &r, 8);
+    }
+    double n0, n1;
+    normal2(&s, &n0, &n1);
+    uint16_t d = to_half((float)fabs(n0 * c->dsig));
+    uint16_t m = to_half((float)fabs(n1 * c->dsig));
+    memcpy(b + 144, &d, 2);
+    memcpy(b + 146, &m, 2);
+  }
+}
+
+void ds4s_q4s(uint8_t *out, int64_t first, int64_t n_superblocks, uint64_t key, float dsig,
+              int nthreads) {
+  q2s_ctx c = {out, first, key, dsig};
+  parallel_for(n_superblocks, nthreads, q4s_range, &c);
+}
+
+/* ---------------------------------------------------------------------- */
 /* Q8_0 block (34 bytes): fp16 d | int8 q[32].                              */
 
 typedef struct {

@@ -572,6 +572,81 @@ def check_dense_vs_f64(ora, seed=19):
         assert np.all(np.abs(y[t].astype(np.float64) - ref) <= bound)
 
 
+# ------------------------------------------------------------ 4-bit (Q4S) --
+
+def check_q4s_dequant_golden(ora):
+    """The hand-worked 4-bit superblock (golden/q4s_superblock.txt), and the
+    whole block against an independent numpy unpacking."""
+    blk = R.parse_golden(os.path.join(GOLDEN, "q4s_superblock.txt"))[0]
+    f, vals = {}, []
+    for head, rest in blk["_rows"]:
+        if head == "block":
+            continue
+        if head in ("sm", "qs"):
+            f[head] = R.expand_hex(rest)
+        elif head in ("d", "dmin"):
+            f[head] = int(rest[0], 16)
+        else:
+            vals.append((int(head), float(rest[0])))
+    assert len(f["sm"]) == 16 and len(f["qs"]) == 128
+    raw = np.frombuffer(bytes(f["sm"]) + bytes(f["qs"]) + f["d"].to_bytes(2, "little") +
+                        f["dmin"].to_bytes(2, "little"), np.uint8).copy()
+    got = ora.q4s_dequant(raw)
+    ref = R.dequant_q4s(raw, 1, 256)[0]
+    for i, v in vals:
+        assert got[i] == v and ref[i] == v, (i, got[i], ref[i], v)
+    assert np.array_equal(got, ref)
+
+
+def check_q4s_dots_exact(ora, seed=23):
+    """4-bit block dots against int64 brute force on unpacked fields, and the
+    float64 identity sum_i w_i * (dx*xq_i) = dx*(d*A - dmin*B)."""
+    rng = np.random.default_rng(seed)
+    for trial in range(30):
+        sb = rng.integers(0, 256, 148, dtype=np.uint8)
+        sb[144:146] = np.frombuffer(np.float16(rng.uniform(0.0005, 0.004)).tobytes(), np.uint8)
+        sb[146:148] = np.frombuffer(np.float16(rng.uniform(0.0005, 0.004)).tobytes(), np.uint8)
+        x = rng.standard_normal(256).astype(np.float32)
+        xq, dx, gs = ora.quantize(x)
+        d, dmin, sc, mn, q = R.unpack_q4s(sb, 1, 256)
+        w64 = R.dequant_q4s(sb, 1, 256)[0]
+        for j in range(8):
+            A, B = ora.q4s_dot(sb, j, xq[32 * j:32 * j + 32], gs[2 * j:2 * j + 2])
+            qq = q[0, 0]
+            a_ref = sum(int(sc[0, 0, g]) * int(np.dot(qq[16 * g:16 * g + 16], xq[16 * g:16 * g + 16].astype(np.int64)))
+                        for g in (2 * j, 2 * j + 1))
+            b_ref = sum(int(mn[0, 0, g]) * int(xq[16 * g:16 * g + 16].astype(np.int64).sum())
+                        for g in (2 * j, 2 * j + 1))
+            assert (A, B) == (a_ref, b_ref)
+            lhs = float(np.dot(w64[32 * j:32 * j + 32], xq[32 * j:32 * j + 32].astype(np.float64))) * float(dx[j])
+            rhs = float(dx[j]) * (float(d[0, 0]) * A - float(dmin[0, 0]) * B)
+            assert abs(lhs - rhs) <= 1e-12 * (1 + abs(lhs))
+
+
+def check_q4s_row_f64(ora, seed=29):
+    """4-bit rows in CAS order against the float64 dot of dequantised values,
+    within the recursive-summation bound."""
+    rng = np.random.default_rng(seed)
+    for K in (4096, 512):
+        row = np.empty(K // 256 * 148, np.uint8)
+        synth.lib().ds4s_q4s(row.ctypes.data, int(rng.integers(1 << 30)), K // 256, 97, 0.002, 1)
+        w = R.dequant_q4s(row, 1, K)[0]
+        x = rng.standard_normal(K).astype(np.float32)
+        xq, dx, gs = ora.quantize(x)
+        xd = xq.astype(np.float64) * np.repeat(dx.astype(np.float64), 32)
+        terms = (w * xd).reshape(-1, 32).sum(1)
+        for S in (1, 8):
+            got = float(ora.row("q4s", row, K, xq, dx, gs, S))
+            assert abs(got - float(terms.sum())) <= _sum_bound(terms) + 1e-30, (K, S)
+
+
+def check_q4s_layer(ora):
+    """A 4-bit-expert layer: every stage against float64, and the whole layer
+    against the textbook float64 MoE on unquantised activations."""
+    check_expert_stages(ora, synth.MICRO_Q4, seed=53, experts=(0, 5, None))
+    check_layer_vs_textbook(ora, synth.MICRO_Q4, seed=55, T=4, tol=3e-2)
+
+
 ALL_CHECKS = [
     check_binary16, check_q2s_dequant_golden, check_q8_dequant_golden, check_quantize_golden,
     check_quantize_vs_f64, check_block_dots_exact, check_row_sum_f64, check_cas_segment_order,
@@ -579,4 +654,5 @@ ALL_CHECKS = [
     check_rmsnorm, check_topk_golden, check_route_invariants, check_route_k_equals_E, check_hash_route,
     check_expert_stages, check_shared_is_swiglu_mlp, check_layer_vs_textbook, check_combine_linearity,
     check_dense_golden, check_dense_segments, check_dense_identity, check_dense_vs_f64,
+    check_q4s_dequant_golden, check_q4s_dots_exact, check_q4s_row_f64, check_q4s_layer,
 ]

@@ -40,11 +40,32 @@ def dequant_q2s(buf, rows, k):
     return w.reshape(rows, k)
 
 
+def unpack_q4s(buf, rows, k):
+    b = np.frombuffer(np.ascontiguousarray(buf).tobytes(), np.uint8).reshape(rows, k // 256, 148)
+    sm = b[:, :, 0:16].astype(np.int64)
+    qs = b[:, :, 16:144].astype(np.int64)
+    d = b[:, :, 144:146].copy().view(np.float16)[..., 0].astype(np.float64)
+    dmin = b[:, :, 146:148].copy().view(np.float16)[..., 0].astype(np.float64)
+    sc, mn = sm & 15, sm >> 4
+    q = ((qs[:, :, :, None] >> np.array([0, 4])) & 15).reshape(rows, k // 256, 256)
+    return d, dmin, sc, mn, q
+
+
+def dequant_q4s(buf, rows, k):
+    d, dmin, sc, mn, q = unpack_q4s(buf, rows, k)
+    scx = np.repeat(sc, 16, axis=2)
+    mnx = np.repeat(mn, 16, axis=2)
+    w = d[:, :, None] * scx * q - dmin[:, :, None] * mnx
+    return w.reshape(rows, k)
+
+
 def dequant(fmt, buf, rows, k):
     if fmt == "q8_0":
         return dequant_q8(buf, rows, k)
     if fmt == "q2s":
         return dequant_q2s(buf, rows, k)
+    if fmt == "q4s":
+        return dequant_q4s(buf, rows, k)
     return np.asarray(buf, np.float64).reshape(rows, k)
 
 

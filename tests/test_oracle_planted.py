@@ -14,8 +14,12 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "ds4oracle.c")
 
 # (name, exact source text, replacement)
 PLANTS = [
-    ("swap_scale_min", "int sc = sb[g] & 15, mn = sb[g] >> 4;", "int sc = sb[g] >> 4, mn = sb[g] & 15;"),
-    ("min_term_sign", "fmaf(d, (float)A, -m)", "fmaf(d, (float)A, m)"),
+    ("swap_scale_min", "    int sc = sb[g] & 15, mn = sb[g] >> 4;\n    int32_t dot = 0;\n    for (int i = 0; i < 16; i++) {\n      int e = 16 * g + i; /* element index within the superblock */\n      int q = (sb[16 + (e >> 2)]",
+     "    int sc = sb[g] >> 4, mn = sb[g] & 15;\n    int32_t dot = 0;\n    for (int i = 0; i < 16; i++) {\n      int e = 16 * g + i; /* element index within the superblock */\n      int q = (sb[16 + (e >> 2)]"),
+    ("min_term_sign", "rd16(sb + 82));\n      float m = dmin * (float)B;\n      float p = dx[b] * fmaf(d, (float)A, -m);",
+     "rd16(sb + 82));\n      float m = dmin * (float)B;\n      float p = dx[b] * fmaf(d, (float)A, m);"),
+    ("q4s_min_term_sign", "rd16(sb + 146));\n      float m = dmin * (float)B;\n      float p = dx[b] * fmaf(d, (float)A, -m);",
+     "rd16(sb + 146));\n      float m = dmin * (float)B;\n      float p = dx[b] * fmaf(d, (float)A, m);"),
     ("q_bit_order", "int q = (sb[16 + (e >> 2)] >> (2 * (e & 3))) & 3;",
      "int q = (sb[16 + (e >> 2)] >> (6 - 2 * (e & 3))) & 3;"),
     ("round_half_even", "float r = roundf(x[i] / d);", "float r = rintf(x[i] / d);"),
@@ -44,6 +48,12 @@ PLANTS = [
     ("bias_ignored", "key[e] = s[e] + L->router_bias[e];", "key[e] = s[e];"),
     ("expert_one_segment", "return units < 8 ? units : 8;", "return 1;"),
     ("expert_four_segments", "return units < 8 ? units : 8;", "return units < 4 ? units : 4;"),
+    ("q4s_nibble_order", "int q = (sb[16 + (e >> 1)] >> (4 * (e & 1))) & 15;",
+     "int q = (sb[16 + (e >> 1)] >> (4 - 4 * (e & 1))) & 15;"),
+    ("q4s_scale_min_swap", "    int g = 2 * j + h;\n    int sc = sb[g] & 15, mn = sb[g] >> 4;\n    int32_t dot = 0;\n    for (int i = 0; i < 16; i++) {\n      int e = 16 * g + i; /* element index within the superblock */\n      int q = (sb[16 + (e >> 1)]",
+     "    int g = 2 * j + h;\n    int sc = sb[g] >> 4, mn = sb[g] & 15;\n    int32_t dot = 0;\n    for (int i = 0; i < 16; i++) {\n      int e = 16 * g + i; /* element index within the superblock */\n      int q = (sb[16 + (e >> 1)]"),
+    ("q4s_scale_offset", "float d = ora_half(rd16(sb + 144)), dmin = ora_half(rd16(sb + 146));",
+     "float d = ora_half(rd16(sb + 146)), dmin = ora_half(rd16(sb + 144));"),
     ("dense_one_segment", "const int S = expert_segs(FMT_Q8_0, c->K);", "const int S = 1;"),
     ("dense_token_stride", "c->xq + (size_t)t * c->K,\n", "c->xq,\n"),
     ("dense_transposed", "c->y[(size_t)t * c->N + n] = ora_row(", "c->y[(size_t)n * c->T + t] = ora_row("),
