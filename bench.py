@@ -55,6 +55,7 @@ STACK_WORKLOADS = {
     "ds4-stack-43-decode-1": (1, "43-layer stack of DeepSeek-V4-Flash-shaped MoE FFN layers, decode batch 1"),
     "ds4-stack-43-decode-8": (8, "43-layer stack, decode batch 8"),
     "ds4-stack-43-prefill-4096": (4096, "43-layer stack, prefill of 4096 tokens"),
+    "ds4-stack-43-q4tail-decode-1": (1, "43-layer stack with the last 6 layers' routed experts 4-bit, decode batch 1"),
 }
 # Dense Q8_0 products beside the MoE: (n_out, n_in, tokens, description).
 DENSE_WORKLOADS = {
@@ -322,14 +323,14 @@ class Stack:
     handle sized for `max_tokens`. A step carries T tokens through all 43
     layers (RMSNorm, then the MoE FFN added to the residual stream)."""
 
-    def __init__(self, max_tokens, dev, keep=()):
+    def __init__(self, max_tokens, dev, keep=(), q4_tail=False):
         import deepseek_v4_flash_gb300 as ds4
         import torch
         self.ds4, self.dev = ds4, dev
         self.L = synth.N_STACK_LAYERS
         self.layers, self.specs, self.host = [], [], {}
         for l in range(self.L):
-            spec = synth.stack_layer_spec(l)
+            spec = synth.stack_layer_spec(l, q4_tail)
             wl = synth.gen_layer(spec, SEED, l)
             if l in keep:
                 self.host[l] = wl
@@ -475,7 +476,7 @@ def run_stack(args):
         ["ds4-stack-43-decode-8", "ds4-stack-43-prefill-4096"]
     max_t = max([T] + [STACK_WORKLOADS[w][0] for w in extras])
     want_cpu = rank == 0 and not args.no_cpu_baseline
-    stack = Stack(max_t, dev, keep=(0, synth.N_HASH_LAYERS) if want_cpu else ())
+    stack = Stack(max_t, dev, keep=(0, synth.N_HASH_LAYERS) if want_cpu else (), q4_tail="q4tail" in args.workload)
     hbm_peak, _, peak_kind = peaks()
 
     clocks = ClockSampler(local)

@@ -20,8 +20,8 @@ from dataclasses import dataclass
 from . import build as _build
 
 ABI_VERSION = 1
-F32, Q8_0, Q2S = 0, 1, 2
-FMT = {"f32": F32, "q8_0": Q8_0, "q2s": Q2S}
+F32, Q8_0, Q2S, Q4S = 0, 1, 2, 3
+FMT = {"f32": F32, "q8_0": Q8_0, "q2s": Q2S, "q4s": Q4S}
 ROUTE_LEARNED, ROUTE_HASH = 0, 1
 STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_OOM", 4: "ERR_CUDA", 5: "ERR_DEVICE"}
 DEVERR_TOKEN_ID, DEVERR_NONFINITE, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8

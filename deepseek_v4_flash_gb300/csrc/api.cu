@@ -28,7 +28,7 @@ bool is_dev_ptr(const void *p) {
   return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
 }
 
-bool fmt_ok(int f) { return f == DS4MOE_Q8_0 || f == DS4MOE_Q2S; }
+bool fmt_ok(int f) { return f == DS4MOE_Q8_0 || f == DS4MOE_Q2S || f == DS4MOE_Q4S; }
 
 // K must be a whole number of K-steps of the format, split evenly into the
 // row-sum segments of an expert row.
@@ -103,6 +103,7 @@ ds4moe_status cuda_status(cudaError_t e) {
 cudaError_t repack(int fmt, const void *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
                    cudaStream_t s) {
   if (fmt == DS4MOE_Q2S) return repack_q2s((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
+  if (fmt == DS4MOE_Q4S) return repack_q4s((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
   return repack_q8((const uint8_t *)src, dst, n_mat, rows, K, pair, which, s);
 }
 

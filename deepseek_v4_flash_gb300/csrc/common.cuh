@@ -35,6 +35,12 @@ namespace ds4 {
 //               2b+1 each), each word's 2-bit fields transposed so that
 //               ((W >> 2s) & 0x03030303) yields q[4s .. 4s+3] of the group
 //               in element order (one dp4a against 4 consecutive int8 x).
+// Q4S RG16 tile = 16 rows x one 4-bit superblock (256 K), 2368 bytes, the
+// Q2S layout with 4-bit fields: [0,256) sm8 and [256,320) dd as for Q2S;
+// [320,2368) qs: 4 chunks c x 32 lanes x 16 bytes: lane l, chunk c holds the
+// four group words of its block h + 2c (group 2b: elements 0-7, 8-15; group
+// 2b+1 the same), each word's nibbles transposed so that (W & 0x0F0F0F0F)
+// yields elements 0-3 of its eight and ((W >> 4) & 0x0F0F0F0F) elements 4-7.
 // Q8 RG16 tile = 16 rows x one Q8_0 block (32 K), 544 bytes:
 //   [0,32)      d: row r -> fp16 at 2r
 //   [32,544)    q: lane l -> 16 bytes: row r, elements 16h .. 16h+15
@@ -48,15 +54,18 @@ namespace ds4 {
 // K-step of a work item is two consecutive tiles.
 constexpr int TILE_ROWS = 16;
 constexpr int Q2S_TILE = 1344, Q2S_SM = 0, Q2S_DD = 256, Q2S_QS = 320, Q2S_KSTEP = 256;
+constexpr int Q4S_TILE = 2368, Q4S_SM = 0, Q4S_DD = 256, Q4S_QS = 320, Q4S_KSTEP = 256;
 constexpr int Q8_TILE = 544, Q8_Q = 32, Q8_KSTEP = 32;
 constexpr int RQ8_TILE = 2176, RQ8_Q = 128, RQ8_KSTEP = 64;
 
-__host__ __device__ constexpr int tile_bytes(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_TILE : Q8_TILE; }
-__host__ __device__ constexpr int kstep(int fmt) { return fmt == DS4MOE_Q2S ? Q2S_KSTEP : Q8_KSTEP; }
+__host__ __device__ constexpr int tile_bytes(int fmt) {
+  return fmt == DS4MOE_Q2S ? Q2S_TILE : fmt == DS4MOE_Q4S ? Q4S_TILE : Q8_TILE;
+}
+__host__ __device__ constexpr int kstep(int fmt) { return fmt == DS4MOE_Q8_0 ? Q8_KSTEP : Q2S_KSTEP; }
 
 // Row-sum segments (CAS step 4): router rows 8; expert rows
-// min(EXPERT_SEGS, K-steps of the row), a K-step being one superblock (Q2S)
-// or one block (Q8_0).
+// min(EXPERT_SEGS, K-steps of the row), a K-step being one superblock (Q2S,
+// Q4S) or one block (Q8_0).
 constexpr int ROUTER_SEGS = 8;
 constexpr int EXPERT_SEGS = 8;
 __host__ __device__ constexpr int expert_segs(int fmt, int K) {

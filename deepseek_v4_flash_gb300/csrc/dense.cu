@@ -263,7 +263,8 @@ ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_token
   const size_t qb = (size_t)max_tokens * n_in, db = (size_t)max_tokens * (n_in / 32) * 4;
   for (const void *fn : {(const void *)k_dense<1>, (const void *)k_dense<2>, (const void *)k_dense<4>,
                          (const void *)k_dense<8>})
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DN_SMEM_LIMIT);
+    if (e == cudaSuccess)  // the static barriers take their part of the block's shared memory
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DN_SMEM_LIMIT - 1024);
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->w, wb);
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->xq, qb);
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->dx, db);

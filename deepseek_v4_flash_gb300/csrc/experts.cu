@@ -44,13 +44,20 @@ __host__ __device__ constexpr int x_warps(int TT) { return XC + x_epi_warps(TT);
 // level parallelism), down 4 slots of 2688 bytes (one K-step of a routed
 // 32-row item). Down at eight tokens: 2 slots, so that its activations
 // (8 tokens x every slot) fit in shared memory beside the ring.
-__host__ __device__ constexpr int x_ring_nst(int TT, bool down) { return down ? (TT >= 8 ? 2 : 4) : 2; }
-__host__ __device__ constexpr int x_ring_stride(bool down) { return down ? 2688 : 5376; }
-__host__ __device__ constexpr int x_ring_bytes(int TT, bool down) { return x_ring_nst(TT, down) * x_ring_stride(down); }
+// With 4-bit routed experts a down K-step takes 4736 bytes: down then uses
+// 2 slots of that size (about the same bytes in flight).
+__host__ __device__ constexpr int x_ring_nst(int TT, bool down, bool wide) {
+  return down ? (wide ? 2 : (TT >= 8 ? 2 : 4)) : 2;
+}
+__host__ __device__ constexpr int x_ring_stride(bool down, bool wide) { return down ? (wide ? 2 * Q4S_TILE : 2688) : 5376; }
+__host__ __device__ constexpr int x_ring_bytes(int TT, bool down, bool wide) {
+  return x_ring_nst(TT, down, wide) * x_ring_stride(down, wide);
+}
 
 struct XArgs {
   int H, F, E, k, NS, n_shared, T, A_cap;
   int rf, sf, down, K, rows;
+  int wide;                      // a 4-bit matrix in the layer: the wider down ring
   int maxj;                      // item-table entries per block
   const uint8_t *w_r, *w_s;      // routed / shared weights (RG16)
   const int8_t *aq;              // activations in global memory: xq or hq
@@ -188,10 +195,11 @@ struct XSmem {
   int ring, bars, ctrl, part, tab, valid, bkt, act, total;
 };
 
-__host__ __device__ inline XSmem x_smem(int TT, bool down, int mats, int nbk, int act_bytes, int maxj, int T) {
+__host__ __device__ inline XSmem x_smem(int TT, bool down, bool wide, int mats, int nbk, int act_bytes, int maxj,
+                                        int T) {
   XSmem s;
   s.ring = 0;
-  s.bars = XC * x_ring_bytes(TT, down);
+  s.bars = XC * x_ring_bytes(TT, down, wide);
   s.ctrl = s.bars + XC * 8 * 8;
   s.part = s.ctrl + 256;  // bucket barrier, item count, then full[8] and empty[8] slot barriers
   s.tab = s.part + x_slots(TT, down) * XC * mats * TT * TILE_ROWS * 4;
@@ -225,7 +233,7 @@ template <int TT, bool AS, bool DOWN>
 __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(XArgs a) {
   constexpr int XE = x_epi_warps(TT), X_WARPS = x_warps(TT);
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int X_NST = x_ring_nst(TT, DOWN), X_STRIDE = x_ring_stride(DOWN);
+  const int X_NST = x_ring_nst(TT, DOWN, a.wide != 0), X_STRIDE = x_ring_stride(DOWN, a.wide != 0);
   constexpr int PS = x_slots(TT, DOWN);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int mats = 2;       // gate and up (16 rows), or the two 16-row halves of 32 rows (down)
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
   const int nbk = bucket_table_ints(a.A_cap, a.T, a.NS);
   const int act_rows = DOWN ? a.T * a.NS : a.T;
   const int act_bytes = AS ? act_rows * (a.K + (a.K >> 5) * 4 + (a.K >> 4) * 2) : 0;
-  const XSmem L = x_smem(TT, DOWN, mats, nbk, act_bytes, a.maxj, a.T);
+  const XSmem L = x_smem(TT, DOWN, a.wide != 0, mats, nbk, act_bytes, a.maxj, a.T);
   volatile int *s_nitems = (volatile int *)(smem + L.ctrl + 8);  // items of this block (after the bucket)
   int *s_claim = (int *)(smem + L.ctrl + 12);                     // the warp that loads the bucket
   const uint32_t full0 = smem_u32(smem + L.ctrl) + 64, empty0 = full0 + 64;  // slot barriers, 8 bytes apart
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
     ag = (const int16_t *)(smem + L.act + act_rows * a.K + act_rows * (a.K >> 5) * 4);
   }
   pdl_launch_dependents();
-  const uint32_t ring = smem_u32(smem + L.ring + warp * x_ring_bytes(TT, DOWN));
+  const uint32_t ring = smem_u32(smem + L.ring + warp * x_ring_bytes(TT, DOWN, a.wide != 0));
   const uint32_t bar = smem_u32(smem + L.bars + warp * 8 * 8);
   const int nsh = a.n_shared ? a.rows / ROWS : 0, RG = a.rows / ROWS;
   const int G = gridDim.x, c = blockIdx.x;
@@ -480,6 +488,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
           for (int j = 0; j < c_ksps; j++) {
             const uint32_t t = st + j * c_kb;
             if (c_fmt == DS4MOE_Q2S) q2s_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, ag, acc);
+            else if (c_fmt == DS4MOE_Q4S) q4s_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, ag, acc);
             else q8_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, acc);
           }
         }
@@ -652,9 +661,14 @@ static int x_maxj(const ds4moe_layer *h, int T, bool down) {
   return (int)((n + G - 1) / G);
 }
 
+// A 4-bit matrix anywhere in the layer: the down kernel's wider ring slots.
+static bool x_wide(const ds4moe_layer *h) {
+  return h->d.routed_fmt == DS4MOE_Q4S || (h->d.n_shared && h->d.shared_fmt == DS4MOE_Q4S);
+}
+
 static size_t x_smem_bytes(const ds4moe_layer *h, int T, bool down, bool as) {
   const int nbk = bucket_table_ints(h->A_max, T, h->NS);
-  return (size_t)x_smem(x_tt(T), down, 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0, x_maxj(h, T, down), T)
+  return (size_t)x_smem(x_tt(T), down, x_wide(h), 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0, x_maxj(h, T, down), T)
       .total;
 }
 
@@ -680,6 +694,7 @@ cudaError_t launch_experts(const ds4moe_layer *h, int T, float *y, int down, cud
   a.hq = h->hq, a.dh = h->dh, a.gsh = h->gsh, a.hbuf = h->hbuf, a.hticket = h->hticket;
   a.apart = h->apart, a.cticket = h->cticket, a.y = y, a.err = h->err;
   a.maxj = x_maxj(h, T, down != 0);
+  a.wide = x_wide(h) ? 1 : 0;
   a.hlimit = h->wait_limit > 0 ? h->wait_limit : WAIT_LIMIT;
   if (!down) {
     a.K = d.hidden, a.rows = d.ffn, a.w_r = h->gu, a.w_s = h->sgu, a.aq = h->xq, a.ad = h->dx, a.ag = h->gs;

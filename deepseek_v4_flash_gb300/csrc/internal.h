@@ -84,6 +84,8 @@ cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, in
                        cudaStream_t s);
 cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
                       cudaStream_t s);
+cudaError_t repack_q4s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
+                       cudaStream_t s);
 cudaError_t repack_rq8(const uint8_t *src, uint8_t *dst, int rows, int rows_pad, int K, cudaStream_t s);
 cudaError_t check_hash_table(const int32_t *table, int64_t n, int E, int32_t *bad_count, cudaStream_t s);
 

@@ -10,11 +10,12 @@
 //
 // The contraction: for every 32-block b of K the integer block dots of the
 // canonical arithmetic are exact products of small integers, so the kernel
-// feeds them to the tensor cores as fp16 values (sc*q in [0, 45] or int8 q,
-// against int8 activation codes; the min term as mn in [0, 15] against 16-
-// group sums in [-2032, 2032]): every product and every 32-term sum is an
-// integer below 2^24, which the fp32 accumulator holds exactly. Each block
-// gets its own accumulator (A_b, and B_b for the 2-bit format), and the
+// feeds them to the tensor cores as fp16 values (sc*q in [0, 45] for the
+// 2-bit format, [0, 225] for the 4-bit one, or int8 q, against int8
+// activation codes; the min term as mn in [0, 15] against 16-group sums in
+// [-2032, 2032]): every product and every 32-term sum is an integer below
+// 2^24, which the fp32 accumulator holds exactly. Each block gets its own
+// accumulator (A_b, and B_b for the superblock formats), and the
 // epilogue applies the block's float terms and the segment-ordered row sum
 // exactly as the decode path and the CPU evaluation do, so the results are
 // bit-identical to theirs.
@@ -46,7 +47,7 @@ constexpr int PF_CW = 4;   // converter warps
 constexpr int PF_EW = 8;   // epilogue warps
 constexpr int PF_WARPS = 2 + PF_CW + PF_EW;
 constexpr int PF_RS = 2;                 // raw stages
-constexpr int PF_RAW = 16 * Q2S_TILE;    // 21504 bytes, the largest raw stage
+constexpr int PF_RAW = 16 * Q4S_TILE;    // 37888 bytes, the largest raw stage
 constexpr int PF_FS = 4;                 // fp16 operand stages, one 32-block each
 constexpr int PF_TS = 4;                 // TMEM stages of 128 columns
 constexpr int PF_XS = 9;                 // side-data stages, >= PF_FS + PF_TS + 1
@@ -168,6 +169,22 @@ __device__ __forceinline__ void q2s_group_to_h(uint32_t W, uint32_t sc2, uint32_
   hi.w = hfma2_u(prmt(t, E, 0x4342), sc2, nsc2);
 }
 
+// One word of the packed 4-bit layout (element j of eight at byte j, low
+// nibble; element j + 4 high nibble) times its scale: eight fp16 values sc*q
+// in element order, one 16-byte core-matrix row. As above, one rounding of
+// an exact integer below 2^11.
+__device__ __forceinline__ uint4 q4s_word_to_h(uint32_t W, uint32_t sc2, uint32_t nsc2) {
+  const uint32_t E = 0x64646464u;
+  uint4 o;
+  uint32_t t = W & 0x0F0F0F0Fu;
+  o.x = hfma2_u(prmt(t, E, 0x4140), sc2, nsc2);
+  o.y = hfma2_u(prmt(t, E, 0x4342), sc2, nsc2);
+  t = (W >> 4) & 0x0F0F0F0Fu;
+  o.z = hfma2_u(prmt(t, E, 0x4140), sc2, nsc2);
+  o.w = hfma2_u(prmt(t, E, 0x4342), sc2, nsc2);
+  return o;
+}
+
 // fp16x2 bit pattern of two small integers 0 <= a, b < 1024 (exact):
 // (1024 + v) from the exponent pattern 0x6400, minus 1024.
 __device__ __forceinline__ uint32_t h2_small(uint32_t a, uint32_t b) {
@@ -258,9 +275,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       const PfItem it = pf_item<MODE>(a, i, RB);
       if (it.nv <= 0) continue;
-      const bool q2 = it.fmt == DS4MOE_Q2S;
+      const bool sbf = it.fmt != DS4MOE_Q8_0;        // superblock format (Q2S, Q4S)
       const int TB = tile_bytes(it.fmt), KS = a.K / kstep(it.fmt);
-      const int ks_per = q2 ? 1 : 2;                 // K-steps per stage
+      const int ks_per = sbf ? 1 : 2;                // K-steps per stage
       const int nchunk = MODE == 0 ? 8 : 4;          // 16-row groups (gate/up) or 32-row groups (down)
       const int chunk = 2 * TB * ks_per;
       const int nst = KS / ks_per;
@@ -297,7 +314,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const PfItem it = pf_item<MODE>(a, i, RB);
         if (it.nv <= 0) continue;
-        const bool q2 = it.fmt == DS4MOE_Q2S;
+        const bool sbf = it.fmt != DS4MOE_Q8_0;
         for (int b = 0; b < nb; b++, fc++) {
           const int fs = fc % PF_FS, ts = fc % PF_TS;
           if (!pf_wait(B.f_full + 8 * fs, (fc / PF_FS) & 1, abort) ||
@@ -313,7 +330,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
             const uint32_t am = f + PF_F_AMAIN + m * 8192;
             umma_f16(d0 + 32 * m, umma_desc(am, 128, 512), umma_desc(f + PF_F_BMAIN, 128, 512), idesc, 0);
             umma_f16(d0 + 32 * m, umma_desc(am + 256, 128, 512), umma_desc(f + PF_F_BMAIN + 256, 128, 512), idesc, 1);
-            if (q2)
+            if (sbf)
               umma_f16(d0 + 64 + 32 * m, umma_desc(f + PF_F_AMIN + m * 4096, 128, 256),
                        umma_desc(f + PF_F_BMIN, 128, 256), idesc, 0);
           }
@@ -337,9 +354,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       const PfItem it = pf_item<MODE>(a, i, RB);
       if (it.nv <= 0) continue;
-      const bool q2 = it.fmt == DS4MOE_Q2S;
+      const bool q2 = it.fmt == DS4MOE_Q2S, q4 = it.fmt == DS4MOE_Q4S, sbf = q2 || q4;
       const int TB = tile_bytes(it.fmt);
-      const int bpst = q2 ? 8 : 2;  // blocks per raw stage
+      const int bpst = sbf ? 8 : 2;  // blocks per raw stage
       // this thread's token column: pass token 2*(col%16) + col/16
       const int pt = 2 * (col & 15) + (col >> 4);
       int arow = -1;
@@ -387,7 +404,54 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
         }
         const uint32_t raw = sm0 + PF_OFF_RAW + rs * PF_RAW;
         // ---- weights: tiles tau0 and (gate/up) tau0 + 8, row rr
-        if (q2) {
+        if (q4) {
+          // a 32-block of one row is one 16-byte chunk: four words of eight
+          // nibble codes (elements 0-7, 8-15 of group 0, then of group 1)
+          uint4 w[2][NH];
+          uint32_t smb[2][NH];
+#pragma unroll
+          for (int h2 = 0; h2 < NH; h2++) {
+            const uint32_t tile = raw + (tau0 + 8 * h2) * TB;
+            if (bin0 == 0) {
+              const uint32_t ddw = ld_shared_u32(tile + Q4S_DD + 4 * rr);
+              dd_d[h2] = half_bits_to_float(ddw), dd_m[h2] = half_bits_to_float(ddw >> 16);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+              const int bin = bin0 + u, L = 2 * rr + (bin & 1), j = bin >> 1;
+              w[u][h2] = ld_shared_v4(tile + Q4S_QS + 512 * j + 16 * L);
+              smb[u][h2] = ld_shared_u32(tile + Q4S_SM + ((8 * L + 2 * j) & ~3)) >> (8 * ((2 * j) & 3));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 2; u++) {
+            const uint32_t f = sm0 + PF_OFF_F + fsu[u] * PF_F_BYTES;
+            const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
+#pragma unroll
+            for (int h2 = 0; h2 < NH; h2++) {
+              const uint32_t sm = smb[u][h2];
+              const uint32_t sc2a = h2_small(sm & 15, sm & 15), sc2b = h2_small((sm >> 8) & 15, (sm >> 8) & 15);
+              const uint32_t nsc2a = hmul2_u(sc2a, 0xE400E400u), nsc2b = hmul2_u(sc2b, 0xE400E400u);
+              const int tau = tau0 + 8 * h2;
+              const int m = MODE == 0 ? (tau & 1) : 0;
+              const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
+              const uint32_t ar = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
+              uint4 o = q4s_word_to_h(w[u][h2].x, sc2a, nsc2a);
+              sts128(ar, o.x, o.y, o.z, o.w);
+              o = q4s_word_to_h(w[u][h2].y, sc2a, nsc2a);
+              sts128(ar + 128, o.x, o.y, o.z, o.w);
+              o = q4s_word_to_h(w[u][h2].z, sc2b, nsc2b);
+              sts128(ar + 256, o.x, o.y, o.z, o.w);
+              o = q4s_word_to_h(w[u][h2].w, sc2b, nsc2b);
+              sts128(ar + 384, o.x, o.y, o.z, o.w);
+              sts128(f + PF_F_AMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, h2_small((sm >> 4) & 15, (sm >> 12) & 15),
+                     0, 0, 0);
+              asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8),
+                           "f"(dd_d[h2]), "f"(dd_m[h2])
+                           : "memory");
+            }
+          }
+        } else if (q2) {
           uint2 w[2][NH];
           uint32_t smb[2][NH];
 #pragma unroll
@@ -486,7 +550,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
           const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
           const uint4 o = i8x8_to_h(xv[u].x, xv[u].y);
           sts128(f + PF_F_BMAIN + ((col >> 3) * 4 + kq) * 128 + (col & 7) * 16, o.x, o.y, o.z, o.w);
-          if (kq == 0 && q2)
+          if (kq == 0 && sbf)
             sts128(f + PF_F_BMIN + (col >> 3) * 256 + (col & 7) * 16,
                    h_of_int((int)(int16_t)(gv[u] & 0xFFFF)) | (h_of_int(gv[u] >> 16) << 16), 0, 0, 0);
           if (kq == 1) asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsd + 4 * col), "f"(dv[u]) : "memory");
@@ -517,7 +581,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       const PfItem it = pf_item<MODE>(a, i, RB);
       if (it.nv <= 0) continue;
-      const bool q2 = it.fmt == DS4MOE_Q2S;
+      const bool sbf = it.fmt != DS4MOE_Q8_0;
       const int nvp = (it.nv - p + 1) >> 1;  // valid columns 16p + j, j < nvp
       // the pair code of column 16p + lane, loaded now so that finishing the
       // item does not wait on it
@@ -571,7 +635,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
                 // A rewrite without the run-time choice must round the
                 // product on its own (a scalar product, or a second use).
                 unsigned long long term;
-                if (q2) term = f2_mul(dx2, f2_fma(d2, a2, f2_mul(nm2, f2_pack(Bm[j], Bm[j + 1]))));
+                if (sbf) term = f2_mul(dx2, f2_fma(d2, a2, f2_mul(nm2, f2_pack(Bm[j], Bm[j + 1]))));
                 else term = f2_mul(f2_mul(d2, dx2), a2);
                 seg[m][k] = f2_add(seg[m][k], term);
               }

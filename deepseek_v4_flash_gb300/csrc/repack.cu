@@ -52,6 +52,46 @@ __global__ void k_repack_q2s(const uint8_t *__restrict__ src, uint8_t *__restric
   }
 }
 
+// One thread per canonical Q4S superblock (148 bytes) -> its two lanes'
+// slices of a 4-bit RG16 tile (common.cuh). Lane 2r + h owns blocks h + 2c
+// (c = 0..3), both groups of each; a group's 16 nibbles become two words,
+// canonical element j (and j + 4) of each eight at byte j of the word, low
+// (and high) nibble.
+__global__ void k_repack_q4s(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
+                             int KS, int npair, int which) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t total = (int64_t)n_mat * rows * KS;
+  if (i >= total) return;
+  const int s = (int)(i % KS);
+  const int64_t mr = i / KS;
+  const int r = (int)(mr % rows), m = (int)(mr / rows);
+  const uint8_t *sb = src + i * 148;
+  const int rg = r >> 4, rr = r & 15;
+  uint8_t *tile = dst + tile_index(m, rows, rg, KS, s, npair, which) * Q4S_TILE;
+  for (int j = 0; j < 4; j++) tile[Q4S_DD + 4 * rr + j] = sb[144 + j];
+  for (int h = 0; h < 2; h++) {
+    const int lane = 2 * rr + h;
+    for (int c = 0; c < 4; c++) {
+      const int b = h + 2 * c;
+      for (int gi = 0; gi < 2; gi++) {
+        const int g = 2 * b + gi;
+        tile[Q4S_SM + 8 * lane + 2 * c + gi] = sb[g];
+        for (int half = 0; half < 2; half++) {  // elements 8*half .. 8*half+7 of the group
+          uint32_t W = 0;
+          for (int j = 0; j < 4; j++) {
+            const int e0 = 16 * g + 8 * half + j, e1 = e0 + 4;
+            const uint32_t q0 = (sb[16 + (e0 >> 1)] >> (4 * (e0 & 1))) & 15u;
+            const uint32_t q1 = (sb[16 + (e1 >> 1)] >> (4 * (e1 & 1))) & 15u;
+            W |= (q0 | (q1 << 4)) << (8 * j);
+          }
+          uint8_t *o = tile + Q4S_QS + 512 * c + 16 * lane + 4 * (2 * gi + half);
+          o[0] = (uint8_t)W, o[1] = (uint8_t)(W >> 8), o[2] = (uint8_t)(W >> 16), o[3] = (uint8_t)(W >> 24);
+        }
+      }
+    }
+  }
+}
+
 // Expert Q8_0 -> RG16: one thread per canonical block (34 bytes).
 __global__ void k_repack_q8(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
                             int KS, int npair, int which) {
@@ -105,6 +145,15 @@ cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, in
   const int64_t n = (int64_t)n_mat * rows * KS;
   if (n == 0) return cudaSuccess;
   k_repack_q2s<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair == 2 ? 3 : pair ? 2 : 1, which);
+  return cudaGetLastError();
+}
+
+cudaError_t repack_q4s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
+                       cudaStream_t s) {
+  const int KS = K / Q4S_KSTEP;
+  const int64_t n = (int64_t)n_mat * rows * KS;
+  if (n == 0) return cudaSuccess;
+  k_repack_q4s<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair == 2 ? 3 : pair ? 2 : 1, which);
   return cudaGetLastError();
 }
 

@@ -132,6 +132,87 @@ __device__ __forceinline__ void q2s_step(uint32_t t0, int lane, int s, int K, co
   }
 }
 
+// Sum over one 16-weight group of q * x for 4-bit codes: its two words (W0:
+// elements 0-7, W1: 8-15; low nibbles the first four of each eight) against
+// the group's 16 int8 activations.
+__device__ __forceinline__ int grp_dot4(uint32_t W0, uint32_t W1, uint4 x) {
+  constexpr uint32_t M4 = 0x0F0F0F0Fu;
+  const int a = __dp4a((int)((W0 >> 4) & M4), (int)x.y, __dp4a((int)(W0 & M4), (int)x.x, 0));
+  const int b = __dp4a((int)((W1 >> 4) & M4), (int)x.w, __dp4a((int)(W1 & M4), (int)x.z, 0));
+  return a + b;
+}
+
+// One Q4S K-step (superblock s) of the two tiles at t0, t0 + Q4S_TILE: as
+// q2s_step, with lane 2r + h owning blocks h + 2c (c = 0..3) of row r, each
+// block's four group words in chunk c. A_b and B_b are complete in the lane
+// (CAS step 2), the lane computes its blocks' terms (CAS step 3) and trades
+// them with its partner, so that lane h = 0 adds all eight terms to the row
+// chain in block order (CAS step 4). acc of lanes with h = 1 is not used.
+template <int TT, bool ACT_SMEM, bool PACK>
+__device__ __forceinline__ void q4s_step(uint32_t t0, int lane, int s, int K, const int *arow, int nt,
+                                         const int8_t *__restrict__ aq, const float *__restrict__ ad,
+                                         const int16_t *__restrict__ ag, Chains<PACK> (&acc)[TT]) {
+  const int h = lane & 1, r = lane >> 1;
+  uint32_t sc[2][2], mn[2][2];
+  float d[2], dmin[2];
+#pragma unroll
+  for (int m = 0; m < 2; m++) {
+    const uint32_t tm = t0 + m * Q4S_TILE;
+    const uint2 smw = ld_shared_v2(tm + Q4S_SM + 8 * lane);
+    const uint32_t dd = ld_shared_u32(tm + Q4S_DD + 4 * r);
+    sc[m][0] = smw.x & 0x0F0F0F0Fu, mn[m][0] = (smw.x >> 4) & 0x0F0F0F0Fu;
+    sc[m][1] = smw.y & 0x0F0F0F0Fu, mn[m][1] = (smw.y >> 4) & 0x0F0F0F0Fu;
+    d[m] = half_bits_to_float(dd), dmin[m] = half_bits_to_float(dd >> 16);
+  }
+  unsigned long long d2 = 0ull, nm2 = 0ull;
+  if constexpr (PACK) d2 = f2_pack(d[0], d[1]), nm2 = f2_pack(-dmin[0], -dmin[1]);
+  const int nb = K >> 5;
+#pragma unroll
+  for (int c = 0; c < 4; c++) {  // block h + 2c
+    uint4 q[2];
+#pragma unroll
+    for (int m = 0; m < 2; m++) q[m] = ld_shared_v4(t0 + m * Q4S_TILE + Q4S_QS + 512 * c + 16 * lane);
+    const int blk = 8 * s + h + 2 * c;
+#pragma unroll
+    for (int t = 0; t < TT; t++) {
+      if (t >= nt) break;  // warp-uniform: only the unit's valid tokens
+      const int8_t *xr = aq + (size_t)arow[t] * K + 32 * blk;
+      const uint4 x0 = act_load<ACT_SMEM>((const uint4 *)xr);
+      const uint4 x1 = act_load<ACT_SMEM>((const uint4 *)(xr + 16));
+      const uint32_t gsw = act_load<ACT_SMEM>((const uint32_t *)(ag + (size_t)arow[t] * (K >> 4) + 2 * blk));
+      const float dxv = act_load<ACT_SMEM>(ad + (size_t)arow[t] * nb + blk);
+      int A[2], B[2];
+#pragma unroll
+      for (int m = 0; m < 2; m++) {
+        const uint32_t P = __byte_perm((uint32_t)grp_dot4(q[m].x, q[m].y, x0), (uint32_t)grp_dot4(q[m].z, q[m].w, x1),
+                                       0x5410);
+        if (c & 1) {
+          A[m] = dp2a_su<true>(P, sc[m][c >> 1], 0);
+          B[m] = dp2a_su<true>(gsw, mn[m][c >> 1], 0);
+        } else {
+          A[m] = dp2a_su<false>(P, sc[m][c >> 1], 0);
+          B[m] = dp2a_su<false>(gsw, mn[m][c >> 1], 0);
+        }
+        if constexpr (!PACK) {
+          const float mine = q2s_term(dxv, d[m], dmin[m], A[m], B[m]);
+          const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+          acc[t].c[m] = __fadd_rn(__fadd_rn(acc[t].c[m], mine), other);
+        }
+      }
+      if constexpr (PACK) {
+        const unsigned long long mine =
+            f2_mul(f2_pack(dxv, dxv), f2_fma(d2, f2_pack(__int2float_rn(A[0]), __int2float_rn(A[1])),
+                                             f2_mul(nm2, f2_pack(__int2float_rn(B[0]), __int2float_rn(B[1])))));
+        float m0, m1;
+        f2_unpack(mine, m0, m1);
+        const unsigned long long other =
+            f2_pack(__shfl_xor_sync(0xffffffffu, m0, 1), __shfl_xor_sync(0xffffffffu, m1, 1));
+        acc[t].v = f2_add(f2_add(acc[t].v, mine), other);
+      }
+    }
+  }
+}
+
 // One Q8_0 K-step (block s) of the two tiles at t0, t0 + Q8_TILE.
 // Lane 2r + h takes elements 16h .. 16h+15 of row r; the partner lane
 // completes I exactly and both lanes add the same term.

@@ -63,9 +63,17 @@ typedef enum {
  *                 group g = i/16, sc = sm[g] & 15, mn = sm[g] >> 4,
  *                 q_i = (qs[i/4] >> 2*(i%4)) & 3,
  *                 w_i = d*sc*q_i - dmin*mn   (2.625 bits per weight).
- * A matrix [R][K] is R rows of K/32 (Q8_0) or K/256 (Q2S) blocks, rows
+ *   DS4MOE_Q4S  : superblocks of 256 weights, 148 bytes (routed experts of
+ *                 the 4-bit layers; this library's own layout -- the DwarfStar
+ *                 README, Model Weights, names a "q2 with the last 6 layers
+ *                 q4" variant but not its bytes):
+ *                 uint8 sm[16] | uint8 qs[128] | fp16 d | fp16 dmin;
+ *                 group g = i/16, sc = sm[g] & 15, mn = sm[g] >> 4,
+ *                 q_i = (qs[i/2] >> 4*(i%2)) & 15,
+ *                 w_i = d*sc*q_i - dmin*mn   (4.625 bits per weight).
+ * A matrix [R][K] is R rows of K/32 (Q8_0) or K/256 (Q2S, Q4S) blocks, rows
  * contiguous; expert tensors stack their E matrices contiguously. */
-typedef enum { DS4MOE_F32 = 0, DS4MOE_Q8_0 = 1, DS4MOE_Q2S = 2 } ds4moe_fmt;
+typedef enum { DS4MOE_F32 = 0, DS4MOE_Q8_0 = 1, DS4MOE_Q2S = 2, DS4MOE_Q4S = 3 } ds4moe_fmt;
 
 typedef enum { DS4MOE_ROUTE_LEARNED = 0, DS4MOE_ROUTE_HASH = 1 } ds4moe_route_kind;
 
@@ -80,13 +88,13 @@ typedef struct {
   int32_t hidden;       /* H: multiple of 256 (4096 for DeepSeek-V4-Flash)          */
   int32_t n_experts;    /* E routed experts, 1..1024 (256)                          */
   int32_t top_k;        /* k, 1..min(E, 16) (6)                                     */
-  int32_t ffn;          /* F: multiple of 64; of 256 when routed/shared use Q2S (2048) */
+  int32_t ffn;          /* F: multiple of 64; of 256 with Q2S/Q4S matrices (2048)   */
   int32_t n_shared;     /* 0 or 1 shared expert, always added with weight 1         */
   int32_t route;        /* ds4moe_route_kind                                        */
   int32_t vocab;        /* hash routing: table rows (129280); ignored otherwise     */
   int32_t router_fmt;   /* DS4MOE_F32 or DS4MOE_Q8_0 (learned routing)              */
-  int32_t routed_fmt;   /* DS4MOE_Q8_0 or DS4MOE_Q2S                                */
-  int32_t shared_fmt;   /* DS4MOE_Q8_0 or DS4MOE_Q2S                                */
+  int32_t routed_fmt;   /* DS4MOE_Q8_0, DS4MOE_Q2S or DS4MOE_Q4S                    */
+  int32_t shared_fmt;   /* DS4MOE_Q8_0, DS4MOE_Q2S or DS4MOE_Q4S                    */
   float route_scale;    /* multiplies the renormalised routed weights (1.0)         */
   int32_t max_tokens;   /* largest n_tok of any later call, 1..1048576. A call of   */
                         /* fewer than 65 tokens runs on the decode path in chunks  */

@@ -4,7 +4,7 @@ import numpy as np
 
 import synth
 
-FMTS = {"f32": 0, "q8_0": 1, "q2s": 2}
+FMTS = {"f32": 0, "q8_0": 1, "q2s": 2, "q4s": 3}
 
 
 def lib_desc(spec, max_tokens):

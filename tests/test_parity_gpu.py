@@ -113,6 +113,23 @@ def test_ds4_zipf_decode_hot_experts(ora, T):
     run_case(ora, synth.DS4_ZIPF, 85, T)
 
 
+# ---- 4-bit routed experts (the "q2 with the last 6 layers q4" variant)
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 8, 9, 33, 64])
+def test_micro_q4_widths(ora, T):
+    run_case(ora, synth.MICRO_Q4, 91, T, max_tokens=65)
+
+
+@pytest.mark.parametrize("T", [7, 130])
+def test_micro_q4_hash(ora, T):
+    run_case(ora, synth.MICRO_Q4_HASH, 93, T, max_tokens=130)
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_ds4_q4_decode(ora, T):
+    run_case(ora, synth.DS4_Q4, 95, T)
+
+
 def test_ds4_batch_invariance(ora):
     """At the full shape, each of five tokens routed one by one gives the same
     bits as the five in one call (batched routing and expert units against
@@ -342,6 +359,8 @@ def prefill_always(monkeypatch):
     (synth.MICRO, 51, 33), (synth.MICRO, 51, 64),
     (synth.TINY, 53, 4),                 # Q8_0 routed experts, fp32 router
     (synth.MICRO_HASH, 55, 130),         # hash routing
+    (synth.MICRO_Q4, 97, 1), (synth.MICRO_Q4, 97, 40),      # 4-bit routed experts
+    (synth.MICRO_Q4_HASH, 99, 130),
 ])
 def test_prefill_path_bit_exact(ora, prefill_always, spec, seed, T):
     run_case(ora, spec, seed, T, max_tokens=max(T, 64))
@@ -367,6 +386,11 @@ def test_ds4_zipf_prefill_256(ora):
     """Zipf(1.1) expert popularity over 256 tokens: hot experts take several
     passes on the prefill path."""
     run_case(ora, synth.DS4_ZIPF, 63, 256)
+
+
+def test_ds4_q4_prefill_256(ora):
+    """4-bit routed experts at the full layer shape on the prefill path."""
+    run_case(ora, synth.DS4_Q4, 101, 256)
 
 
 def test_decode_and_prefill_paths_agree(ora, monkeypatch):
