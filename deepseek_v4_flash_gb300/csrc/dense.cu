@@ -3,16 +3,24 @@
 //
 // Two kernels, chained with programmatic dependent launch:
 //   k_dense_quant  CAS step 1 on x: one warp per 32-block of a token;
-//   k_dense<TT>    persistent, one block per SM: each warp owns whole items of
-//                  32 output rows (two 16-row tiles per K step, the layout of
-//                  an expert's down matrix) and streams an item's tiles through
-//                  its own ring of 1-D bulk copies. The warp keeps a row's CAS
-//                  segment chain and adds each finished segment to the row sum
-//                  in order (CAS step 4, S = min(8, K/32) as for an expert row),
-//                  so no other warp takes part in a row. The tokens' codes are
-//                  staged in shared memory once per pass of up to TT tokens.
-// Rows are independent, so nothing waits on another block: the weight stream
-// is bounded only by the rings' bytes in flight.
+//   k_dense<TT>    persistent, one block per SM, eight warps. The work is cut
+//                  into units: 32 output rows (two 16-row tiles per K step,
+//                  the layout of an expert's down matrix) times a run of
+//                  whole CAS segments of K. A warp streams its units' tiles
+//                  through its own ring of 1-D bulk copies; lane l owns row
+//                  l of the unit and keeps, per token, the row's segment chain
+//                  (CAS step 3: (d * dx) * I, added in block order).
+//                  Unsplit rows (one unit covers all S segments) add each
+//                  finished segment to the row sum in order (CAS step 4) and
+//                  store y. Split rows store their segment sums.
+//                  The tokens' codes sit in shared memory once per pass of up
+//                  to TT tokens, TT chosen per call from n_tok.
+//   k_dense_fix    (split calls only) adds each split row's S segment sums
+//                  in segment order and stores y.
+// Units go to warps SM-first (unit u to warp u / G of block u % G), so that a
+// small matrix still spreads over every SM; rows are split where that evens
+// out the units per warp. Nothing in the streaming kernel waits on another
+// warp.
 #include <stdlib.h>
 #include <string.h>
 
@@ -20,39 +28,36 @@
 
 #include "common.cuh"
 #include "internal.h"
-#include "tiles.cuh"
 
 struct ds4moe_dense {
-  int N, K, N_pad, max_tokens, device, n_sm;
+  int N, K, N_pad, max_tokens, part_tokens, device, n_sm;
+  int dbg_ks, dbg_nst, dbg_ns;  // launch geometry overrides, 0 = automatic
   uint8_t *w;        // [N_pad/32][K/32][2][Q8 tile]
   int8_t *xq;        // [max_tokens][K]
   float *dx;         // [max_tokens][K/32]
+  float *part;       // [S][part_tokens][N_pad] segment sums of split rows
   uint32_t *err;     // device error flags
   uint64_t bytes, launches;
 };
 
 namespace ds4 {
 
-constexpr int DN_WARPS = 8;              // warps per block, each owning whole items
-constexpr int DN_KB = 2 * Q8_TILE;       // one K step of an item: two 16-row tiles
-constexpr int DN_MAX_KS = 4;             // K steps per ring stage, at most
+constexpr int DN_WARPS = 8;              // warps per block
+constexpr int DN_KB = 2 * Q8_TILE;       // one K step of a unit: two 16-row tiles, 1088 bytes
+constexpr int DN_MAX_KS = 8;             // K steps per ring stage, at most
+constexpr int DN_MAX_NST = 6;            // ring stages per warp, at most
+constexpr int DN_TT_MAX = 8;             // tokens per pass, at most
 constexpr size_t DN_SMEM_LIMIT = 227 * 1024;
-
-// K steps per ring stage: the largest divisor of a segment's blocks up to 4,
-// so that no stage straddles two segments.
-__host__ __device__ inline int dn_ks(int K) {
-  const int nb = K / 32, S = expert_segs(DS4MOE_Q8_0, K), per = nb / S;
-  int ks = per < DN_MAX_KS ? per : DN_MAX_KS;
-  while (ks > 1 && per % ks) ks--;
-  return ks;
-}
+constexpr size_t DN_STATIC = 1024;       // kept for the static barriers
 
 struct DnArgs {
-  int N, K, T, nst;   // nst: ring stages per warp
+  int N, N_pad, K, T;
+  int ks, nst, ns;    // K steps per stage, ring stages per warp, units per row
   const uint8_t *w;
   const int8_t *xq;
   const float *dx;
   float *y;
+  float *part;
   uint32_t *err;
 };
 
@@ -70,135 +75,224 @@ __global__ void __launch_bounds__(256) k_dense_quant(const float *x, int K, int8
   if (lane == 0) dx[(size_t)t * (K / 32) + b] = d;
 }
 
+// 32-element integer dot of a row block and an activation block.
+__device__ __forceinline__ int dn_dot32(const uint4 &q0, const uint4 &q1, const uint4 &x0, const uint4 &x1) {
+  int I = __dp4a((int)q0.x, (int)x0.x, 0);
+  I = __dp4a((int)q0.y, (int)x0.y, I);
+  I = __dp4a((int)q0.z, (int)x0.z, I);
+  I = __dp4a((int)q0.w, (int)x0.w, I);
+  I = __dp4a((int)q1.x, (int)x1.x, I);
+  I = __dp4a((int)q1.y, (int)x1.y, I);
+  I = __dp4a((int)q1.z, (int)x1.z, I);
+  return __dp4a((int)q1.w, (int)x1.w, I);
+}
+
+__device__ __forceinline__ uint32_t dn_lds_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
 template <int TT>
 __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
-  constexpr bool PACK = TT > 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = a.K >> 5, S = expert_segs(DS4MOE_Q8_0, a.K), per = nb / S, ks = dn_ks(a.K);
-  const int sbytes = ks * DN_KB, nstage = nb / ks;
-  const int n_items = (a.N + 31) >> 5, wstride = gridDim.x * DN_WARPS;
-  const int first = blockIdx.x * DN_WARPS + warp;
-  const int my_items = first < n_items ? (n_items - 1 - first) / wstride + 1 : 0;
+  const int nb = a.K >> 5, S = expert_segs(DS4MOE_Q8_0, a.K), per = nb / S;
+  const int ks = a.ks, ns = a.ns, nst = a.nst;
+  const int sbytes = ks * DN_KB;
+  const int nbu = nb / ns, ust = nbu / ks;  // blocks and ring stages of one unit
+  const int sst = per / ks;                 // ring stages of one segment
+  const int n_units = (a.N_pad >> 5) * ns;
+  const int G = gridDim.x, W = G * DN_WARPS, gw = warp * G + blockIdx.x;
+  const int my_units = gw < n_units ? (n_units - 1 - gw) / W + 1 : 0;
   const int n_pass = (a.T + TT - 1) / TT;
   // shared memory: the pass's codes [TT][K], scales [TT][K/32], then the rings
   int8_t *xs = (int8_t *)smem;
   float *ds = (float *)(smem + TT * a.K);
-  const int ring_off = (TT * a.K + TT * (a.K >> 5) * 4 + 127) & ~127;
-  const uint32_t ring = smem_u32(smem + ring_off + warp * a.nst * sbytes);
-  __shared__ uint64_t bars[DN_WARPS][8];
+  const int ring_off = (TT * a.K + TT * nb * 4 + 127) & ~127;
+  const uint32_t ring = smem_u32(smem + ring_off + warp * nst * sbytes);
+  __shared__ uint64_t bars[DN_WARPS][DN_MAX_NST];
   const uint32_t bar = smem_u32(&bars[warp][0]);
   if (lane == 0) {
-    for (int i = 0; i < a.nst; i++) mbar_init(bar + 8 * i, 1);
+    for (int i = 0; i < nst; i++) mbar_init(bar + 8 * i, 1);
     fence_mbar_init();
   }
   __syncwarp();
   const size_t item_bytes = (size_t)nb * DN_KB;
-  // producer cursor over (pass, item, stage) of this warp
-  int pp = 0, pi = 0, pst = 0;
+  // producer cursor over (pass, unit, stage) of this warp; every lane keeps
+  // it, lane 0 issues the copies. A slot is refilled only after every lane
+  // has used the values it loaded from it (the warp barrier at the end of a
+  // stage), so the copy cannot overwrite bytes still to be read.
+  int pp = 0, pu = 0, pst = 0;
   uint32_t g_prod = 0, g_cons = 0;
   auto fill = [&]() {
-    while (pp < n_pass && g_prod - g_cons < (uint32_t)a.nst) {
-      if (pi >= my_items) {
-        pp++, pi = 0, pst = 0;
+    while (pp < n_pass && g_prod - g_cons < (uint32_t)nst) {
+      if (pu >= my_units) {
+        pp++, pu = 0, pst = 0;
         continue;
       }
-      const uint32_t slot = g_prod % a.nst;
+      const int u = gw + pu * W, item = u / ns, part = u - item * ns;
+      const uint32_t slot = g_prod % nst;
       if (lane == 0) {
-        if (g_prod >= (uint32_t)a.nst) fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar + 8 * slot, sbytes);
-        bulk_g2s(ring + slot * sbytes, a.w + (size_t)(first + pi * wstride) * item_bytes + (size_t)pst * sbytes,
+        bulk_g2s(ring + slot * sbytes, a.w + (size_t)item * item_bytes + ((size_t)part * nbu + (size_t)pst * ks) * DN_KB,
                  sbytes, bar + 8 * slot);
       }
       g_prod++;
-      if (++pst == nstage) pst = 0, pi++;
+      if (++pst == ust) pst = 0, pu++;
     }
   };
   fill();  // constant weights, before the codes of x exist
   pdl_launch_dependents();
   pdl_wait();
+  const int m = lane >> 4, rr = lane & 15;  // this lane's row: row rr of tile m
+  const uint32_t lane_off = m * Q8_TILE;
   bool failed = false;
   for (int p = 0; p < n_pass; p++) {
     const int t0 = p * TT, nt = min(TT, a.T - t0);
     __syncthreads();  // the previous pass is done with the staged codes
     {
-      const int nq = nt * a.K / 16, nd = nt * (a.K >> 5);
+      const int nq = nt * a.K / 16, nd = nt * nb;
       const uint4 *src = (const uint4 *)(a.xq + (size_t)t0 * a.K);
       for (int i = threadIdx.x; i < nq; i += blockDim.x) ((uint4 *)xs)[i] = __ldg(src + i);
-      for (int i = threadIdx.x; i < nd; i += blockDim.x) ds[i] = __ldg(a.dx + (size_t)t0 * (a.K >> 5) + i);
+      for (int i = threadIdx.x; i < nd; i += blockDim.x) ds[i] = __ldg(a.dx + (size_t)t0 * nb + i);
     }
     __syncthreads();
-    int arow[TT];
-#pragma unroll
-    for (int i = 0; i < TT; i++) arow[i] = i;
-    // a warp that gave up a wait skips its items but still meets every pass
+    // a warp that gave up a wait skips its units but still meets every pass
     // barrier of its block
-    for (int it = 0; it < my_items && !failed; it++) {
-      Chains<PACK> acc[TT], tot[TT];
+    for (int iu = 0; iu < my_units && !failed; iu++) {
+      const int u = gw + iu * W, item = u / ns, part = u - item * ns;
+      const int row = 32 * item + 16 * m + rr;
+      float acc[TT], tot[TT];
 #pragma unroll
-      for (int i = 0; i < TT; i++) chains_zero(acc[i]), chains_zero(tot[i]);
-      for (int st = 0; st < nstage; st++) {
+      for (int t = 0; t < TT; t++) acc[t] = 0.0f, tot[t] = 0.0f;
+      int seg = part * (nbu / per);
+      for (int st = 0; st < ust; st++) {
         fill();
-        const uint32_t slot = g_cons % a.nst;
-        if (!mbar_wait_bounded(bar + 8 * slot, (g_cons / a.nst) & 1)) {
+        const uint32_t slot = g_cons % nst;
+        if (!mbar_wait_bounded(bar + 8 * slot, (g_cons / nst) & 1)) {
           failed = true;
           break;
         }
-        __syncwarp();
-        const uint32_t tile = ring + slot * sbytes;
-        for (int j = 0; j < ks; j++) {
-          const int s = st * ks + j;
-          q8_step<TT, true, PACK>(tile + j * DN_KB, lane, s, a.K, arow, nt, xs, ds, acc);
-          if ((s + 1) % per == 0) {  // a segment is complete: into the row sum, in order
+        const uint32_t tile = ring + slot * sbytes + lane_off;
+        const int bst = part * nbu + st * ks;
+        // the K steps of the stage, unrolled so that their loads and integer
+        // dots overlap; the float terms join each token's chain in block order
 #pragma unroll
-            for (int i = 0; i < TT; i++) {
-              if constexpr (PACK) tot[i].v = f2_add(tot[i].v, acc[i].v);
-              else tot[i].c[0] = __fadd_rn(tot[i].c[0], acc[i].c[0]), tot[i].c[1] = __fadd_rn(tot[i].c[1], acc[i].c[1]);
-              chains_zero(acc[i]);
+        for (int j = 0; j < DN_MAX_KS; j++) {
+          if (j < ks) {
+            const int b = bst + j;
+            const uint32_t tb = tile + j * DN_KB;
+            const float d = half_bits_to_float(dn_lds_u16(tb + 2 * rr));
+            const uint4 q0 = ld_shared_v4(tb + Q8_Q + 32 * rr), q1 = ld_shared_v4(tb + Q8_Q + 32 * rr + 16);
+#pragma unroll
+            for (int t = 0; t < TT; t++) {
+              if (t < nt) {  // warp-uniform
+                const uint4 *xp = (const uint4 *)(xs + t * a.K + 32 * b);
+                const int I = dn_dot32(q0, q1, xp[0], xp[1]);
+                acc[t] = __fadd_rn(acc[t], __fmul_rn(__fmul_rn(d, ds[t * nb + b]), __int2float_rn(I)));
+              }
             }
           }
         }
-        __syncwarp();
+        if ((st + 1) % sst == 0) {  // a segment is complete (stages never straddle one)
+#pragma unroll
+          for (int t = 0; t < TT; t++) {
+            if (t < nt) {
+              if (ns == 1) tot[t] = __fadd_rn(tot[t], acc[t]);
+              else a.part[((size_t)seg * a.T + t0 + t) * a.N_pad + row] = acc[t];
+            }
+            acc[t] = 0.0f;
+          }
+          seg++;
+        }
+        __syncwarp();  // every lane is done with the slot before it is refilled
         g_cons++;
       }
       if (failed) break;
-      // lanes 2r hold rows r (tile 0) and 16 + r (tile 1) of the item
-      if ((lane & 1) == 0) {
-        const int r0 = 32 * (first + it * wstride) + (lane >> 1);
+      if (ns == 1) {
 #pragma unroll
-        for (int i = 0; i < TT; i++) {
-          if (i < nt) {
-            float v0, v1;
-            chains_get(tot[i], v0, v1);
-            if (r0 < a.N) a.y[(size_t)(t0 + i) * a.N + r0] = v0;
-            if (r0 + 16 < a.N) a.y[(size_t)(t0 + i) * a.N + r0 + 16] = v1;
-          }
-        }
+        for (int t = 0; t < TT; t++)
+          if (t < nt && row < a.N) a.y[(size_t)(t0 + t) * a.N + row] = tot[t];
       }
     }
   }
   if (failed) {
     if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
     // the warp's own copies in flight land before the block may leave
-    for (uint32_t g = g_cons; g < g_prod; g++) (void)mbar_wait_bounded(bar + 8 * (g % a.nst), (g / a.nst) & 1);
+    for (uint32_t g = g_cons; g < g_prod; g++) (void)mbar_wait_bounded(bar + 8 * (g % nst), (g / nst) & 1);
   }
 }
 
-// Tokens per pass for K: the codes of a pass take at most 64 KB.
-static int dn_tt(int K) {
+// Split rows: y[t][r] = the CAS row sum of the S stored segment sums, in
+// segment order. One thread per (token, row).
+__global__ void __launch_bounds__(256) k_dense_fix(const float *__restrict__ part, float *y, int N, int N_pad, int T,
+                                                   int S) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)T * N) return;
+  const int t = (int)(i / N), r = (int)(i - (long long)t * N);
+  float s = 0.0f;
+  for (int sg = 0; sg < S; sg++) s = __fadd_rn(s, __ldcg(part + ((size_t)sg * T + t) * N_pad + r));
+  y[i] = s;
+}
+
+// Tokens per pass, at most, for K: the codes of a pass take at most 64 KB.
+static int dn_tt_cap(int K) {
   const size_t per_tok = (size_t)K + (size_t)(K / 32) * 4;
-  return per_tok * 8 <= 65536 ? 8 : per_tok * 4 <= 65536 ? 4 : per_tok * 2 <= 65536 ? 2 : 1;
+  int tt = DN_TT_MAX;
+  while (tt > 1 && (size_t)tt * per_tok > 65536) tt >>= 1;
+  return tt;
+}
+
+// Tokens per pass for a call of T tokens: the smallest power of two that
+// holds them, up to the cap.
+static int dn_tt(int K, int T) {
+  const int cap = dn_tt_cap(K);
+  int tt = 1;
+  while (tt < T && tt < cap) tt <<= 1;
+  return tt;
 }
 
 static size_t dn_stage_smem(int TT, int K) {
   return ((size_t)TT * K + (size_t)TT * (K / 32) * 4 + 127) & ~(size_t)127;
 }
 
-static int dn_nst(int TT, int K) {
-  const size_t left = DN_SMEM_LIMIT - 1024 - dn_stage_smem(TT, K);  // 1 KB: the static barriers
-  const size_t per_stage = (size_t)DN_WARPS * dn_ks(K) * DN_KB;
-  const size_t n = left / per_stage;
-  return n > 6 ? 6 : (int)n;
+// Ring geometry: the largest K steps per stage (a divisor of a segment's
+// blocks, at most 8) that still leaves every warp two stages, else one K
+// step per stage; stages per warp from the shared memory left. Long stages
+// win: a stage's K steps run unrolled, and each stage costs a wait.
+static void dn_ring(int TT, int K, int &ks, int &nst) {
+  const int nb = K / 32, per = nb / expert_segs(DS4MOE_Q8_0, K);
+  const size_t left = DN_SMEM_LIMIT - DN_STATIC - dn_stage_smem(TT, K);
+  for (ks = per < DN_MAX_KS ? per : DN_MAX_KS; ks > 1; ks--) {
+    if (per % ks) continue;
+    if (left / ((size_t)DN_WARPS * ks * DN_KB) >= 2) break;
+  }
+  const size_t n = left / ((size_t)DN_WARPS * ks * DN_KB);
+  nst = n > DN_MAX_NST ? DN_MAX_NST : (int)n;
+}
+
+// Units per 32-row item: the split (a power of two dividing S) that best
+// evens out the units per warp, the smallest one within 2 % of the best;
+// only for a call of one pass that the segment-sum scratch holds. A split
+// costs a store and a load of S sums per row and token, and the fix-up
+// launch.
+static int dn_split(const ds4moe_dense *h, int T, int TT) {
+  if (T > TT || T > h->part_tokens || !h->part) return 1;
+  const int S = expert_segs(DS4MOE_Q8_0, h->K);
+  const long long items = h->N_pad / 32, W = (long long)h->n_sm * DN_WARPS;
+  auto eff = [&](int ns) {
+    const long long u = items * ns, rounds = (u + W - 1) / W;
+    return (double)u / (double)(rounds * W);
+  };
+  double best = 0.0;
+  for (int ns = 1; ns <= S; ns <<= 1)
+    if (S % ns == 0 && eff(ns) > best) best = eff(ns);
+  for (int ns = 1; ns <= S; ns <<= 1)
+    if (S % ns == 0 && eff(ns) >= best - 0.02) return ns;
+  return 1;
 }
 
 }  // namespace ds4
@@ -227,16 +321,33 @@ void dn_free(ds4moe_dense *h) {
   if (h->w) cudaFree(h->w);
   if (h->xq) cudaFree(h->xq);
   if (h->dx) cudaFree(h->dx);
+  if (h->part) cudaFree(h->part);
   if (h->err) cudaFree(h->err);
 }
 
 template <int TT>
 cudaError_t dn_launch(ds4moe_dense *h, const DnArgs &a0, cudaStream_t s) {
   DnArgs a = a0;
-  a.nst = dn_nst(TT, h->K);
+  dn_ring(TT, h->K, a.ks, a.nst);
+  a.ns = dn_split(h, a.T, TT);
+  if (h->dbg_ks || h->dbg_nst) {
+    const int ks = h->dbg_ks ? h->dbg_ks : a.ks, nst = h->dbg_nst ? h->dbg_nst : a.nst;
+    if (dn_stage_smem(TT, h->K) + (size_t)DN_WARPS * nst * ks * DN_KB <= DN_SMEM_LIMIT - DN_STATIC)
+      a.ks = ks, a.nst = nst;
+  }
+  if (h->dbg_ns) a.ns = (a.T <= TT && a.T <= h->part_tokens) ? h->dbg_ns : 1;
   void *args[] = {&a};
-  const size_t smem = dn_stage_smem(TT, h->K) + (size_t)DN_WARPS * a.nst * dn_ks(h->K) * DN_KB;
-  return launch_pdl((const void *)k_dense<TT>, dim3(h->n_sm), dim3(DN_WARPS * 32), smem, s, args, true);
+  const size_t smem = dn_stage_smem(TT, h->K) + (size_t)DN_WARPS * a.nst * a.ks * DN_KB;
+  cudaError_t e = launch_pdl((const void *)k_dense<TT>, dim3(h->n_sm), dim3(DN_WARPS * 32), smem, s, args, true);
+  h->launches++;
+  if (e == cudaSuccess && a.ns > 1) {
+    int S = expert_segs(DS4MOE_Q8_0, h->K);
+    const long long n = (long long)a.T * h->N;
+    void *fargs[] = {(void *)&a.part, (void *)&a.y, (void *)&a.N, (void *)&a.N_pad, (void *)&a.T, (void *)&S};
+    e = launch_pdl((const void *)k_dense_fix, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, fargs, true);
+    h->launches++;
+  }
+  return e;
 }
 
 }  // namespace
@@ -252,22 +363,29 @@ ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_token
   if (max_tokens < 1 || max_tokens > (1 << 16)) return DS4MOE_ERR_INVALID_ARG;
   if ((long long)max_tokens * n_out >= (1ll << 40)) return DS4MOE_ERR_INVALID_ARG;
   if (!dn_dev_ptr(w_q8)) return DS4MOE_ERR_INVALID_ARG;
-  if (dn_nst(dn_tt(n_in), n_in) < 2) return DS4MOE_ERR_UNSUPPORTED;
+  {
+    int ks, nst;
+    dn_ring(dn_tt_cap(n_in), n_in, ks, nst);
+    if (nst < 2) return DS4MOE_ERR_UNSUPPORTED;
+  }
   ds4moe_dense *h = new (std::nothrow) ds4moe_dense;
   if (!h) return DS4MOE_ERR_OOM;
   memset(h, 0, sizeof(*h));
   h->N = n_out, h->K = n_in, h->N_pad = (n_out + 31) / 32 * 32, h->max_tokens = max_tokens;
+  h->part_tokens = max_tokens < DN_TT_MAX ? max_tokens : DN_TT_MAX;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->device);
   const size_t wb = (size_t)h->N_pad / 32 * (n_in / 32) * DN_KB;
   const size_t qb = (size_t)max_tokens * n_in, db = (size_t)max_tokens * (n_in / 32) * 4;
+  const size_t pb = (size_t)expert_segs(DS4MOE_Q8_0, n_in) * h->part_tokens * h->N_pad * 4;
   for (const void *fn : {(const void *)k_dense<1>, (const void *)k_dense<2>, (const void *)k_dense<4>,
                          (const void *)k_dense<8>})
     if (e == cudaSuccess)  // the static barriers take their part of the block's shared memory
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DN_SMEM_LIMIT - 1024);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(DN_SMEM_LIMIT - DN_STATIC));
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->w, wb);
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->xq, qb);
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->dx, db);
+  if (e == cudaSuccess) e = cudaMalloc((void **)&h->part, pb);
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->err, 64);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->w, 0, wb, 0);  // padding rows stay zero
   if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, 64, 0);
@@ -281,7 +399,7 @@ ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_token
     delete h;
     return st;
   }
-  h->bytes = wb + qb + db + 64;
+  h->bytes = wb + qb + db + pb + 64;
   *out = h;
   return DS4MOE_OK;
 }
@@ -306,15 +424,16 @@ ds4moe_status ds4moe_dense_forward(ds4moe_dense *h, const float *x, int32_t n_to
   }
   if (e == cudaSuccess) {
     DnArgs a = {};
-    a.N = h->N, a.K = K, a.T = n_tok, a.w = h->w, a.xq = h->xq, a.dx = h->dx, a.y = y, a.err = h->err;
-    switch (dn_tt(K)) {
+    a.N = h->N, a.N_pad = h->N_pad, a.K = K, a.T = n_tok;
+    a.w = h->w, a.xq = h->xq, a.dx = h->dx, a.y = y, a.part = h->part, a.err = h->err;
+    switch (dn_tt(K, n_tok)) {
       case 8: e = dn_launch<8>(h, a, s); break;
       case 4: e = dn_launch<4>(h, a, s); break;
       case 2: e = dn_launch<2>(h, a, s); break;
       default: e = dn_launch<1>(h, a, s); break;
     }
   }
-  h->launches += 2;
+  h->launches++;  // the quantisation; dn_launch counts its own
   return dn_status(e);
 }
 
@@ -327,6 +446,16 @@ ds4moe_status ds4moe_dense_get_device_error(ds4moe_dense *h, void *stream, uint3
   if (e != cudaSuccess) return dn_status(e);
   if (flags_out) *flags_out = f;
   return f ? DS4MOE_ERR_DEVICE : DS4MOE_OK;
+}
+
+ds4moe_status ds4moe_dense_debug_config(ds4moe_dense *h, int32_t ks, int32_t nst, int32_t ns) {
+  if (!h || ks < 0 || nst < 0 || ns < 0) return DS4MOE_ERR_INVALID_ARG;
+  const int S = expert_segs(DS4MOE_Q8_0, h->K), per = h->K / 32 / S;
+  if (ks && (ks > DN_MAX_KS || per % ks)) return DS4MOE_ERR_INVALID_ARG;
+  if (nst && (nst < 2 || nst > DN_MAX_NST)) return DS4MOE_ERR_INVALID_ARG;
+  if (ns && S % ns) return DS4MOE_ERR_INVALID_ARG;
+  h->dbg_ks = ks, h->dbg_nst = nst, h->dbg_ns = ns;
+  return DS4MOE_OK;
 }
 
 uint64_t ds4moe_dense_device_bytes(const ds4moe_dense *h) { return h ? h->bytes : 0; }

@@ -287,14 +287,20 @@ ds4moe_status ds4moe_profile_read(const ds4moe_layer *h, double *ms_out, int32_t
  *   of n_in/32 blocks of 34 bytes) in DEVICE memory, read only during the call
  *   (re-laid out into a handle-owned copy; rows padded to a multiple of 32).
  *   n_out 1..2^24; n_in a multiple of 32, up to 65536, with n_in/32 a multiple
- *   of min(8, n_in/32); max_tokens 1..65536 sizes the activation scratch.
- *   Synchronises. Errors: INVALID_ARG, UNSUPPORTED (n_in too wide for a
- *   block's shared memory), OOM, CUDA; on error *out is NULL.
+ *   of min(8, n_in/32); max_tokens 1..65536 sizes the activation scratch
+ *   and the segment-sum scratch of split rows (min(8, n_in/32) x
+ *   min(max_tokens, 8) x n_out floats). Synchronises. Errors: INVALID_ARG,
+ *   UNSUPPORTED (n_in too wide for a block's shared memory), OOM, CUDA; on
+ *   error *out is NULL.
  * ds4moe_dense_forward: y[t][n] = sum_k W[n][k] x[t][k] for t < n_tok
  *   (x [n_tok][n_in] fp32, y [n_tok][n_out] fp32, overwritten; device
- *   pointers), enqueued on `stream` (two launches, no allocation, no host
- *   synchronisation). Built for decode-sized n_tok: the matrix is streamed
- *   once per pass of up to 8 tokens (fewer for very wide n_in).
+ *   pointers), enqueued on `stream` (two launches, three for split rows; no
+ *   allocation, no host synchronisation). Built for decode-sized n_tok: the
+ *   matrix is streamed once per pass of up to 8 tokens (fewer for very wide
+ *   n_in); a call of one pass may split rows over several warps by whole
+ *   segments, whose sums a third launch adds in segment order (the same bits
+ *   as unsplit). Calls on one handle must not run concurrently (shared
+ *   scratch).
  *   Errors: INVALID_ARG (pointers, n_tok outside 0..max_tokens), CUDA.
  * ds4moe_dense_get_device_error: as ds4moe_get_device_error, for the dense
  *   handle's flag (DS4MOE_DEVERR_NONFINITE, DS4MOE_DEVERR_TIMEOUT).
@@ -307,6 +313,16 @@ ds4moe_status ds4moe_dense_get_device_error(ds4moe_dense *h, void *stream, uint3
 void ds4moe_dense_destroy(ds4moe_dense *h);
 uint64_t ds4moe_dense_device_bytes(const ds4moe_dense *h);
 uint64_t ds4moe_dense_launch_count(const ds4moe_dense *h);
+/* ds4moe_dense_debug_config: overrides the dense kernel's launch geometry for
+ *   later calls (a tuning and test hook; the results are the same bits under
+ *   every setting): ks = K steps per ring stage (a divisor of n_in/32/S, at
+ *   most 8), nst = ring stages per warp (2..6, within shared memory), ns =
+ *   units per 32-row item (a divisor of S). 0 keeps the automatic choice of
+ *   that value. A call whose tokens do not fit one pass of the segment-sum
+ *   scratch runs unsplit (ns = 1) whatever ns says; a (ks, nst) that does
+ *   not fit a call's shared memory falls back to the automatic ring.
+ *   Errors: INVALID_ARG (NULL, a value outside its range). */
+ds4moe_status ds4moe_dense_debug_config(ds4moe_dense *h, int32_t ks, int32_t nst, int32_t ns);
 
 /* Test hooks for failure detection (no counterpart in the pages; they make
  * failures happen on the host side or through a short wait bound, never by

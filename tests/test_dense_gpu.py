@@ -40,6 +40,60 @@ def test_dense_shapes(n_out, n_in, T):
     _run(n_out, n_in, T, seed=n_out + n_in + T)
 
 
+@pytest.mark.parametrize("n_out,n_in,T", [
+    (4096, 4096, 3),    # split rows, passes of 4 tokens
+    (4096, 4096, 2),    # split rows, passes of 2 tokens
+    (3000, 1024, 1),    # split rows, ragged last item
+    (300, 2048, 8),     # split rows, a full pass of 8
+])
+def test_dense_split_rows(n_out, n_in, T):
+    """Rows split by segments over several warps (small matrices, one pass):
+    the in-order sum of the stored segment sums gives the unsplit bits."""
+    _run(n_out, n_in, T, seed=3 * n_out + n_in + T, max_tokens=8)
+
+
+def test_dense_repeated_calls():
+    """Calls of different widths on one handle: the arrival counters of split
+    rows start over after every call."""
+    import torch
+    import deepseek_v4_flash_gb300 as ds4
+    n_out, n_in = 2048, 4096
+    w = synth.gen_q8_matrix(41, n_out, n_in)
+    d = ds4.Dense(n_out, n_in, torch.from_numpy(w).cuda(), max_tokens=12)
+    for i, T in enumerate([1, 8, 3, 12, 1, 5]):
+        x = synth.gen_dense_x(100 + i, T, n_in)
+        ref = oracle.get().dense_q8(w, n_out, n_in, x)
+        got = d.forward(torch.from_numpy(x).cuda()).cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"call {i} (T={T}) not bit-exact"
+    assert d.device_error() == 0
+    d.close()
+
+
+def test_dense_launch_geometries_same_bits():
+    """Every ring geometry and row split gives the oracle's bits."""
+    import torch
+    import deepseek_v4_flash_gb300 as ds4
+    n_out, n_in = 1024, 4096
+    w = synth.gen_q8_matrix(43, n_out, n_in)
+    d = ds4.Dense(n_out, n_in, torch.from_numpy(w).cuda(), max_tokens=8)
+    for T in (1, 3, 8):
+        x = synth.gen_dense_x(200 + T, T, n_in)
+        ref = oracle.get().dense_q8(w, n_out, n_in, x).view(np.uint32)
+        xd = torch.from_numpy(x).cuda()
+        for ks, nst, ns in [(1, 6, 1), (2, 3, 2), (4, 2, 4), (8, 2, 8), (16 // 2, 3, 1), (4, 6, 8)]:
+            d.debug_config(ks, nst, ns)
+            got = d.forward(xd).cpu().numpy().view(np.uint32)
+            assert np.array_equal(got, ref), f"T={T} ks={ks} nst={nst} ns={ns}"
+    with pytest.raises(ds4.Ds4MoeError):
+        d.debug_config(3, 0, 0)   # 3 does not divide the 16 blocks of a segment
+    with pytest.raises(ds4.Ds4MoeError):
+        d.debug_config(0, 7, 0)
+    with pytest.raises(ds4.Ds4MoeError):
+        d.debug_config(0, 0, 3)
+    assert d.device_error() == 0
+    d.close()
+
+
 def test_dense_output_head_one_token():
     """The output head at full size: 129280 x 4096 (563 MB of Q8_0)."""
     _run(129280, 4096, 1, seed=777)
