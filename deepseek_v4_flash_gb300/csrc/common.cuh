@@ -229,16 +229,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test with a suspend-time hint: the warp is parked (issuing
+// nothing) until the phase completes or about MBAR_SUSPEND_NS pass.
+constexpr uint32_t MBAR_SUSPEND_NS = 20000;
+__device__ __forceinline__ bool mbar_try_wait_parked(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(MBAR_SUSPEND_NS)
+      : "memory");
+  return ok != 0;
+}
+
 // The bound of every on-chip wait: ~2^31 SM cycles (about a second).
 constexpr long long WAIT_LIMIT = 1ll << 31;
 
 // Bounded wait: gives up after `limit` SM cycles and returns false; callers
-// then raise DS4MOE_DEVERR_TIMEOUT and leave. No sleep between tests: these
-// waits sit on the decode path's latency chain.
+// then raise DS4MOE_DEVERR_TIMEOUT and leave. Between tests the warp is
+// parked by the hardware, so waiting warps take no issue slots from the
+// working ones and wake as soon as the phase completes.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit = WAIT_LIMIT) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_parked(bar, parity)) {
     if (clock64() - t0 > limit) return false;
   }
   return true;

@@ -370,9 +370,10 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
         }
         p_ok = true;
       }
+      // a slot is refilled only after the warp barrier that ends its use:
+      // every lane has consumed the values it loaded from it
       const uint32_t slot = g_prod % X_NST;
       if (lane == 0) {
-        if (g_prod >= X_NST) fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar + 8 * slot, psb);
         bulk_g2s(ring + slot * X_STRIDE, psrc + (size_t)pstage * psb, psb, bar + 8 * slot);
       }
