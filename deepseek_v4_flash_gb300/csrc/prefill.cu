@@ -43,9 +43,9 @@ namespace ds4 {
 
 constexpr int PF_NP = 32;  // tokens per pass (MMA N)
 constexpr int PF_M = 128;  // rows per item (MMA M)
-constexpr int PF_CW = 4;   // converter warps
+constexpr int PF_CW = 4;   // converter warps (weights)
 constexpr int PF_EW = 8;   // epilogue warps
-constexpr int PF_WARPS = 2 + PF_CW + PF_EW;
+constexpr int PF_WARPS = 2 + PF_CW + PF_EW + 1;  // + the token warp
 constexpr int PF_RS = 2;                 // raw stages
 constexpr int PF_RAW = 16 * Q4S_TILE;    // 37888 bytes, the largest raw stage
 constexpr int PF_FS = 4;                 // fp16 operand stages, one 32-block each
@@ -214,18 +214,15 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *smem) {
   return p;
 }
 
-// Bounded wait that also gives up once another role has aborted; sleeps
-// between tests (growing to 256 ns) so that waiting roles do not take issue
+// Bounded wait that also gives up once another role has aborted; the warp
+// is parked by the hardware between tests, so waiting roles take no issue
 // slots from the working ones.
 __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  unsigned ns = 32;
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_parked(bar, parity)) {
     if (*abort) return false;
     if (clock64() - t0 > (1ll << 31)) return false;
-    __nanosleep(ns);
-    ns = ns < 256 ? 2 * ns : 256;
   }
   return true;
 }
@@ -253,9 +250,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
   if (threadIdx.x == 0) {
     *abort = 0;
     for (int i = 0; i < PF_RS; i++) mbar_init(B.raw_full + 8 * i, 1), mbar_init(B.raw_empty + 8 * i, PF_CW);
-    for (int i = 0; i < PF_FS; i++) mbar_init(B.f_full + 8 * i, PF_CW), mbar_init(B.f_empty + 8 * i, 1);
+    for (int i = 0; i < PF_FS; i++) mbar_init(B.f_full + 8 * i, PF_CW + 1), mbar_init(B.f_empty + 8 * i, 1);
     for (int i = 0; i < PF_TS; i++) mbar_init(B.t_full + 8 * i, 1), mbar_init(B.t_empty + 8 * i, PF_EW);
-    for (int i = 0; i < PF_XS; i++) mbar_init(B.x_full + 8 * i, PF_CW);
+    for (int i = 0; i < PF_XS; i++) mbar_init(B.x_full + 8 * i, PF_CW + 1);
     fence_mbar_init();
   }
   // the parts of the min tiles that no block writes stay zero
@@ -347,8 +344,6 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
     // ===================== converters (128 threads)
     const int c = threadIdx.x - 64;
     const int rr = c & 15, tau0 = c >> 4;      // weight rows: tiles tau0 (+8), row rr
-    const int col = c >> 2, kq = c & 3;        // token side: column col, elements 8kq..8kq+7
-    const int cw = warp - 2;
     uint32_t fc = 0, gst = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
@@ -357,27 +352,6 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
       const bool q2 = it.fmt == DS4MOE_Q2S, q4 = it.fmt == DS4MOE_Q4S, sbf = q2 || q4;
       const int TB = tile_bytes(it.fmt);
       const int bpst = sbf ? 8 : 2;  // blocks per raw stage
-      // this thread's token column: pass token 2*(col%16) + col/16
-      const int pt = 2 * (col & 15) + (col >> 4);
-      int arow = -1;
-      if (pt < it.nv) {
-        const int code = __ldg(a.list + it.list_off + pt);
-        arow = MODE == 0 ? (code >> 5) : (code >> 5) * a.NS + (code & 31);
-      }
-      // software prefetch of the token data two blocks ahead
-      uint2 xv[2];
-      int gv[2];
-      float dv[2];
-      auto load_tok = [&](int b, uint2 &x, int &gsv, float &d) {
-        x = make_uint2(0, 0), gsv = 0, d = 0.0f;
-        if (arow >= 0 && b < nb) {
-          x = __ldg((const uint2 *)(a.aq + (size_t)arow * a.K + 32 * b + 8 * kq));
-          if (kq == 0) gsv = __ldg((const int *)(a.ag + (size_t)arow * (a.K >> 4) + 2 * b));
-          if (kq == 1) d = __ldg(a.ad + (size_t)arow * nb + b);
-        }
-      };
-      load_tok(0, xv[0], gv[0], dv[0]);
-      load_tok(1, xv[1], gv[1], dv[1]);
       float dd_d[2] = {0.0f, 0.0f}, dd_m[2] = {0.0f, 0.0f};
       // Two 32-blocks per step (b, b + 1: always in the same raw stage), each
       // phase for both at once, so that the loads, conversions and stores of
@@ -543,20 +517,6 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
             }
           }
         }
-        // ---- tokens: B main (codes), B min (group sums), dx
-#pragma unroll
-        for (int u = 0; u < 2; u++) {
-          const uint32_t f = sm0 + PF_OFF_F + fsu[u] * PF_F_BYTES;
-          const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
-          const uint4 o = i8x8_to_h(xv[u].x, xv[u].y);
-          sts128(f + PF_F_BMAIN + ((col >> 3) * 4 + kq) * 128 + (col & 7) * 16, o.x, o.y, o.z, o.w);
-          if (kq == 0 && sbf)
-            sts128(f + PF_F_BMIN + (col >> 3) * 256 + (col & 7) * 16,
-                   h_of_int((int)(int16_t)(gv[u] & 0xFFFF)) | (h_of_int(gv[u] >> 16) << 16), 0, 0, 0);
-          if (kq == 1) asm volatile("st.shared.f32 [%0], %1;" ::"r"(xsd + 4 * col), "f"(dv[u]) : "memory");
-        }
-        load_tok(b + 2, xv[0], gv[0], dv[0]);
-        load_tok(b + 3, xv[1], gv[1], dv[1]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -570,7 +530,67 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
         }
       }
     }
-    (void)cw;
+    if (!ok) pf_fail(abort, a.err);
+  } else if (warp == PF_WARPS - 1) {
+    // ===================== token warp: lane l fills column l of B (pass
+    // token 2*(l%16) + l/16, so that the epilogue's two halves take the even
+    // and odd tokens) and the scale dx, one 32-block at a time
+    uint32_t fc = 0;
+    bool ok = true;
+    const int pt = 2 * (lane & 15) + (lane >> 4);
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const PfItem it = pf_item<MODE>(a, i, RB);
+      if (it.nv <= 0) continue;
+      const bool sbf = it.fmt != DS4MOE_Q8_0;
+      int arow = -1;
+      if (pt < it.nv) {
+        const int code = __ldg(a.list + it.list_off + pt);
+        arow = MODE == 0 ? (code >> 5) : (code >> 5) * a.NS + (code & 31);
+      }
+      // software prefetch four blocks ahead; slot 0 holds block b
+      uint4 xv[4][2];
+      int gv[4];
+      float dv[4];
+      auto load_tok = [&](int b, uint4 (&x)[2], int &gsv, float &d) {
+        x[0] = make_uint4(0, 0, 0, 0), x[1] = x[0], gsv = 0, d = 0.0f;
+        if (arow >= 0 && b < nb) {
+          const uint4 *src = (const uint4 *)(a.aq + (size_t)arow * a.K + 32 * b);
+          x[0] = __ldg(src), x[1] = __ldg(src + 1);
+          gsv = __ldg((const int *)(a.ag + (size_t)arow * (a.K >> 4) + 2 * b));
+          d = __ldg(a.ad + (size_t)arow * nb + b);
+        }
+      };
+#pragma unroll
+      for (int u = 0; u < 4; u++) load_tok(u, xv[u], gv[u], dv[u]);
+      for (int b = 0; b < nb; b++, fc++) {
+        const int fs = fc % PF_FS, xs = fc % PF_XS;
+        if (fc >= PF_FS && !pf_wait(B.f_empty + 8 * fs, ((fc / PF_FS) - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        const uint32_t f = sm0 + PF_OFF_F + fs * PF_F_BYTES;
+        const uint32_t bm = f + PF_F_BMAIN + (lane >> 3) * 512 + (lane & 7) * 16;
+        uint4 o = i8x8_to_h(xv[0][0].x, xv[0][0].y);
+        sts128(bm, o.x, o.y, o.z, o.w);
+        o = i8x8_to_h(xv[0][0].z, xv[0][0].w);
+        sts128(bm + 128, o.x, o.y, o.z, o.w);
+        o = i8x8_to_h(xv[0][1].x, xv[0][1].y);
+        sts128(bm + 256, o.x, o.y, o.z, o.w);
+        o = i8x8_to_h(xv[0][1].z, xv[0][1].w);
+        sts128(bm + 384, o.x, o.y, o.z, o.w);
+        if (sbf)
+          sts128(f + PF_F_BMIN + (lane >> 3) * 256 + (lane & 7) * 16,
+                 h_of_int((int)(int16_t)(gv[0] & 0xFFFF)) | (h_of_int(gv[0] >> 16) << 16), 0, 0, 0);
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sm0 + PF_OFF_X + xs * PF_X_BYTES + 4 * lane), "f"(dv[0])
+                     : "memory");
+#pragma unroll
+        for (int u = 0; u < 3; u++) xv[u][0] = xv[u + 1][0], xv[u][1] = xv[u + 1][1], gv[u] = gv[u + 1], dv[u] = dv[u + 1];
+        load_tok(b + 4, xv[3], gv[3], dv[3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.f_full + 8 * fs), mbar_arrive(B.x_full + 8 * xs);
+      }
+    }
     if (!ok) pf_fail(abort, a.err);
   } else {
     // ===================== epilogue (8 warps)
@@ -593,6 +613,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
       for (int m = 0; m < MATS; m++)
 #pragma unroll
         for (int k = 0; k < 8; k++) seg[m][k] = 0ull, tot[m][k] = 0ull;
+      int segleft = bseg;  // blocks left in the current segment
       for (int b = 0; b < nb; b++, fc++) {
         const int ts = fc % PF_TS, xs = fc % PF_XS;
         if (!pf_wait(B.t_full + 8 * ts, (fc / PF_TS) & 1, abort) ||
@@ -642,7 +663,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
             }
           }
         }
-        if ((b + 1) % bseg == 0) {
+        if (--segleft == 0) {
+          segleft = bseg;
 #pragma unroll
           for (int m = 0; m < MATS; m++)
 #pragma unroll
