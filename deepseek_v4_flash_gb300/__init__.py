@@ -88,7 +88,7 @@ def lib():
             "ds4moe_dense_destroy": (None, [vp]),
             "ds4moe_dense_device_bytes": (ctypes.c_uint64, [vp]),
             "ds4moe_dense_launch_count": (ctypes.c_uint64, [vp]),
-            "ds4moe_dense_debug_config": (i32, [vp, i32, i32, i32]),
+            "ds4moe_dense_debug_config": (i32, [vp, i32, i32, i32, i32]),
         }
         for name, (res, args) in sigs.items():
             f = getattr(L, name)
@@ -287,11 +287,12 @@ class Dense:
     def launch_count(self) -> int:
         return int(lib().ds4moe_dense_launch_count(self._h))
 
-    def debug_config(self, ks=0, nst=0, ns=0):
-        """Override the kernel's K steps per stage, stages per warp and units
-        per 32 rows (0: automatic); a tuning and test hook
-        (ds4moe_dense_debug_config)."""
-        _check(lib().ds4moe_dense_debug_config(self._h, int(ks), int(nst), int(ns)), "ds4moe_dense_debug_config")
+    def debug_config(self, ks=0, nst=0, ns=0, tc=0):
+        """Override the kernel's K steps per stage, stages per warp, units per
+        32 rows and block-dot step (tc 1: dp4a, 2: tensor cores; 0:
+        automatic); a tuning and test hook (ds4moe_dense_debug_config)."""
+        _check(lib().ds4moe_dense_debug_config(self._h, int(ks), int(nst), int(ns), int(tc)),
+               "ds4moe_dense_debug_config")
 
 
 def rmsnorm(x, out, eps: float = 1e-6, stream=None):

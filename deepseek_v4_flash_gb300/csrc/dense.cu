@@ -3,13 +3,19 @@
 //
 // Two kernels, chained with programmatic dependent launch:
 //   k_dense_quant  CAS step 1 on x: one warp per 32-block of a token;
-//   k_dense<TT>    persistent, one block per SM, eight warps. The work is cut
+//   k_dense<TT,MMA> persistent, one block per SM, eight warps. The work is cut
 //                  into units: 32 output rows (two 16-row tiles per K step,
 //                  the layout of an expert's down matrix) times a run of
 //                  whole CAS segments of K. A warp streams its units' tiles
 //                  through its own ring of 1-D bulk copies; lane l owns row
 //                  l of the unit and keeps, per token, the row's segment chain
 //                  (CAS step 3: (d * dx) * I, added in block order).
+//                  Calls of two or more tokens take the block dots I of 16
+//                  rows x 8 tokens from one int8 tensor-core instruction
+//                  (mma.sync m16n8k32: the Q8_0 codes are already int8, and
+//                  the int32 sums are exact); lane (g, t) then keeps the
+//                  chains of rows g, g + 8 of both tiles for tokens 2t,
+//                  2t + 1.
 //                  Unsplit rows (one unit covers all S segments) add each
 //                  finished segment to the row sum in order (CAS step 4) and
 //                  store y. Split rows store their segment sums.
@@ -32,6 +38,7 @@
 struct ds4moe_dense {
   int N, K, N_pad, max_tokens, part_tokens, device, n_sm;
   int dbg_ks, dbg_nst, dbg_ns;  // launch geometry overrides, 0 = automatic
+  int dbg_tc;                   // 0 automatic, 1 dp4a path only, 2 tensor-core path where it fits
   uint8_t *w;        // [N_pad/32][K/32][2][Q8 tile]
   int8_t *xq;        // [max_tokens][K]
   float *dx;         // [max_tokens][K/32]
@@ -93,8 +100,42 @@ __device__ __forceinline__ uint32_t dn_lds_u16(uint32_t addr) {
   return v;
 }
 
-template <int TT>
+// ldmatrix: four 8x8 b16 matrices; lane i gives the address of row i % 8 of
+// matrix i / 8 and receives, from each matrix, bytes 4*(i%4)..+3 of row i/4.
+__device__ __forceinline__ void dn_ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A B for A 16x32 (rows, K) and B 32x8 (K, tokens) of int8: the exact
+// int32 block dots of 16 rows and 8 tokens. Lane (g, t) = (lane / 4,
+// lane % 4) holds A rows g and g + 8 at K 4t..4t+3 and 16+4t..16+4t+3, B
+// token g at the same K, and D rows g, g + 8 for tokens 2t, 2t + 1.
+__device__ __forceinline__ void dn_mma_s8(const uint32_t (&a)[4], uint32_t b0, uint32_t b1, int (&d)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+}
+
+// The terms (d_r * dx_k) * I of one row r for the lane's two tokens, added
+// to the row's packed pair of chains; the second products are scalar (a
+// packed product whose only use is a packed add would be fused into one
+// rounding).
+__device__ __forceinline__ void dn_mma_terms(unsigned long long &acc, float d, unsigned long long dx2, int i0, int i1) {
+  float dd0, dd1;
+  f2_unpack(f2_mul(f2_pack(d, d), dx2), dd0, dd1);
+  acc = f2_add(acc, f2_pack(__fmul_rn(dd0, __int2float_rn(i0)), __fmul_rn(dd1, __int2float_rn(i1))));
+}
+
+// MMA = false: lane l owns row l of the unit and a chain per token (TT
+// tokens per pass, dp4a dots). MMA = true: eight tokens per pass on the
+// tensor cores (mma.sync m16n8k32, int8), lane (g, t) owns rows g, g + 8 of
+// both tiles for tokens 2t, 2t + 1.
+template <int TT, bool MMA>
 __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
+  static_assert(!MMA || TT == 8, "the tensor-core step takes eight tokens");
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = a.K >> 5, S = expert_segs(DS4MOE_Q8_0, a.K), per = nb / S;
@@ -145,8 +186,12 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
   fill();  // constant weights, before the codes of x exist
   pdl_launch_dependents();
   pdl_wait();
-  const int m = lane >> 4, rr = lane & 15;  // this lane's row: row rr of tile m
-  const uint32_t lane_off = m * Q8_TILE;
+  // dp4a step: row rr of tile m; tensor-core step: g, t4 as above, and the
+  // ldmatrix row address of this lane within a tile
+  const int m = lane >> 4, rr = lane & 15;
+  const int g = lane >> 2, t4 = lane & 3;
+  const uint32_t lm_off = Q8_Q + 32 * (((lane >> 3) & 1) * 8 + (lane & 7)) + 16 * (lane >> 4);
+  const uint32_t xs_s = smem_u32(xs);
   bool failed = false;
   for (int p = 0; p < n_pass; p++) {
     const int t0 = p * TT, nt = min(TT, a.T - t0);
@@ -162,10 +207,15 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
     // barrier of its block
     for (int iu = 0; iu < my_units && !failed; iu++) {
       const int u = gw + iu * W, item = u / ns, part = u - item * ns;
-      const int row = 32 * item + 16 * m + rr;
-      float acc[TT], tot[TT];
+      float acc[MMA ? 1 : TT], tot[MMA ? 1 : TT];
+      unsigned long long macc[2][2], mtot[2][2];  // [tile][row g, g + 8]: tokens (2t4, 2t4 + 1)
+      if constexpr (MMA) {
 #pragma unroll
-      for (int t = 0; t < TT; t++) acc[t] = 0.0f, tot[t] = 0.0f;
+        for (int i = 0; i < 4; i++) macc[i >> 1][i & 1] = 0ull, mtot[i >> 1][i & 1] = 0ull;
+      } else {
+#pragma unroll
+        for (int t = 0; t < TT; t++) acc[t] = 0.0f, tot[t] = 0.0f;
+      }
       int seg = part * (nbu / per);
       for (int st = 0; st < ust; st++) {
         fill();
@@ -174,35 +224,69 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
           failed = true;
           break;
         }
-        const uint32_t tile = ring + slot * sbytes + lane_off;
+        const uint32_t stage = ring + slot * sbytes;
         const int bst = part * nbu + st * ks;
         // the K steps of the stage, unrolled so that their loads and integer
-        // dots overlap; the float terms join each token's chain in block order
+        // dots overlap; the float terms join each chain in block order
 #pragma unroll
         for (int j = 0; j < DN_MAX_KS; j++) {
           if (j < ks) {
             const int b = bst + j;
-            const uint32_t tb = tile + j * DN_KB;
-            const float d = half_bits_to_float(dn_lds_u16(tb + 2 * rr));
-            const uint4 q0 = ld_shared_v4(tb + Q8_Q + 32 * rr), q1 = ld_shared_v4(tb + Q8_Q + 32 * rr + 16);
+            if constexpr (MMA) {
+              const uint32_t b0 = ld_shared_u32(xs_s + g * a.K + 32 * b + 4 * t4);
+              const uint32_t b1 = ld_shared_u32(xs_s + g * a.K + 32 * b + 16 + 4 * t4);
+              const unsigned long long dx2 = f2_pack(ds[(2 * t4) * nb + b], ds[(2 * t4 + 1) * nb + b]);
 #pragma unroll
-            for (int t = 0; t < TT; t++) {
-              if (t < nt) {  // warp-uniform
-                const uint4 *xp = (const uint4 *)(xs + t * a.K + 32 * b);
-                const int I = dn_dot32(q0, q1, xp[0], xp[1]);
-                acc[t] = __fadd_rn(acc[t], __fmul_rn(__fmul_rn(d, ds[t * nb + b]), __int2float_rn(I)));
+              for (int mt = 0; mt < 2; mt++) {
+                const uint32_t tb = stage + j * DN_KB + mt * Q8_TILE;
+                uint32_t af[4];
+                dn_ldsm_x4(tb + lm_off, af[0], af[1], af[2], af[3]);
+                int dv[4];
+                dn_mma_s8(af, b0, b1, dv);
+                dn_mma_terms(macc[mt][0], half_bits_to_float(dn_lds_u16(tb + 2 * g)), dx2, dv[0], dv[1]);
+                dn_mma_terms(macc[mt][1], half_bits_to_float(dn_lds_u16(tb + 2 * (g + 8))), dx2, dv[2], dv[3]);
+              }
+            } else {
+              const uint32_t tb = stage + j * DN_KB + m * Q8_TILE;
+              const float d = half_bits_to_float(dn_lds_u16(tb + 2 * rr));
+              const uint4 q0 = ld_shared_v4(tb + Q8_Q + 32 * rr), q1 = ld_shared_v4(tb + Q8_Q + 32 * rr + 16);
+#pragma unroll
+              for (int t = 0; t < TT; t++) {
+                if (t < nt) {  // warp-uniform
+                  const uint4 *xp = (const uint4 *)(xs + t * a.K + 32 * b);
+                  const int I = dn_dot32(q0, q1, xp[0], xp[1]);
+                  acc[t] = __fadd_rn(acc[t], __fmul_rn(__fmul_rn(d, ds[t * nb + b]), __int2float_rn(I)));
+                }
               }
             }
           }
         }
         if ((st + 1) % sst == 0) {  // a segment is complete (stages never straddle one)
+          if constexpr (MMA) {
 #pragma unroll
-          for (int t = 0; t < TT; t++) {
-            if (t < nt) {
-              if (ns == 1) tot[t] = __fadd_rn(tot[t], acc[t]);
-              else a.part[((size_t)seg * a.T + t0 + t) * a.N_pad + row] = acc[t];
+            for (int i = 0; i < 4; i++) {
+              const int mt = i >> 1, h = i & 1;
+              if (ns == 1) {
+                mtot[mt][h] = f2_add(mtot[mt][h], macc[mt][h]);
+              } else {
+                const int row = 32 * item + 16 * mt + g + 8 * h;
+                float v0, v1;
+                f2_unpack(macc[mt][h], v0, v1);
+                if (2 * t4 < nt) a.part[((size_t)seg * a.T + t0 + 2 * t4) * a.N_pad + row] = v0;
+                if (2 * t4 + 1 < nt) a.part[((size_t)seg * a.T + t0 + 2 * t4 + 1) * a.N_pad + row] = v1;
+              }
+              macc[mt][h] = 0ull;
             }
-            acc[t] = 0.0f;
+          } else {
+            const int row = 32 * item + 16 * m + rr;
+#pragma unroll
+            for (int t = 0; t < TT; t++) {
+              if (t < nt) {
+                if (ns == 1) tot[t] = __fadd_rn(tot[t], acc[t]);
+                else a.part[((size_t)seg * a.T + t0 + t) * a.N_pad + row] = acc[t];
+              }
+              acc[t] = 0.0f;
+            }
           }
           seg++;
         }
@@ -211,16 +295,31 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
       }
       if (failed) break;
       if (ns == 1) {
+        if constexpr (MMA) {
 #pragma unroll
-        for (int t = 0; t < TT; t++)
-          if (t < nt && row < a.N) a.y[(size_t)(t0 + t) * a.N + row] = tot[t];
+          for (int i = 0; i < 4; i++) {
+            const int mt = i >> 1, h = i & 1;
+            const int row = 32 * item + 16 * mt + g + 8 * h;
+            float v0, v1;
+            f2_unpack(mtot[mt][h], v0, v1);
+            if (row < a.N) {
+              if (2 * t4 < nt) a.y[(size_t)(t0 + 2 * t4) * a.N + row] = v0;
+              if (2 * t4 + 1 < nt) a.y[(size_t)(t0 + 2 * t4 + 1) * a.N + row] = v1;
+            }
+          }
+        } else {
+          const int row = 32 * item + 16 * m + rr;
+#pragma unroll
+          for (int t = 0; t < TT; t++)
+            if (t < nt && row < a.N) a.y[(size_t)(t0 + t) * a.N + row] = tot[t];
+        }
       }
     }
   }
   if (failed) {
     if (lane == 0) raise_flag(a.err, DS4MOE_DEVERR_TIMEOUT);
     // the warp's own copies in flight land before the block may leave
-    for (uint32_t g = g_cons; g < g_prod; g++) (void)mbar_wait_bounded(bar + 8 * (g % nst), (g / nst) & 1);
+    for (uint32_t gg = g_cons; gg < g_prod; gg++) (void)mbar_wait_bounded(bar + 8 * (gg % nst), (gg / nst) & 1);
   }
 }
 
@@ -325,7 +424,7 @@ void dn_free(ds4moe_dense *h) {
   if (h->err) cudaFree(h->err);
 }
 
-template <int TT>
+template <int TT, bool MMA>
 cudaError_t dn_launch(ds4moe_dense *h, const DnArgs &a0, cudaStream_t s) {
   DnArgs a = a0;
   dn_ring(TT, h->K, a.ks, a.nst);
@@ -338,7 +437,7 @@ cudaError_t dn_launch(ds4moe_dense *h, const DnArgs &a0, cudaStream_t s) {
   if (h->dbg_ns) a.ns = (a.T <= TT && a.T <= h->part_tokens) ? h->dbg_ns : 1;
   void *args[] = {&a};
   const size_t smem = dn_stage_smem(TT, h->K) + (size_t)DN_WARPS * a.nst * a.ks * DN_KB;
-  cudaError_t e = launch_pdl((const void *)k_dense<TT>, dim3(h->n_sm), dim3(DN_WARPS * 32), smem, s, args, true);
+  cudaError_t e = launch_pdl((const void *)k_dense<TT, MMA>, dim3(h->n_sm), dim3(DN_WARPS * 32), smem, s, args, true);
   h->launches++;
   if (e == cudaSuccess && a.ns > 1) {
     int S = expert_segs(DS4MOE_Q8_0, h->K);
@@ -378,8 +477,9 @@ ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_token
   const size_t wb = (size_t)h->N_pad / 32 * (n_in / 32) * DN_KB;
   const size_t qb = (size_t)max_tokens * n_in, db = (size_t)max_tokens * (n_in / 32) * 4;
   const size_t pb = (size_t)expert_segs(DS4MOE_Q8_0, n_in) * h->part_tokens * h->N_pad * 4;
-  for (const void *fn : {(const void *)k_dense<1>, (const void *)k_dense<2>, (const void *)k_dense<4>,
-                         (const void *)k_dense<8>})
+  for (const void *fn : {(const void *)k_dense<1, false>, (const void *)k_dense<2, false>,
+                         (const void *)k_dense<4, false>, (const void *)k_dense<8, false>,
+                         (const void *)k_dense<8, true>})
     if (e == cudaSuccess)  // the static barriers take their part of the block's shared memory
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(DN_SMEM_LIMIT - DN_STATIC));
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->w, wb);
@@ -426,11 +526,19 @@ ds4moe_status ds4moe_dense_forward(ds4moe_dense *h, const float *x, int32_t n_to
     DnArgs a = {};
     a.N = h->N, a.N_pad = h->N_pad, a.K = K, a.T = n_tok;
     a.w = h->w, a.xq = h->xq, a.dx = h->dx, a.y = y, a.part = h->part, a.err = h->err;
-    switch (dn_tt(K, n_tok)) {
-      case 8: e = dn_launch<8>(h, a, s); break;
-      case 4: e = dn_launch<4>(h, a, s); break;
-      case 2: e = dn_launch<2>(h, a, s); break;
-      default: e = dn_launch<1>(h, a, s); break;
+    // two or more tokens: the tensor-core step (passes of eight tokens),
+    // where eight tokens' codes fit the pass buffer
+    const bool fits = dn_tt_cap(K) == DN_TT_MAX;
+    const bool tc = fits && (h->dbg_tc == 2 || (h->dbg_tc == 0 && n_tok >= 2));
+    if (tc) {
+      e = dn_launch<8, true>(h, a, s);
+    } else {
+      switch (dn_tt(K, n_tok)) {
+        case 8: e = dn_launch<8, false>(h, a, s); break;
+        case 4: e = dn_launch<4, false>(h, a, s); break;
+        case 2: e = dn_launch<2, false>(h, a, s); break;
+        default: e = dn_launch<1, false>(h, a, s); break;
+      }
     }
   }
   h->launches++;  // the quantisation; dn_launch counts its own
@@ -448,13 +556,13 @@ ds4moe_status ds4moe_dense_get_device_error(ds4moe_dense *h, void *stream, uint3
   return f ? DS4MOE_ERR_DEVICE : DS4MOE_OK;
 }
 
-ds4moe_status ds4moe_dense_debug_config(ds4moe_dense *h, int32_t ks, int32_t nst, int32_t ns) {
-  if (!h || ks < 0 || nst < 0 || ns < 0) return DS4MOE_ERR_INVALID_ARG;
+ds4moe_status ds4moe_dense_debug_config(ds4moe_dense *h, int32_t ks, int32_t nst, int32_t ns, int32_t tc) {
+  if (!h || ks < 0 || nst < 0 || ns < 0 || tc < 0 || tc > 2) return DS4MOE_ERR_INVALID_ARG;
   const int S = expert_segs(DS4MOE_Q8_0, h->K), per = h->K / 32 / S;
   if (ks && (ks > DN_MAX_KS || per % ks)) return DS4MOE_ERR_INVALID_ARG;
   if (nst && (nst < 2 || nst > DN_MAX_NST)) return DS4MOE_ERR_INVALID_ARG;
   if (ns && S % ns) return DS4MOE_ERR_INVALID_ARG;
-  h->dbg_ks = ks, h->dbg_nst = nst, h->dbg_ns = ns;
+  h->dbg_ks = ks, h->dbg_nst = nst, h->dbg_ns = ns, h->dbg_tc = tc;
   return DS4MOE_OK;
 }
 

@@ -70,7 +70,8 @@ def test_dense_repeated_calls():
 
 
 def test_dense_launch_geometries_same_bits():
-    """Every ring geometry and row split gives the oracle's bits."""
+    """Every ring geometry, row split and block-dot step (dp4a, int8 tensor
+    cores) gives the oracle's bits."""
     import torch
     import deepseek_v4_flash_gb300 as ds4
     n_out, n_in = 1024, 4096
@@ -80,16 +81,19 @@ def test_dense_launch_geometries_same_bits():
         x = synth.gen_dense_x(200 + T, T, n_in)
         ref = oracle.get().dense_q8(w, n_out, n_in, x).view(np.uint32)
         xd = torch.from_numpy(x).cuda()
-        for ks, nst, ns in [(1, 6, 1), (2, 3, 2), (4, 2, 4), (8, 2, 8), (16 // 2, 3, 1), (4, 6, 8)]:
-            d.debug_config(ks, nst, ns)
-            got = d.forward(xd).cpu().numpy().view(np.uint32)
-            assert np.array_equal(got, ref), f"T={T} ks={ks} nst={nst} ns={ns}"
+        for tc in (1, 2):
+            for ks, nst, ns in [(1, 6, 1), (2, 3, 2), (4, 2, 4), (8, 2, 8), (8, 3, 1), (4, 6, 8)]:
+                d.debug_config(ks, nst, ns, tc)
+                got = d.forward(xd).cpu().numpy().view(np.uint32)
+                assert np.array_equal(got, ref), f"T={T} ks={ks} nst={nst} ns={ns} tc={tc}"
     with pytest.raises(ds4.Ds4MoeError):
         d.debug_config(3, 0, 0)   # 3 does not divide the 16 blocks of a segment
     with pytest.raises(ds4.Ds4MoeError):
         d.debug_config(0, 7, 0)
     with pytest.raises(ds4.Ds4MoeError):
         d.debug_config(0, 0, 3)
+    with pytest.raises(ds4.Ds4MoeError):
+        d.debug_config(0, 0, 0, 3)
     assert d.device_error() == 0
     d.close()
 
