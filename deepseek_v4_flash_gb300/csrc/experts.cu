@@ -445,6 +445,14 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
     bool c_ok = false;
     int arow[TT], nt = 0;
     Chains<(TT > 1)> acc[TT];  // per token: the two tiles' row chains
+    // units of eight tokens that hold at least MMA_MIN_NT of them: the int8
+    // tensor-core steps (with fewer tokens most of the MMA's columns would
+    // idle, and the dp4a steps skip the empty ones); this lane's rows of
+    // activations: B token lane / 4, D tokens 2 (lane % 4) and + 1
+    constexpr int MMA_MIN_NT = 3;
+    bool mma = false;
+    MChains macc;
+    int ar_g = 0, ar0 = 0, ar1 = 0;
     for (;;) {
       if (!c_ok) {  // the consumer's next item
         if (cj >= n_sh_items && !wait_items()) {
@@ -465,11 +473,21 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
       }
       if (cstage == 0) {  // a new unit: its tokens
         nt = min(TT, n_tok - cpass * TT);
-#pragma unroll
-        for (int i = 0; i < TT; i++) {
+        mma = TT == 8 && nt >= MMA_MIN_NT;
+        if (mma) {
           int sr;
-          x_token(a, list_off, list, min(cpass * TT + i, n_tok - 1), &sr, &arow[i]);
-          chains_zero(acc[i]);
+          const int u0 = cpass * TT, last = n_tok - 1;
+          x_token(a, list_off, list, min(u0 + (lane >> 2), last), &sr, &ar_g);
+          x_token(a, list_off, list, min(u0 + 2 * (lane & 3), last), &sr, &ar0);
+          x_token(a, list_off, list, min(u0 + 2 * (lane & 3) + 1, last), &sr, &ar1);
+          mchains_zero(macc);
+        } else {
+#pragma unroll
+          for (int i = 0; i < TT; i++) {
+            int sr;
+            x_token(a, list_off, list, min(cpass * TT + i, n_tok - 1), &sr, &arow[i]);
+            chains_zero(acc[i]);
+          }
         }
       }
       if (c_nst > 0) {
@@ -482,7 +500,14 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
         __syncwarp();
         const uint32_t st = ring + slot * X_STRIDE;
         const int s0 = c_ks0 + cstage * c_ksps;
-        if (c_fmt == DS4MOE_Q2S && c_ksps == 2) {  // two K-steps in one block of code: their dots overlap
+        if (TT == 8 && mma) {
+          for (int j = 0; j < c_ksps; j++) {
+            const uint32_t t = st + j * c_kb;
+            if (c_fmt == DS4MOE_Q2S) sb_step_mma<AS, false>(t, lane, s0 + j, a.K, ar_g, ar0, ar1, aq, ad, ag, macc);
+            else if (c_fmt == DS4MOE_Q4S) sb_step_mma<AS, true>(t, lane, s0 + j, a.K, ar_g, ar0, ar1, aq, ad, ag, macc);
+            else q8_step_mma<AS>(t, lane, s0 + j, a.K, ar_g, ar0, ar1, aq, ad, macc);
+          }
+        } else if (c_fmt == DS4MOE_Q2S && c_ksps == 2) {  // two K-steps in one block of code: their dots overlap
           q2s_step<TT, AS, (TT > 1)>(st, lane, s0, a.K, arow, nt, aq, ad, ag, acc);
           q2s_step<TT, AS, (TT > 1)>(st + c_kb, lane, s0 + 1, a.K, arow, nt, aq, ad, ag, acc);
         } else {
@@ -503,7 +528,19 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
           failed = true;
           break;
         }
-        if (c_nst > 0 && (lane & 1) == 0) {
+        if (TT == 8 && mma && c_nst > 0) {
+          // [tile][token][row]: rows g, g + 8 of both tiles, tokens 2t, 2t + 1
+          float *dst = part + (size_t)(ps * XC + warp) * mats * TT * TILE_ROWS;
+          const int g = lane >> 2, k0 = 2 * (lane & 3);
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const int m = i >> 1, hh = i & 1;
+            float v0, v1;
+            f2_unpack(macc.v[m][hh], v0, v1);
+            if (k0 < nt) dst[(m * TT + k0) * TILE_ROWS + g + 8 * hh] = v0;
+            if (k0 + 1 < nt) dst[(m * TT + k0 + 1) * TILE_ROWS + g + 8 * hh] = v1;
+          }
+        } else if (c_nst > 0 && (lane & 1) == 0) {
           float *dst = part + (size_t)(ps * XC + warp) * mats * TT * TILE_ROWS;
 #pragma unroll
           for (int i = 0; i < TT; i++) {

@@ -254,4 +254,178 @@ __device__ __forceinline__ void q8_step(uint32_t t0, int lane, int s, int K, con
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Int8 tensor-core steps for units of eight tokens (mma.sync m16n8k32).
+// Lane (g, t) = (lane / 4, lane % 4) holds A rows g and g + 8 of a 16-row
+// tile at K 4t..4t+3 and 16+4t..16+4t+3, B column (token) g at the same K,
+// and D rows g, g + 8 for tokens 2t, 2t + 1. A is the exact integer weight of
+// CAS step 2 (sc*q for the superblock formats, q for Q8_0) and B the int8
+// codes, so D holds the exact block dots A_b (I_b) of 16 rows and 8 tokens.
+// The lane keeps the chains of rows g, g + 8 of both tiles for tokens 2t,
+// 2t + 1 as packed pairs, adding the block terms in block order.
+struct MChains {
+  unsigned long long v[2][2];  // [tile][row g, g + 8]: tokens (2t, 2t + 1)
+};
+
+__device__ __forceinline__ void mchains_zero(MChains &c) {
+#pragma unroll
+  for (int i = 0; i < 4; i++) c.v[i >> 1][i & 1] = 0ull;
+}
+
+// Unsigned weights (sc*q <= 225) against signed codes.
+__device__ __forceinline__ void mma_u8s8(const uint32_t (&a)[4], uint32_t b0, uint32_t b1, int (&d)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+}
+
+__device__ __forceinline__ void mma_s8s8(const uint32_t (&a)[4], uint32_t b0, uint32_t b1, int (&d)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+}
+
+// Four 8x8 b16 matrices: lane i gives the address of row i % 8 of matrix
+// i / 8 and receives, from each, bytes 4*(i%4)..+3 of row i / 4.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// The lane's activation data of 32-block blk: B fragment (token g, rows
+// ar_g), and scales and group sums of its D tokens (rows ar0, ar1).
+struct MTok {
+  uint32_t b0, b1, gs0, gs1;
+  float dx0, dx1;
+};
+
+template <bool ACT_SMEM, bool GS>
+__device__ __forceinline__ MTok m_tok(int blk, int t, int K, int ar_g, int ar0, int ar1, const int8_t *__restrict__ aq,
+                                      const float *__restrict__ ad, const int16_t *__restrict__ ag) {
+  MTok o;
+  const int8_t *xr = aq + (size_t)ar_g * K + 32 * blk + 4 * t;
+  o.b0 = act_load<ACT_SMEM>((const uint32_t *)xr);
+  o.b1 = act_load<ACT_SMEM>((const uint32_t *)(xr + 16));
+  const int nb = K >> 5;
+  o.dx0 = act_load<ACT_SMEM>(ad + (size_t)ar0 * nb + blk);
+  o.dx1 = act_load<ACT_SMEM>(ad + (size_t)ar1 * nb + blk);
+  o.gs0 = o.gs1 = 0u;
+  if constexpr (GS) {
+    o.gs0 = act_load<ACT_SMEM>((const uint32_t *)(ag + (size_t)ar0 * (K >> 4) + 2 * blk));
+    o.gs1 = act_load<ACT_SMEM>((const uint32_t *)(ag + (size_t)ar1 * (K >> 4) + 2 * blk));
+  }
+  return o;
+}
+
+// Superblock-format terms of one row for the lane's two tokens (CAS step 3:
+// dx * fma(d, A, -(dmin * B))); the products by dx are scalar, so that no
+// packed product is fused into the chain's add.
+__device__ __forceinline__ void m_sb_terms(unsigned long long &acc, float d, float dmin, int A0, int A1, int B0,
+                                           int B1, float dx0, float dx1) {
+  const unsigned long long f =
+      f2_fma(f2_pack(d, d), f2_pack(__int2float_rn(A0), __int2float_rn(A1)),
+             f2_mul(f2_pack(-dmin, -dmin), f2_pack(__int2float_rn(B0), __int2float_rn(B1))));
+  float f0, f1;
+  f2_unpack(f, f0, f1);
+  acc = f2_add(acc, f2_pack(__fmul_rn(dx0, f0), __fmul_rn(dx1, f1)));
+}
+
+// B_b = mn0 * gs0 + mn1 * gs1 of one row (scale/min byte pair smp) for a
+// token's packed group sums.
+__device__ __forceinline__ int m_minterm(uint32_t smp, uint32_t gsw) {
+  return (int)((smp >> 4) & 15) * (int)(int16_t)(gsw & 0xFFFF) + (int)((smp >> 12) & 15) * (int)(int16_t)(gsw >> 16);
+}
+
+// One Q2S (4-bit: Q4S) K-step (superblock s) of the two tiles at t0.
+// Row r's scale/min bytes: 16 at SM + 16r, block b = h + 2j, group gi at
+// byte 8h + 2j + gi; its group words: lane L = 2r + h's chunk (see q2s_step,
+// q4s_step).
+template <bool ACT_SMEM, bool Q4>
+__device__ __forceinline__ void sb_step_mma(uint32_t t0, int lane, int s, int K, int ar_g, int ar0, int ar1,
+                                            const int8_t *__restrict__ aq, const float *__restrict__ ad,
+                                            const int16_t *__restrict__ ag, MChains &acc) {
+  constexpr int TILE = Q4 ? Q4S_TILE : Q2S_TILE, SM = Q4 ? Q4S_SM : Q2S_SM, DD = Q4 ? Q4S_DD : Q2S_DD,
+                QS = Q4 ? Q4S_QS : Q2S_QS;
+  const int g = lane >> 2, t = lane & 3;
+  uint4 smr[2][2];
+  float d[2][2], dmin[2][2];
+#pragma unroll
+  for (int m = 0; m < 2; m++)
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++) {
+      const int r = g + 8 * hh;
+      const uint32_t tm = t0 + m * TILE;
+      smr[m][hh] = ld_shared_v4(tm + SM + 16 * r);
+      const uint32_t dd = ld_shared_u32(tm + DD + 4 * r);
+      d[m][hh] = half_bits_to_float(dd), dmin[m][hh] = half_bits_to_float(dd >> 16);
+    }
+#pragma unroll
+  for (int b = 0; b < 8; b++) {
+    const int h = b & 1, j = b >> 1, blk = 8 * s + b;
+    const MTok tk = m_tok<ACT_SMEM, true>(blk, t, K, ar_g, ar0, ar1, aq, ad, ag);
+    const int byte = 8 * h + 2 * j;  // scale/min bytes of groups 0, 1: byte, byte + 1
+#pragma unroll
+    for (int m = 0; m < 2; m++) {
+      uint32_t af[4], smp[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        const int r = g + 8 * hh;
+        const uint32_t wsel = byte >> 2;
+        const uint32_t sw = wsel == 0 ? smr[m][hh].x : wsel == 1 ? smr[m][hh].y : wsel == 2 ? smr[m][hh].z : smr[m][hh].w;
+        smp[hh] = sw >> (8 * (byte & 3));  // byte pair (group 0, group 1) in the low 16 bits
+        uint32_t w0, w1;                   // the lane's code words of groups 0, 1
+        if constexpr (Q4) {
+          const uint32_t base = t0 + m * TILE + QS + 512 * j + 16 * (2 * r + h) + 4 * (t >> 1);
+          w0 = ld_shared_u32(base), w1 = ld_shared_u32(base + 8);
+          w0 = (w0 >> (4 * (t & 1))) & 0x0F0F0F0Fu, w1 = (w1 >> (4 * (t & 1))) & 0x0F0F0F0Fu;
+        } else {
+          const uint2 w = ld_shared_v2(t0 + m * TILE + QS + 512 * (j >> 1) + 16 * (2 * r + h) + 8 * (j & 1));
+          w0 = (w.x >> (2 * t)) & M2, w1 = (w.y >> (2 * t)) & M2;
+        }
+        af[hh] = w0 * (smp[hh] & 15u);              // rows g / g + 8, K 4t..: group 0
+        af[2 + hh] = w1 * ((smp[hh] >> 8) & 15u);   // K 16+4t..: group 1
+      }
+      int D[4];
+      mma_u8s8(af, tk.b0, tk.b1, D);
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        m_sb_terms(acc.v[m][hh], d[m][hh], dmin[m][hh], D[2 * hh], D[2 * hh + 1], m_minterm(smp[hh], tk.gs0),
+                   m_minterm(smp[hh], tk.gs1), tk.dx0, tk.dx1);
+    }
+  }
+}
+
+// One Q8_0 K-step (block s) of the two tiles at t0: A straight from the
+// tiles' int8 rows with ldmatrix; terms (d * dx) * I.
+template <bool ACT_SMEM>
+__device__ __forceinline__ void q8_step_mma(uint32_t t0, int lane, int s, int K, int ar_g, int ar0, int ar1,
+                                            const int8_t *__restrict__ aq, const float *__restrict__ ad,
+                                            MChains &acc) {
+  const int g = lane >> 2, t = lane & 3;
+  const MTok tk = m_tok<ACT_SMEM, false>(s, t, K, ar_g, ar0, ar1, aq, ad, nullptr);
+  const unsigned long long dx2 = f2_pack(tk.dx0, tk.dx1);
+  const uint32_t lm = Q8_Q + 32 * (((lane >> 3) & 1) * 8 + (lane & 7)) + 16 * (lane >> 4);
+#pragma unroll
+  for (int m = 0; m < 2; m++) {
+    const uint32_t tm = t0 + m * Q8_TILE;
+    uint32_t af[4];
+    ldsm_x4(tm + lm, af);
+    int D[4];
+    mma_s8s8(af, tk.b0, tk.b1, D);
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++) {
+      const uint32_t dw = ld_shared_u32(tm + 4 * ((g + 8 * hh) >> 1));
+      const float dr = half_bits_to_float((g & 1) ? dw >> 16 : dw);
+      float dd0, dd1;
+      f2_unpack(f2_mul(f2_pack(dr, dr), dx2), dd0, dd1);
+      acc.v[m][hh] = f2_add(acc.v[m][hh], f2_pack(__fmul_rn(dd0, __int2float_rn(D[2 * hh])),
+                                                  __fmul_rn(dd1, __int2float_rn(D[2 * hh + 1]))));
+    }
+  }
+}
+
 }  // namespace ds4
