@@ -147,10 +147,13 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
   const int G = gridDim.x, W = G * DN_WARPS, gw = warp * G + blockIdx.x;
   const int my_units = gw < n_units ? (n_units - 1 - gw) / W + 1 : 0;
   const int n_pass = (a.T + TT - 1) / TT;
-  // shared memory: the pass's codes [TT][K], scales [TT][K/32], then the rings
+  // shared memory: the pass's codes [TT][K + 16] and scales [TT][K/32 + 4]
+  // (rows padded by 16 bytes, so that the tensor-core step's loads of eight
+  // tokens' rows fall in different banks), then the rings
+  const int xrow = a.K + 16, drow = nb + 4;
   int8_t *xs = (int8_t *)smem;
-  float *ds = (float *)(smem + TT * a.K);
-  const int ring_off = (TT * a.K + TT * nb * 4 + 127) & ~127;
+  float *ds = (float *)(smem + TT * xrow);
+  const int ring_off = (TT * xrow + TT * drow * 4 + 127) & ~127;
   const uint32_t ring = smem_u32(smem + ring_off + warp * nst * sbytes);
   __shared__ uint64_t bars[DN_WARPS][DN_MAX_NST];
   const uint32_t bar = smem_u32(&bars[warp][0]);
@@ -197,10 +200,16 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
     const int t0 = p * TT, nt = min(TT, a.T - t0);
     __syncthreads();  // the previous pass is done with the staged codes
     {
-      const int nq = nt * a.K / 16, nd = nt * nb;
+      const int qrow = a.K / 16, nq = nt * qrow, nd = nt * nb;
       const uint4 *src = (const uint4 *)(a.xq + (size_t)t0 * a.K);
-      for (int i = threadIdx.x; i < nq; i += blockDim.x) ((uint4 *)xs)[i] = __ldg(src + i);
-      for (int i = threadIdx.x; i < nd; i += blockDim.x) ds[i] = __ldg(a.dx + (size_t)t0 * nb + i);
+      for (int i = threadIdx.x; i < nq; i += blockDim.x) {
+        const int r = i / qrow;
+        *(uint4 *)(xs + r * xrow + 16 * (i - r * qrow)) = __ldg(src + i);
+      }
+      for (int i = threadIdx.x; i < nd; i += blockDim.x) {
+        const int r = i / nb;
+        ds[r * drow + (i - r * nb)] = __ldg(a.dx + (size_t)t0 * nb + i);
+      }
     }
     __syncthreads();
     // a warp that gave up a wait skips its units but still meets every pass
@@ -233,9 +242,9 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
           if (j < ks) {
             const int b = bst + j;
             if constexpr (MMA) {
-              const uint32_t b0 = ld_shared_u32(xs_s + g * a.K + 32 * b + 4 * t4);
-              const uint32_t b1 = ld_shared_u32(xs_s + g * a.K + 32 * b + 16 + 4 * t4);
-              const unsigned long long dx2 = f2_pack(ds[(2 * t4) * nb + b], ds[(2 * t4 + 1) * nb + b]);
+              const uint32_t b0 = ld_shared_u32(xs_s + g * xrow + 32 * b + 4 * t4);
+              const uint32_t b1 = ld_shared_u32(xs_s + g * xrow + 32 * b + 16 + 4 * t4);
+              const unsigned long long dx2 = f2_pack(ds[(2 * t4) * drow + b], ds[(2 * t4 + 1) * drow + b]);
 #pragma unroll
               for (int mt = 0; mt < 2; mt++) {
                 const uint32_t tb = stage + j * DN_KB + mt * Q8_TILE;
@@ -253,9 +262,9 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
 #pragma unroll
               for (int t = 0; t < TT; t++) {
                 if (t < nt) {  // warp-uniform
-                  const uint4 *xp = (const uint4 *)(xs + t * a.K + 32 * b);
+                  const uint4 *xp = (const uint4 *)(xs + t * xrow + 32 * b);
                   const int I = dn_dot32(q0, q1, xp[0], xp[1]);
-                  acc[t] = __fadd_rn(acc[t], __fmul_rn(__fmul_rn(d, ds[t * nb + b]), __int2float_rn(I)));
+                  acc[t] = __fadd_rn(acc[t], __fmul_rn(__fmul_rn(d, ds[t * drow + b]), __int2float_rn(I)));
                 }
               }
             }
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(256) k_dense_fix(const float *__restrict__ par
 
 // Tokens per pass, at most, for K: the codes of a pass take at most 64 KB.
 static int dn_tt_cap(int K) {
-  const size_t per_tok = (size_t)K + (size_t)(K / 32) * 4;
+  const size_t per_tok = (size_t)(K + 16) + (size_t)(K / 32 + 4) * 4;
   int tt = DN_TT_MAX;
   while (tt > 1 && (size_t)tt * per_tok > 65536) tt >>= 1;
   return tt;
@@ -355,7 +364,7 @@ static int dn_tt(int K, int T) {
 }
 
 static size_t dn_stage_smem(int TT, int K) {
-  return ((size_t)TT * K + (size_t)TT * (K / 32) * 4 + 127) & ~(size_t)127;
+  return ((size_t)TT * (K + 16) + (size_t)TT * (K / 32 + 4) * 4 + 127) & ~(size_t)127;
 }
 
 // Ring geometry: the largest K steps per stage (a divisor of a segment's
