@@ -308,6 +308,19 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
     bool ok = true;
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_f16(PF_M, PF_NP);
+      // the operand descriptors of fp16 stage 0; stage fs adds its byte
+      // offset / 16 to the start-address field (14 bits: shared-memory
+      // addresses below 256 KB never carry out of it)
+      const uint32_t f0 = sm0 + PF_OFF_F;
+      uint64_t dam[2][2], dan[2], dbm[2];
+#pragma unroll
+      for (int m = 0; m < 2; m++) {
+        dam[m][0] = umma_desc(f0 + PF_F_AMAIN + m * 8192, 128, 512);
+        dam[m][1] = umma_desc(f0 + PF_F_AMAIN + m * 8192 + 256, 128, 512);
+        dan[m] = umma_desc(f0 + PF_F_AMIN + m * 4096, 128, 256);
+        dbm[m] = umma_desc(f0 + PF_F_BMAIN + 256 * m, 128, 512);
+      }
+      const uint64_t dbn = umma_desc(f0 + PF_F_BMIN, 128, 256);
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const PfItem it = pf_item<MODE>(a, i, RB);
         if (it.nv <= 0) continue;
@@ -320,16 +333,13 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
             break;
           }
           tc_fence_after();
-          const uint32_t f = sm0 + PF_OFF_F + fs * PF_F_BYTES;
+          const uint64_t off = (uint64_t)((fs * PF_F_BYTES) >> 4);
           const uint32_t d0 = tbase + ts * 128;
 #pragma unroll
           for (int m = 0; m < MATS; m++) {
-            const uint32_t am = f + PF_F_AMAIN + m * 8192;
-            umma_f16(d0 + 32 * m, umma_desc(am, 128, 512), umma_desc(f + PF_F_BMAIN, 128, 512), idesc, 0);
-            umma_f16(d0 + 32 * m, umma_desc(am + 256, 128, 512), umma_desc(f + PF_F_BMAIN + 256, 128, 512), idesc, 1);
-            if (sbf)
-              umma_f16(d0 + 64 + 32 * m, umma_desc(f + PF_F_AMIN + m * 4096, 128, 256),
-                       umma_desc(f + PF_F_BMIN, 128, 256), idesc, 0);
+            umma_f16(d0 + 32 * m, dam[m][0] + off, dbm[0] + off, idesc, 0);
+            umma_f16(d0 + 32 * m, dam[m][1] + off, dbm[1] + off, idesc, 1);
+            if (sbf) umma_f16(d0 + 64 + 32 * m, dan[m] + off, dbn + off, idesc, 0);
           }
           umma_commit(B.f_empty + 8 * fs);
           umma_commit(B.t_full + 8 * ts);
