@@ -25,14 +25,17 @@
 // tokens (MMA N). A persistent block walks items c, c + G, ... with four
 // warp roles connected by mbarriers:
 //   producer   1-D bulk copies of the packed weight tiles (raw ring)
-//   converters expand one 32-block of weights into fp16 operand tiles in the
-//              canonical no-swizzle K-major layout, and the tokens' codes
-//              (fp16 ring), plus the epilogue's scales (side ring)
-//   MMA        one thread issues the block's MMAs into a TMEM stage and
-//              commits to the fp16 ring's and the TMEM stage's barriers
+//   converters expand the weights of a pair of 32-blocks into fp16 operand
+//              tiles in the canonical no-swizzle K-major layout (fp16 ring),
+//              plus the epilogue's scales (side ring)
+//   token warp the pass's token codes, group sums and scales of the pair
+//   MMA        one thread issues the pair's MMAs into a TMEM stage (a region
+//              of 128 columns per block) and commits to the fp16 ring's and
+//              the TMEM stage's barriers
 //   epilogue   8 warps; warp w reads TMEM lanes 32*(w%4).. (rows) for one
 //              half of the pass's token columns, adds the block terms to the
-//              segment chains, and finishes the item.
+//              segment chains in block order, and finishes the item.
+// Every hand-off between these roles moves a pair of 32-blocks.
 // Every wait is bounded; on a timeout the block raises DS4MOE_DEVERR_TIMEOUT,
 // drains what it has in flight and leaves.
 #include "common.cuh"
@@ -48,9 +51,14 @@ constexpr int PF_EW = 8;   // epilogue warps
 constexpr int PF_WARPS = 2 + PF_CW + PF_EW + 1;  // + the token warp
 constexpr int PF_RS = 2;                 // raw stages
 constexpr int PF_RAW = 16 * Q4S_TILE;    // 37888 bytes, the largest raw stage
-constexpr int PF_FS = 4;                 // fp16 operand stages, one 32-block each
-constexpr int PF_TS = 4;                 // TMEM stages of 128 columns
-constexpr int PF_XS = 9;                 // side-data stages, >= PF_FS + PF_TS + 1
+// The pipeline between the converters, the MMA thread and the epilogue moves
+// pairs of 32-blocks (b, b + 1): one barrier hand-off per pair.
+constexpr int PF_FS = 4;                 // fp16 operand slots, one 32-block each
+constexpr int PF_TS = 4;                 // TMEM regions of 128 columns, one 32-block each
+constexpr int PF_FP = PF_FS / 2;         // fp16 pair stages
+constexpr int PF_TP = PF_TS / 2;         // TMEM pair stages
+constexpr int PF_XP = 5;                 // side-data pair stages, >= PF_FP + PF_TP + 1
+constexpr int PF_XS = 2 * PF_XP;         // side-data slots, one 32-block each
 constexpr int PF_TMEM_COLS = PF_TS * 128;
 // fp16 stage: A main [2 mats][128 x 32] | A min [2][128 x 16] | B main [32 x 32] | B min [32 x 16]
 constexpr int PF_F_AMAIN = 0, PF_F_AMIN = 16384, PF_F_BMAIN = 24576, PF_F_BMIN = 26624, PF_F_BYTES = 27648;
@@ -60,10 +68,10 @@ constexpr int PF_OFF_RAW = 0;
 constexpr int PF_OFF_F = PF_OFF_RAW + PF_RS * PF_RAW;
 constexpr int PF_OFF_X = PF_OFF_F + PF_FS * PF_F_BYTES;
 constexpr int PF_OFF_BAR = PF_OFF_X + PF_XS * PF_X_BYTES;
-constexpr int PF_NBARS = 2 * PF_RS + 2 * PF_FS + 2 * PF_TS + PF_XS;
+constexpr int PF_NBARS = 2 * PF_RS + 2 * PF_FP + 2 * PF_TP + PF_XP;
 constexpr int PF_OFF_MISC = PF_OFF_BAR + PF_NBARS * 8;
 constexpr int PF_SMEM = PF_OFF_MISC + 64;
-static_assert(PF_XS >= PF_FS + PF_TS + 1, "side ring too short");
+static_assert(PF_XP >= PF_FP + PF_TP + 1, "side ring too short");
 static_assert(PF_SMEM <= 227 * 1024, "prefill kernel does not fit shared memory");
 
 struct PfArgs {
@@ -207,10 +215,10 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *smem) {
   p.raw_full = b;
   p.raw_empty = p.raw_full + 8 * PF_RS;
   p.f_full = p.raw_empty + 8 * PF_RS;
-  p.f_empty = p.f_full + 8 * PF_FS;
-  p.t_full = p.f_empty + 8 * PF_FS;
-  p.t_empty = p.t_full + 8 * PF_TS;
-  p.x_full = p.t_empty + 8 * PF_TS;
+  p.f_empty = p.f_full + 8 * PF_FP;
+  p.t_full = p.f_empty + 8 * PF_FP;
+  p.t_empty = p.t_full + 8 * PF_TP;
+  p.x_full = p.t_empty + 8 * PF_TP;
   return p;
 }
 
@@ -250,9 +258,9 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
   if (threadIdx.x == 0) {
     *abort = 0;
     for (int i = 0; i < PF_RS; i++) mbar_init(B.raw_full + 8 * i, 1), mbar_init(B.raw_empty + 8 * i, PF_CW);
-    for (int i = 0; i < PF_FS; i++) mbar_init(B.f_full + 8 * i, PF_CW + 1), mbar_init(B.f_empty + 8 * i, 1);
-    for (int i = 0; i < PF_TS; i++) mbar_init(B.t_full + 8 * i, 1), mbar_init(B.t_empty + 8 * i, PF_EW);
-    for (int i = 0; i < PF_XS; i++) mbar_init(B.x_full + 8 * i, PF_CW + 1);
+    for (int i = 0; i < PF_FP; i++) mbar_init(B.f_full + 8 * i, PF_CW + 1), mbar_init(B.f_empty + 8 * i, 1);
+    for (int i = 0; i < PF_TP; i++) mbar_init(B.t_full + 8 * i, 1), mbar_init(B.t_empty + 8 * i, PF_EW);
+    for (int i = 0; i < PF_XP; i++) mbar_init(B.x_full + 8 * i, PF_CW + 1);
     fence_mbar_init();
   }
   // the parts of the min tiles that no block writes stay zero
@@ -325,29 +333,32 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
         const PfItem it = pf_item<MODE>(a, i, RB);
         if (it.nv <= 0) continue;
         const bool sbf = it.fmt != DS4MOE_Q8_0;
-        for (int b = 0; b < nb; b++, fc++) {
-          const int fs = fc % PF_FS, ts = fc % PF_TS;
-          if (!pf_wait(B.f_full + 8 * fs, (fc / PF_FS) & 1, abort) ||
-              (fc >= PF_TS && !pf_wait(B.t_empty + 8 * ts, ((fc / PF_TS) - 1) & 1, abort))) {
+        for (int b = 0; b < nb; b += 2, fc++) {  // fc: pairs
+          const int fp = fc % PF_FP, tp = fc % PF_TP;
+          if (!pf_wait(B.f_full + 8 * fp, (fc / PF_FP) & 1, abort) ||
+              (fc >= PF_TP && !pf_wait(B.t_empty + 8 * tp, ((fc / PF_TP) - 1) & 1, abort))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t off = (uint64_t)((fs * PF_F_BYTES) >> 4);
-          const uint32_t d0 = tbase + ts * 128;
 #pragma unroll
-          for (int m = 0; m < MATS; m++) {
-            umma_f16(d0 + 32 * m, dam[m][0] + off, dbm[0] + off, idesc, 0);
-            umma_f16(d0 + 32 * m, dam[m][1] + off, dbm[1] + off, idesc, 1);
-            if (sbf) umma_f16(d0 + 64 + 32 * m, dan[m] + off, dbn + off, idesc, 0);
+          for (int u = 0; u < 2; u++) {
+            const uint64_t off = (uint64_t)(((2 * fp + u) * PF_F_BYTES) >> 4);
+            const uint32_t d0 = tbase + (2 * tp + u) * 128;
+#pragma unroll
+            for (int m = 0; m < MATS; m++) {
+              umma_f16(d0 + 32 * m, dam[m][0] + off, dbm[0] + off, idesc, 0);
+              umma_f16(d0 + 32 * m, dam[m][1] + off, dbm[1] + off, idesc, 1);
+              if (sbf) umma_f16(d0 + 64 + 32 * m, dan[m] + off, dbn + off, idesc, 0);
+            }
           }
-          umma_commit(B.f_empty + 8 * fs);
-          umma_commit(B.t_full + 8 * ts);
+          umma_commit(B.f_empty + 8 * fp);
+          umma_commit(B.t_full + 8 * tp);
         }
       }
       if (!ok) pf_fail(abort, a.err);
       // the last MMAs must be complete before TMEM is released
-      if (fc > 0) (void)mbar_wait_bounded(B.t_full + 8 * ((fc - 1) % PF_TS), ((fc - 1) / PF_TS) & 1);
+      if (fc > 0) (void)mbar_wait_bounded(B.t_full + 8 * ((fc - 1) % PF_TP), ((fc - 1) / PF_TP) & 1);
     }
     __syncwarp();
   } else if (warp < 2 + PF_CW) {
@@ -374,14 +385,12 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
           ok = false;
           break;
         }
-        int fsu[2], xsu[2];
+        // pair fc: blocks b, b + 1 into fp16 slots 2*fp, 2*fp + 1 and side
+        // slots 2*xp, 2*xp + 1
+        const int fp = fc % PF_FP, xp = fc % PF_XP;
+        const int fsu[2] = {2 * fp, 2 * fp + 1}, xsu[2] = {2 * xp, 2 * xp + 1};
         bool waited = true;
-#pragma unroll
-        for (int u = 0; u < 2; u++) {
-          const uint32_t fcu = fc + u;
-          fsu[u] = fcu % PF_FS, xsu[u] = fcu % PF_XS;
-          if (fcu >= PF_FS && !pf_wait(B.f_empty + 8 * fsu[u], ((fcu / PF_FS) - 1) & 1, abort)) waited = false;
-        }
+        if (fc >= PF_FP && !pf_wait(B.f_empty + 8 * fp, ((fc / PF_FP) - 1) & 1, abort)) waited = false;
         if (!waited) {
           ok = false;
           break;
@@ -529,11 +538,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-          for (int u = 0; u < 2; u++) mbar_arrive(B.f_full + 8 * fsu[u]), mbar_arrive(B.x_full + 8 * xsu[u]);
-        }
-        fc += 2;
+        if (lane == 0) mbar_arrive(B.f_full + 8 * fp), mbar_arrive(B.x_full + 8 * xp);
+        fc++;
         if (bin0 + 1 == bpst - 1) {
           if (lane == 0) mbar_arrive(B.raw_empty + 8 * rs);
           gst++;
@@ -557,7 +563,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
         const int code = __ldg(a.list + it.list_off + pt);
         arow = MODE == 0 ? (code >> 5) : (code >> 5) * a.NS + (code & 31);
       }
-      // software prefetch four blocks ahead; slot 0 holds block b
+      // software prefetch four blocks ahead: slots 0, 1 hold the pair's
+      // blocks b, b + 1, slots 2, 3 the next pair's
       uint4 xv[4][2];
       int gv[4];
       float dv[4];
@@ -572,33 +579,38 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
       };
 #pragma unroll
       for (int u = 0; u < 4; u++) load_tok(u, xv[u], gv[u], dv[u]);
-      for (int b = 0; b < nb; b++, fc++) {
-        const int fs = fc % PF_FS, xs = fc % PF_XS;
-        if (fc >= PF_FS && !pf_wait(B.f_empty + 8 * fs, ((fc / PF_FS) - 1) & 1, abort)) {
+      for (int b = 0; b < nb; b += 2, fc++) {  // fc: pairs
+        const int fp = fc % PF_FP, xp = fc % PF_XP;
+        if (fc >= PF_FP && !pf_wait(B.f_empty + 8 * fp, ((fc / PF_FP) - 1) & 1, abort)) {
           ok = false;
           break;
         }
-        const uint32_t f = sm0 + PF_OFF_F + fs * PF_F_BYTES;
-        const uint32_t bm = f + PF_F_BMAIN + (lane >> 3) * 512 + (lane & 7) * 16;
-        uint4 o = i8x8_to_h(xv[0][0].x, xv[0][0].y);
-        sts128(bm, o.x, o.y, o.z, o.w);
-        o = i8x8_to_h(xv[0][0].z, xv[0][0].w);
-        sts128(bm + 128, o.x, o.y, o.z, o.w);
-        o = i8x8_to_h(xv[0][1].x, xv[0][1].y);
-        sts128(bm + 256, o.x, o.y, o.z, o.w);
-        o = i8x8_to_h(xv[0][1].z, xv[0][1].w);
-        sts128(bm + 384, o.x, o.y, o.z, o.w);
-        if (sbf)
-          sts128(f + PF_F_BMIN + (lane >> 3) * 256 + (lane & 7) * 16,
-                 h_of_int((int)(int16_t)(gv[0] & 0xFFFF)) | (h_of_int(gv[0] >> 16) << 16), 0, 0, 0);
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sm0 + PF_OFF_X + xs * PF_X_BYTES + 4 * lane), "f"(dv[0])
-                     : "memory");
 #pragma unroll
-        for (int u = 0; u < 3; u++) xv[u][0] = xv[u + 1][0], xv[u][1] = xv[u + 1][1], gv[u] = gv[u + 1], dv[u] = dv[u + 1];
-        load_tok(b + 4, xv[3], gv[3], dv[3]);
+        for (int u = 0; u < 2; u++) {
+          const uint32_t f = sm0 + PF_OFF_F + (2 * fp + u) * PF_F_BYTES;
+          const uint32_t bm = f + PF_F_BMAIN + (lane >> 3) * 512 + (lane & 7) * 16;
+          uint4 o = i8x8_to_h(xv[u][0].x, xv[u][0].y);
+          sts128(bm, o.x, o.y, o.z, o.w);
+          o = i8x8_to_h(xv[u][0].z, xv[u][0].w);
+          sts128(bm + 128, o.x, o.y, o.z, o.w);
+          o = i8x8_to_h(xv[u][1].x, xv[u][1].y);
+          sts128(bm + 256, o.x, o.y, o.z, o.w);
+          o = i8x8_to_h(xv[u][1].z, xv[u][1].w);
+          sts128(bm + 384, o.x, o.y, o.z, o.w);
+          if (sbf)
+            sts128(f + PF_F_BMIN + (lane >> 3) * 256 + (lane & 7) * 16,
+                   h_of_int((int)(int16_t)(gv[u] & 0xFFFF)) | (h_of_int(gv[u] >> 16) << 16), 0, 0, 0);
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sm0 + PF_OFF_X + (2 * xp + u) * PF_X_BYTES + 4 * lane),
+                       "f"(dv[u])
+                       : "memory");
+        }
+#pragma unroll
+        for (int u = 0; u < 2; u++) xv[u][0] = xv[u + 2][0], xv[u][1] = xv[u + 2][1], gv[u] = gv[u + 2], dv[u] = dv[u + 2];
+        load_tok(b + 4, xv[2], gv[2], dv[2]);
+        load_tok(b + 5, xv[3], gv[3], dv[3]);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(B.f_full + 8 * fs), mbar_arrive(B.x_full + 8 * xs);
+        if (lane == 0) mbar_arrive(B.f_full + 8 * fp), mbar_arrive(B.x_full + 8 * xp);
       }
     }
     if (!ok) pf_fail(abort, a.err);
@@ -624,61 +636,64 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
 #pragma unroll
         for (int k = 0; k < 8; k++) seg[m][k] = 0ull, tot[m][k] = 0ull;
       int segleft = bseg;  // blocks left in the current segment
-      for (int b = 0; b < nb; b++, fc++) {
-        const int ts = fc % PF_TS, xs = fc % PF_XS;
-        if (!pf_wait(B.t_full + 8 * ts, (fc / PF_TS) & 1, abort) ||
-            !pf_wait(B.x_full + 8 * xs, (fc / PF_XS) & 1, abort)) {
+      for (int b = 0; b < nb; b += 2, fc++) {  // fc: pairs
+        const int tp = fc % PF_TP, xp = fc % PF_XP;
+        if (!pf_wait(B.t_full + 8 * tp, (fc / PF_TP) & 1, abort) ||
+            !pf_wait(B.x_full + 8 * xp, (fc / PF_XP) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t xsd = sm0 + PF_OFF_X + xs * PF_X_BYTES;
-        const uint32_t t0 = tbase + ((uint32_t)(32 * q) << 16) + ts * 128 + 16 * p;
 #pragma unroll
-        for (int m = 0; m < MATS; m++) {
-          float A[16], Bm[16];
-          tmem_ld16x2(t0 + 32 * m, t0 + 64 + 32 * m, A, Bm);
-          if (m == MATS - 1) {  // every load of the stage is done: release it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.t_empty + 8 * ts);
-          }
-          const uint2 ddv = ld_shared_v2(xsd + PF_X_DD + (m * 128 + row) * 8);
-          const float d = __uint_as_float(ddv.x), dmin = __uint_as_float(ddv.y);
-          // (-dmin) * B is exactly -(dmin * B): the block term is
-          // dx * fma(d, A, -(dmin * B)) (2-bit) or (d * dx) * I (Q8_0)
-          const unsigned long long d2 = f2_pack(d, d), nm2 = f2_pack(-dmin, -dmin);
+        for (int u = 0; u < 2; u++) {  // the pair's blocks in order
+          const uint32_t xsd = sm0 + PF_OFF_X + (2 * xp + u) * PF_X_BYTES;
+          const uint32_t t0 = tbase + ((uint32_t)(32 * q) << 16) + (2 * tp + u) * 128 + 16 * p;
 #pragma unroll
-          for (int j4 = 0; j4 < 4; j4++) {
-            if (4 * j4 < nvp) {
-              const uint4 v = ld_shared_v4(xsd + 4 * (16 * p + 4 * j4));
+          for (int m = 0; m < MATS; m++) {
+            float A[16], Bm[16];
+            tmem_ld16x2(t0 + 32 * m, t0 + 64 + 32 * m, A, Bm);
+            if (u == 1 && m == MATS - 1) {  // every load of the pair stage is done: release it
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(B.t_empty + 8 * tp);
+            }
+            const uint2 ddv = ld_shared_v2(xsd + PF_X_DD + (m * 128 + row) * 8);
+            const float d = __uint_as_float(ddv.x), dmin = __uint_as_float(ddv.y);
+            // (-dmin) * B is exactly -(dmin * B): the block term is
+            // dx * fma(d, A, -(dmin * B)) (2-bit) or (d * dx) * I (Q8_0)
+            const unsigned long long d2 = f2_pack(d, d), nm2 = f2_pack(-dmin, -dmin);
 #pragma unroll
-              for (int jp = 0; jp < 2; jp++) {
-                const int j = 4 * j4 + 2 * jp, k = j >> 1;
-                const unsigned long long dx2 =
-                    jp ? f2_pack(__uint_as_float(v.z), __uint_as_float(v.w))
-                       : f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
-                const unsigned long long a2 = f2_pack(A[j], A[j + 1]);
-                // ptxas merges a packed product whose only use is a packed
-                // add into one single-rounding multiply-add (.rn or not);
-                // here the add takes one of two products chosen at run time
-                // and stays separate (the parity tests hold it to the bit).
-                // A rewrite without the run-time choice must round the
-                // product on its own (a scalar product, or a second use).
-                unsigned long long term;
-                if (sbf) term = f2_mul(dx2, f2_fma(d2, a2, f2_mul(nm2, f2_pack(Bm[j], Bm[j + 1]))));
-                else term = f2_mul(f2_mul(d2, dx2), a2);
-                seg[m][k] = f2_add(seg[m][k], term);
+            for (int j4 = 0; j4 < 4; j4++) {
+              if (4 * j4 < nvp) {
+                const uint4 v = ld_shared_v4(xsd + 4 * (16 * p + 4 * j4));
+#pragma unroll
+                for (int jp = 0; jp < 2; jp++) {
+                  const int j = 4 * j4 + 2 * jp, k = j >> 1;
+                  const unsigned long long dx2 =
+                      jp ? f2_pack(__uint_as_float(v.z), __uint_as_float(v.w))
+                         : f2_pack(__uint_as_float(v.x), __uint_as_float(v.y));
+                  const unsigned long long a2 = f2_pack(A[j], A[j + 1]);
+                  // ptxas merges a packed product whose only use is a packed
+                  // add into one single-rounding multiply-add (.rn or not);
+                  // here the add takes one of two products chosen at run time
+                  // and stays separate (the parity tests hold it to the bit).
+                  // A rewrite without the run-time choice must round the
+                  // product on its own (a scalar product, or a second use).
+                  unsigned long long term;
+                  if (sbf) term = f2_mul(dx2, f2_fma(d2, a2, f2_mul(nm2, f2_pack(Bm[j], Bm[j + 1]))));
+                  else term = f2_mul(f2_mul(d2, dx2), a2);
+                  seg[m][k] = f2_add(seg[m][k], term);
+                }
               }
             }
           }
-        }
-        if (--segleft == 0) {
-          segleft = bseg;
+          if (--segleft == 0) {
+            segleft = bseg;
 #pragma unroll
-          for (int m = 0; m < MATS; m++)
+            for (int m = 0; m < MATS; m++)
 #pragma unroll
-            for (int k = 0; k < 8; k++) tot[m][k] = f2_add(tot[m][k], seg[m][k]), seg[m][k] = 0ull;
+              for (int k = 0; k < 8; k++) tot[m][k] = f2_add(tot[m][k], seg[m][k]), seg[m][k] = 0ull;
+          }
         }
       }
       if (!ok) break;
