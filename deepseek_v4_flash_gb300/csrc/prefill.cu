@@ -50,29 +50,36 @@ constexpr int PF_CW = 4;   // converter warps (weights)
 constexpr int PF_EW = 8;   // epilogue warps
 constexpr int PF_WARPS = 2 + PF_CW + PF_EW + 1;  // + the token warp
 constexpr int PF_RS = 2;                 // raw stages
-constexpr int PF_RAW = 16 * Q4S_TILE;    // 37888 bytes, the largest raw stage
 // The pipeline between the converters, the MMA thread and the epilogue moves
-// pairs of 32-blocks (b, b + 1): one barrier hand-off per pair.
-constexpr int PF_FS = 4;                 // fp16 operand slots, one 32-block each
-constexpr int PF_TS = 4;                 // TMEM regions of 128 columns, one 32-block each
-constexpr int PF_FP = PF_FS / 2;         // fp16 pair stages
-constexpr int PF_TP = PF_TS / 2;         // TMEM pair stages
-constexpr int PF_XP = 5;                 // side-data pair stages, >= PF_FP + PF_TP + 1
-constexpr int PF_XS = 2 * PF_XP;         // side-data slots, one 32-block each
-constexpr int PF_TMEM_COLS = PF_TS * 128;
-// fp16 stage: A main [2 mats][128 x 32] | A min [2][128 x 16] | B main [32 x 32] | B min [32 x 16]
-constexpr int PF_F_AMAIN = 0, PF_F_AMIN = 16384, PF_F_BMAIN = 24576, PF_F_BMIN = 26624, PF_F_BYTES = 27648;
-// side stage: dx [32 columns] f32 | (d, dmin) [2 mats][128 rows] float2
-constexpr int PF_X_DD = 128, PF_X_BYTES = 128 + 2 * 128 * 8;
-constexpr int PF_OFF_RAW = 0;
-constexpr int PF_OFF_F = PF_OFF_RAW + PF_RS * PF_RAW;
-constexpr int PF_OFF_X = PF_OFF_F + PF_FS * PF_F_BYTES;
-constexpr int PF_OFF_BAR = PF_OFF_X + PF_XS * PF_X_BYTES;
+// G 32-blocks per barrier hand-off: stages of G fp16 slots, G TMEM regions
+// (all of TMEM in two stages) and G side slots.
+constexpr int PF_FP = 2;                 // fp16 stages
+constexpr int PF_TP = 2;                 // TMEM stages
+constexpr int PF_XP = 5;                 // side-data stages, >= PF_FP + PF_TP + 1
+constexpr int PF_TMEM_COLS = 512;
+constexpr int PF_X_DD = 128;             // side slot: dx [32 columns] f32, then (d, dmin) [mats][128 rows] float2
 constexpr int PF_NBARS = 2 * PF_RS + 2 * PF_FP + 2 * PF_TP + PF_XP;
-constexpr int PF_OFF_MISC = PF_OFF_BAR + PF_NBARS * 8;
-constexpr int PF_SMEM = PF_OFF_MISC + 64;
 static_assert(PF_XP >= PF_FP + PF_TP + 1, "side ring too short");
-static_assert(PF_SMEM <= 227 * 1024, "prefill kernel does not fit shared memory");
+
+// Geometry of the gate/up (MODE 0: two matrices, 128 TMEM columns per block:
+// A and B of each) and the down kernel (MODE 1: one matrix, 64 columns).
+template <int MODE>
+struct PfL {
+  static constexpr int MATS = MODE == 0 ? 2 : 1;
+  static constexpr int TCOLS = 64 * MATS;             // TMEM columns per 32-block
+  static constexpr int G = PF_TMEM_COLS / (PF_TP * TCOLS);  // 32-blocks per hand-off: 2 or 4
+  static constexpr int FS = PF_FP * G, XS = PF_XP * G;
+  // raw stage: 16 (gate/up) or 8 (down) tiles of the largest format
+  static constexpr int RAW = (MODE == 0 ? 16 : 8) * Q4S_TILE;
+  // fp16 slot: A main [mats][128 x 32] | A min [mats][128 x 16] | B main [32 x 32] | B min [32 x 16]
+  static constexpr int FAMAIN = 0, FAMIN = MATS * 8192, FBMAIN = FAMIN + MATS * 4096, FBMIN = FBMAIN + 2048,
+                       FBYTES = FBMIN + 1024;
+  static constexpr int XBYTES = PF_X_DD + MATS * 128 * 8;
+  static constexpr int OFF_F = PF_RS * RAW, OFF_X = OFF_F + FS * FBYTES, OFF_BAR = OFF_X + XS * XBYTES;
+  static constexpr int OFF_MISC = OFF_BAR + PF_NBARS * 8, SMEM = OFF_MISC + 64;
+  static_assert(SMEM <= 227 * 1024, "prefill kernel does not fit shared memory");
+  static_assert(G * PF_TP * TCOLS == PF_TMEM_COLS, "TMEM stages");
+};
 
 struct PfArgs {
   int H, F, k, NS, T, E;
@@ -209,8 +216,9 @@ struct PfBars {
   uint32_t raw_full, raw_empty, f_full, f_empty, t_full, t_empty, x_full;
 };
 
+template <int MODE>
 __device__ __forceinline__ PfBars pf_bars(uint8_t *smem) {
-  const uint32_t b = smem_u32(smem + PF_OFF_BAR);
+  const uint32_t b = smem_u32(smem + PfL<MODE>::OFF_BAR);
   PfBars p;
   p.raw_full = b;
   p.raw_empty = p.raw_full + 8 * PF_RS;
@@ -245,11 +253,12 @@ __device__ __forceinline__ void pf_fail(volatile int *abort, uint32_t *err) {
 template <int MODE>
 __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  constexpr int MATS = MODE == 0 ? 2 : 1;
+  using L = PfL<MODE>;
+  constexpr int MATS = L::MATS, G = L::G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const PfBars B = pf_bars(smem);
-  volatile int *abort = (volatile int *)(smem + PF_OFF_MISC);
-  uint32_t *tslot = (uint32_t *)(smem + PF_OFF_MISC + 16);
+  const PfBars B = pf_bars<MODE>(smem);
+  volatile int *abort = (volatile int *)(smem + L::OFF_MISC);
+  uint32_t *tslot = (uint32_t *)(smem + L::OFF_MISC + 16);
   const int RB = a.rows / PF_M;
   const int n_items = __ldg(a.pass_off + a.E + 1) * RB;
   const int nb = a.K >> 5;
@@ -264,8 +273,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
     fence_mbar_init();
   }
   // the parts of the min tiles that no block writes stay zero
-  for (int i = threadIdx.x; i < PF_FS * (PF_F_BYTES / 16); i += blockDim.x)
-    sts128(sm0 + PF_OFF_F + 16 * i, 0, 0, 0, 0);
+  for (int i = threadIdx.x; i < L::FS * (L::FBYTES / 16); i += blockDim.x)
+    sts128(sm0 + L::OFF_F + 16 * i, 0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) tmem_alloc(smem_u32(tslot), PF_TMEM_COLS);
   tc_fence_before();
@@ -300,7 +309,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
         if (lane < nchunk) {
           const int grp = it.rb * nchunk + lane;  // 16-row group (gate/up) or 32-row group (down)
           const uint8_t *src = it.base + ((size_t)grp * KS + (size_t)st * ks_per) * 2 * TB;
-          bulk_g2s(sm0 + PF_OFF_RAW + rs * PF_RAW + lane * chunk, src, chunk, B.raw_full + 8 * rs);
+          bulk_g2s(sm0 + rs * L::RAW + lane * chunk, src, chunk, B.raw_full + 8 * rs);
         }
       }
     }
@@ -319,21 +328,21 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
       // the operand descriptors of fp16 stage 0; stage fs adds its byte
       // offset / 16 to the start-address field (14 bits: shared-memory
       // addresses below 256 KB never carry out of it)
-      const uint32_t f0 = sm0 + PF_OFF_F;
+      const uint32_t f0 = sm0 + L::OFF_F;
       uint64_t dam[2][2], dan[2], dbm[2];
 #pragma unroll
       for (int m = 0; m < 2; m++) {
-        dam[m][0] = umma_desc(f0 + PF_F_AMAIN + m * 8192, 128, 512);
-        dam[m][1] = umma_desc(f0 + PF_F_AMAIN + m * 8192 + 256, 128, 512);
-        dan[m] = umma_desc(f0 + PF_F_AMIN + m * 4096, 128, 256);
-        dbm[m] = umma_desc(f0 + PF_F_BMAIN + 256 * m, 128, 512);
+        dam[m][0] = umma_desc(f0 + L::FAMAIN + m * 8192, 128, 512);
+        dam[m][1] = umma_desc(f0 + L::FAMAIN + m * 8192 + 256, 128, 512);
+        dan[m] = umma_desc(f0 + L::FAMIN + m * 4096, 128, 256);
+        dbm[m] = umma_desc(f0 + L::FBMAIN + 256 * m, 128, 512);
       }
-      const uint64_t dbn = umma_desc(f0 + PF_F_BMIN, 128, 256);
+      const uint64_t dbn = umma_desc(f0 + L::FBMIN, 128, 256);
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const PfItem it = pf_item<MODE>(a, i, RB);
         if (it.nv <= 0) continue;
         const bool sbf = it.fmt != DS4MOE_Q8_0;
-        for (int b = 0; b < nb; b += 2, fc++) {  // fc: pairs
+        for (int b = 0; b < nb; b += G, fc++) {  // fc: stages of G blocks
           const int fp = fc % PF_FP, tp = fc % PF_TP;
           if (!pf_wait(B.f_full + 8 * fp, (fc / PF_FP) & 1, abort) ||
               (fc >= PF_TP && !pf_wait(B.t_empty + 8 * tp, ((fc / PF_TP) - 1) & 1, abort))) {
@@ -342,14 +351,14 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
           }
           tc_fence_after();
 #pragma unroll
-          for (int u = 0; u < 2; u++) {
-            const uint64_t off = (uint64_t)(((2 * fp + u) * PF_F_BYTES) >> 4);
-            const uint32_t d0 = tbase + (2 * tp + u) * 128;
+          for (int u = 0; u < G; u++) {
+            const uint64_t off = (uint64_t)(((G * fp + u) * L::FBYTES) >> 4);
+            const uint32_t d0 = tbase + (G * tp + u) * L::TCOLS;  // A of the mats, then B of the mats
 #pragma unroll
             for (int m = 0; m < MATS; m++) {
               umma_f16(d0 + 32 * m, dam[m][0] + off, dbm[0] + off, idesc, 0);
               umma_f16(d0 + 32 * m, dam[m][1] + off, dbm[1] + off, idesc, 1);
-              if (sbf) umma_f16(d0 + 64 + 32 * m, dan[m] + off, dbn + off, idesc, 0);
+              if (sbf) umma_f16(d0 + 32 * MATS + 32 * m, dan[m] + off, dbn + off, idesc, 0);
             }
           }
           umma_commit(B.f_empty + 8 * fp);
@@ -385,17 +394,18 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
           ok = false;
           break;
         }
-        // pair fc: blocks b, b + 1 into fp16 slots 2*fp, 2*fp + 1 and side
-        // slots 2*xp, 2*xp + 1
-        const int fp = fc % PF_FP, xp = fc % PF_XP;
-        const int fsu[2] = {2 * fp, 2 * fp + 1}, xsu[2] = {2 * xp, 2 * xp + 1};
+        // blocks b, b + 1 of stage fc (G blocks) into fp16 slots G*fp + w,
+        // + 1 and side slots G*xp + w, + 1 (w = b % G); the stage's slots are
+        // free once its previous MMAs are done
+        const int fp = fc % PF_FP, xp = fc % PF_XP, w = b % G;
+        const int fsu[2] = {G * fp + w, G * fp + w + 1}, xsu[2] = {G * xp + w, G * xp + w + 1};
         bool waited = true;
-        if (fc >= PF_FP && !pf_wait(B.f_empty + 8 * fp, ((fc / PF_FP) - 1) & 1, abort)) waited = false;
+        if (w == 0 && fc >= PF_FP && !pf_wait(B.f_empty + 8 * fp, ((fc / PF_FP) - 1) & 1, abort)) waited = false;
         if (!waited) {
           ok = false;
           break;
         }
-        const uint32_t raw = sm0 + PF_OFF_RAW + rs * PF_RAW;
+        const uint32_t raw = sm0 + rs * L::RAW;
         // ---- weights: tiles tau0 and (gate/up) tau0 + 8, row rr
         if (q4) {
           // a 32-block of one row is one 16-byte chunk: four words of eight
@@ -418,8 +428,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
           }
 #pragma unroll
           for (int u = 0; u < 2; u++) {
-            const uint32_t f = sm0 + PF_OFF_F + fsu[u] * PF_F_BYTES;
-            const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
+            const uint32_t f = sm0 + L::OFF_F + fsu[u] * L::FBYTES;
+            const uint32_t xsd = sm0 + L::OFF_X + xsu[u] * L::XBYTES;
 #pragma unroll
             for (int h2 = 0; h2 < NH; h2++) {
               const uint32_t sm = smb[u][h2];
@@ -428,7 +438,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
               const int tau = tau0 + 8 * h2;
               const int m = MODE == 0 ? (tau & 1) : 0;
               const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
-              const uint32_t ar = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
+              const uint32_t ar = f + L::FAMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
               uint4 o = q4s_word_to_h(w[u][h2].x, sc2a, nsc2a);
               sts128(ar, o.x, o.y, o.z, o.w);
               o = q4s_word_to_h(w[u][h2].y, sc2a, nsc2a);
@@ -437,7 +447,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
               sts128(ar + 256, o.x, o.y, o.z, o.w);
               o = q4s_word_to_h(w[u][h2].w, sc2b, nsc2b);
               sts128(ar + 384, o.x, o.y, o.z, o.w);
-              sts128(f + PF_F_AMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, h2_small((sm >> 4) & 15, (sm >> 12) & 15),
+              sts128(f + L::FAMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, h2_small((sm >> 4) & 15, (sm >> 12) & 15),
                      0, 0, 0);
               asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8),
                            "f"(dd_d[h2]), "f"(dd_m[h2])
@@ -475,19 +485,19 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
             }
 #pragma unroll
           for (int u = 0; u < 2; u++) {
-            const uint32_t f = sm0 + PF_OFF_F + fsu[u] * PF_F_BYTES;
-            const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
+            const uint32_t f = sm0 + L::OFF_F + fsu[u] * L::FBYTES;
+            const uint32_t xsd = sm0 + L::OFF_X + xsu[u] * L::XBYTES;
 #pragma unroll
             for (int h2 = 0; h2 < NH; h2++) {
               const int tau = tau0 + 8 * h2;
               const int m = MODE == 0 ? (tau & 1) : 0;
               const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
-              const uint32_t ar = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
+              const uint32_t ar = f + L::FAMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
               sts128(ar, lo[u][h2][0].x, lo[u][h2][0].y, lo[u][h2][0].z, lo[u][h2][0].w);
               sts128(ar + 128, hi[u][h2][0].x, hi[u][h2][0].y, hi[u][h2][0].z, hi[u][h2][0].w);
               sts128(ar + 256, lo[u][h2][1].x, lo[u][h2][1].y, lo[u][h2][1].z, lo[u][h2][1].w);
               sts128(ar + 384, hi[u][h2][1].x, hi[u][h2][1].y, hi[u][h2][1].z, hi[u][h2][1].w);
-              sts128(f + PF_F_AMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, mnw[u][h2], 0, 0, 0);
+              sts128(f + L::FAMIN + m * 4096 + (r >> 3) * 256 + (r & 7) * 16, mnw[u][h2], 0, 0, 0);
               asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(xsd + PF_X_DD + (m * 128 + r) * 8),
                            "f"(dd_d[h2]), "f"(dd_m[h2])
                            : "memory");
@@ -518,14 +528,14 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
             }
 #pragma unroll
           for (int u = 0; u < 2; u++) {
-            const uint32_t f = sm0 + PF_OFF_F + fsu[u] * PF_F_BYTES;
-            const uint32_t xsd = sm0 + PF_OFF_X + xsu[u] * PF_X_BYTES;
+            const uint32_t f = sm0 + L::OFF_F + fsu[u] * L::FBYTES;
+            const uint32_t xsd = sm0 + L::OFF_X + xsu[u] * L::XBYTES;
 #pragma unroll
             for (int h2 = 0; h2 < NH; h2++) {
               const int tau = tau0 + 8 * h2;
               const int m = MODE == 0 ? (tau & 1) : 0;
               const int r = MODE == 0 ? 16 * (tau >> 1) + rr : 16 * tau + rr;
-              const uint32_t ar = f + PF_F_AMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
+              const uint32_t ar = f + L::FAMAIN + m * 8192 + (r >> 3) * 512 + (r & 7) * 16;
 #pragma unroll
               for (int kc = 0; kc < 4; kc++)
                 sts128(ar + 128 * kc, o[u][h2][kc].x, o[u][h2][kc].y, o[u][h2][kc].z, o[u][h2][kc].w);
@@ -536,10 +546,12 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
             }
           }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(B.f_full + 8 * fp), mbar_arrive(B.x_full + 8 * xp);
-        fc++;
+        if (w + 2 == G) {  // the stage's last two blocks: publish it
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B.f_full + 8 * fp), mbar_arrive(B.x_full + 8 * xp);
+          fc++;
+        }
         if (bin0 + 1 == bpst - 1) {
           if (lane == 0) mbar_arrive(B.raw_empty + 8 * rs);
           gst++;
@@ -563,8 +575,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
         const int code = __ldg(a.list + it.list_off + pt);
         arow = MODE == 0 ? (code >> 5) : (code >> 5) * a.NS + (code & 31);
       }
-      // software prefetch four blocks ahead: slots 0, 1 hold the pair's
-      // blocks b, b + 1, slots 2, 3 the next pair's
+      // software prefetch four blocks ahead: slots 0 .. G-1 hold the
+      // stage's blocks (G = 2: slots 2, 3 the next stage's)
       uint4 xv[4][2];
       int gv[4];
       float dv[4];
@@ -579,16 +591,16 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
       };
 #pragma unroll
       for (int u = 0; u < 4; u++) load_tok(u, xv[u], gv[u], dv[u]);
-      for (int b = 0; b < nb; b += 2, fc++) {  // fc: pairs
+      for (int b = 0; b < nb; b += G, fc++) {  // fc: stages of G blocks
         const int fp = fc % PF_FP, xp = fc % PF_XP;
         if (fc >= PF_FP && !pf_wait(B.f_empty + 8 * fp, ((fc / PF_FP) - 1) & 1, abort)) {
           ok = false;
           break;
         }
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
-          const uint32_t f = sm0 + PF_OFF_F + (2 * fp + u) * PF_F_BYTES;
-          const uint32_t bm = f + PF_F_BMAIN + (lane >> 3) * 512 + (lane & 7) * 16;
+        for (int u = 0; u < G; u++) {
+          const uint32_t f = sm0 + L::OFF_F + (G * fp + u) * L::FBYTES;
+          const uint32_t bm = f + L::FBMAIN + (lane >> 3) * 512 + (lane & 7) * 16;
           uint4 o = i8x8_to_h(xv[u][0].x, xv[u][0].y);
           sts128(bm, o.x, o.y, o.z, o.w);
           o = i8x8_to_h(xv[u][0].z, xv[u][0].w);
@@ -598,16 +610,21 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
           o = i8x8_to_h(xv[u][1].z, xv[u][1].w);
           sts128(bm + 384, o.x, o.y, o.z, o.w);
           if (sbf)
-            sts128(f + PF_F_BMIN + (lane >> 3) * 256 + (lane & 7) * 16,
+            sts128(f + L::FBMIN + (lane >> 3) * 256 + (lane & 7) * 16,
                    h_of_int((int)(int16_t)(gv[u] & 0xFFFF)) | (h_of_int(gv[u] >> 16) << 16), 0, 0, 0);
-          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sm0 + PF_OFF_X + (2 * xp + u) * PF_X_BYTES + 4 * lane),
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sm0 + L::OFF_X + (G * xp + u) * L::XBYTES + 4 * lane),
                        "f"(dv[u])
                        : "memory");
         }
+        if constexpr (G == 2) {
 #pragma unroll
-        for (int u = 0; u < 2; u++) xv[u][0] = xv[u + 2][0], xv[u][1] = xv[u + 2][1], gv[u] = gv[u + 2], dv[u] = dv[u + 2];
-        load_tok(b + 4, xv[2], gv[2], dv[2]);
-        load_tok(b + 5, xv[3], gv[3], dv[3]);
+          for (int u = 0; u < 2; u++) xv[u][0] = xv[u + 2][0], xv[u][1] = xv[u + 2][1], gv[u] = gv[u + 2], dv[u] = dv[u + 2];
+          load_tok(b + 4, xv[2], gv[2], dv[2]);
+          load_tok(b + 5, xv[3], gv[3], dv[3]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; u++) load_tok(b + 4 + u, xv[u], gv[u], dv[u]);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(B.f_full + 8 * fp), mbar_arrive(B.x_full + 8 * xp);
@@ -636,7 +653,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
 #pragma unroll
         for (int k = 0; k < 8; k++) seg[m][k] = 0ull, tot[m][k] = 0ull;
       int segleft = bseg;  // blocks left in the current segment
-      for (int b = 0; b < nb; b += 2, fc++) {  // fc: pairs
+      for (int b = 0; b < nb; b += G, fc++) {  // fc: stages of G blocks
         const int tp = fc % PF_TP, xp = fc % PF_XP;
         if (!pf_wait(B.t_full + 8 * tp, (fc / PF_TP) & 1, abort) ||
             !pf_wait(B.x_full + 8 * xp, (fc / PF_XP) & 1, abort)) {
@@ -645,14 +662,14 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) k_pf_experts(PfArgs a) {
         }
         tc_fence_after();
 #pragma unroll
-        for (int u = 0; u < 2; u++) {  // the pair's blocks in order
-          const uint32_t xsd = sm0 + PF_OFF_X + (2 * xp + u) * PF_X_BYTES;
-          const uint32_t t0 = tbase + ((uint32_t)(32 * q) << 16) + (2 * tp + u) * 128 + 16 * p;
+        for (int u = 0; u < G; u++) {  // the stage's blocks in order
+          const uint32_t xsd = sm0 + L::OFF_X + (G * xp + u) * L::XBYTES;
+          const uint32_t t0 = tbase + ((uint32_t)(32 * q) << 16) + (G * tp + u) * L::TCOLS + 16 * p;
 #pragma unroll
           for (int m = 0; m < MATS; m++) {
             float A[16], Bm[16];
-            tmem_ld16x2(t0 + 32 * m, t0 + 64 + 32 * m, A, Bm);
-            if (u == 1 && m == MATS - 1) {  // every load of the pair stage is done: release it
+            tmem_ld16x2(t0 + 32 * m, t0 + 32 * MATS + 32 * m, A, Bm);
+            if (u == G - 1 && m == MATS - 1) {  // every load of the stage is done: release it
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(B.t_empty + 8 * tp);
@@ -814,8 +831,9 @@ bool prefill_supported(const ds4moe_layer_desc &d) {
 }
 
 cudaError_t prefill_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(k_pf_experts<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_pf_experts<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(k_pf_experts<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfL<0>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_pf_experts<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfL<1>::SMEM);
   return e;
 }
 
@@ -847,14 +865,14 @@ cudaError_t launch_prefill(ds4moe_layer *h, const float *x, const int32_t *tok, 
   if (e == cudaSuccess) {
     PfArgs g = a;
     g.K = d.hidden, g.rows = d.ffn, g.w_r = h->gu, g.w_s = h->sgu, g.aq = h->xq, g.ad = h->dx, g.ag = h->gs;
-    k_pf_experts<0><<<grid, PF_WARPS * 32, PF_SMEM, s>>>(g);
+    k_pf_experts<0><<<grid, PF_WARPS * 32, PfL<0>::SMEM, s>>>(g);
     e = cudaGetLastError();
   }
   mark(4);
   if (e == cudaSuccess) {
     PfArgs g = a;
     g.K = d.ffn, g.rows = d.hidden, g.w_r = h->dn, g.w_s = h->sdn, g.aq = h->hq, g.ad = h->dh, g.ag = h->gsh;
-    k_pf_experts<1><<<grid, PF_WARPS * 32, PF_SMEM, s>>>(g);
+    k_pf_experts<1><<<grid, PF_WARPS * 32, PfL<1>::SMEM, s>>>(g);
     e = cudaGetLastError();
   }
   mark(5);
