@@ -98,9 +98,9 @@ typedef struct {
   float route_scale;    /* multiplies the renormalised routed weights (1.0)         */
   int32_t max_tokens;   /* largest n_tok of any later call, 1..1048576. A call of   */
                         /* fewer than 65 tokens runs on the decode path in chunks  */
-                        /* of at most 64 tokens; a larger one (when the layer's    */
-                        /* formats allow it) on the prefill path in chunks of at   */
-                        /* most 4096 tokens. Scratch is sized at create for        */
+                        /* of at most 64 tokens; a larger one (when hidden and ffn */
+                        /* are multiples of 128) on the prefill path in chunks of  */
+                        /* at most 4096 tokens. Scratch is sized at create for     */
                         /* Ts = max(min(max_tokens, 64), min(max_tokens, 4096))    */
                         /* tokens: about 560 MB at 4096 tokens and the DS4 shape   */
 } ds4moe_layer_desc;
@@ -199,9 +199,11 @@ ds4moe_status ds4moe_route_noalloc(const ds4moe_layer_desc *desc, const ds4moe_w
  *   y         [n_tok][H] fp32, read and written (must not alias x)
  * n_tok in 0..max_tokens. Enqueued on `stream`; no host synchronisation.
  * Calls of fewer than 65 tokens take the decode path (router, gate/up and
- * down kernels, chunks of at most 64 tokens); larger calls the prefill path
- * (tensor-core grouped GEMMs, chunks of at most 4096 tokens). Both give the
- * same bits. */
+ * down kernels, chunks of at most 64 tokens; units of eight tokens take
+ * their int8 block dots from the tensor cores); larger calls the prefill
+ * path (tensor-core grouped GEMMs, chunks of at most 4096 tokens; when hidden
+ * and ffn are multiples of 128, else the decode path). All give the same
+ * bits. */
 ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids,
                              float *y, void *stream);
 
