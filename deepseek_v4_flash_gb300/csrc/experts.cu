@@ -229,7 +229,10 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // to the others; the compute warps meanwhile run the shared expert's items,
 // which need no routing. The shared expert's weights are requested before
 // the wait for the previous kernel.
-template <int TT, bool AS, bool DOWN>
+// Q4: the 4-bit steps compiled in. The one-token kernels of layers without
+// a 4-bit matrix leave them out (a smaller instruction footprint: 2 % faster
+// at one token, measured; at eight tokens it measured slower, so only there).
+template <int TT, bool AS, bool DOWN, bool Q4 = true>
 __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(XArgs a) {
   constexpr int XE = x_epi_warps(TT), X_WARPS = x_warps(TT);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -504,7 +507,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
           for (int j = 0; j < c_ksps; j++) {
             const uint32_t t = st + j * c_kb;
             if (c_fmt == DS4MOE_Q2S) sb_step_mma<AS, false>(t, lane, s0 + j, a.K, ar_g, ar0, ar1, aq, ad, ag, macc);
-            else if (c_fmt == DS4MOE_Q4S) sb_step_mma<AS, true>(t, lane, s0 + j, a.K, ar_g, ar0, ar1, aq, ad, ag, macc);
+            else if (Q4 && c_fmt == DS4MOE_Q4S) sb_step_mma<AS, true>(t, lane, s0 + j, a.K, ar_g, ar0, ar1, aq, ad, ag, macc);
             else q8_step_mma<AS>(t, lane, s0 + j, a.K, ar_g, ar0, ar1, aq, ad, macc);
           }
         } else if (c_fmt == DS4MOE_Q2S && c_ksps == 2) {  // two K-steps in one block of code: their dots overlap
@@ -514,7 +517,7 @@ __global__ void __launch_bounds__(x_warps(TT) * 32, TT == 1 ? 2 : 1) k_experts(X
           for (int j = 0; j < c_ksps; j++) {
             const uint32_t t = st + j * c_kb;
             if (c_fmt == DS4MOE_Q2S) q2s_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, ag, acc);
-            else if (c_fmt == DS4MOE_Q4S) q4s_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, ag, acc);
+            else if (Q4 && c_fmt == DS4MOE_Q4S) q4s_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, ag, acc);
             else q8_step<TT, AS, (TT > 1)>(t, lane, s0 + j, a.K, arow, nt, aq, ad, acc);
           }
         }
@@ -716,9 +719,11 @@ size_t experts_smem(const ds4moe_layer *h) {
   return a > b ? a : b;
 }
 
+// q4: the layer holds a 4-bit matrix (the one-token kernels then keep the
+// 4-bit steps; the others always do)
 template <bool AS, bool DOWN>
-static const void *x_fn(int T) {
-  return T <= 2 ? (const void *)k_experts<1, AS, DOWN>
+static const void *x_fn(int T, bool q4) {
+  return T <= 2 ? (q4 ? (const void *)k_experts<1, AS, DOWN> : (const void *)k_experts<1, AS, DOWN, false>)
        : T <= 4 ? (const void *)k_experts<4, AS, DOWN> : (const void *)k_experts<8, AS, DOWN>;
 }
 
@@ -744,17 +749,21 @@ cudaError_t launch_experts(const ds4moe_layer *h, int T, float *y, int down, cud
   const size_t lim = T <= 2 ? (size_t)(228 * 1024 / 2 - 1024) : DEC_SMEM_LIMIT;
   const bool as = x_smem_bytes(h, T, down != 0, true) <= lim;
 
-  const void *fn = down ? (as ? x_fn<true, true>(T) : x_fn<false, true>(T)) : (as ? x_fn<true, false>(T) : x_fn<false, false>(T));
+  const bool q4 = x_wide(h);  // a 4-bit matrix anywhere in the layer
+  const void *fn = down ? (as ? x_fn<true, true>(T, q4) : x_fn<false, true>(T, q4))
+                        : (as ? x_fn<true, false>(T, q4) : x_fn<false, false>(T, q4));
   void *args[] = {&a};
   return launch_pdl(fn, dim3(x_blocks(h, T)), dim3(x_warps(x_tt(T)) * 32), x_smem_bytes(h, T, down != 0, as), s, args,
                     true);
 }
 
 cudaError_t experts_set_attributes() {
-  const void *fns[] = {x_fn<true, false>(1),  x_fn<true, false>(2),  x_fn<true, false>(4),  x_fn<true, false>(8),
-                       x_fn<false, false>(1), x_fn<false, false>(2), x_fn<false, false>(4), x_fn<false, false>(8),
-                       x_fn<true, true>(1),   x_fn<true, true>(2),   x_fn<true, true>(4),   x_fn<true, true>(8),
-                       x_fn<false, true>(1),  x_fn<false, true>(2),  x_fn<false, true>(4),  x_fn<false, true>(8)};
+  const void *fns[] = {x_fn<true, false>(1, true),  x_fn<true, false>(4, true),  x_fn<true, false>(8, true),
+                       x_fn<false, false>(1, true), x_fn<false, false>(4, true), x_fn<false, false>(8, true),
+                       x_fn<true, true>(1, true),   x_fn<true, true>(4, true),   x_fn<true, true>(8, true),
+                       x_fn<false, true>(1, true),  x_fn<false, true>(4, true),  x_fn<false, true>(8, true),
+                       x_fn<true, false>(1, false), x_fn<false, false>(1, false), x_fn<true, true>(1, false),
+                       x_fn<false, true>(1, false)};
   cudaError_t e = cudaSuccess;
   for (const void *f : fns)
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM_LIMIT);
