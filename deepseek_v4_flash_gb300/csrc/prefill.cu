@@ -25,17 +25,18 @@
 // tokens (MMA N). A persistent block walks items c, c + G, ... with four
 // warp roles connected by mbarriers:
 //   producer   1-D bulk copies of the packed weight tiles (raw ring)
-//   converters expand the weights of a pair of 32-blocks into fp16 operand
-//              tiles in the canonical no-swizzle K-major layout (fp16 ring),
-//              plus the epilogue's scales (side ring)
-//   token warp the pass's token codes, group sums and scales of the pair
-//   MMA        one thread issues the pair's MMAs into a TMEM stage (a region
-//              of 128 columns per block) and commits to the fp16 ring's and
-//              the TMEM stage's barriers
+//   converters expand the weights of a stage of 32-blocks into fp16
+//              operand tiles in the canonical no-swizzle K-major layout (fp16
+//              ring), plus the epilogue's scales (side ring)
+//   token warp the pass's token codes, group sums and scales of the stage
+//   MMA        one thread issues the stage's MMAs into a TMEM stage (a region
+//              of 128 columns per block for gate/up, 64 for down) and commits
+//              to the fp16 ring's and the TMEM stage's barriers
 //   epilogue   8 warps; warp w reads TMEM lanes 32*(w%4).. (rows) for one
 //              half of the pass's token columns, adds the block terms to the
 //              segment chains in block order, and finishes the item.
-// Every hand-off between these roles moves a pair of 32-blocks.
+// Every hand-off between these roles moves a stage of G 32-blocks: two for
+// gate/up, four for down (PfL).
 // Every wait is bounded; on a timeout the block raises DS4MOE_DEVERR_TIMEOUT,
 // drains what it has in flight and leaves.
 #include "common.cuh"
