@@ -321,12 +321,15 @@ def stack_cpu_baseline(w_hash, w_learned, budget_s=15.0):
 class Stack:
     """The 43-layer stack: every layer's weights resident (about 92 GB), each
     handle sized for `max_tokens`. A step carries T tokens through all 43
-    layers (RMSNorm, then the MoE FFN added to the residual stream)."""
+    layers (RMSNorm, then the MoE FFN added to the residual stream): by
+    default one ds4moe_forward_rmsnorm per layer on h in place (the RMSNorm
+    folded into the router kernel); with `fused` false, ds4moe_rmsnorm into
+    a buffer then ds4moe_forward (same bits)."""
 
-    def __init__(self, max_tokens, dev, keep=(), q4_tail=False):
+    def __init__(self, max_tokens, dev, keep=(), q4_tail=False, fused=True):
         import deepseek_v4_flash_gb300 as ds4
         import torch
-        self.ds4, self.dev = ds4, dev
+        self.ds4, self.dev, self.fused = ds4, dev, fused
         self.L = synth.N_STACK_LAYERS
         self.layers, self.specs, self.host = [], [], {}
         for l in range(self.L):
@@ -344,8 +347,12 @@ class Stack:
     def step(self, h, xn, T):
         ds4 = self.ds4
         for l in range(self.L):
-            ds4.rmsnorm(h[:T], xn[:T], 1e-6)
-            self.layers[l].forward(xn[:T], h[:T], self.tok[:T] if self.specs[l].route == "hash" else None)
+            tk = self.tok[:T] if self.specs[l].route == "hash" else None
+            if self.fused:
+                self.layers[l].forward_rmsnorm(h[:T], h[:T], 1e-6, tk)
+            else:
+                ds4.rmsnorm(h[:T], xn[:T], 1e-6)
+                self.layers[l].forward(xn[:T], h[:T], tk)
 
     def unique_experts(self, x0, T):
         """Routed experts each layer touches when x0 passes through the stack."""
@@ -389,7 +396,7 @@ class Stack:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             step()
-        launches = sum(Ly.launch_count() for Ly in self.layers) - n0 + self.L  # + the RMSNorm launches
+        launches = sum(Ly.launch_count() for Ly in self.layers) - n0 + (0 if self.fused else self.L)  # + RMSNorm
         for i in range(warmup):
             x_in.copy_(xs[i % NX])
             g.replay()
@@ -424,8 +431,12 @@ class Stack:
         for r in range(reps):
             h.copy_(xs[r % len(xs)])
             for l in range(self.L):
-                self.ds4.rmsnorm(h, xn, 1e-6)
-                self.layers[l].forward(xn, h, self.tok[:T] if self.specs[l].route == "hash" else None)
+                tk = self.tok[:T] if self.specs[l].route == "hash" else None
+                if self.fused:
+                    self.layers[l].forward_rmsnorm(h, h, 1e-6, tk)
+                else:
+                    self.ds4.rmsnorm(h, xn, 1e-6)
+                    self.layers[l].forward(xn, h, tk)
                 self.layers[l].profile_collect()
         per = {"hash": {}, "learned": {}}
         cnt = {"hash": 0, "learned": 0}
@@ -542,8 +553,9 @@ def run_stack(args):
         line["e2e"] = {"value": args.e2e_steps * T / dt, "unit": "tokens/s",
                        "h2d_bytes_per_step": T * synth.DS4.hidden * 4,
                        "d2h_bytes_per_step": T * synth.DS4.hidden * 4, "steps": args.e2e_steps,
-                       "how": "pinned host input copied in, ds4moe_rmsnorm + ds4moe_forward per layer "
-                              "(eager), result copied out, wall clock"}
+                       "how": "pinned host input copied in, " +
+                              ("ds4moe_forward_rmsnorm" if stack.fused else "ds4moe_rmsnorm + ds4moe_forward") +
+                              " per layer (eager), result copied out, wall clock"}
     if want_cpu:
         line["cpu_baseline"] = stack_cpu_baseline(stack.host[0], stack.host[synth.N_HASH_LAYERS])
     if rank == 0:

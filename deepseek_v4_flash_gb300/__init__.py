@@ -7,8 +7,9 @@ if the compiled library cannot be loaded, importing the binding fails.
 
 Entry points mirror the C ABI in include/ds4moe.h:
 ``Layer(desc, weights)`` = ds4moe_create, ``Layer.route`` = ds4moe_route,
-``Layer.forward`` = ds4moe_forward, ``Layer.forward_host`` =
-ds4moe_forward_host, ``rmsnorm`` = ds4moe_rmsnorm, ``route_noalloc`` =
+``Layer.forward`` = ds4moe_forward, ``Layer.forward_rmsnorm`` =
+ds4moe_forward_rmsnorm, ``Layer.forward_host`` = ds4moe_forward_host,
+``rmsnorm`` = ds4moe_rmsnorm, ``route_noalloc`` =
 ds4moe_route_noalloc, ``Dense`` = the ds4moe_dense_* calls.
 """
 from __future__ import annotations
@@ -69,6 +70,7 @@ def lib():
                                            vp, vp]),
             "ds4moe_forward": (i32, [vp, vp, i32, vp, vp, vp]),
             "ds4moe_forward_host": (i32, [vp, vp, i32, vp, vp, vp]),
+            "ds4moe_forward_rmsnorm": (i32, [vp, vp, i32, vp, ctypes.c_float, vp, vp]),
             "ds4moe_rmsnorm": (i32, [vp, vp, i32, i32, ctypes.c_float, vp]),
             "ds4moe_get_device_error": (i32, [vp, vp, ctypes.POINTER(u32)]),
             "ds4moe_debug_scratch": (i32, [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_uint64)]),
@@ -202,6 +204,12 @@ class Layer:
         n = x.shape[0] if n_tok is None else n_tok
         _check(lib().ds4moe_forward(self._h, _ptr(x), n, _ptr(token_ids), _ptr(y), _stream(stream)),
                "ds4moe_forward")
+
+    def forward_rmsnorm(self, x, y, eps: float = 1e-6, token_ids=None, stream=None, n_tok=None):
+        """y += MoE(RMSNorm(x)) on the device (ds4moe_forward_rmsnorm); y may be x."""
+        n = x.shape[0] if n_tok is None else n_tok
+        _check(lib().ds4moe_forward_rmsnorm(self._h, _ptr(x), n, _ptr(token_ids), eps, _ptr(y), _stream(stream)),
+               "ds4moe_forward_rmsnorm")
 
     def forward_host(self, x, y, token_ids=None, stream=None):
         """y += MoE(x) on host tensors (ds4moe_forward_host; synchronises)."""

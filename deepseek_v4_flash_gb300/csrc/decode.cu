@@ -1,7 +1,8 @@
 // decode.cu -- the router kernel of a decode-sized call (n_tok <= DEC_MAX_T)
 // and the launch helper shared with the expert kernels (experts.cu):
 //
-//   k_router_dec : int8 quantisation of x, the router GEMV segment sums,
+//   k_router_dec : (optionally) the RMSNorm of x, its int8 quantisation,
+//                  the router GEMV segment sums,
 //                  then (block 0 of each token's cluster) the token's routing
 //                  -- logits, sigmoid, bias top-k and renormalisation, or the
 //                  hash lookup -- and (the block that routed the last token)
@@ -23,7 +24,10 @@ namespace ds4 {
 // K1: quantisation, router segment sums, routing and bucketing.
 //
 // grid (ROUTER_SEGS, T), clusters of ROUTER_SEGS blocks: the cluster of
-// token t has one block per K segment. Block seg quantises the token's
+// token t has one block per K segment. When the call normalises its input,
+// every block first takes the inverse RMS norm of each of its tokens (warp
+// i: token i, the whole row, the RMSNorm kernel's arithmetic) and scales the
+// values it reads by it. Block seg quantises the token's
 // 32-blocks of its segment (and publishes them), then sums every router row
 // over the segment (warp w: row groups w, w + RC_WARPS, ...; lane = row) into
 // block 0's shared memory (distributed shared memory stores). After one
@@ -42,7 +46,8 @@ struct RouteDecArgs {
   const float *x;
   int T, H, E, E_pad, k, NS, n_shared, learned, q8, vocab, A_cap;
   int tg;               // tokens per cluster (1, or ROUTER_SEGS: block r routes token r)
-  float scale;
+  int norm;             // x is the un-normalised input: RMSNorm it first (eps)
+  float scale, eps;
   const uint8_t *W;     // router (RQ8 or F32 [E][H])
   const float *bias;
   const int32_t *hash, *tok;
@@ -84,6 +89,35 @@ __device__ __forceinline__ void quant_value(float v, int H, int t, int b, int la
   if ((lane & 15) == 0) gs_g[(size_t)t * (H >> 4) + 2 * b + (lane >> 4)] = (int16_t)s;
 }
 
+// CAS step 8 of one row v (H floats, 16-byte aligned, H a multiple of 256)
+// by one warp: 1 / sqrt(mean(v^2) + eps). Lane l keeps the fma chain of the
+// l-th of 32 contiguous segments in element order; the 32 segment sums are
+// then added in order, as the RMSNorm kernel does. A segment of up to 128
+// values is loaded in one round (one L2 round trip).
+__device__ __forceinline__ float rms_inv_warp(const float *v, int H, float eps, int lane) {
+  constexpr int RW = 32;  // float4 words per round
+  const int n4 = H >> 7;  // float4 words of a segment
+  const float4 *p = (const float4 *)(v + (size_t)lane * (H >> 5));
+  float acc = 0.0f;
+  for (int i = 0; i < n4; i += RW) {
+    float4 r[RW];
+#pragma unroll
+    for (int j = 0; j < RW; j++) r[j] = i + j < n4 ? __ldg(p + i + j) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < RW; j++) {
+      if (i + j < n4) {
+        acc = __fmaf_rn(r[j].x, r[j].x, acc);
+        acc = __fmaf_rn(r[j].y, r[j].y, acc);
+        acc = __fmaf_rn(r[j].z, r[j].z, acc);
+        acc = __fmaf_rn(r[j].w, r[j].w, acc);
+      }
+    }
+  }
+  float ss = 0.0f;
+  for (int l = 0; l < 32; l++) ss = __fadd_rn(ss, __shfl_sync(0xffffffffu, acc, l));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -123,6 +157,7 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   const int seg_bytes = a.q8 ? (c1 - c0) * RQ8_TILE : 0;
   const int nrg = a.learned ? (a.E_pad >> 5) : 0;
   int *s_flag = (int *)smem;
+  float *ninv = (float *)(smem + 16);  // [tg] inverse RMS norms of the cluster's tokens (header bytes 16..47)
   uint64_t *bars = (uint64_t *)(smem + 64);
   float *lgp = (float *)(smem + RC_HDR);
   float *dx_s = (float *)(smem + rc_dx_off(a.E_pad));                  // [tg][per]
@@ -154,22 +189,35 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   // weights while this kernel routes
   pdl_launch_dependents();
   // quantise the segment's blocks of the cluster's tokens (warp w: pairs
-  // (token, block) w, w + RC_WARPS, ...), all loads of a round first
+  // (token, block) w, w + RC_WARPS, ...), all loads of a round first; with
+  // the RMSNorm, the first round's loads are issued before the norms
   if (a.x) {
     constexpr int QB = 4;
     const int np = ntg * per;
-    for (int pp = warp; pp < np; pp += RC_WARPS * QB) {
-      float v[QB];
+    float v[QB];
+    auto load = [&](int pp) {
 #pragma unroll
       for (int j = 0; j < QB; j++) {
         const int p = pp + j * RC_WARPS, i = p / per, b = p - i * per;
         v[j] = p < np ? __ldg(a.x + (size_t)(t0 + i) * a.H + 32 * (b0 + b) + lane) : 0.0f;
       }
+    };
+    load(warp);
+    if (a.norm) {
+      if (warp < ntg) {
+        const float r = rms_inv_warp(a.x + (size_t)(t0 + warp) * a.H, a.H, a.eps, lane);
+        if (lane == 0) ninv[warp] = r;
+      }
+      __syncthreads();
+    }
+    for (int pp = warp; pp < np; pp += RC_WARPS * QB) {
+      if (pp != warp) load(pp);
 #pragma unroll
       for (int j = 0; j < QB; j++) {
         const int p = pp + j * RC_WARPS, i = p / per, b = p - i * per;
         if (p < np)
-          quant_value(v[j], a.H, t0 + i, b0 + b, lane, xq_s + 32 * p, dx_s + p, a.xq, a.dx, a.gs, a.err);
+          quant_value(a.norm ? __fmul_rn(v[j], ninv[i]) : v[j], a.H, t0 + i, b0 + b, lane, xq_s + 32 * p, dx_s + p,
+                      a.xq, a.dx, a.gs, a.err);
       }
     }
   }
@@ -217,7 +265,12 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
           const int j0 = seg * (a.H / ROUTER_SEGS), j1 = j0 + a.H / ROUTER_SEGS;
           const float *wr = (const float *)a.W + (size_t)r * a.H;
           const float *xv = a.x + (size_t)(t0 + i) * a.H;
-          for (int j = j0; j < j1; j++) acc = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), acc);
+          if (a.norm) {
+            const float inv = ninv[i];
+            for (int j = j0; j < j1; j++) acc = __fmaf_rn(__ldg(wr + j), __fmul_rn(__ldg(xv + j), inv), acc);
+          } else {
+            for (int j = j0; j < j1; j++) acc = __fmaf_rn(__ldg(wr + j), __ldg(xv + j), acc);
+          }
         }
         st_cluster_f32(lgp + seg * a.E_pad + r, i, acc);
       }
@@ -308,12 +361,13 @@ size_t route_dec_smem(const ds4moe_layer *h) {
 }
 
 cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
-                             float *w, bool bucket, cudaStream_t s) {
+                             float *w, bool bucket, cudaStream_t s, bool norm, float eps) {
   const ds4moe_layer_desc &d = h->d;
   RouteDecArgs r = {};
   r.x = x, r.T = T, r.H = d.hidden, r.E = d.n_experts, r.E_pad = h->E_pad, r.k = d.top_k, r.NS = h->NS;
   r.n_shared = d.n_shared, r.vocab = d.vocab, r.scale = d.route_scale, r.A_cap = h->A_max;
   r.learned = d.route == DS4MOE_ROUTE_LEARNED;
+  r.norm = norm && x, r.eps = eps;
   r.q8 = r.learned && d.router_fmt == DS4MOE_Q8_0;
   r.W = h->router, r.bias = h->bias, r.hash = h->hash, r.tok = tok;
   r.xq = h->xq, r.dx = h->dx, r.gs = h->gs, r.err = h->err;

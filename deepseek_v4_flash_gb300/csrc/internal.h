@@ -48,6 +48,7 @@ struct ds4moe_layer {
   int32_t *pf_meta;      // prefill: [E+1][2] {pairs, list offset} per group (0 shared, 1+e routed)
   int32_t *pf_pass;      // prefill: [E+2] first pass of each group, then the total
   int32_t *pf_list;      // prefill: [Tp*k + Tp] pair codes (token << 5) | slot, grouped
+  float *xnorm;          // [H] the normalised row of a one-token ds4moe_forward_rmsnorm call
 
   // Staging for ds4moe_forward_host.
   float *x_dev, *y_dev;
@@ -73,7 +74,7 @@ struct ds4moe_layer {
   long long wait_limit;  // hand-off wait bound of the decode expert kernels (0: WAIT_LIMIT)
 
   uint64_t bytes;        // total device bytes owned
-  void *allocs[32];
+  void *allocs[40];
   int n_allocs;
 };
 
@@ -97,7 +98,7 @@ constexpr int DEC_MAX_T = 64;  // largest n_tok served by the decode path
 static_assert(DS4_HOST_GRAPHS == DEC_MAX_T + 1, "one forward_host graph per decode chunk size");
 size_t route_dec_smem(const ds4moe_layer *h);
 cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
-                             float *w, bool bucket, cudaStream_t s);
+                             float *w, bool bucket, cudaStream_t s, bool norm = false, float eps = 0.0f);
 cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args, bool pdl);
 
 // prefill.cu
@@ -107,7 +108,7 @@ bool prefill_supported(const ds4moe_layer_desc &d);
 cudaError_t prefill_set_attributes();
 size_t prefill_list_ints(int T, int k, int n_shared);
 cudaError_t launch_prefill(ds4moe_layer *h, const float *x, const int32_t *tok, int T, float *y, cudaStream_t s,
-                           cudaEvent_t *ev);
+                           cudaEvent_t *ev, bool norm = false, float eps = 0.0f);
 
 // experts.cu
 size_t experts_smem(const ds4moe_layer *h);

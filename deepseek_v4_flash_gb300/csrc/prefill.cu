@@ -841,7 +841,7 @@ cudaError_t prefill_set_attributes() {
 size_t prefill_list_ints(int T, int k, int n_shared) { return (size_t)T * k + (size_t)(n_shared ? T : 0); }
 
 cudaError_t launch_prefill(ds4moe_layer *h, const float *x, const int32_t *tok, int T, float *y, cudaStream_t s,
-                           cudaEvent_t *ev) {
+                           cudaEvent_t *ev, bool norm, float eps) {
   const ds4moe_layer_desc &d = h->d;
   auto mark = [&](int i) {
     if (ev) cudaEventRecord(ev[i], s);
@@ -849,7 +849,7 @@ cudaError_t launch_prefill(ds4moe_layer *h, const float *x, const int32_t *tok, 
   const int E = d.n_experts, k = d.top_k;
   mark(0);
   mark(1);
-  cudaError_t e = launch_dec_route(h, x, tok, T, h->ids, h->wts, false, s);
+  cudaError_t e = launch_dec_route(h, x, tok, T, h->ids, h->wts, false, s, norm, eps);
   mark(2);
   if (e == cudaSuccess) {
     const size_t smem = (size_t)(E + 1 + 32) * 4;

@@ -207,6 +207,26 @@ ds4moe_status ds4moe_route_noalloc(const ds4moe_layer_desc *desc, const ds4moe_w
 ds4moe_status ds4moe_forward(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids,
                              float *y, void *stream);
 
+/* One layer of a stack: the RMSNorm with unit gain of ds4moe_rmsnorm (same
+ * arithmetic, same bits) folded into the forward,
+ *   y[t] += MoE(x[t] / sqrt(mean(x[t]^2) + eps)),
+ * for a residual stream that passes RMSNorm, then the MoE FFN added to it
+ * ("DeepSeek V4 Flash -- DFlash Integration", Forward Pass). From two tokens
+ * on (and on the prefill path) the router kernel normalises the rows as it
+ * quantises them, so no normalised copy is written and no extra kernel runs;
+ * a one-token decode call runs the RMSNorm kernel into a row buffer of the
+ * handle first (faster there). Bit-identical to ds4moe_rmsnorm into a
+ * buffer followed by ds4moe_forward on it.
+ *   x  [n_tok][H] fp32, read only, 16-byte aligned
+ *   y  [n_tok][H] fp32, read and written; may be x itself (y += on the
+ *      residual in place: every read of x completes before any write of y),
+ *      else must not overlap it
+ * Other arguments, paths, errors and stream behaviour as ds4moe_forward;
+ * DS4MOE_ERR_INVALID_ARG also for a NaN eps, an unaligned x or a partial
+ * overlap of x and y. */
+ds4moe_status ds4moe_forward_rmsnorm(ds4moe_layer *h, const float *x, int32_t n_tok, const int32_t *token_ids,
+                                     float eps, float *y, void *stream);
+
 /* ds4moe_forward on HOST buffers (pinned or pageable): y_host += MoE(x_host),
  * synchronising `stream` before it returns. Decode-sized calls (n_tok up to
  * min(max_tokens, 64)) on pinned buffers: the kernels read x and token_ids

@@ -73,6 +73,7 @@ def test_create_rejects_bad_abi_version(L):
 def test_calls_reject_null_handle_and_bad_sizes(L):
     assert L.ds4moe_forward(None, None, 1, None, None, None) == 1
     assert L.ds4moe_forward_host(None, None, 1, None, None, None) == 1
+    assert L.ds4moe_forward_rmsnorm(None, None, 1, None, 1e-6, None, None) == 1
     assert L.ds4moe_route(None, None, None, 1, None, None, None) == 1
     assert L.ds4moe_get_device_error(None, None, None) == 1
     assert L.ds4moe_rmsnorm(None, None, 1, 100, 1e-6, None) == 1   # hidden % 32

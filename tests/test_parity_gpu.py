@@ -332,6 +332,66 @@ def test_rmsnorm_bit_exact(ora, H):
     assert torch.equal(out, xd)
 
 
+# ds4moe_forward_rmsnorm: the RMSNorm folded into the router kernel, on rows
+# of very different scales, in place (y = x, the residual stream) and into a
+# separate y, against the oracle's RMSNorm followed by its forward. Covers
+# the decode path (one token per router cluster), the prefill path (clusters
+# of eight tokens from 16 tokens on), the fp32 router (TINY) and hash routing.
+@pytest.mark.parametrize("spec,seed,T,pf", [
+    (synth.MICRO, 61, 1, False), (synth.MICRO, 61, 2, False), (synth.MICRO, 61, 9, False),
+    (synth.MICRO, 61, 64, False), (synth.MICRO, 61, 130, False),
+    (synth.MICRO_HASH, 63, 33, False), (synth.TINY, 65, 4, False),
+    (synth.MICRO, 67, 3, True), (synth.MICRO, 67, 20, True), (synth.TINY, 69, 37, True),
+    (synth.MICRO_HASH, 71, 17, True),
+    (synth.DS4, 73, 1, False), (synth.DS4, 73, 8, False),
+])
+def test_forward_rmsnorm_bit_exact(ora, monkeypatch, spec, seed, T, pf):
+    import torch
+    if pf:
+        monkeypatch.setenv("DS4MOE_PREFILL_MIN_TOKENS", "1")
+    w = synth.gen_layer(spec, seed, 0)
+    ol = ora.layer(spec, w)
+    layer = make_layer(spec, w, T)
+    rng = np.random.default_rng(seed + T)
+    x = (synth.gen_x(spec, seed, T) * rng.uniform(0.01, 100, (T, 1))).astype(np.float32)
+    tok = synth.gen_token_ids(spec, seed, T) if spec.route == "hash" else None
+    y0 = (rng.standard_normal(x.shape) * 10).astype(np.float32)
+    xr = ora.rmsnorm(x, 1e-6)
+    ref_in_place, _, _, _ = ol.forward(xr, x.copy(), tok)
+    ref_sep, _, _, _ = ol.forward(xr, y0.copy(), tok)
+    td = torch.from_numpy(tok).cuda() if tok is not None else None
+    hd = torch.from_numpy(x).cuda()
+    xd, yd = hd.clone(), torch.from_numpy(y0).cuda()
+    layer.forward_rmsnorm(xd, yd, 1e-6, td)
+    layer.forward_rmsnorm(hd, hd, 1e-6, td)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    got_sep, got_in_place = yd.cpu().numpy(), hd.cpu().numpy()
+    assert np.array_equal(xd.cpu().numpy(), x), "x was written"
+    assert np.array_equal(got_sep.view(np.uint32), ref_sep.view(np.uint32)), \
+        f"separate y: {np.count_nonzero(got_sep != ref_sep)} values differ"
+    assert np.array_equal(got_in_place.view(np.uint32), ref_in_place.view(np.uint32)), \
+        f"in place: {np.count_nonzero(got_in_place != ref_in_place)} values differ"
+    layer.close()
+
+
+def test_forward_rmsnorm_rejects_overlap_and_misalignment(ora):
+    import torch
+    import deepseek_v4_flash_gb300 as ds4
+    spec = synth.MICRO
+    w, ol, layer = _layer_pair(ora, spec, 39, 65)
+    buf = torch.zeros(8 * spec.hidden + 4, device="cuda")
+    x = buf[:4 * spec.hidden].view(4, spec.hidden)
+    with pytest.raises(ds4.Ds4MoeError):  # y overlaps x by part
+        layer.forward_rmsnorm(x, buf[spec.hidden:5 * spec.hidden].view(4, spec.hidden))
+    with pytest.raises(ds4.Ds4MoeError):  # x not 16-byte aligned
+        layer.forward_rmsnorm(buf[1:1 + 4 * spec.hidden].view(4, spec.hidden), buf[4 * spec.hidden + 4:].view(4, spec.hidden))
+    with pytest.raises(ds4.Ds4MoeError):
+        layer.forward_rmsnorm(x, x, float("nan"))
+    layer.forward_rmsnorm(x, x, 1e-6, n_tok=0)
+    assert layer.device_error() == 0
+
+
 def test_empty_and_too_many_tokens(ora):
     import torch
     import deepseek_v4_flash_gb300 as ds4
