@@ -39,7 +39,7 @@ struct ds4moe_dense {
   int N, K, N_pad, max_tokens, part_tokens, device, n_sm;
   int dbg_ks, dbg_nst, dbg_ns;  // launch geometry overrides, 0 = automatic
   int dbg_tc;                   // 0 automatic, 1 dp4a path only, 2 tensor-core path where it fits
-  uint8_t *w;        // [N_pad/32][K/32][2][Q8 tile]
+  uint8_t *w;        // [N_pad/32][K/32][2][Q8 tile], row halves swizzled (k_repack_q8 swz)
   int8_t *xq;        // [max_tokens][K]
   float *dx;         // [max_tokens][K/32]
   float *part;       // [S][part_tokens][N_pad] segment sums of split rows
@@ -190,10 +190,12 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
   pdl_launch_dependents();
   pdl_wait();
   // dp4a step: row rr of tile m; tensor-core step: g, t4 as above, and the
-  // ldmatrix row address of this lane within a tile
-  const int m = lane >> 4, rr = lane & 15;
+  // ldmatrix row address of this lane within a tile. Rows 4-7 and 12-15 of a
+  // tile hold their two 16-byte halves swapped (bank-conflict-free reads).
+  const int m = lane >> 4, rr = lane & 15, rsw = 16 * ((rr >> 2) & 1);
   const int g = lane >> 2, t4 = lane & 3;
-  const uint32_t lm_off = Q8_Q + 32 * (((lane >> 3) & 1) * 8 + (lane & 7)) + 16 * (lane >> 4);
+  const int lr = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const uint32_t lm_off = Q8_Q + 32 * lr + 16 * ((lane >> 4) ^ ((lr >> 2) & 1));
   const uint32_t xs_s = smem_u32(xs);
   bool failed = false;
   for (int p = 0; p < n_pass; p++) {
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
             } else {
               const uint32_t tb = stage + j * DN_KB + m * Q8_TILE;
               const float d = half_bits_to_float(dn_lds_u16(tb + 2 * rr));
-              const uint4 q0 = ld_shared_v4(tb + Q8_Q + 32 * rr), q1 = ld_shared_v4(tb + Q8_Q + 32 * rr + 16);
+              const uint4 q0 = ld_shared_v4(tb + Q8_Q + 32 * rr + rsw), q1 = ld_shared_v4(tb + Q8_Q + 32 * rr + (16 - rsw));
 #pragma unroll
               for (int t = 0; t < TT; t++) {
                 if (t < nt) {  // warp-uniform
@@ -498,7 +500,7 @@ ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_token
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->err, 64);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->w, 0, wb, 0);  // padding rows stay zero
   if (e == cudaSuccess) e = cudaMemsetAsync(h->err, 0, 64, 0);
-  if (e == cudaSuccess) e = repack_q8((const uint8_t *)w_q8, h->w, 1, n_out, n_in, 2, 0, 0);
+  if (e == cudaSuccess) e = repack_q8((const uint8_t *)w_q8, h->w, 1, n_out, n_in, 2, 0, 0, true);
   if (e == cudaSuccess) e = cudaStreamSynchronize(0);
   if (e != cudaSuccess) {
     const ds4moe_status st = dn_status(e);

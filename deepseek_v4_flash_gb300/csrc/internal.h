@@ -84,7 +84,7 @@ namespace ds4 {
 cudaError_t repack_q2s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
                        cudaStream_t s);
 cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
-                      cudaStream_t s);
+                      cudaStream_t s, bool swz = false);
 cudaError_t repack_q4s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
                        cudaStream_t s);
 cudaError_t repack_rq8(const uint8_t *src, uint8_t *dst, int rows, int rows_pad, int K, cudaStream_t s);

@@ -92,9 +92,12 @@ __global__ void k_repack_q4s(const uint8_t *__restrict__ src, uint8_t *__restric
   }
 }
 
-// Expert Q8_0 -> RG16: one thread per canonical block (34 bytes).
+// Expert Q8_0 -> RG16: one thread per canonical block (34 bytes). swz: the
+// two 16-byte halves of rows 4-7 and 12-15 of a tile trade places, so that
+// eight consecutive rows' halves at a 32-byte row stride fall in 32
+// different banks (ldmatrix and 16-byte loads without conflicts).
 __global__ void k_repack_q8(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst, int n_mat, int rows,
-                            int KS, int npair, int which) {
+                            int KS, int npair, int which, int swz) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = (int64_t)n_mat * rows * KS;
   if (i >= total) return;
@@ -105,8 +108,9 @@ __global__ void k_repack_q8(const uint8_t *__restrict__ src, uint8_t *__restrict
   const int rg = r >> 4, rr = r & 15;
   uint8_t *tile = dst + tile_index(m, rows, rg, KS, c, npair, which) * Q8_TILE;
   tile[2 * rr + 0] = b[0], tile[2 * rr + 1] = b[1];
+  const int hs = swz ? (rr >> 2) & 1 : 0;
   for (int h = 0; h < 2; h++)
-    for (int j = 0; j < 16; j++) tile[Q8_Q + 16 * (2 * rr + h) + j] = b[2 + 16 * h + j];
+    for (int j = 0; j < 16; j++) tile[Q8_Q + 16 * (2 * rr + (h ^ hs)) + j] = b[2 + 16 * h + j];
 }
 
 // Router Q8_0 -> RQ8: one thread per pair of canonical blocks (2 x 34 bytes);
@@ -158,11 +162,12 @@ cudaError_t repack_q4s(const uint8_t *src, uint8_t *dst, int n_mat, int rows, in
 }
 
 cudaError_t repack_q8(const uint8_t *src, uint8_t *dst, int n_mat, int rows, int K, int pair, int which,
-                      cudaStream_t s) {
+                      cudaStream_t s, bool swz) {
   const int KS = K / Q8_KSTEP;
   const int64_t n = (int64_t)n_mat * rows * KS;
   if (n == 0) return cudaSuccess;
-  k_repack_q8<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair == 2 ? 3 : pair ? 2 : 1, which);
+  k_repack_q8<<<blocks_for(n, 256), 256, 0, s>>>(src, dst, n_mat, rows, KS, pair == 2 ? 3 : pair ? 2 : 1, which,
+                                                 swz ? 1 : 0);
   return cudaGetLastError();
 }
 
