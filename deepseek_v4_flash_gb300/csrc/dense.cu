@@ -11,16 +11,23 @@
 //                  l of the unit and keeps, per token, the row's segment chain
 //                  (CAS step 3: (d * dx) * I, added in block order).
 //                  Calls of two or more tokens take the block dots I of 16
-//                  rows x 8 tokens from one int8 tensor-core instruction
-//                  (mma.sync m16n8k32: the Q8_0 codes are already int8, and
-//                  the int32 sums are exact); lane (g, t) then keeps the
+//                  rows x 8 tokens from two fp16 tensor-core instructions
+//                  (mma.sync m16n8k16, f32 accumulation): the int8 codes are
+//                  exact in fp16 and every partial sum is an integer below
+//                  2^24, so I comes out exact. (The int8 form, m16n8k32,
+//                  would give the same bits but runs at a quarter of the
+//                  fp16 form's rate here: 68 against 8.5 cycles per
+//                  instruction and sub-partition, measured.) The tokens'
+//                  codes are staged as fp16; the weights' codes are widened
+//                  in registers after ldmatrix. Lane (g, t) then keeps the
 //                  chains of rows g, g + 8 of both tiles for tokens 2t,
 //                  2t + 1.
 //                  Unsplit rows (one unit covers all S segments) add each
 //                  finished segment to the row sum in order (CAS step 4) and
 //                  store y. Split rows store their segment sums.
 //                  The tokens' codes sit in shared memory once per pass of up
-//                  to TT tokens, TT chosen per call from n_tok.
+//                  to TT tokens (int8, or fp16 for the tensor-core step), TT
+//                  chosen per call from n_tok.
 //   k_dense_fix    (split calls only) adds each split row's S segment sums
 //                  in segment order and stores y.
 // Units go to warps SM-first (unit u to warp u / G of block u % G), so that a
@@ -108,31 +115,49 @@ __device__ __forceinline__ void dn_ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t
                : "r"(addr));
 }
 
-// D = A B for A 16x32 (rows, K) and B 32x8 (K, tokens) of int8: the exact
-// int32 block dots of 16 rows and 8 tokens. Lane (g, t) = (lane / 4,
-// lane % 4) holds A rows g and g + 8 at K 4t..4t+3 and 16+4t..16+4t+3, B
-// token g at the same K, and D rows g, g + 8 for tokens 2t, 2t + 1.
-__device__ __forceinline__ void dn_mma_s8(const uint32_t (&a)[4], uint32_t b0, uint32_t b1, int (&d)[4]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+// Four int8 codes (one word, element j in byte j) -> the same integers as
+// fp16 pairs: lo = (e0, e1), hi = (e2, e3). Each half is built as
+// 1024 + 128 + q (the byte q ^ 0x80 under the exponent byte 0x64) and 1152
+// is subtracted: exact, as every value involved is an integer below 2^11.
+__device__ __forceinline__ void dn_i8x4_to_h(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u, E = 0x64646464u, C = 0x64806480u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(E));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(E));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(C));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(C));
 }
 
-// The terms (d_r * dx_k) * I of one row r for the lane's two tokens, added
-// to the row's packed pair of chains; the second products are scalar (a
-// packed product whose only use is a packed add would be fused into one
-// rounding).
-__device__ __forceinline__ void dn_mma_terms(unsigned long long &acc, float d, unsigned long long dx2, int i0, int i1) {
+// D += A B for A 16x16 (rows, K) and B 16x8 (K, tokens) of fp16, D f32.
+// Lane (g, t) = (lane / 4, lane % 4) holds A rows g, g + 8 at K slots 2t,
+// 2t + 1 (a0, a1) and 8 + 2t, 9 + 2t (a2, a3), B token g at the same slots,
+// and D rows g, g + 8 for tokens 2t, 2t + 1. The K order inside one
+// instruction is free (a sum): slot pairs (2t, 2t + 1) and (8 + 2t, 9 + 2t)
+// carry the codes 4t, 4t + 1 and 4t + 2, 4t + 3 of the 16-code half, so that
+// one 32-bit word of codes feeds both pairs of a lane.
+__device__ __forceinline__ void dn_mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The terms (d_r * dx_k) * I of one row r for the lane's two tokens (I the
+// exact block dots as floats), added to the row's packed pair of chains; the
+// second products are scalar (a packed product whose only use is a packed
+// add would be fused into one rounding).
+__device__ __forceinline__ void dn_mma_terms(unsigned long long &acc, float d, unsigned long long dx2, float i0,
+                                             float i1) {
   float dd0, dd1;
   f2_unpack(f2_mul(f2_pack(d, d), dx2), dd0, dd1);
-  acc = f2_add(acc, f2_pack(__fmul_rn(dd0, __int2float_rn(i0)), __fmul_rn(dd1, __int2float_rn(i1))));
+  acc = f2_add(acc, f2_pack(__fmul_rn(dd0, i0), __fmul_rn(dd1, i1)));
 }
 
 // MMA = false: lane l owns row l of the unit and a chain per token (TT
 // tokens per pass, dp4a dots). MMA = true: eight tokens per pass on the
-// tensor cores (mma.sync m16n8k32, int8), lane (g, t) owns rows g, g + 8 of
-// both tiles for tokens 2t, 2t + 1.
+// tensor cores (mma.sync m16n8k16, fp16 codes), lane (g, t) owns rows g,
+// g + 8 of both tiles for tokens 2t, 2t + 1.
 template <int TT, bool MMA>
 __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
   static_assert(!MMA || TT == 8, "the tensor-core step takes eight tokens");
@@ -147,13 +172,20 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
   const int G = gridDim.x, W = G * DN_WARPS, gw = warp * G + blockIdx.x;
   const int my_units = gw < n_units ? (n_units - 1 - gw) / W + 1 : 0;
   const int n_pass = (a.T + TT - 1) / TT;
-  // shared memory: the pass's codes [TT][K + 16] and scales [TT][K/32 + 4]
-  // (rows padded by 16 bytes, so that the tensor-core step's loads of eight
-  // tokens' rows fall in different banks), then the rings
-  const int xrow = a.K + 16, drow = nb + 4;
+  // shared memory: the pass's codes [TT][K + 16] int8 (dp4a step) or
+  // [TT][K + 16] fp16 (tensor-core step) and scales [TT][K/32 + 4], then the
+  // rings; the rows' padding puts the tensor-core step's loads of eight
+  // tokens' rows in different banks
+  constexpr int CB = MMA ? 2 : 1;  // bytes per staged code
+  const int xrow = CB * (a.K + 16), drow = nb + 4;
   int8_t *xs = (int8_t *)smem;
   float *ds = (float *)(smem + TT * xrow);
   const int ring_off = (TT * xrow + TT * drow * 4 + 127) & ~127;
+  if constexpr (MMA) {  // rows of a short last pass stay defined (zero)
+    for (int i = threadIdx.x; i < (TT * xrow + TT * drow * 4) / 16; i += blockDim.x)
+      *(uint4 *)(smem + 16 * i) = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+  }
   const uint32_t ring = smem_u32(smem + ring_off + warp * nst * sbytes);
   __shared__ uint64_t bars[DN_WARPS][DN_MAX_NST];
   const uint32_t bar = smem_u32(&bars[warp][0]);
@@ -206,7 +238,18 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
       const uint4 *src = (const uint4 *)(a.xq + (size_t)t0 * a.K);
       for (int i = threadIdx.x; i < nq; i += blockDim.x) {
         const int r = i / qrow;
-        *(uint4 *)(xs + r * xrow + 16 * (i - r * qrow)) = __ldg(src + i);
+        const uint4 v = __ldg(src + i);
+        if constexpr (MMA) {
+          uint4 lo, hi;
+          dn_i8x4_to_h(v.x, lo.x, lo.y);
+          dn_i8x4_to_h(v.y, lo.z, lo.w);
+          dn_i8x4_to_h(v.z, hi.x, hi.y);
+          dn_i8x4_to_h(v.w, hi.z, hi.w);
+          uint4 *d = (uint4 *)(xs + r * xrow + 32 * (i - r * qrow));
+          d[0] = lo, d[1] = hi;
+        } else {
+          *(uint4 *)(xs + r * xrow + 16 * (i - r * qrow)) = v;
+        }
       }
       for (int i = threadIdx.x; i < nd; i += blockDim.x) {
         const int r = i / nb;
@@ -244,16 +287,21 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
           if (j < ks) {
             const int b = bst + j;
             if constexpr (MMA) {
-              const uint32_t b0 = ld_shared_u32(xs_s + g * xrow + 32 * b + 4 * t4);
-              const uint32_t b1 = ld_shared_u32(xs_s + g * xrow + 32 * b + 16 + 4 * t4);
+              // token g's codes 32b + 4t4 .. +3 (first half) and 32b + 16 + 4t4 .. +3
+              const uint2 bl = ld_shared_v2(xs_s + g * xrow + 64 * b + 8 * t4);
+              const uint2 bh = ld_shared_v2(xs_s + g * xrow + 64 * b + 32 + 8 * t4);
               const unsigned long long dx2 = f2_pack(ds[(2 * t4) * drow + b], ds[(2 * t4 + 1) * drow + b]);
 #pragma unroll
               for (int mt = 0; mt < 2; mt++) {
                 const uint32_t tb = stage + j * DN_KB + mt * Q8_TILE;
-                uint32_t af[4];
+                // af: rows g, g + 8 at codes 4t4..+3 (af[0], af[1]) and 16 + 4t4..+3 (af[2], af[3])
+                uint32_t af[4], al[4], ah[4];
                 dn_ldsm_x4(tb + lm_off, af[0], af[1], af[2], af[3]);
-                int dv[4];
-                dn_mma_s8(af, b0, b1, dv);
+#pragma unroll
+                for (int q = 0; q < 4; q++) dn_i8x4_to_h(af[q], al[q], ah[q]);
+                float dv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                dn_mma_f16(dv, al[0], al[1], ah[0], ah[1], bl.x, bl.y);
+                dn_mma_f16(dv, al[2], al[3], ah[2], ah[3], bh.x, bh.y);
                 dn_mma_terms(macc[mt][0], half_bits_to_float(dn_lds_u16(tb + 2 * g)), dx2, dv[0], dv[1]);
                 dn_mma_terms(macc[mt][1], half_bits_to_float(dn_lds_u16(tb + 2 * (g + 8))), dx2, dv[2], dv[3]);
               }
@@ -365,17 +413,23 @@ static int dn_tt(int K, int T) {
   return tt;
 }
 
-static size_t dn_stage_smem(int TT, int K) {
-  return ((size_t)TT * (K + 16) + (size_t)TT * (K / 32 + 4) * 4 + 127) & ~(size_t)127;
+// The pass's staged codes (int8, or fp16 for the tensor-core step) and scales.
+static size_t dn_stage_smem(int TT, int K, bool mma) {
+  return ((size_t)TT * (K + 16) * (mma ? 2 : 1) + (size_t)TT * (K / 32 + 4) * 4 + 127) & ~(size_t)127;
 }
 
 // Ring geometry: the largest K steps per stage (a divisor of a segment's
 // blocks, at most 8) that still leaves every warp two stages, else one K
 // step per stage; stages per warp from the shared memory left. Long stages
 // win: a stage's K steps run unrolled, and each stage costs a wait.
-static void dn_ring(int TT, int K, int &ks, int &nst) {
+static void dn_ring(int TT, int K, bool mma, int &ks, int &nst) {
   const int nb = K / 32, per = nb / expert_segs(DS4MOE_Q8_0, K);
-  const size_t left = DN_SMEM_LIMIT - DN_STATIC - dn_stage_smem(TT, K);
+  const size_t st = dn_stage_smem(TT, K, mma);
+  if (st + (size_t)DN_WARPS * 2 * DN_KB > DN_SMEM_LIMIT - DN_STATIC) {  // not even two one-step stages
+    ks = 1, nst = 0;
+    return;
+  }
+  const size_t left = DN_SMEM_LIMIT - DN_STATIC - st;
   for (ks = per < DN_MAX_KS ? per : DN_MAX_KS; ks > 1; ks--) {
     if (per % ks) continue;
     if (left / ((size_t)DN_WARPS * ks * DN_KB) >= 2) break;
@@ -438,16 +492,16 @@ void dn_free(ds4moe_dense *h) {
 template <int TT, bool MMA>
 cudaError_t dn_launch(ds4moe_dense *h, const DnArgs &a0, cudaStream_t s) {
   DnArgs a = a0;
-  dn_ring(TT, h->K, a.ks, a.nst);
+  dn_ring(TT, h->K, MMA, a.ks, a.nst);
   a.ns = dn_split(h, a.T, TT);
   if (h->dbg_ks || h->dbg_nst) {
     const int ks = h->dbg_ks ? h->dbg_ks : a.ks, nst = h->dbg_nst ? h->dbg_nst : a.nst;
-    if (dn_stage_smem(TT, h->K) + (size_t)DN_WARPS * nst * ks * DN_KB <= DN_SMEM_LIMIT - DN_STATIC)
+    if (dn_stage_smem(TT, h->K, MMA) + (size_t)DN_WARPS * nst * ks * DN_KB <= DN_SMEM_LIMIT - DN_STATIC)
       a.ks = ks, a.nst = nst;
   }
   if (h->dbg_ns) a.ns = (a.T <= TT && a.T <= h->part_tokens) ? h->dbg_ns : 1;
   void *args[] = {&a};
-  const size_t smem = dn_stage_smem(TT, h->K) + (size_t)DN_WARPS * a.nst * a.ks * DN_KB;
+  const size_t smem = dn_stage_smem(TT, h->K, MMA) + (size_t)DN_WARPS * a.nst * a.ks * DN_KB;
   cudaError_t e = launch_pdl((const void *)k_dense<TT, MMA>, dim3(h->n_sm), dim3(DN_WARPS * 32), smem, s, args, true);
   h->launches++;
   if (e == cudaSuccess && a.ns > 1) {
@@ -475,7 +529,7 @@ ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_token
   if (!dn_dev_ptr(w_q8)) return DS4MOE_ERR_INVALID_ARG;
   {
     int ks, nst;
-    dn_ring(dn_tt_cap(n_in), n_in, ks, nst);
+    dn_ring(dn_tt_cap(n_in), n_in, false, ks, nst);
     if (nst < 2) return DS4MOE_ERR_UNSUPPORTED;
   }
   ds4moe_dense *h = new (std::nothrow) ds4moe_dense;
@@ -538,8 +592,10 @@ ds4moe_status ds4moe_dense_forward(ds4moe_dense *h, const float *x, int32_t n_to
     a.N = h->N, a.N_pad = h->N_pad, a.K = K, a.T = n_tok;
     a.w = h->w, a.xq = h->xq, a.dx = h->dx, a.y = y, a.part = h->part, a.err = h->err;
     // two or more tokens: the tensor-core step (passes of eight tokens),
-    // where eight tokens' codes fit the pass buffer
-    const bool fits = dn_tt_cap(K) == DN_TT_MAX;
+    // where eight tokens' fp16 codes leave room for the rings
+    int tks, tnst;
+    dn_ring(DN_TT_MAX, K, true, tks, tnst);
+    const bool fits = tnst >= 2;
     const bool tc = fits && (h->dbg_tc == 2 || (h->dbg_tc == 0 && n_tok >= 2));
     if (tc) {
       e = dn_launch<8, true>(h, a, s);

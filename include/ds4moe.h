@@ -319,8 +319,10 @@ ds4moe_status ds4moe_profile_read(const ds4moe_layer *h, double *ms_out, int32_t
  *   pointers), enqueued on `stream` (two launches, three for split rows; no
  *   allocation, no host synchronisation). Built for decode-sized n_tok: the
  *   matrix is streamed once per pass of up to 8 tokens (fewer for very wide
- *   n_in); from two tokens on the int8 block dots run on the tensor cores
- *   (exact int32 sums, the same bits); a call of one pass may split rows over several warps by whole
+ *   n_in); from two tokens on the integer block dots run on the tensor
+ *   cores (the int8 codes as fp16 with f32 accumulation: every partial sum
+ *   is an integer below 2^24, so the dots are exact and the bits the same);
+ *   a call of one pass may split rows over several warps by whole
  *   segments, whose sums a third launch adds in segment order (the same bits
  *   as unsplit). Calls on one handle must not run concurrently (shared
  *   scratch).
@@ -341,8 +343,8 @@ uint64_t ds4moe_dense_launch_count(const ds4moe_dense *h);
  *   every setting): ks = K steps per ring stage (a divisor of n_in/32/S, at
  *   most 8), nst = ring stages per warp (2..6, within shared memory), ns =
  *   units per 32-row item (a divisor of S), tc = the block-dot step: 1 the
- *   dp4a step only, 2 the int8 tensor-core step for every call (where eight
- *   tokens' codes fit a pass; the automatic choice takes it from two tokens
+ *   dp4a step only, 2 the tensor-core step for every call (where eight
+ *   tokens' fp16 codes fit a pass; the automatic choice takes it from two tokens
  *   on). 0 keeps the automatic choice of that value. A call whose tokens do
  *   not fit one pass of the segment-sum scratch runs unsplit (ns = 1)
  *   whatever ns says; a (ks, nst) that does not fit a call's shared memory

@@ -103,6 +103,43 @@ def test_dense_output_head_one_token():
     _run(129280, 4096, 1, seed=777)
 
 
+def test_dense_output_head_eight_tokens():
+    """The output head at full size for a pass of 8 tokens (the tensor-core
+    step, rows unsplit)."""
+    _run(129280, 4096, 8, seed=778)
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_dense_extreme_codes(T):
+    """Every weight and activation code at +-127: the block dots reach
+    +-32 * 127^2 = +-516,128, the largest the format allows, and must come out
+    exact on both steps (fp16 codes, f32 accumulation on the tensor cores)."""
+    import torch
+    import deepseek_v4_flash_gb300 as ds4
+    n_out, n_in = 256, 1024
+    nb = n_in // 32
+    blk = np.zeros((n_out, nb, 34), np.uint8)
+    r = np.arange(n_out)[:, None]
+    b = np.arange(nb)[None, :]
+    d = (0.001 * (1 + (r * 7 + b * 3) % 50)).astype(np.float16)
+    blk[:, :, 0:2] = d.view(np.uint8).reshape(n_out, nb, 2)
+    sign = np.where(((r + b) % 3 == 0)[..., None], -127, 127).astype(np.int8)
+    blk[:, :, 2:] = np.broadcast_to(sign, (n_out, nb, 32)).view(np.uint8)
+    w = blk.reshape(-1)
+    # each 32-block of x is constant up to sign: codes +-127
+    x = np.ones((T, n_in), np.float32)
+    x *= np.where((np.arange(n_in)[None, :] // 32 + np.arange(T)[:, None]) % 2 == 0, 1.0, -3.5).astype(np.float32)
+    ref = oracle.get().dense_q8(w, n_out, n_in, x)
+    dn = ds4.Dense(n_out, n_in, torch.from_numpy(w).cuda(), max_tokens=T)
+    y = dn.forward(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert dn.device_error() == 0
+    got = y.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), \
+        f"not bit-exact: {np.count_nonzero(got != ref)} of {got.size} differ"
+    dn.close()
+
+
 def test_dense_wide_input():
     """n_in 16384: passes of 2 tokens (the codes of a pass fit 64 KB)."""
     _run(256, 16384, 3, seed=5)
