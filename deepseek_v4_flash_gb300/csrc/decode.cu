@@ -25,9 +25,11 @@ namespace ds4 {
 //
 // grid (ROUTER_SEGS, T), clusters of ROUTER_SEGS blocks: the cluster of
 // token t has one block per K segment. When the call normalises its input,
-// every block first takes the inverse RMS norm of each of its tokens (warp
-// i: token i, the whole row, the RMSNorm kernel's arithmetic) and scales the
-// values it reads by it. Block seg quantises the token's
+// every block first needs the inverse RMS norm of each of its tokens (one
+// warp over the whole row, the RMSNorm kernel's arithmetic): with one token
+// per cluster each block takes it itself; with tg tokens block r takes
+// token r's and stores it into every block of the cluster (one cluster
+// barrier). The block scales the values it reads by it. Block seg quantises the token's
 // 32-blocks of its segment (and publishes them), then sums every router row
 // over the segment (warp w: row groups w, w + RC_WARPS, ...; lane = row) into
 // block 0's shared memory (distributed shared memory stores). After one
@@ -118,6 +120,14 @@ __device__ __forceinline__ float rms_inv_warp(const float *v, int H, float eps, 
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
 }
 
+// The cluster barrier in two halves: every block arrives when it starts and
+// waits before its first access to another block's shared memory, so that
+// no block is written before it runs.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -166,6 +176,7 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   const uint32_t bar = smem_u32(&bars[warp]);
   const uint32_t wbuf = smem_u32(work + warp * seg_bytes);
   const size_t rg_stride = (size_t)(a.H / RQ8_KSTEP) * RQ8_TILE;
+  cluster_arrive_relaxed();
   if (a.q8 && lane == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
@@ -188,6 +199,7 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
   // the gate/up kernel may launch now: it requests the shared expert's
   // weights while this kernel routes
   pdl_launch_dependents();
+  cluster_wait();  // every block of the cluster runs: shared-memory stores between them may start
   // quantise the segment's blocks of the cluster's tokens (warp w: pairs
   // (token, block) w, w + RC_WARPS, ...), all loads of a round first; with
   // the RMSNorm, the first round's loads are issued before the norms
@@ -204,11 +216,21 @@ __global__ void __cluster_dims__(ROUTER_SEGS, 1, 1) __launch_bounds__(RC_WARPS *
     };
     load(warp);
     if (a.norm) {
-      if (warp < ntg) {
-        const float r = rms_inv_warp(a.x + (size_t)(t0 + warp) * a.H, a.H, a.eps, lane);
-        if (lane == 0) ninv[warp] = r;
+      if (tg == 1) {
+        if (warp == 0) {
+          const float r = rms_inv_warp(a.x + (size_t)t0 * a.H, a.H, a.eps, lane);
+          if (lane == 0) ninv[0] = r;
+        }
+        __syncthreads();
+      } else {
+        // clusters of tg tokens: block r takes token r's norm and stores it
+        // into every block of the cluster (lane j: block j)
+        if (warp == 0 && seg < ntg) {
+          const float r = rms_inv_warp(a.x + (size_t)(t0 + seg) * a.H, a.H, a.eps, lane);
+          if (lane < ROUTER_SEGS) st_cluster_f32(ninv + seg, lane, r);
+        }
+        cluster_sync_all();
       }
-      __syncthreads();
     }
     for (int pp = warp; pp < np; pp += RC_WARPS * QB) {
       if (pp != warp) load(pp);
