@@ -3,7 +3,9 @@
 //
 // Two kernels, chained with programmatic dependent launch:
 //   k_dense_quant  CAS step 1 on x: one warp per 32-block of a token;
-//   k_dense<TT,MMA> persistent, one block per SM, eight warps. The work is cut
+//   k_dense<TT,MMA,NW> persistent, one block per SM, NW warps (16 for matrices
+//                  of more 32-row items than 8-warp blocks have warps, else
+//                  8). The work is cut
 //                  into units: 32 output rows (two 16-row tiles per K step,
 //                  the layout of an expert's down matrix) times a run of
 //                  whole CAS segments of K. A warp streams its units' tiles
@@ -46,6 +48,7 @@ struct ds4moe_dense {
   int N, K, N_pad, max_tokens, part_tokens, device, n_sm;
   int dbg_ks, dbg_nst, dbg_ns;  // launch geometry overrides, 0 = automatic
   int dbg_tc;                   // 0 automatic, 1 dp4a path only, 2 tensor-core path where it fits
+  int nw;                       // warps per block
   uint8_t *w;        // [N_pad/32][K/32][2][Q8 tile], row halves swizzled (k_repack_q8 swz)
   int8_t *xq;        // [max_tokens][K]
   float *dx;         // [max_tokens][K/32]
@@ -56,7 +59,6 @@ struct ds4moe_dense {
 
 namespace ds4 {
 
-constexpr int DN_WARPS = 8;              // warps per block
 constexpr int DN_KB = 2 * Q8_TILE;       // one K step of a unit: two 16-row tiles, 1088 bytes
 constexpr int DN_MAX_KS = 8;             // K steps per ring stage, at most
 constexpr int DN_MAX_NST = 6;            // ring stages per warp, at most
@@ -158,8 +160,8 @@ __device__ __forceinline__ void dn_mma_terms(unsigned long long &acc, float d, u
 // tokens per pass, dp4a dots). MMA = true: eight tokens per pass on the
 // tensor cores (mma.sync m16n8k16, fp16 codes), lane (g, t) owns rows g,
 // g + 8 of both tiles for tokens 2t, 2t + 1.
-template <int TT, bool MMA>
-__global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
+template <int TT, bool MMA, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) k_dense(DnArgs a) {
   static_assert(!MMA || TT == 8, "the tensor-core step takes eight tokens");
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
   const int nbu = nb / ns, ust = nbu / ks;  // blocks and ring stages of one unit
   const int sst = per / ks;                 // ring stages of one segment
   const int n_units = (a.N_pad >> 5) * ns;
-  const int G = gridDim.x, W = G * DN_WARPS, gw = warp * G + blockIdx.x;
+  const int G = gridDim.x, W = G * NW, gw = warp * G + blockIdx.x;
   const int my_units = gw < n_units ? (n_units - 1 - gw) / W + 1 : 0;
   const int n_pass = (a.T + TT - 1) / TT;
   // shared memory: the pass's codes [TT][K + 16] int8 (dp4a step) or
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(DN_WARPS * 32, 1) k_dense(DnArgs a) {
     __syncthreads();
   }
   const uint32_t ring = smem_u32(smem + ring_off + warp * nst * sbytes);
-  __shared__ uint64_t bars[DN_WARPS][DN_MAX_NST];
+  __shared__ uint64_t bars[NW][DN_MAX_NST];
   const uint32_t bar = smem_u32(&bars[warp][0]);
   if (lane == 0) {
     for (int i = 0; i < nst; i++) mbar_init(bar + 8 * i, 1);
@@ -422,19 +424,19 @@ static size_t dn_stage_smem(int TT, int K, bool mma) {
 // blocks, at most 8) that still leaves every warp two stages, else one K
 // step per stage; stages per warp from the shared memory left. Long stages
 // win: a stage's K steps run unrolled, and each stage costs a wait.
-static void dn_ring(int TT, int K, bool mma, int &ks, int &nst) {
+static void dn_ring(int TT, int K, bool mma, int nw, int &ks, int &nst) {
   const int nb = K / 32, per = nb / expert_segs(DS4MOE_Q8_0, K);
   const size_t st = dn_stage_smem(TT, K, mma);
-  if (st + (size_t)DN_WARPS * 2 * DN_KB > DN_SMEM_LIMIT - DN_STATIC) {  // not even two one-step stages
+  if (st + (size_t)nw * 2 * DN_KB > DN_SMEM_LIMIT - DN_STATIC) {  // not even two one-step stages
     ks = 1, nst = 0;
     return;
   }
   const size_t left = DN_SMEM_LIMIT - DN_STATIC - st;
   for (ks = per < DN_MAX_KS ? per : DN_MAX_KS; ks > 1; ks--) {
     if (per % ks) continue;
-    if (left / ((size_t)DN_WARPS * ks * DN_KB) >= 2) break;
+    if (left / ((size_t)nw * ks * DN_KB) >= 2) break;
   }
-  const size_t n = left / ((size_t)DN_WARPS * ks * DN_KB);
+  const size_t n = left / ((size_t)nw * ks * DN_KB);
   nst = n > DN_MAX_NST ? DN_MAX_NST : (int)n;
 }
 
@@ -446,7 +448,7 @@ static void dn_ring(int TT, int K, bool mma, int &ks, int &nst) {
 static int dn_split(const ds4moe_dense *h, int T, int TT) {
   if (T > TT || T > h->part_tokens || !h->part) return 1;
   const int S = expert_segs(DS4MOE_Q8_0, h->K);
-  const long long items = h->N_pad / 32, W = (long long)h->n_sm * DN_WARPS;
+  const long long items = h->N_pad / 32, W = (long long)h->n_sm * h->nw;
   auto eff = [&](int ns) {
     const long long u = items * ns, rounds = (u + W - 1) / W;
     return (double)u / (double)(rounds * W);
@@ -489,20 +491,20 @@ void dn_free(ds4moe_dense *h) {
   if (h->err) cudaFree(h->err);
 }
 
-template <int TT, bool MMA>
-cudaError_t dn_launch(ds4moe_dense *h, const DnArgs &a0, cudaStream_t s) {
+template <int TT, bool MMA, int NW>
+cudaError_t dn_launch_nw(ds4moe_dense *h, const DnArgs &a0, cudaStream_t s) {
   DnArgs a = a0;
-  dn_ring(TT, h->K, MMA, a.ks, a.nst);
+  dn_ring(TT, h->K, MMA, NW, a.ks, a.nst);
   a.ns = dn_split(h, a.T, TT);
   if (h->dbg_ks || h->dbg_nst) {
     const int ks = h->dbg_ks ? h->dbg_ks : a.ks, nst = h->dbg_nst ? h->dbg_nst : a.nst;
-    if (dn_stage_smem(TT, h->K, MMA) + (size_t)DN_WARPS * nst * ks * DN_KB <= DN_SMEM_LIMIT - DN_STATIC)
+    if (dn_stage_smem(TT, h->K, MMA) + (size_t)NW * nst * ks * DN_KB <= DN_SMEM_LIMIT - DN_STATIC)
       a.ks = ks, a.nst = nst;
   }
   if (h->dbg_ns) a.ns = (a.T <= TT && a.T <= h->part_tokens) ? h->dbg_ns : 1;
   void *args[] = {&a};
-  const size_t smem = dn_stage_smem(TT, h->K, MMA) + (size_t)DN_WARPS * a.nst * a.ks * DN_KB;
-  cudaError_t e = launch_pdl((const void *)k_dense<TT, MMA>, dim3(h->n_sm), dim3(DN_WARPS * 32), smem, s, args, true);
+  const size_t smem = dn_stage_smem(TT, h->K, MMA) + (size_t)NW * a.nst * a.ks * DN_KB;
+  cudaError_t e = launch_pdl((const void *)k_dense<TT, MMA, NW>, dim3(h->n_sm), dim3(NW * 32), smem, s, args, true);
   h->launches++;
   if (e == cudaSuccess && a.ns > 1) {
     int S = expert_segs(DS4MOE_Q8_0, h->K);
@@ -512,6 +514,11 @@ cudaError_t dn_launch(ds4moe_dense *h, const DnArgs &a0, cudaStream_t s) {
     h->launches++;
   }
   return e;
+}
+
+template <int TT, bool MMA>
+cudaError_t dn_launch(ds4moe_dense *h, const DnArgs &a, cudaStream_t s) {
+  return h->nw == 16 ? dn_launch_nw<TT, MMA, 16>(h, a, s) : dn_launch_nw<TT, MMA, 8>(h, a, s);
 }
 
 }  // namespace
@@ -527,9 +534,19 @@ ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_token
   if (max_tokens < 1 || max_tokens > (1 << 16)) return DS4MOE_ERR_INVALID_ARG;
   if ((long long)max_tokens * n_out >= (1ll << 40)) return DS4MOE_ERR_INVALID_ARG;
   if (!dn_dev_ptr(w_q8)) return DS4MOE_ERR_INVALID_ARG;
+  // Warps per block: 16 where every warp of 8-warp blocks would get more
+  // than one 32-row item, else 8. Measured: the 129280 x 4096 head 1-4 %
+  // faster with 16 (more warps hide the per-block latencies), a 4096 x 4096
+  // projection 5 % slower (its units fit one 8-warp ring in flight).
+  int n_sm = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DS4MOE_ERR_CUDA;
+  }
+  const int nw = (long long)((n_out + 31) / 32) > (long long)n_sm * 8 ? 16 : 8;
   {
     int ks, nst;
-    dn_ring(dn_tt_cap(n_in), n_in, false, ks, nst);
+    dn_ring(dn_tt_cap(n_in), n_in, false, nw, ks, nst);
     if (nst < 2) return DS4MOE_ERR_UNSUPPORTED;
   }
   ds4moe_dense *h = new (std::nothrow) ds4moe_dense;
@@ -537,14 +554,17 @@ ds4moe_status ds4moe_dense_create(int32_t n_out, int32_t n_in, int32_t max_token
   memset(h, 0, sizeof(*h));
   h->N = n_out, h->K = n_in, h->N_pad = (n_out + 31) / 32 * 32, h->max_tokens = max_tokens;
   h->part_tokens = max_tokens < DN_TT_MAX ? max_tokens : DN_TT_MAX;
+  h->nw = nw;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->device);
   const size_t wb = (size_t)h->N_pad / 32 * (n_in / 32) * DN_KB;
   const size_t qb = (size_t)max_tokens * n_in, db = (size_t)max_tokens * (n_in / 32) * 4;
   const size_t pb = (size_t)expert_segs(DS4MOE_Q8_0, n_in) * h->part_tokens * h->N_pad * 4;
-  for (const void *fn : {(const void *)k_dense<1, false>, (const void *)k_dense<2, false>,
-                         (const void *)k_dense<4, false>, (const void *)k_dense<8, false>,
-                         (const void *)k_dense<8, true>})
+  for (const void *fn : {(const void *)k_dense<1, false, 8>, (const void *)k_dense<2, false, 8>,
+                         (const void *)k_dense<4, false, 8>, (const void *)k_dense<8, false, 8>,
+                         (const void *)k_dense<8, true, 8>, (const void *)k_dense<1, false, 16>,
+                         (const void *)k_dense<2, false, 16>, (const void *)k_dense<4, false, 16>,
+                         (const void *)k_dense<8, false, 16>, (const void *)k_dense<8, true, 16>})
     if (e == cudaSuccess)  // the static barriers take their part of the block's shared memory
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(DN_SMEM_LIMIT - DN_STATIC));
   if (e == cudaSuccess) e = cudaMalloc((void **)&h->w, wb);
@@ -594,7 +614,7 @@ ds4moe_status ds4moe_dense_forward(ds4moe_dense *h, const float *x, int32_t n_to
     // two or more tokens: the tensor-core step (passes of eight tokens),
     // where eight tokens' fp16 codes leave room for the rings
     int tks, tnst;
-    dn_ring(DN_TT_MAX, K, true, tks, tnst);
+    dn_ring(DN_TT_MAX, K, true, h->nw, tks, tnst);
     const bool fits = tnst >= 2;
     const bool tc = fits && (h->dbg_tc == 2 || (h->dbg_tc == 0 && n_tok >= 2));
     if (tc) {

@@ -35,6 +35,8 @@ def _run(n_out, n_in, T, seed, max_tokens=None, scale=1.0):
     (96, 768, 9),       # 24 blocks (stages of 3), two passes of 8 tokens
     (4096, 4096, 5),    # an attention-projection shape
     (1000, 4096, 17),   # three passes, ragged last pass
+    (40000, 512, 3),    # more 32-row items than 8-warp blocks have warps: 16 warps per block
+    (39008, 256, 9),    # the same, two passes
 ])
 def test_dense_shapes(n_out, n_in, T):
     _run(n_out, n_in, T, seed=n_out + n_in + T)
