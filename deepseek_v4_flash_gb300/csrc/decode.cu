@@ -382,7 +382,7 @@ cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_
   const ds4moe_layer_desc &d = h->d;
   RouteDecArgs r = {};
   r.x = x, r.T = T, r.H = d.hidden, r.E = d.n_experts, r.E_pad = h->E_pad, r.k = d.top_k, r.NS = h->NS;
-  r.n_shared = d.n_shared, r.vocab = d.vocab, r.scale = d.route_scale, r.A_cap = h->A_max;
+  r.n_shared = d.n_shared, r.vocab = d.vocab, r.scale = d.route_scale, r.A_cap = bucket_cap(h, T);
   r.learned = d.route == DS4MOE_ROUTE_LEARNED;
   r.norm = norm && x, r.eps = eps;
   r.q8 = r.learned && d.router_fmt == DS4MOE_Q8_0;

@@ -708,7 +708,7 @@ static bool x_wide(const ds4moe_layer *h) {
 }
 
 static size_t x_smem_bytes(const ds4moe_layer *h, int T, bool down, bool as) {
-  const int nbk = bucket_table_ints(h->A_max, T, h->NS);
+  const int nbk = bucket_table_ints(bucket_cap(h, T), T, h->NS);
   return (size_t)x_smem(x_tt(T), down, x_wide(h), 2, nbk, as ? (int)x_act_bytes(h, T, down) : 0, x_maxj(h, T, down), T)
       .total;
 }
@@ -731,7 +731,7 @@ cudaError_t launch_experts(const ds4moe_layer *h, int T, float *y, int down, cud
   const ds4moe_layer_desc &d = h->d;
   XArgs a = {};
   a.H = d.hidden, a.F = d.ffn, a.E = d.n_experts, a.k = d.top_k, a.NS = h->NS, a.n_shared = d.n_shared, a.T = T;
-  a.A_cap = h->A_max, a.rf = d.routed_fmt, a.sf = d.n_shared ? d.shared_fmt : d.routed_fmt, a.down = down;
+  a.A_cap = bucket_cap(h, T), a.rf = d.routed_fmt, a.sf = d.n_shared ? d.shared_fmt : d.routed_fmt, a.down = down;
   a.bucket = h->bucket, a.ids = h->ids, a.w = h->wts;
   a.xq_ready = h->xq_ready, a.xq_parts = ROUTER_SEGS * T;
   a.hq = h->hq, a.dh = h->dh, a.gsh = h->gsh, a.hbuf = h->hbuf, a.hticket = h->hticket;

@@ -97,6 +97,15 @@ cudaError_t launch_rmsnorm(const float *x, float *out, int T, int H, float eps, 
 constexpr int DEC_MAX_T = 64;  // largest n_tok served by the decode path
 static_assert(DS4_HOST_GRAPHS == DEC_MAX_T + 1, "one forward_host graph per decode chunk size");
 size_t route_dec_smem(const ds4moe_layer *h);
+// Capacity of the bucket table's expert list for a decode call of T tokens:
+// min(E, T*k) + n_shared (at most A_max). The router and both expert kernels
+// of a call lay the table out with it, so a small call's table (and the
+// expert kernels' shared-memory copy of it) stays small.
+inline int bucket_cap(const ds4moe_layer *h, int T) {
+  const long long routed = (long long)T * h->d.top_k;
+  const int c = (int)(routed < h->d.n_experts ? routed : h->d.n_experts) + h->d.n_shared;
+  return c < h->A_max ? c : h->A_max;
+}
 cudaError_t launch_dec_route(const ds4moe_layer *h, const float *x, const int32_t *tok, int T, int32_t *ids,
                              float *w, bool bucket, cudaStream_t s, bool norm = false, float eps = 0.0f);
 cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args, bool pdl);
