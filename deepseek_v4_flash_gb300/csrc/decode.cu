@@ -24,21 +24,22 @@ namespace ds4 {
 // K1: quantisation, router segment sums, routing and bucketing.
 //
 // grid (ROUTER_SEGS, T), clusters of ROUTER_SEGS blocks: the cluster of
-// token t has one block per K segment. When the call normalises its input,
-// every block first needs the inverse RMS norm of each of its tokens (one
-// warp over the whole row, the RMSNorm kernel's arithmetic): with one token
-// per cluster each block takes it itself; with tg tokens block r takes
-// token r's and stores it into every block of the cluster (one cluster
-// barrier). The block scales the values it reads by it. Block seg quantises the token's
-// 32-blocks of its segment (and publishes them), then sums every router row
-// over the segment (warp w: row groups w, w + RC_WARPS, ...; lane = row) into
-// block 0's shared memory (distributed shared memory stores). After one
-// cluster barrier the other blocks are done; block 0 adds the eight segment
-// sums of each row in segment order from its own shared memory and routes
-// the token with all its threads (route.cuh; hash
-// routing: the table lookup). When bucketing is asked for, the block that
-// routed the call's last token (a self-resetting ticket; none for one token)
-// buckets the call (bucket.cuh).
+// token t has one block per K segment. The blocks pass one cluster barrier
+// in their prologue, so no block's shared memory is written before it runs.
+// When the call normalises its input, every block first needs the inverse
+// RMS norm of each of its tokens (one warp over the whole row, the RMSNorm
+// kernel's arithmetic): with one token per cluster each block takes it
+// itself; with tg tokens block r takes token r's and stores it into every
+// block of the cluster (one more cluster barrier). The block scales the
+// values it reads by it. Block seg quantises the token's 32-blocks of its
+// segment (and publishes them), then sums every router row over the segment
+// (warp w: row groups w, w + RC_WARPS, ...; lane = row) into block 0's
+// shared memory (distributed shared memory stores). After one cluster
+// barrier the other blocks are done; block 0 adds the eight segment sums of
+// each row in segment order from its own shared memory and routes the token
+// with all its threads (route.cuh; hash routing: the table lookup). When
+// bucketing is asked for, the block that routed the call's last token (a
+// self-resetting ticket; none for one token) buckets the call (bucket.cuh).
 
 constexpr int RC_WARPS = 8;   // warps per block
 constexpr int RC_HDR = 128;   // shared memory header: ticket flag, mbarriers
